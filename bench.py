@@ -1,0 +1,477 @@
+#!/usr/bin/env python3
+"""Benchmark of the Q4_G64_FP16 linear layer on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--t T] [--profile]
+
+Timing (the linear-benchmark contract, section 6, and the Q4 measurement
+report's header table): every sample is one complete public call captured in
+a CUDA graph; before each sample a 256 MiB buffer is written and then read
+back (the write evicts L2, the read leaves it clean so no dirty lines are
+written back inside the sample); CUDA events on the launching stream bracket
+only the graph launch; the flush and the graph are queued back to back with
+no host synchronisation.  The primary figure is the median; min and p95 are
+reported too.  Metrics follow the contract's sections 4-5 (weight_only_bit_q4_gb300.metrics).
+
+A step is one call of the layer on one batch of the workload's synthetic
+input.  Default workload: the decode GEMV, N=6144 K=5120 T=1.
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the layer does not exchange data between GPUs); value = the units all ranks
+processed / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from weight_only_bit_q4_gb300 import metrics, synth  # noqa: E402
+
+METRIC = "Q4 linear µs + logical GB/s (small T) / eff. TFLOP/s (large T) vs GB300 roofline"
+FLUSH_BYTES = 256 << 20
+
+# name -> (N, K, T, scale distribution, outlier channels, weight seed, x seed)
+WORKLOADS = {
+    "q4_512x1024_t8": (512, 1024, 8, "halfnormal", False, 0, 0),
+    "q4_6144x5120_t1": (6144, 5120, 1, "halfnormal", False, 0, 0),
+    "q4_6144x5120": (6144, 5120, None, "halfnormal", False, 0, None),       # --t, X seed = T
+    "q4_14336x5120": (14336, 5120, None, "lognormal", True, 0, None),       # --t in {1,16,128,1024}
+    "q4_34816x5120_t1024": (34816, 5120, 1024, "halfnormal", False, 0, 0),
+    "q4_5120x17408_t1024": (5120, 17408, 1024, "halfnormal", False, 0, 0),
+}
+DEFAULT_WORKLOAD = "q4_6144x5120_t1"
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    p.add_argument("--t", type=int, default=None, help="T for the sweep workloads")
+    p.add_argument("--profile", action="store_true",
+                   help="one call between cudaProfilerStart/Stop after warm-up and flush (for ncu --profile-from-start off)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    a = p.parse_args(argv)
+    a.warmup = max(a.warmup, 3)
+    a.steps = max(a.steps, 1)
+    return a
+
+
+def workload(args):
+    N, K, T, dist, outl, ws, xs = WORKLOADS[args.workload]
+    if T is None:
+        T = args.t if args.t is not None else 1
+    elif args.t is not None and args.t != T:
+        raise SystemExit(f"workload {args.workload} has fixed T={T}")
+    if xs is None:
+        xs = T
+    name = args.workload if WORKLOADS[args.workload][2] is not None else f"{args.workload}_t{T}"
+    return dict(name=name, N=N, K=K, T=T, dist=dist, outliers=outl, w_seed=ws, x_seed=xs)
+
+
+def small_t(wl):
+    # HBM-bound below the ridge (~280 FLOP/B at 6.8 TB/s and 1.9 PF/s): T <~ 75
+    return wl["T"] <= 64
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_max(values, world, device=None):
+    """Elementwise max over ranks of a list of floats (identity when world == 1)."""
+    if world == 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t_start = self.t_stop = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._reader = threading.Thread(target=self._read, daemon=True)
+        self._reader.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def mark_start(self):
+        self.t_start = time.monotonic()
+
+    def mark_stop(self):
+        self.t_stop = time.monotonic()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [l for (t, l) in self.lines if self.t_start is not None and self.t_start <= t <= (self.t_stop or t) + 0.1]
+        if not rows:
+            rows = [l for (_, l) in self.lines[-3:]]
+        sm, mx, reasons = [], [], set()
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- traffic record
+def kernel_source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "weight_only_bit_q4_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(wl_name):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernels."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(wl_name)
+        if e and e.get("src_digest") == kernel_source_digest():
+            return float(e["dram_bytes_per_launch"]), e.get("kernel")
+    except (OSError, ValueError, KeyError):
+        pass
+    return None, None
+
+
+# ----------------------------------------------------------------------------- our arm
+def measure_ours(args, wl, rank, world, local):
+    import torch
+    from weight_only_bit_q4_gb300 import build, q4lin
+
+    build.build()
+    q4lin.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    N, K, T = wl["N"], wl["K"], wl["T"]
+    wq = synth.packed_codes(N, K, wl["w_seed"])
+    sc = synth.group_scales(N, K, wl["w_seed"], wl["dist"])
+    x = synth.activations(T, K, wl["x_seed"], wl["outliers"])
+    import numpy as np
+    wq_d = torch.from_numpy(wq).to(dev)
+    sc_d = torch.from_numpy(sc.view(np.int16)).to(dev)
+    x_d = torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+    y_d = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
+    ws_n = q4lin.workspace_bytes(N, K, T)
+    ws_d = torch.empty(max(ws_n, 256), dtype=torch.uint8, device=dev)
+    route = q4lin.select_route(N, K, T)
+    launches = q4lin.kernel_launches(N, K, T)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    flush_sink = torch.empty((), dtype=torch.int64, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def do_flush(i):
+        flush.fill_(i & 0x7FFF)
+        torch.sum(flush, dtype=torch.int64, out=flush_sink)
+
+    def call():
+        q4lin.linear(wq_d, sc_d, x_d, y=y_d, workspace=ws_d if ws_n else None, stream=stream)
+
+    with torch.cuda.stream(stream):
+        call()
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            call()
+        torch.cuda.synchronize(dev)
+
+        if args.profile:
+            for i in range(args.warmup):
+                graph.replay()
+            do_flush(1)
+            torch.cuda.synchronize(dev)
+            torch.cuda.profiler.start()
+            call()
+            torch.cuda.synchronize(dev)
+            torch.cuda.profiler.stop()
+            return None
+
+        for i in range(args.warmup):
+            do_flush(i)
+            graph.replay()
+        torch.cuda.synchronize(dev)
+
+        cvd = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+        sampler = ClockSampler(cvd[local].strip() if local < len(cvd) else str(local))
+        sampler.start()
+        time.sleep(0.5)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        region0, region1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        sampler.mark_start()
+        region0.record(stream)
+        for i in range(args.steps):
+            do_flush(i)
+            ev[i][0].record(stream)
+            graph.replay()
+            ev[i][1].record(stream)
+        region1.record(stream)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        sampler.mark_stop()
+        clocks = sampler.stop()
+        us = sorted(a.elapsed_time(b) * 1e3 for a, b in ev)
+        region_ms = region0.elapsed_time(region1)
+
+        # end to end: host X (pinned) -> device, call, device Y -> host (pinned), per sample
+        e2e = None
+        if not args.no_e2e:
+            x_h = torch.from_numpy(x.view(np.int16)).pin_memory()
+            y_h = torch.empty((T, N), dtype=torch.int16).pin_memory()
+            n_e2e = min(args.steps, 2000)
+            ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_e2e)]
+            for i in range(args.warmup + n_e2e):
+                do_flush(i)
+                if i >= args.warmup:
+                    ee[i - args.warmup][0].record(stream)
+                x_d.view(torch.int16).copy_(x_h, non_blocking=True)
+                call()
+                y_h.copy_(y_d.view(torch.int16), non_blocking=True)
+                if i >= args.warmup:
+                    ee[i - args.warmup][1].record(stream)
+            torch.cuda.synchronize(dev)
+            e2e_us = sorted(a.elapsed_time(b) * 1e3 for a, b in ee)
+            e2e = dict(us=e2e_us, h2d=2 * K * T, d2h=2 * N * T)
+
+    return dict(us=us, region_ms=region_ms, clocks=clocks, route=q4lin.ROUTE_NAMES.get(route, str(route)),
+                launches=launches, e2e=e2e, ws_bytes=ws_n)
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) arms
+def oracle_rows_for_budget(wl, seconds_per_step):
+    """Rows of W per oracle sample so one sample costs about ``seconds_per_step``."""
+    N, K, T = wl["N"], wl["K"], wl["T"]
+    # decode + FP64 matmul, measured on this class of host at roughly 2e8 weight*token/s per call
+    per_row = K * (1.0 + T / 8.0) / 2.0e8
+    return int(max(1, min(N, seconds_per_step / max(per_row, 1e-12))))
+
+
+def time_oracle(wl, rows, reps_budget_s, max_reps, exact=False):
+    import numpy as np
+    import oracle
+
+    N, K, T = wl["N"], wl["K"], wl["T"]
+    wq = synth.packed_codes(rows, K, wl["w_seed"])   # the first `rows` rows of the same weight stream
+    sc = synth.group_scales(N, K, wl["w_seed"], wl["dist"])[:rows]
+    x = synth.activations(T, K, wl["x_seed"], wl["outliers"])
+    times = []
+    t_end = time.monotonic() + reps_budget_s
+    while len(times) < max_reps and (exact or len(times) < 3 or time.monotonic() < t_end):
+        t0 = time.perf_counter()
+        y = oracle.linear(wq, sc, x)
+        times.append(time.perf_counter() - t0)
+        assert y.shape == (T, rows) and np.isfinite(y).all()
+    return times
+
+
+def oracle_units(wl, rows):
+    K, T = wl["K"], wl["T"]
+    b = metrics.model_bytes(rows, K, T)
+    f = metrics.useful_flops(rows, K, T)
+    return b, f
+
+
+def blas_threads():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        v = os.environ.get(var)
+        if v and v.isdigit():
+            return int(v)
+    return os.cpu_count() or 1
+
+
+def cpu_baseline(wl):
+    rows = oracle_rows_for_budget(wl, 2.0)
+    times = time_oracle(wl, rows, 12.0, 30)
+    med = statistics.median(times)
+    b, f = oracle_units(wl, rows)
+    value = b / med / 1e9 if small_t(wl) else f / med / 1e12
+    return {"value": round(value, 4), "unit": "GB/s" if small_t(wl) else "TFLOP/s",
+            "cores": blas_threads(), "kind": "oracle",
+            "sample": f"FP64 oracle (numpy decode + BLAS matmul) on rows 0..{rows - 1} of the {wl['name']} weight "
+                      f"with all {wl['T']} tokens; median of {len(times)} runs; logical units of that sub-problem"}
+
+
+def reference_arm(args, wl, rank, world):
+    if rank != 0:
+        return 0
+    budget = 150.0
+    per_step = min(2.0, budget / (args.steps + args.warmup))
+    rows = oracle_rows_for_budget(wl, per_step)
+    times = time_oracle(wl, rows, 0.0, args.warmup + args.steps, exact=True)[args.warmup:]
+    med = statistics.median(times)
+    b, f = oracle_units(wl, rows)
+    small = small_t(wl)
+    value = b / med / 1e9 if small else f / med / 1e12
+    unit = "GB/s" if small else "TFLOP/s"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": unit,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(med * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl["name"], "N": wl["N"], "K": wl["K"], "T": wl["T"]},
+        "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": blas_threads(), "kind": "oracle",
+                         "sample": f"each step: FP64 oracle on rows 0..{rows - 1} of the weight, all {wl['T']} tokens"},
+        "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- main
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    wl = workload(args)
+    if args.impl == "reference":
+        return reference_arm(args, wl, rank, world)
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    res = measure_ours(args, wl, rank, world, local)
+    if res is None:
+        return 0
+    us = res["us"]
+    med, mean, mn, p95 = statistics.median(us), statistics.fmean(us), us[0], metrics.percentile(us, 95)
+    dev = torch.device("cuda", local)
+    med_max, mean_max, region_max = reduce_max([med, mean, res["region_ms"]], world, dev)
+    N, K, T = wl["N"], wl["K"], wl["T"]
+    mb, fl = metrics.model_bytes(N, K, T), metrics.useful_flops(N, K, T)
+    small = small_t(wl)
+    per_rank = mb / (med_max * 1e-6) / 1e9 if small else fl / (med_max * 1e-6) / 1e12
+    value = per_rank * world
+    peaks = load_peaks()
+    # roofline of the dominant kernel: algorithmic bytes (or FLOPs) per launch over its mean duration
+    per_launch_us = mean_max / max(1, res["launches"])
+    if small:
+        achieved = mb / max(1, res["launches"]) / (per_launch_us * 1e-6) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        achieved = fl / max(1, res["launches"]) / (per_launch_us * 1e-6) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["peak_source"] = peaks["source"]
+    traffic, tkernel = recorded_traffic(wl["name"])
+    roof["traffic"] = traffic
+    if tkernel:
+        roof["traffic_kernel"] = tkernel
+
+    e2e = None
+    if res["e2e"]:
+        e = res["e2e"]
+        emed = reduce_max([statistics.median(e["us"])], world, dev)[0]
+        ev = (mb / (emed * 1e-6) / 1e9 if small else fl / (emed * 1e-6) / 1e12) * world
+        e2e = {"value": round(ev, 3), "unit": "GB/s" if small else "TFLOP/s", "us": round(emed, 3),
+               "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]}
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "GB/s" if small else "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(med_max * 1e-3, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if res["route"] == "gemv" else "f16xf16->f32",
+        "data": "synthetic",
+        "config": {"workload": wl["name"], "N": N, "K": K, "T": T, "route": res["route"],
+                   "timing": "CUDA graph of one call per sample, events around the graph launch only",
+                   "l2": "flushed before every sample (256 MiB write then read)",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "us": {"median": round(med, 3), "min": round(mn, 3), "p95": round(p95, 3), "mean": round(mean, 3)},
+        "logical_gbs": round(mb / (med * 1e-6) / 1e9, 2),
+        "tflops": round(fl / (med * 1e-6) / 1e12, 3),
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": res["launches"] * args.steps,
+        "clocks": res["clocks"],
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

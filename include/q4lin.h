@@ -1,0 +1,124 @@
+/*
+ * q4lin -- weight-only 4-bit linear layer  Y[N,T] = W[N,K] . X[K,T]  on GB300.
+ *
+ * Operation (the problem statement of the Q4 linear measurement report,
+ * q4-linear.md, header table, and the linear-benchmark contract,
+ * linear-benchmark.md, "status and scope" and section 4):
+ *
+ *   y[t*N + n] = bf16( sum_k w[n,k] * x[t*K + k] ),  accumulated in FP32,
+ *   w[n,k]     = (q[n,k] - 8) * s[n, k/64],
+ *   q[n,2j]    = wq[n*(K/2) + j] & 0xF,   q[n,2j+1] = wq[n*(K/2) + j] >> 4.
+ *
+ * Weight format Q4_G64_FP16 "row-split" (linear-benchmark.md section 4,
+ * format table: 32 code bytes + 2 scale bytes per group of 64): two separate
+ * planes, codes [N, K/2] uint8 and scales [N, K/64] IEEE fp16, both
+ * row-major.  X and Y are bf16, row-major [T, K] and [T, N] -- the same bytes
+ * as the column-major X[K,T] / Y[N,T] views the report binds.
+ *
+ * Ownership: the caller owns every buffer.  The library never allocates or
+ * frees memory and keeps no state between calls except its error word.
+ * Inputs (wq, scales, x) are only read.  Exactly the N*T elements of y are
+ * written.  The workspace belongs to the call for its stream-ordered
+ * duration.
+ *
+ * Execution: every compute entry point is asynchronous on `stream` (a
+ * cudaStream_t passed as void*; NULL = the legacy default stream), performs
+ * no host synchronisation and no allocation, and may be captured into a CUDA
+ * graph.  Results are deterministic run to run (no floating-point atomics).
+ *
+ * Errors: status codes (q4lin_status); no exception crosses this boundary.
+ * Argument errors are detected on the host before anything is launched.
+ * Device-side bounded waits that expire set a sticky device error word,
+ * read with q4lin_device_status().
+ */
+#ifndef Q4LIN_H
+#define Q4LIN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  Q4LIN_OK = 0,
+  Q4LIN_ERR_INVALID_ARG = 1,       /* null pointer with nonzero size, negative size, size overflow */
+  Q4LIN_ERR_UNSUPPORTED_SHAPE = 2, /* K not a multiple of 128 */
+  Q4LIN_ERR_MISALIGNED = 3,        /* a device pointer not 16-byte aligned */
+  Q4LIN_ERR_WORKSPACE = 4,         /* workspace NULL while q4lin_workspace_bytes() > 0 */
+  Q4LIN_ERR_DEVICE = 5,            /* current device is not compute capability 10.x (sm_100 family) */
+  Q4LIN_ERR_CUDA = 6,              /* a CUDA runtime/driver call or a launch failed */
+  Q4LIN_ERR_TIMEOUT = 7            /* a device-side bounded wait expired (see q4lin_device_status) */
+} q4lin_status;
+
+/* Routes: which kernel organisation q4lin_linear uses for a shape. */
+typedef enum {
+  Q4LIN_ROUTE_AUTO = 0,     /* let the library choose (what q4lin_linear does) */
+  Q4LIN_ROUTE_GEMV = 1,     /* CUDA-core GEMV, weights decoded once per token block of <= 4 */
+  Q4LIN_ROUTE_TC_SPLITK = 2,/* tcgen05 tile, K split across a thread-block cluster (small T) */
+  Q4LIN_ROUTE_TC = 3        /* tcgen05 tile, whole K per CTA, TMEM accumulator (large T) */
+} q4lin_route;
+
+/*
+ * Bytes of device workspace q4lin_linear needs for (N, K, T); 0 means none
+ * (the workspace pointer may then be NULL).  The linear-benchmark contract
+ * (section 1.1) allocates workspace before timing through such a capacity
+ * query.  Returns 0 for invalid sizes (q4lin_linear reports the error).
+ * The value is a multiple of 256.
+ */
+size_t q4lin_workspace_bytes(int64_t N, int64_t K, int64_t T);
+
+/*
+ * Y = W . X (see the top of this file).
+ *   wq        device, uint8  [N, K/2]  packed codes, 16-byte aligned
+ *   scales    device, fp16   [N, K/64] bit patterns, 16-byte aligned
+ *   x         device, bf16   [T, K]    bit patterns, 16-byte aligned
+ *   y         device, bf16   [T, N]    bit patterns, 16-byte aligned (output)
+ *   N, T      >= 0; N == 0 or T == 0 is an empty problem: Q4LIN_OK, nothing launched
+ *   K         >= 0, multiple of 128 (K == 0 writes y = +0)
+ *   workspace device, >= q4lin_workspace_bytes(N, K, T) bytes, 256-byte aligned
+ *   stream    cudaStream_t as void*
+ * Returns Q4LIN_OK once the work is enqueued.
+ */
+int q4lin_linear(const uint8_t* wq, const uint16_t* scales, const uint16_t* x, uint16_t* y,
+                 int64_t N, int64_t K, int64_t T, void* workspace, void* stream);
+
+/*
+ * Diagnostic form of q4lin_linear that runs a given route instead of the
+ * library's choice (the same arguments; route Q4LIN_ROUTE_AUTO is
+ * q4lin_linear itself).  Tests use it to compare every route with the
+ * oracle on the same shapes; the benchmark never does.  Workspace
+ * requirement: q4lin_route_workspace_bytes(route, N, K, T).
+ */
+int q4lin_linear_route(int route, const uint8_t* wq, const uint16_t* scales, const uint16_t* x,
+                       uint16_t* y, int64_t N, int64_t K, int64_t T, void* workspace, void* stream);
+size_t q4lin_route_workspace_bytes(int route, int64_t N, int64_t K, int64_t T);
+
+/* The route q4lin_linear picks for (N, K, T) on the current device (host-only logic). */
+int q4lin_select_route(int64_t N, int64_t K, int64_t T);
+
+/* Number of kernel launches one q4lin_linear call issues for (N, K, T) (host-only logic; 0 for
+ * an empty problem or invalid sizes). */
+int q4lin_kernel_launches(int64_t N, int64_t K, int64_t T);
+
+/* Human-readable text of a q4lin_status (never NULL). */
+const char* q4lin_status_string(int status);
+
+/*
+ * Sticky device-side error word of the current device (0 = none; otherwise a
+ * q4lin_status, e.g. Q4LIN_ERR_TIMEOUT, set by a kernel whose bounded wait
+ * expired).  Synchronises the device to read it.  q4lin_clear_device_status
+ * resets it to 0.  Both return Q4LIN_ERR_CUDA (as the value) if the read fails.
+ */
+int q4lin_device_status(void);
+int q4lin_clear_device_status(void);
+
+/* Library version, "major.minor.patch". */
+const char* q4lin_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q4LIN_H */

@@ -8,7 +8,7 @@ __all__ = ["q4lin", "synth", "metrics"]
 
 
 def __getattr__(name):
-    if name == "q4lin":
-        from . import q4lin as mod
-        return mod
+    if name in __all__:
+        import importlib
+        return importlib.import_module(f"{__name__}.{name}")
     raise AttributeError(name)

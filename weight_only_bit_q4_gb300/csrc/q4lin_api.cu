@@ -1,0 +1,166 @@
+// C-ABI entry points of q4lin: argument checks, route selection, dispatch.
+//
+// The public call mirrors the linear-benchmark contract's operation
+// (linear-benchmark.md, "status and scope": linear(x, w, out, policy,
+// workspace, stream)) with a workspace capacity query (section 1.1) and a
+// format selector that rejects unsupported points (section 1.1) and returns
+// one host launcher per exact (N, K, T) (section 8.2).
+#include <cstdio>
+#include <cstring>
+
+#include "q4lin.h"
+#include "q4_internal.h"
+
+namespace {
+
+constexpr int64_t kMaxDim = (int64_t)1 << 40;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int validate_sizes(int64_t N, int64_t K, int64_t T) {
+  if (N < 0 || K < 0 || T < 0) return Q4LIN_ERR_INVALID_ARG;
+  if (N > kMaxDim || K > kMaxDim || T > kMaxDim) return Q4LIN_ERR_INVALID_ARG;
+  // every byte count derived from the sizes must stay far from int64 overflow
+  if ((double)N * (double)K > 9.0e17 || (double)T * (double)K > 9.0e17 ||
+      (double)N * (double)T > 9.0e17)
+    return Q4LIN_ERR_INVALID_ARG;
+  if (K % 128 != 0) return Q4LIN_ERR_UNSUPPORTED_SHAPE;
+  return Q4LIN_OK;
+}
+
+// Host-only argument validation; touches no CUDA API.
+int validate(const uint8_t* wq, const uint16_t* scales, const uint16_t* x, uint16_t* y,
+             int64_t N, int64_t K, int64_t T) {
+  const int st = validate_sizes(N, K, T);
+  if (st != Q4LIN_OK) return st;
+  if (N == 0 || T == 0) return Q4LIN_OK;
+  if (y == nullptr) return Q4LIN_ERR_INVALID_ARG;
+  if (!aligned16(y)) return Q4LIN_ERR_MISALIGNED;
+  if (K == 0) return Q4LIN_OK;
+  if (wq == nullptr || scales == nullptr || x == nullptr) return Q4LIN_ERR_INVALID_ARG;
+  if (!aligned16(wq) || !aligned16(scales) || !aligned16(x)) return Q4LIN_ERR_MISALIGNED;
+  return Q4LIN_OK;
+}
+
+int check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return Q4LIN_ERR_CUDA;
+  static int cached[128];   // 0 unknown, 1 ok, 2 not supported
+  if (dev >= 0 && dev < 128 && cached[dev] != 0) return cached[dev] == 1 ? Q4LIN_OK : Q4LIN_ERR_DEVICE;
+  int major = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+    return Q4LIN_ERR_CUDA;
+  const int ok = (major == 10) ? 1 : 2;
+  if (dev >= 0 && dev < 128) cached[dev] = ok;
+  return ok == 1 ? Q4LIN_OK : Q4LIN_ERR_DEVICE;
+}
+
+int route_for(int64_t N, int64_t K, int64_t T) {
+  (void)N;
+  (void)K;
+  (void)T;
+  return Q4LIN_ROUTE_GEMV;
+}
+
+size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+size_t route_ws(int route, int64_t N, int64_t K, int64_t T) {
+  switch (route) {
+    case Q4LIN_ROUTE_GEMV: return round256(q4::gemv_workspace_bytes(N, K, T));
+    default: return 0;
+  }
+}
+
+int run(int route, const uint8_t* wq, const uint16_t* scales, const uint16_t* x, uint16_t* y,
+        int64_t N, int64_t K, int64_t T, void* workspace, void* stream) {
+  int st = validate(wq, scales, x, y, N, K, T);
+  if (st != Q4LIN_OK) return st;
+  if (N == 0 || T == 0) return Q4LIN_OK;
+  if (route == Q4LIN_ROUTE_AUTO) route = route_for(N, K, T);
+  if (route < Q4LIN_ROUTE_GEMV || route > Q4LIN_ROUTE_TC) return Q4LIN_ERR_INVALID_ARG;
+  const size_t ws = route_ws(route, N, K, T);
+  if (ws > 0 && workspace == nullptr) return Q4LIN_ERR_WORKSPACE;
+  if (ws > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return Q4LIN_ERR_MISALIGNED;
+  st = check_device();
+  if (st != Q4LIN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K == 0) {
+    return cudaMemsetAsync(y, 0, (size_t)N * (size_t)T * 2, s) == cudaSuccess ? Q4LIN_OK : Q4LIN_ERR_CUDA;
+  }
+  q4::LinearArgs a{wq, scales, x, y, N, K, T, workspace, s};
+  switch (route) {
+    case Q4LIN_ROUTE_GEMV: return q4::gemv_launch(a);
+    default: return Q4LIN_ERR_INVALID_ARG;
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t q4lin_workspace_bytes(int64_t N, int64_t K, int64_t T) {
+  if (validate_sizes(N, K, T) != Q4LIN_OK || N == 0 || K == 0 || T == 0) return 0;
+  return route_ws(route_for(N, K, T), N, K, T);
+}
+
+size_t q4lin_route_workspace_bytes(int route, int64_t N, int64_t K, int64_t T) {
+  if (validate_sizes(N, K, T) != Q4LIN_OK || N == 0 || K == 0 || T == 0) return 0;
+  if (route == Q4LIN_ROUTE_AUTO) route = route_for(N, K, T);
+  return route_ws(route, N, K, T);
+}
+
+int q4lin_select_route(int64_t N, int64_t K, int64_t T) { return route_for(N, K, T); }
+
+int q4lin_kernel_launches(int64_t N, int64_t K, int64_t T) {
+  if (validate_sizes(N, K, T) != Q4LIN_OK || N == 0 || T == 0) return 0;
+  if (K == 0) return 1;  // the zero fill
+  switch (route_for(N, K, T)) {
+    case Q4LIN_ROUTE_GEMV: return q4::gemv_launch_count(N, K, T);
+    default: return 0;
+  }
+}
+
+int q4lin_linear(const uint8_t* wq, const uint16_t* scales, const uint16_t* x, uint16_t* y,
+                 int64_t N, int64_t K, int64_t T, void* workspace, void* stream) {
+  return run(Q4LIN_ROUTE_AUTO, wq, scales, x, y, N, K, T, workspace, stream);
+}
+
+int q4lin_linear_route(int route, const uint8_t* wq, const uint16_t* scales, const uint16_t* x,
+                       uint16_t* y, int64_t N, int64_t K, int64_t T, void* workspace, void* stream) {
+  return run(route, wq, scales, x, y, N, K, T, workspace, stream);
+}
+
+const char* q4lin_status_string(int status) {
+  switch (status) {
+    case Q4LIN_OK: return "ok";
+    case Q4LIN_ERR_INVALID_ARG: return "invalid argument (null pointer, negative or overflowing size)";
+    case Q4LIN_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (K must be a multiple of 128)";
+    case Q4LIN_ERR_MISALIGNED: return "misaligned pointer (16-byte buffers, 256-byte workspace)";
+    case Q4LIN_ERR_WORKSPACE: return "workspace required but NULL";
+    case Q4LIN_ERR_DEVICE: return "unsupported device (needs compute capability 10.x)";
+    case Q4LIN_ERR_CUDA: return "CUDA error";
+    case Q4LIN_ERR_TIMEOUT: return "device-side bounded wait expired";
+    default: return "unknown status";
+  }
+}
+
+static int read_status(bool clear) {
+  int worst = 0, v = 0;
+  if (q4::gemv_status(&v, clear) != Q4LIN_OK) return Q4LIN_ERR_CUDA;
+  if (v) worst = v;
+  return worst;
+}
+
+int q4lin_device_status(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return Q4LIN_ERR_CUDA;
+  return read_status(false);
+}
+
+int q4lin_clear_device_status(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return Q4LIN_ERR_CUDA;
+  return read_status(true) == Q4LIN_ERR_CUDA ? Q4LIN_ERR_CUDA : Q4LIN_OK;
+}
+
+const char* q4lin_version(void) { return "0.1.0"; }
+
+}  // extern "C"

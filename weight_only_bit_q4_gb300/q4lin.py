@@ -1,0 +1,153 @@
+"""ctypes binding of libq4lin.so (argument marshalling only).
+
+Every step of the layer runs in the library's CUDA kernels; this module only
+turns torch tensors into pointers and sizes and raises on a nonzero status.
+If the library has not been built it raises: there is no other path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libq4lin.so")
+
+OK = 0
+STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED_SHAPE", 3: "MISALIGNED", 4: "WORKSPACE",
+          5: "DEVICE", 6: "CUDA", 7: "TIMEOUT"}
+ROUTE_AUTO, ROUTE_GEMV, ROUTE_TC_SPLITK, ROUTE_TC = 0, 1, 2, 3
+ROUTE_NAMES = {ROUTE_AUTO: "auto", ROUTE_GEMV: "gemv", ROUTE_TC_SPLITK: "tc_splitk", ROUTE_TC: "tc"}
+
+EXPORTS = ("q4lin_workspace_bytes", "q4lin_linear", "q4lin_linear_route",
+           "q4lin_route_workspace_bytes", "q4lin_select_route", "q4lin_kernel_launches",
+           "q4lin_status_string",
+           "q4lin_device_status", "q4lin_clear_device_status", "q4lin_version")
+
+_lib = None
+
+
+class Q4LinError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"q4lin: {what}{STATUS.get(status, status)}: {status_string(status)}")
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load the library (once).  Raises if it is missing: build it first."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} not found: build it with `python -m weight_only_bit_q4_gb300.build`")
+    lib = ctypes.CDLL(p)
+    i64, sz, vp = ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p
+    lib.q4lin_workspace_bytes.argtypes = [i64, i64, i64]
+    lib.q4lin_workspace_bytes.restype = sz
+    lib.q4lin_route_workspace_bytes.argtypes = [ctypes.c_int, i64, i64, i64]
+    lib.q4lin_route_workspace_bytes.restype = sz
+    lib.q4lin_linear.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp]
+    lib.q4lin_linear.restype = ctypes.c_int
+    lib.q4lin_linear_route.argtypes = [ctypes.c_int, vp, vp, vp, vp, i64, i64, i64, vp, vp]
+    lib.q4lin_linear_route.restype = ctypes.c_int
+    lib.q4lin_select_route.argtypes = [i64, i64, i64]
+    lib.q4lin_select_route.restype = ctypes.c_int
+    lib.q4lin_kernel_launches.argtypes = [i64, i64, i64]
+    lib.q4lin_kernel_launches.restype = ctypes.c_int
+    lib.q4lin_status_string.argtypes = [ctypes.c_int]
+    lib.q4lin_status_string.restype = ctypes.c_char_p
+    lib.q4lin_device_status.argtypes = []
+    lib.q4lin_device_status.restype = ctypes.c_int
+    lib.q4lin_clear_device_status.argtypes = []
+    lib.q4lin_clear_device_status.restype = ctypes.c_int
+    lib.q4lin_version.argtypes = []
+    lib.q4lin_version.restype = ctypes.c_char_p
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().q4lin_status_string(int(status)).decode()
+
+
+def version() -> str:
+    return load().q4lin_version().decode()
+
+
+def workspace_bytes(N: int, K: int, T: int, route: int = ROUTE_AUTO) -> int:
+    if route == ROUTE_AUTO:
+        return int(load().q4lin_workspace_bytes(N, K, T))
+    return int(load().q4lin_route_workspace_bytes(route, N, K, T))
+
+
+def select_route(N: int, K: int, T: int) -> int:
+    return int(load().q4lin_select_route(N, K, T))
+
+
+def kernel_launches(N: int, K: int, T: int) -> int:
+    return int(load().q4lin_kernel_launches(N, K, T))
+
+
+_IMPLEMENTED = (ROUTE_GEMV,)
+
+
+def implemented_routes():
+    """Routes the library can run (the others return INVALID_ARG)."""
+    return _IMPLEMENTED
+
+
+def device_status() -> int:
+    return int(load().q4lin_device_status())
+
+
+def clear_device_status() -> int:
+    return int(load().q4lin_clear_device_status())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def linear_raw(wq_ptr, scales_ptr, x_ptr, y_ptr, N, K, T, ws_ptr=None, stream=None,
+               route: int = ROUTE_AUTO) -> int:
+    """Pointer-level call; returns the status code (no exception)."""
+    lib = load()
+    if route == ROUTE_AUTO:
+        return int(lib.q4lin_linear(wq_ptr, scales_ptr, x_ptr, y_ptr, N, K, T, ws_ptr, stream))
+    return int(lib.q4lin_linear_route(route, wq_ptr, scales_ptr, x_ptr, y_ptr, N, K, T, ws_ptr, stream))
+
+
+def linear(wq, scales, x, y=None, workspace=None, stream=None, route: int = ROUTE_AUTO):
+    """Y[T, N] (bf16) = dequant(wq, scales) applied to X[T, K] (bf16) on the GPU.
+
+    wq: uint8 [N, K/2]; scales: fp16 (or int16/uint16 bit patterns) [N, K/64];
+    x: bf16 [T, K]; all CUDA, contiguous.  ``y`` (bf16 [T, N]) and
+    ``workspace`` (uint8, >= workspace_bytes) are allocated here with torch if
+    not given.  Runs on ``stream`` (a torch.cuda.Stream) or the current stream.
+    """
+    import torch
+
+    N, half = wq.shape
+    K = 2 * half
+    T = x.shape[0]
+    if x.shape[1] != K or scales.shape != (N, K // 64):
+        raise ValueError(f"shape mismatch: wq {tuple(wq.shape)} scales {tuple(scales.shape)} x {tuple(x.shape)}")
+    for name, t in (("wq", wq), ("scales", scales), ("x", x)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if wq.dtype != torch.uint8 or x.dtype != torch.bfloat16 or scales.element_size() != 2:
+        raise ValueError("dtypes: wq uint8, scales fp16 bits, x bf16")
+    if y is None:
+        y = torch.empty((T, N), dtype=torch.bfloat16, device=x.device)
+    elif y.shape != (T, N) or y.dtype != torch.bfloat16 or not y.is_contiguous():
+        raise ValueError("y must be a contiguous bf16 [T, N] tensor")
+    need = workspace_bytes(N, K, T, route)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    s = (stream or torch.cuda.current_stream(x.device)).cuda_stream
+    st = linear_raw(_ptr(wq), _ptr(scales), _ptr(x), _ptr(y), N, K, T,
+                    _ptr(workspace) if need else None, ctypes.c_void_p(s), route)
+    if st != OK:
+        raise Q4LinError(st)
+    return y
