@@ -232,12 +232,12 @@ def measure_ours(args, wl, rank, world, local):
     route = q4lin.select_route(N, K, T)
     launches = q4lin.kernel_launches(N, K, T)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-    flush_sink = torch.empty((), dtype=torch.int64, device=dev)
+    flush_sink = torch.empty((), dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(dev)
 
     def do_flush(i):
         flush.fill_(i & 0x7FFF)
-        torch.sum(flush, dtype=torch.int64, out=flush_sink)
+        torch.sum(flush, dim=0, out=flush_sink)
 
     def call():
         q4lin.linear(wq_d, sc_d, x_d, y=y_d, workspace=ws_d if ws_n else None, stream=stream)

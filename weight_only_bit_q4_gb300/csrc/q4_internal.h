@@ -21,7 +21,15 @@ int gemv_launch(const LinearArgs& a);
 size_t gemv_workspace_bytes(int64_t N, int64_t K, int64_t T);
 int gemv_launch_count(int64_t N, int64_t K, int64_t T);
 
+// tcgen05 tile route: X converted to fp16 in the workspace, then one CTA per
+// 128-row x BN-token output tile with the accumulator in tensor memory.
+int tc_launch(const LinearArgs& a);
+size_t tc_workspace_bytes(int64_t N, int64_t K, int64_t T);
+int tc_launch_count(int64_t N, int64_t K, int64_t T);
+bool tc_supported(int64_t N, int64_t K, int64_t T);
+
 // Reads (and optionally clears) the device error word of one translation unit.
 int gemv_status(int* value, bool clear);
+int tc_status(int* value, bool clear);
 
 }  // namespace q4

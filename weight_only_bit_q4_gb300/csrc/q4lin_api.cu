@@ -56,10 +56,8 @@ int check_device() {
 }
 
 int route_for(int64_t N, int64_t K, int64_t T) {
-  (void)N;
-  (void)K;
-  (void)T;
-  return Q4LIN_ROUTE_GEMV;
+  if (T <= 4 || !q4::tc_supported(N, K, T)) return Q4LIN_ROUTE_GEMV;
+  return Q4LIN_ROUTE_TC;
 }
 
 size_t round256(size_t b) { return (b + 255) / 256 * 256; }
@@ -67,6 +65,7 @@ size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 size_t route_ws(int route, int64_t N, int64_t K, int64_t T) {
   switch (route) {
     case Q4LIN_ROUTE_GEMV: return round256(q4::gemv_workspace_bytes(N, K, T));
+    case Q4LIN_ROUTE_TC: return round256(q4::tc_workspace_bytes(N, K, T));
     default: return 0;
   }
 }
@@ -90,6 +89,7 @@ int run(int route, const uint8_t* wq, const uint16_t* scales, const uint16_t* x,
   q4::LinearArgs a{wq, scales, x, y, N, K, T, workspace, s};
   switch (route) {
     case Q4LIN_ROUTE_GEMV: return q4::gemv_launch(a);
+    case Q4LIN_ROUTE_TC: return q4::tc_launch(a);
     default: return Q4LIN_ERR_INVALID_ARG;
   }
 }
@@ -116,6 +116,7 @@ int q4lin_kernel_launches(int64_t N, int64_t K, int64_t T) {
   if (K == 0) return 1;  // the zero fill
   switch (route_for(N, K, T)) {
     case Q4LIN_ROUTE_GEMV: return q4::gemv_launch_count(N, K, T);
+    case Q4LIN_ROUTE_TC: return q4::tc_launch_count(N, K, T);
     default: return 0;
   }
 }
@@ -147,6 +148,8 @@ const char* q4lin_status_string(int status) {
 static int read_status(bool clear) {
   int worst = 0, v = 0;
   if (q4::gemv_status(&v, clear) != Q4LIN_OK) return Q4LIN_ERR_CUDA;
+  if (v) worst = v;
+  if (q4::tc_status(&v, clear) != Q4LIN_OK) return Q4LIN_ERR_CUDA;
   if (v) worst = v;
   return worst;
 }

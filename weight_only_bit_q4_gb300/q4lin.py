@@ -89,7 +89,7 @@ def kernel_launches(N: int, K: int, T: int) -> int:
     return int(load().q4lin_kernel_launches(N, K, T))
 
 
-_IMPLEMENTED = (ROUTE_GEMV,)
+_IMPLEMENTED = (ROUTE_GEMV, ROUTE_TC)
 
 
 def implemented_routes():
