@@ -114,6 +114,11 @@ const char* q4lin_status_string(int status);
 int q4lin_device_status(void);
 int q4lin_clear_device_status(void);
 
+/* Text describing the last error a q4lin call returned on this host thread (which call failed
+ * and the CUDA error text, if any); "" if the last call succeeded.  Owned by the library, valid
+ * until the next q4lin call on the same thread. */
+const char* q4lin_last_error_detail(void);
+
 /* Library version, "major.minor.patch". */
 const char* q4lin_version(void);
 

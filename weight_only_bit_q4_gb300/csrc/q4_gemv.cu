@@ -142,7 +142,7 @@ int gemv_launch(const LinearArgs& a) {
       case 3: q4_gemv_kernel<3><<<(unsigned)grid, kWarps * 32, 0, a.stream>>>(a.wq, a.scales, a.x, a.y, a.N, a.K, t0); break;
       default: q4_gemv_kernel<4><<<(unsigned)grid, kWarps * 32, 0, a.stream>>>(a.wq, a.scales, a.x, a.y, a.N, a.K, t0); break;
     }
-    if (cudaGetLastError() != cudaSuccess) return Q4LIN_ERR_CUDA;
+    if (cuda_check(cudaGetLastError(), "gemv: kernel launch")) return Q4LIN_ERR_CUDA;
   }
   return Q4LIN_OK;
 }

@@ -6,6 +6,11 @@
 
 namespace q4 {
 
+// Records why a call failed (thread-local; read by q4lin_last_error_detail)
+// and returns Q4LIN_ERR_CUDA when `e` is an error, Q4LIN_OK otherwise.
+int cuda_check(cudaError_t e, const char* where);
+void set_error_detail(const char* what);
+
 struct LinearArgs {
   const uint8_t* wq;
   const uint16_t* scales;
@@ -21,9 +26,14 @@ int gemv_launch(const LinearArgs& a);
 size_t gemv_workspace_bytes(int64_t N, int64_t K, int64_t T);
 int gemv_launch_count(int64_t N, int64_t K, int64_t T);
 
-// tcgen05 tile route: X converted to fp16 in the workspace, then one CTA per
-// 128-row x BN-token output tile with the accumulator in tensor memory.
-int tc_launch(const LinearArgs& a);
+// tcgen05 tile routes: one CTA per 128-row x BN-token output tile (per K
+// share when split across a cluster), group partials in tensor memory.
+struct TcPlan {
+  int bn;      // token tile (MMA N)
+  int splitk;  // cluster size along K
+};
+TcPlan tc_plan(int route, int64_t N, int64_t K, int64_t T, int sms);
+int tc_launch(const LinearArgs& a, int route);
 size_t tc_workspace_bytes(int64_t N, int64_t K, int64_t T);
 int tc_launch_count(int64_t N, int64_t K, int64_t T);
 bool tc_supported(int64_t N, int64_t K, int64_t T);

@@ -1,39 +1,37 @@
 // Tensor-core route of the Q4_G64_FP16 linear layer: TMA -> on-chip decode ->
-// tcgen05.mma (kind::f16) with the FP32 accumulator in tensor memory.
+// tcgen05.mma (kind::f16, bf16 operands) with per-group accumulators in tensor
+// memory and the group scales applied in FP32.
 //
 // This is the tiled-MMA route of the Q4 linear measurement report
 // (q4-linear.md, route notes: BF16 input, FP32-accumulating dense MMA for the
-// larger token counts), re-designed for sm_103a:
+// larger token counts), re-designed for sm_103a.  One CTA computes a 128-row
+// x BN-token output tile (with split-K, one K share of it; the shares of a
+// tile form a thread-block cluster and are summed through distributed shared
+// memory):
 //
-//   * one CTA computes a 128-row x BN-token tile D[n, t] = sum_k W[n,k] X[t,k]
-//     (the MMA's M is the weight row, its N the token); D lives in TMEM;
-//   * warp 0 streams the packed code plane (TMA, 128-B swizzle, 4 groups per
-//     stage) and the token tile of X (TMA, 128-B swizzle, one group per stage);
-//   * warps 2..9 decode one 64-wide group per step: codes -> fp16
-//     (q - 8) * s written into the MMA's 128-B-swizzled K-major A layout;
-//   * one thread of warp 1 issues 4 x tcgen05.mma (K = 16) per group and
-//     commits each stage back to the producers;
-//   * warps 2..9 then read D from TMEM, round to bf16 and store Y[t, n].
+//   * two TMA producer threads stream the packed code plane (128-byte swizzle,
+//     4 groups per stage) and the bf16 token tile of X straight from the
+//     caller's buffer (128-byte swizzle, one 64-wide group per stage);
+//   * a decode warpgroup turns each group's codes into the exact bf16 values
+//     q - 8, written in the MMA's 128-byte-swizzled K-major A layout;
+//   * one thread issues 4 x tcgen05.mma (K = 16) per group into one of two
+//     TMEM buffers, D_g[n, t] = sum_{k in g} (q[n,k] - 8) x[t,k];
+//   * two accumulate warpgroups read D_g back (tcgen05.ld) and add
+//     s[n,g] * D_g[n,t] to FP32 registers, then round to bf16 and store Y[t, n].
 //
-// Operand precision: the MMA runs on fp16 operands.  A bf16 rounding of the
-// dequantised weight (q - 8) * s needs ~14 significant bits and misses the
-// layer's 1e-3 rms accuracy bound on a few percent of outputs, while fp16's
-// 11-bit rounding stays well inside it; X is converted bf16 -> fp16, exact in
-// fp16's normal range.  A kind::f16 MMA takes A and B of one type, so X is
-// converted first (q4_x_to_f16 below), and its K order inside every 8-element
-// block is permuted to [0,2,4,6,1,3,5,7] -- the order in which the decoder
-// produces weights from one 32-bit code word with four byte-permutes.  The
-// contraction is invariant under a common permutation of K.
+// Every product (q - 8) * x is exact in FP32 and the group scale multiplies
+// an FP32 partial sum, so the only rounding is FP32 accumulation and the final
+// bf16 store.  (Folding the scale into a 16-bit weight instead rounds
+// (q - 8) * s to 11 bits -- about 2e-4 of rms(y) -- which brushes the layer's
+// 1e-3 rms accuracy floor on large outputs; bf16 folding misses it outright.)
 //
 // Every mbarrier wait is bounded: on expiry the kernel records
 // Q4LIN_ERR_TIMEOUT in its device error word, drains what it issued (again
 // bounded) and exits instead of hanging.
-#include <cuda.h>
-
 #include <mutex>
 
-#include "q4_common.cuh"
 #include "q4_internal.h"
+#include "q4_sm100.cuh"
 
 namespace q4 {
 
@@ -41,209 +39,46 @@ namespace {
 
 __device__ int g_tc_status = 0;
 
-// ----------------------------------------------------------------- PTX wrappers
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait for the phase of `parity` to complete.  Returns false if the
-// CTA is aborting (another thread timed out) or this wait itself timed out.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-  }
-  *abort_flag = 1;
-  atomicExch(&g_tc_status, (int)Q4LIN_ERR_TIMEOUT);
-  return false;
-}
-
-// Drain wait used after an abort: bounded, ignores the abort flag.
-__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i)
-    if (mbar_try_wait(bar, parity)) return;
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t c0,
-                                            int32_t c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
-      : "memory");
-}
-
-__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
-// D[tmem] (+)= A[smem] . B[smem]^T, both K-major, fp16 in, fp32 accumulate.
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                        uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrive on `bar` once all tcgen05 operations this thread issued so far complete.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
-
-// 16 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// Shared-memory matrix descriptor (tcgen05 format): K-major operand whose rows
-// are 128-byte lines in the 128-byte swizzle, 8-row groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);  // start address
-  d |= (uint64_t)1 << 16;                             // leading byte offset (unused here)
-  d |= (uint64_t)(1024 >> 4) << 32;                   // stride byte offset: 8 rows x 128 B
-  d |= (uint64_t)1 << 46;                             // descriptor version
-  d |= (uint64_t)2 << 61;                             // 128-byte swizzle
-  return d;
-}
-
-// Instruction descriptor, kind::f16: D f32, A f16, B f16, both K-major, M x N.
-constexpr uint32_t idesc_f16(int M, int N) {
-  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
-
-// One 32-bit code word (8 weights, byte j = q[2j] | q[2j+1] << 4) -> 8 fp16
-// (q - 8) * s in the order [q0,q2,q4,q6,q1,q3,q5,q7]: bytes {q, 0x64} form the
-// exact half 1024 + q, minus 1032 gives q - 8 exactly, times s rounds once.
-__device__ __forceinline__ uint4 decode_word_f16(uint32_t w, __half2 s2) {
-  const uint32_t lo = w & 0x0F0F0F0Fu;
-  const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;
-  const uint32_t m = 0x64646464u;
-  const __half2 bias = __half2half2(__ushort_as_half(0x6408));  // 1032
-  uint32_t h[4] = {__byte_perm(lo, m, 0x4140), __byte_perm(lo, m, 0x4342), __byte_perm(hi, m, 0x4140),
-                   __byte_perm(hi, m, 0x4342)};
-  uint4 out;
-  uint32_t* o = reinterpret_cast<uint32_t*>(&out);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    __half2 v = __hsub2(*reinterpret_cast<__half2*>(&h[i]), bias);
-    v = __hmul2(v, s2);
-    o[i] = *reinterpret_cast<uint32_t*>(&v);
-  }
-  return out;
-}
-
-// ----------------------------------------------------------------- X pre-pass
-// bf16 [T, K] -> fp16 [T, K] with each 8-element block reordered to [0,2,4,6,1,3,5,7].
-__global__ void __launch_bounds__(256) q4_x_to_f16(const uint16_t* __restrict__ x, uint16_t* __restrict__ xh,
-                                                   int64_t n8) {
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
-    const uint4 v = ld_stream_u4(x + i * 8);
-    const __half2 a = __floats2half2_rn(bf16lo(v.x), bf16lo(v.y));
-    const __half2 b = __floats2half2_rn(bf16lo(v.z), bf16lo(v.w));
-    const __half2 c = __floats2half2_rn(bf16hi(v.x), bf16hi(v.y));
-    const __half2 d = __floats2half2_rn(bf16hi(v.z), bf16hi(v.w));
-    uint4 o;
-    o.x = *reinterpret_cast<const uint32_t*>(&a);
-    o.y = *reinterpret_cast<const uint32_t*>(&b);
-    o.z = *reinterpret_cast<const uint32_t*>(&c);
-    o.w = *reinterpret_cast<const uint32_t*>(&d);
-    *reinterpret_cast<uint4*>(xh + i * 8) = o;
-  }
-}
-
-// ----------------------------------------------------------------- the tile kernel
 struct TcParams {
   const uint16_t* scales;
   uint16_t* y;
   int64_t N, K, T;
-  int nk;  // groups (K-steps of 64)
+  int nk;      // groups (K-steps of 64)
+  int splitk;  // CTAs of a cluster sharing one output tile along K (1 = no split)
 };
 
-constexpr int kThreads = 320;        // warp 0 TMA, warp 1 MMA/TMEM, warps 2..9 decode + epilogue
-constexpr int kDqThreads = 256;
+// Warpgroup roles (setmaxnreg works per warpgroup):
+//   wg0: warp 0 TMA producer (X), warp 1 TMEM owner + MMA issuer,
+//        warp 2 TMA producer (code plane), warp 3 idle
+//   wg1: decode (one thread per tile row, one whole 64-wide group per step)
+//   wg2, wg3: FP32 accumulation of scaled group partials + epilogue
+//             (one thread per row and column half; warp % 4 = TMEM lane quadrant)
+constexpr int kThreads = 512;
 constexpr int kTileM = 128;
-constexpr int kGroupsPerW = 4;       // code stage: 128 rows x 128 bytes = 4 groups
-constexpr uint32_t kABytes = kTileM * 128;   // one group of decoded A: 128 rows x 64 fp16
+constexpr int kGroupsPerW = 4;               // code stage: 128 rows x 128 bytes = 4 groups
+constexpr uint32_t kABytes = kTileM * 128;   // one group of A: 128 rows x 64 bf16
 constexpr uint32_t kWBytes = kTileM * 128;   // one code stage
+constexpr int kRegsLow = 64;                 // wg0, wg1 after the split
+constexpr int kRegsHigh = 192;               // wg2, wg3 after the split
+static_assert((2 * kRegsLow + 2 * kRegsHigh) * 128 <= 65536, "register split exceeds the launch budget");
+static_assert((2 * kRegsLow + 2 * kRegsHigh) * 128 == (65536 / kThreads) * kThreads,
+              "register split must equal the launch allocation");
 
 template <int BN, int S, int SW>
 struct TcSmem {
-  static constexpr uint32_t kB = BN * 128;  // one group of X: BN rows x 64 fp16
+  static constexpr uint32_t kB = BN * 128;  // one group of X: BN rows x 64 bf16
   static constexpr uint32_t a_off = 0;
   static constexpr uint32_t b_off = a_off + S * kABytes;
   static constexpr uint32_t w_off = b_off + S * kB;
   static constexpr uint32_t bar_off = w_off + SW * kWBytes;
-  // barriers: full_a[S], full_b[S], empty[S], w_full[SW], w_empty[SW], acc_full
-  static constexpr uint32_t n_bars = 3 * S + 2 * SW + 1;
+  // full_a[S], full_b[S], empty[S], w_full[SW], w_empty[SW], mma_done[2], tmem_free[2]
+  static constexpr uint32_t n_bars = 3 * S + 2 * SW + 4;
   static constexpr uint32_t misc_off = bar_off + n_bars * 8;
   static constexpr uint32_t bytes = misc_off + 16;
   static constexpr uint32_t alloc = bytes + 1024;  // slack for 1024-byte alignment
-  static constexpr uint32_t tmem_cols = BN < 32 ? 32 : BN;
+  static constexpr uint32_t tmem_cols = 2 * BN < 32 ? 32 : 2 * BN;
+  // split-K partial sums of the other CTAs of the cluster reuse the pipeline buffers
+  static constexpr int max_splitk = 1 + (int)(bar_off / (kTileM * BN * 4));
 };
 
 template <int BN, int S, int SW>
@@ -251,6 +86,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_x,
              const TcParams p) {
   using L = TcSmem<BN, S, SW>;
+  constexpr int kCols = BN / 2;  // accumulator columns per accumulate thread
+  constexpr int kChunk = kCols >= 128 ? 16 : (kCols >= 32 ? 32 : kCols);  // TMEM columns per load
+  static_assert(kCols % 8 == 0 && kCols % kChunk == 0, "BN must be a multiple of 16");
+
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -260,27 +99,42 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
   auto empty = [&](int s) { return bars + 8u * (2 * S + s); };
   auto w_full = [&](int s) { return bars + 8u * (3 * S + s); };
   auto w_empty = [&](int s) { return bars + 8u * (3 * S + SW + s); };
-  const uint32_t acc_full = bars + 8u * (3 * S + 2 * SW);
+  auto mma_done = [&](int b) { return bars + 8u * (3 * S + 2 * SW + b); };
+  auto tmem_free = [&](int b) { return bars + 8u * (3 * S + 2 * SW + 2 + b); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int wg = warp >> 2;
   const int64_t m0 = (int64_t)blockIdx.x * kTileM;
   const int64_t t0 = (int64_t)blockIdx.y * BN;
-  const int nk = p.nk;
+
+  // This CTA's share of the K groups (the whole K without a split).
+  const int splitk = p.splitk;
+  uint32_t crank = 0;
+  int g_begin = 0, g_end = p.nk;
+  if (splitk > 1) {
+    crank = cluster_ctarank();
+    g_begin = (int)(((int64_t)p.nk * crank) / splitk);
+    g_end = (int)(((int64_t)p.nk * (crank + 1)) / splitk);
+  }
+  const int ng = g_end - g_begin;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full_a(s), kDqThreads / 32);
+      mbar_init(full_a(s), 4);   // the 4 decode warps
       mbar_init(full_b(s), 1);
       mbar_init(empty(s), 1);
     }
     for (int s = 0; s < SW; ++s) {
       mbar_init(w_full(s), 1);
-      mbar_init(w_empty(s), kDqThreads / 32);
+      mbar_init(w_empty(s), 4);
     }
-    mbar_init(acc_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(mma_done(b), 1);
+      mbar_init(tmem_free(b), 8);  // the 8 accumulate warps
+    }
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_codes);
@@ -290,126 +144,184 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem_d = *tmem_slot;
+  const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------- TMA producer
-    if (lane == 0) {
-      int last_w = -1, last_b = -1;
+  if (wg == 0) {
+    setmaxnreg_dec<kRegsLow>();
+    if (warp == 0 && lane == 0) {
+      // ----------------------------------------------------------- TMA producer: token tiles of X
+      int last_b = -1;
       bool ok = true;
-      for (int ks = 0; ks < nk && ok; ++ks) {
-        if (ks % kGroupsPerW == 0) {
-          const int ws = ks / kGroupsPerW, slot = ws % SW;
-          ok = mbar_wait(w_empty(slot), ((ws / SW) & 1) ^ 1, abort_flag);
-          if (!ok) break;
-          mbar_expect_tx(w_full(slot), kWBytes);
-          tma_load_2d(sbase + L::w_off + slot * kWBytes, &tm_codes, w_full(slot), ws * 128, (int32_t)m0);
-          last_w = ws;
-        }
-        const int s = ks % S;
-        ok = mbar_wait(empty(s), ((ks / S) & 1) ^ 1, abort_flag);
-        if (!ok) break;
+      for (int i = 0; i < ng; ++i) {
+        const int s = i % S;
+        if (!(ok = mbar_wait(empty(s), ((i / S) & 1) ^ 1, abort_flag, &g_tc_status))) break;
         mbar_expect_tx(full_b(s), L::kB);
-        tma_load_2d(sbase + L::b_off + s * L::kB, &tm_x, full_b(s), ks * 64, (int32_t)t0);
-        last_b = ks;
+        tma_load_2d(sbase + L::b_off + s * L::kB, &tm_x, full_b(s), (g_begin + i) * 64, (int32_t)t0);
+        last_b = i;
       }
-      if (!ok) {
-        // let every copy already issued land before the CTA's shared memory goes away
+      if (!ok)  // let every copy already issued land before shared memory is released
+        for (int i = (last_b - S + 1 > 0 ? last_b - S + 1 : 0); i <= last_b; ++i)
+          mbar_drain(full_b(i % S), (i / S) & 1);
+    } else if (warp == 2 && lane == 0) {
+      // ----------------------------------------------------------- TMA producer: code plane stages
+      const int nws = (ng + kGroupsPerW - 1) / kGroupsPerW;
+      int last_w = -1;
+      bool ok = true;
+      for (int ws = 0; ws < nws; ++ws) {
+        const int slot = ws % SW;
+        if (!(ok = mbar_wait(w_empty(slot), ((ws / SW) & 1) ^ 1, abort_flag, &g_tc_status))) break;
+        mbar_expect_tx(w_full(slot), kWBytes);
+        tma_load_2d(sbase + L::w_off + slot * kWBytes, &tm_codes, w_full(slot), (g_begin + ws * kGroupsPerW) * 32,
+                    (int32_t)m0);
+        last_w = ws;
+      }
+      if (!ok)
         for (int ws = (last_w - SW + 1 > 0 ? last_w - SW + 1 : 0); ws <= last_w; ++ws)
           mbar_drain(w_full(ws % SW), (ws / SW) & 1);
-        for (int ks = (last_b - S + 1 > 0 ? last_b - S + 1 : 0); ks <= last_b; ++ks)
-          mbar_drain(full_b(ks % S), (ks / S) & 1);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16(kTileM, BN);
-      for (int ks = 0; ks < nk; ++ks) {
-        const int s = ks % S;
-        const uint32_t par = (ks / S) & 1;
-        if (!mbar_wait(full_a(s), par, abort_flag)) break;
-        if (!mbar_wait(full_b(s), par, abort_flag)) break;
+    } else if (warp == 1 && lane == 0) {
+      // ----------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = idesc_kind_f16(kTileM, BN, 1);  // bf16 x bf16 -> f32
+      for (int i = 0; i < ng; ++i) {
+        const int s = i % S, buf = i & 1;
+        const uint32_t par = (i / S) & 1;
+        if (!mbar_wait(full_a(s), par, abort_flag, &g_tc_status)) break;
+        if (!mbar_wait(full_b(s), par, abort_flag, &g_tc_status)) break;
+        if (i >= 2 && !mbar_wait(tmem_free(buf), ((i >> 1) - 1) & 1, abort_flag, &g_tc_status)) break;
         tc_fence_after();
         const uint32_t a_addr = sbase + L::a_off + s * kABytes;
         const uint32_t b_addr = sbase + L::b_off + s * L::kB;
+        const uint32_t d = tmem_base + (uint32_t)(buf * BN);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_f16(tmem_d, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32), idesc, (ks | kk) != 0);
+          mma_f16(d, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32), idesc, kk != 0);
         mma_commit(empty(s));
+        mma_commit(mma_done(buf));
       }
-      mma_commit(acc_full);  // also on abort: lets the teardown wait for MMAs in flight
+    }
+    __syncwarp();  // reconverge lane 0 (producer / MMA) with the rest of its warp
+    if (splitk > 1) {  // the accumulate warpgroups reduce between these two cluster barriers
+      cluster_sync();
+      cluster_sync();
+    }
+  } else if (wg == 1) {
+    setmaxnreg_dec<kRegsLow>();
+    // ------------------------------------------------------------- decode
+    const int r = (warp - 4) * 32 + lane;  // tile row
+    for (int i = 0; i < ng; ++i) {
+      const int ws = i / kGroupsPerW, gi = i % kGroupsPerW, slot = ws % SW;
+      if (gi == 0 && !warp_wait(w_full(slot), (ws / SW) & 1, abort_flag, &g_tc_status)) break;
+      const int s = i % S;
+      if (!warp_wait(empty(s), ((i / S) & 1) ^ 1, abort_flag, &g_tc_status)) break;
+      const uint32_t csrc = sbase + L::w_off + slot * kWBytes + r * 128;
+      const uint4 c0 = ld_shared_v4(csrc + (((2 * gi) ^ (r & 7)) << 4));
+      const uint4 c1 = ld_shared_v4(csrc + (((2 * gi + 1) ^ (r & 7)) << 4));
+      const uint32_t adst = sbase + L::a_off + s * kABytes + r * 128;
+      const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      uint4 dec[8];  // decode all eight words before storing: the stores are compiler barriers
+#pragma unroll
+      for (int j = 0; j < 8; ++j) dec[j] = decode_word_bf16(words[j]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) st_shared_v4(adst + ((j ^ (r & 7)) << 4), dec[j]);
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(full_a(s));
+        if (gi == kGroupsPerW - 1 || i == ng - 1) mbar_arrive(w_empty(slot));
+      }
+    }
+    __syncwarp();
+    if (splitk > 1) {
+      cluster_sync();
+      cluster_sync();
     }
   } else {
-    // ------------------------------------------------------------- decode warps
-    const int dq = threadIdx.x - 64;
-    const int r = dq & (kTileM - 1);   // row within the tile
-    const int h = dq >> 7;             // which 32-wide half of each group
-    const int64_t row = m0 + r;
+    setmaxnreg_inc<kRegsHigh>();
+    // ------------------------------------------------------------- accumulate
+    const int quad = warp & 3;            // TMEM lane quadrant
+    const int chalf = (warp - 8) >> 2;    // column half
+    const int r_acc = quad * 32 + lane;   // tile row
+    float2 acc[kCols / 2];
+#pragma unroll
+    for (int i = 0; i < kCols / 2; ++i) acc[i] = make_float2(0.f, 0.f);
+    bool acc_ok = true;
+    const int64_t row = m0 + r_acc;
     const bool row_ok = row < p.N;
     const uint16_t* srow = p.scales + (row_ok ? row : 0) * (p.K >> 6);
     uint16_t s_cur[kGroupsPerW], s_nxt[kGroupsPerW];
 #pragma unroll
-    for (int g = 0; g < kGroupsPerW; ++g) {
-      s_cur[g] = (row_ok && g < nk) ? srow[g] : (uint16_t)0;
-      s_nxt[g] = 0;
+    for (int j = 0; j < kGroupsPerW; ++j) {
+      s_cur[j] = 0;
+      s_nxt[j] = (row_ok && j < ng) ? srow[g_begin + j] : (uint16_t)0;
     }
-    bool ok = true;
-    for (int ks = 0; ks < nk && ok; ++ks) {
-      const int ws = ks / kGroupsPerW, gi = ks % kGroupsPerW, slot = ws % SW;
+    const uint32_t tlane = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(chalf * kCols);
+    for (int i = 0; i < ng; ++i) {
+      const int buf = i & 1, gi = i % kGroupsPerW;
       if (gi == 0) {
-        ok = mbar_wait(w_full(slot), (ws / SW) & 1, abort_flag);
-        if (!ok) break;
 #pragma unroll
-        for (int g = 0; g < kGroupsPerW; ++g) {
-          const int gg = (ws + 1) * kGroupsPerW + g;
-          s_nxt[g] = (row_ok && gg < nk) ? srow[gg] : (uint16_t)0;
+        for (int j = 0; j < kGroupsPerW; ++j) {
+          s_cur[j] = s_nxt[j];
+          const int ii = i + kGroupsPerW + j;
+          s_nxt[j] = (row_ok && ii < ng) ? srow[g_begin + ii] : (uint16_t)0;
         }
       }
-      const int s = ks % S;
-      ok = mbar_wait(empty(s), ((ks / S) & 1) ^ 1, abort_flag);
-      if (!ok) break;
       uint16_t sb = s_cur[0];
 #pragma unroll
-      for (int g = 1; g < kGroupsPerW; ++g) sb = (gi == g) ? s_cur[g] : sb;
-      const __half2 s2 = __half2half2(__ushort_as_half(sb));
-      // 16 code bytes of this row: logical 16-byte chunk (2*gi + h) of the 128-byte line
-      const uint32_t csrc = sbase + L::w_off + slot * kWBytes + r * 128 + ((((2 * gi + h) ^ (r & 7))) << 4);
-      const uint4 cw = ld_shared_v4(csrc);
-      const uint32_t adst = sbase + L::a_off + s * kABytes + r * 128;
-      const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+      for (int j = 1; j < kGroupsPerW; ++j) sb = (gi == j) ? s_cur[j] : sb;
+      const float sf = fp16_bits_to_float(sb);
+      const float2 s2 = make_float2(sf, sf);
+      if (!(acc_ok = warp_wait(mma_done(buf), (i >> 1) & 1, abort_flag, &g_tc_status))) break;
+      tc_fence_after();
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 o = decode_word_f16(words[i], s2);
-        st_shared_v4(adst + ((((4 * h + i) ^ (r & 7))) << 4), o.x, o.y, o.z, o.w);
+      for (int c = 0; c < kCols; c += kChunk) {
+        uint32_t v[kChunk];
+        if constexpr (kChunk == 32) tmem_ld32(tlane + buf * BN + c, v);
+        else if constexpr (kChunk == 16) tmem_ld16(tlane + buf * BN + c, v);
+        else tmem_ld8(tlane + buf * BN + c, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < kChunk; j += 2)
+          acc[(c + j) / 2] =
+              ffma2(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), s2, acc[(c + j) / 2]);
       }
-      fence_proxy_async();
+      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(full_a(s));
-      if (gi == kGroupsPerW - 1 || ks == nk - 1) {
-        if (lane == 0) mbar_arrive(w_empty(slot));
+      if (lane == 0) mbar_arrive(tmem_free(buf));
+    }
+
+    // ----------------------------------------------------------- split-K reduction across the cluster
+    __syncwarp();
+    if (splitk > 1) {
+      cluster_sync();  // every CTA of the cluster is past its main loop: rank 0's buffers are free
+      if (crank > 0) {
+        const uint32_t remote0 = mapa_shared(sbase, 0);
 #pragma unroll
-        for (int g = 0; g < kGroupsPerW; ++g) s_cur[g] = s_nxt[g];
+        for (int c = 0; c < kCols; c += 4) {
+          const uint32_t off = (((crank - 1) * (BN / 4) + (chalf * kCols + c) / 4) * kTileM + r_acc) * 16;
+          st_cluster_v4(remote0 + off, acc[c / 2].x, acc[c / 2].y, acc[c / 2 + 1].x, acc[c / 2 + 1].y);
+        }
+      }
+      cluster_sync();  // partial sums have landed in rank 0
+      if (crank == 0) {
+#pragma unroll 1
+        for (int q = 1; q < splitk; ++q) {
+#pragma unroll
+          for (int c = 0; c < kCols; c += 4) {
+            const uint32_t off = (((q - 1) * (BN / 4) + (chalf * kCols + c) / 4) * kTileM + r_acc) * 16;
+            const float4 v = ld_shared_f4(sbase + off);
+            acc[c / 2] = fadd2(acc[c / 2], make_float2(v.x, v.y));
+            acc[c / 2 + 1] = fadd2(acc[c / 2 + 1], make_float2(v.z, v.w));
+          }
+        }
       }
     }
 
-    // ------------------------------------------------------------- epilogue
-    if (ok && mbar_wait(acc_full, 0, abort_flag)) {
-      tc_fence_after();
-      const int quad = warp & 3;                 // TMEM lanes this warp may access
-      const int half = (warp - 2) >> 2;          // which half of the BN columns
-      const int64_t orow = m0 + quad * 32 + lane;
-      const bool orow_ok = orow < p.N;
-      constexpr int kCols = BN / 2;
-#pragma unroll 1
-      for (int c = half * kCols; c < (half + 1) * kCols; c += 16) {
-        float v[16];
-        tmem_ld16(tmem_d + ((uint32_t)(quad * 32) << 16) + (uint32_t)c, v);
+    // ----------------------------------------------------------- epilogue: Y[t, row] = bf16(acc)
+    if (crank == 0 && acc_ok && !*abort_flag && row_ok) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int64_t t = t0 + c + j;
-          if (orow_ok && t < p.T) p.y[t * p.N + orow] = float_to_bf16_bits(v[j]);
-        }
+      for (int j = 0; j < kCols; ++j) {
+        const int64_t t = t0 + chalf * kCols + j;
+        const float v = (j & 1) ? acc[j / 2].y : acc[j / 2].x;
+        if (t < p.T) p.y[t * p.N + row] = float_to_bf16_bits(v);
       }
     }
   }
@@ -417,9 +329,14 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
-    if (*abort_flag) mbar_drain(acc_full, 0);  // MMAs in flight must finish before TMEM is freed
+    if (*abort_flag && lane == 0) {
+      // MMAs in flight must finish before TMEM is released: wait for the last commits.
+      mbar_drain(mma_done(0), 0);
+      mbar_drain(mma_done(1), 0);
+    }
+    __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_d, L::tmem_cols);
+    tmem_dealloc(tmem_base, L::tmem_cols);
   }
 }
 
@@ -432,12 +349,12 @@ EncodeTiledFn encode_fn() {
   static EncodeTiledFn fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
-    void* p = nullptr;
+    void* f = nullptr;
     cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
+      fn = reinterpret_cast<EncodeTiledFn>(f);
   });
   return fn;
 }
@@ -456,62 +373,122 @@ bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint6
 }
 
 template <int BN, int S, int SW>
-int launch_tile(const LinearArgs& a, const uint16_t* xh) {
+int launch_tile(const LinearArgs& a, int splitk) {
   using L = TcSmem<BN, S, SW>;
   static_assert(L::alloc <= 232448, "shared memory budget");
+  if (splitk < 1 || splitk > 8 || splitk > L::max_splitk) {
+    set_error_detail("tc: split-K factor out of range for this tile");
+    return Q4LIN_ERR_INVALID_ARG;
+  }
   static bool attr_set[64] = {};
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(q4_tc_kernel<BN, S, SW>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc) !=
-        cudaSuccess)
+  if (cuda_check(cudaGetDevice(&dev), "cudaGetDevice")) return Q4LIN_ERR_CUDA;
+  if (dev >= 64 || !attr_set[dev]) {
+    if (cuda_check(cudaFuncSetAttribute(q4_tc_kernel<BN, S, SW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        L::alloc),
+                   "tc: cudaFuncSetAttribute(max dynamic shared memory)"))
       return Q4LIN_ERR_CUDA;
-    attr_set[dev] = true;
+    if (cuda_check(cudaFuncSetAttribute(q4_tc_kernel<BN, S, SW>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0),
+                   "tc: cudaFuncSetAttribute(cluster size)"))
+      return Q4LIN_ERR_CUDA;
+    if (dev < 64) attr_set[dev] = true;
   }
   CUtensorMap tm_codes, tm_x;
   if (!make_map_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.wq, (uint64_t)(a.K / 2), (uint64_t)a.N,
                    (uint64_t)(a.K / 2), 128, kTileM) ||
-      !make_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xh, (uint64_t)a.K, (uint64_t)a.T, (uint64_t)a.K * 2, 64,
-                   BN))
+      !make_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, (uint64_t)a.K, (uint64_t)a.T, (uint64_t)a.K * 2,
+                   64, BN)) {
+    set_error_detail("tc: cuTensorMapEncodeTiled failed (or is unavailable)");
     return Q4LIN_ERR_CUDA;
-  TcParams p{a.scales, a.y, a.N, a.K, a.T, (int)(a.K / 64)};
-  const dim3 grid((unsigned)((a.N + kTileM - 1) / kTileM), (unsigned)((a.T + BN - 1) / BN));
-  q4_tc_kernel<BN, S, SW><<<grid, kThreads, L::alloc, a.stream>>>(tm_codes, tm_x, p);
-  return cudaGetLastError() == cudaSuccess ? Q4LIN_OK : Q4LIN_ERR_CUDA;
+  }
+  const TcParams p{a.scales, a.y, a.N, a.K, a.T, (int)(a.K / 64), splitk};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((a.N + kTileM - 1) / kTileM), (unsigned)((a.T + BN - 1) / BN), (unsigned)splitk);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = L::alloc;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = (unsigned)splitk;
+  cfg.attrs = attr;
+  cfg.numAttrs = splitk > 1 ? 1 : 0;
+  return cuda_check(cudaLaunchKernelEx(&cfg, q4_tc_kernel<BN, S, SW>, tm_codes, tm_x, p), "tc: kernel launch");
 }
 
-int pick_bn(int64_t T) {
-  if (T > 128) return 256;
-  if (T > 64) return 128;
-  if (T > 32) return 64;
-  return 32;
+int max_splitk_for(int bn) {
+  switch (bn) {
+    case 256: return TcSmem<256, 4, 2>::max_splitk;
+    case 128: return TcSmem<128, 5, 3>::max_splitk;
+    case 64: return TcSmem<64, 6, 4>::max_splitk;
+    case 32: return TcSmem<32, 6, 6>::max_splitk;
+    default: return TcSmem<16, 6, 6>::max_splitk;
+  }
+}
+
+int sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev < 64 && cached[dev]) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (dev < 64) cached[dev] = n;
+  return n;
 }
 
 }  // namespace
 
-size_t tc_workspace_bytes(int64_t, int64_t K, int64_t T) { return (size_t)T * (size_t)K * 2; }
-
-int tc_launch_count(int64_t, int64_t, int64_t) { return 2; }
-
-bool tc_supported(int64_t N, int64_t K, int64_t T) {
-  // TMA coordinates are 32-bit and the grid's y extent is limited.
-  return N < ((int64_t)1 << 31) && K / 2 < ((int64_t)1 << 31) && T < ((int64_t)1 << 31) && (T + 31) / 32 < 65535 &&
-         K / 64 < ((int64_t)1 << 30);
+TcPlan tc_plan(int route, int64_t N, int64_t K, int64_t T, int sms) {
+  TcPlan pl{};
+  // token tile: the smallest MMA N (multiple of 16, <= 256) covering T, else 256
+  if (T > 128) pl.bn = 256;
+  else if (T > 64) pl.bn = 128;
+  else if (T > 32) pl.bn = 64;
+  else if (T > 16) pl.bn = 32;
+  else pl.bn = 16;
+  pl.splitk = 1;
+  if (route == Q4LIN_ROUTE_TC_SPLITK) {
+    // split K across a cluster until the CTA count fills whole waves of the GPU
+    const int64_t tiles = ((N + kTileM - 1) / kTileM) * ((T + pl.bn - 1) / pl.bn);
+    const int64_t nk = K / 64;
+    double best = -1.0;
+    const int smax = max_splitk_for(pl.bn) < 8 ? max_splitk_for(pl.bn) : 8;
+    for (int s = 1; s <= smax && s <= nk; ++s) {
+      const int64_t ctas = tiles * s;
+      const int64_t waves = (ctas + sms - 1) / sms;
+      const double eff = (double)ctas / (double)(waves * sms);
+      if (eff > best + 1e-9) {
+        best = eff;
+        pl.splitk = s;
+      }
+    }
+  }
+  return pl;
 }
 
-int tc_launch(const LinearArgs& a) {
-  if (!tc_supported(a.N, a.K, a.T)) return Q4LIN_ERR_INVALID_ARG;
-  uint16_t* xh = static_cast<uint16_t*>(a.workspace);
-  const int64_t n8 = a.T * a.K / 8;
-  int64_t blocks = (n8 + 255) / 256;
-  if (blocks > 152 * 16) blocks = 152 * 16;
-  q4_x_to_f16<<<(unsigned)blocks, 256, 0, a.stream>>>(a.x, xh, n8);
-  if (cudaGetLastError() != cudaSuccess) return Q4LIN_ERR_CUDA;
-  switch (pick_bn(a.T)) {
-    case 256: return launch_tile<256, 4, 2>(a, xh);
-    case 128: return launch_tile<128, 5, 3>(a, xh);
-    case 64: return launch_tile<64, 6, 4>(a, xh);
-    default: return launch_tile<32, 6, 6>(a, xh);
+size_t tc_workspace_bytes(int64_t, int64_t, int64_t) { return 0; }
+
+int tc_launch_count(int64_t, int64_t, int64_t) { return 1; }
+
+bool tc_supported(int64_t N, int64_t K, int64_t T) {
+  // TMA coordinates are 32-bit signed and the grid's y extent is limited.
+  return N < ((int64_t)1 << 31) && K < ((int64_t)1 << 31) && T < ((int64_t)1 << 31) && (T + 15) / 16 < 65535;
+}
+
+int tc_launch(const LinearArgs& a, int route) {
+  if (!tc_supported(a.N, a.K, a.T)) {
+    set_error_detail("tc: shape beyond the tensor-core route's limits");
+    return Q4LIN_ERR_INVALID_ARG;
+  }
+  const TcPlan pl = tc_plan(route, a.N, a.K, a.T, sm_count());
+  switch (pl.bn) {
+    case 256: return launch_tile<256, 4, 2>(a, pl.splitk);
+    case 128: return launch_tile<128, 5, 3>(a, pl.splitk);
+    case 64: return launch_tile<64, 6, 4>(a, pl.splitk);
+    case 32: return launch_tile<32, 6, 6>(a, pl.splitk);
+    default: return launch_tile<16, 6, 6>(a, pl.splitk);
   }
 }
 

@@ -11,6 +11,24 @@
 #include "q4lin.h"
 #include "q4_internal.h"
 
+namespace q4 {
+
+static thread_local char g_detail[512];
+
+void set_error_detail(const char* what) {
+  std::snprintf(g_detail, sizeof(g_detail), "%s", what);
+}
+
+int cuda_check(cudaError_t e, const char* where) {
+  if (e == cudaSuccess) return 0;
+  std::snprintf(g_detail, sizeof(g_detail), "%s: %s (%s)", where, cudaGetErrorString(e), cudaGetErrorName(e));
+  return 6;  // Q4LIN_ERR_CUDA
+}
+
+}  // namespace q4
+
+extern "C" const char* q4lin_status_string(int status);
+
 namespace {
 
 constexpr int64_t kMaxDim = (int64_t)1 << 40;
@@ -57,6 +75,7 @@ int check_device() {
 
 int route_for(int64_t N, int64_t K, int64_t T) {
   if (T <= 4 || !q4::tc_supported(N, K, T)) return Q4LIN_ROUTE_GEMV;
+  if (T <= 64) return Q4LIN_ROUTE_TC_SPLITK;
   return Q4LIN_ROUTE_TC;
 }
 
@@ -65,13 +84,14 @@ size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 size_t route_ws(int route, int64_t N, int64_t K, int64_t T) {
   switch (route) {
     case Q4LIN_ROUTE_GEMV: return round256(q4::gemv_workspace_bytes(N, K, T));
-    case Q4LIN_ROUTE_TC: return round256(q4::tc_workspace_bytes(N, K, T));
+    case Q4LIN_ROUTE_TC:
+    case Q4LIN_ROUTE_TC_SPLITK: return round256(q4::tc_workspace_bytes(N, K, T));
     default: return 0;
   }
 }
 
-int run(int route, const uint8_t* wq, const uint16_t* scales, const uint16_t* x, uint16_t* y,
-        int64_t N, int64_t K, int64_t T, void* workspace, void* stream) {
+int run_impl(int route, const uint8_t* wq, const uint16_t* scales, const uint16_t* x, uint16_t* y,
+             int64_t N, int64_t K, int64_t T, void* workspace, void* stream) {
   int st = validate(wq, scales, x, y, N, K, T);
   if (st != Q4LIN_OK) return st;
   if (N == 0 || T == 0) return Q4LIN_OK;
@@ -83,15 +103,22 @@ int run(int route, const uint8_t* wq, const uint16_t* scales, const uint16_t* x,
   st = check_device();
   if (st != Q4LIN_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (K == 0) {
-    return cudaMemsetAsync(y, 0, (size_t)N * (size_t)T * 2, s) == cudaSuccess ? Q4LIN_OK : Q4LIN_ERR_CUDA;
-  }
+  if (K == 0) return q4::cuda_check(cudaMemsetAsync(y, 0, (size_t)N * (size_t)T * 2, s), "zero fill of y");
   q4::LinearArgs a{wq, scales, x, y, N, K, T, workspace, s};
   switch (route) {
     case Q4LIN_ROUTE_GEMV: return q4::gemv_launch(a);
-    case Q4LIN_ROUTE_TC: return q4::tc_launch(a);
+    case Q4LIN_ROUTE_TC:
+    case Q4LIN_ROUTE_TC_SPLITK: return q4::tc_launch(a, route);
     default: return Q4LIN_ERR_INVALID_ARG;
   }
+}
+
+int run(int route, const uint8_t* wq, const uint16_t* scales, const uint16_t* x, uint16_t* y, int64_t N,
+        int64_t K, int64_t T, void* workspace, void* stream) {
+  q4::set_error_detail("");
+  const int st = run_impl(route, wq, scales, x, y, N, K, T, workspace, stream);
+  if (st != Q4LIN_OK && q4::g_detail[0] == 0) q4::set_error_detail(q4lin_status_string(st));
+  return st;
 }
 
 }  // namespace
@@ -116,7 +143,8 @@ int q4lin_kernel_launches(int64_t N, int64_t K, int64_t T) {
   if (K == 0) return 1;  // the zero fill
   switch (route_for(N, K, T)) {
     case Q4LIN_ROUTE_GEMV: return q4::gemv_launch_count(N, K, T);
-    case Q4LIN_ROUTE_TC: return q4::tc_launch_count(N, K, T);
+    case Q4LIN_ROUTE_TC:
+    case Q4LIN_ROUTE_TC_SPLITK: return q4::tc_launch_count(N, K, T);
     default: return 0;
   }
 }
@@ -165,5 +193,7 @@ int q4lin_clear_device_status(void) {
 }
 
 const char* q4lin_version(void) { return "0.1.0"; }
+
+const char* q4lin_last_error_detail(void) { return q4::g_detail; }
 
 }  // extern "C"

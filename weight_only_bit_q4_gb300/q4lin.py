@@ -21,7 +21,8 @@ ROUTE_NAMES = {ROUTE_AUTO: "auto", ROUTE_GEMV: "gemv", ROUTE_TC_SPLITK: "tc_spli
 EXPORTS = ("q4lin_workspace_bytes", "q4lin_linear", "q4lin_linear_route",
            "q4lin_route_workspace_bytes", "q4lin_select_route", "q4lin_kernel_launches",
            "q4lin_status_string",
-           "q4lin_device_status", "q4lin_clear_device_status", "q4lin_version")
+           "q4lin_device_status", "q4lin_clear_device_status", "q4lin_last_error_detail",
+           "q4lin_version")
 
 _lib = None
 
@@ -29,7 +30,13 @@ _lib = None
 class Q4LinError(RuntimeError):
     def __init__(self, status: int, what: str = ""):
         self.status = status
-        super().__init__(f"q4lin: {what}{STATUS.get(status, status)}: {status_string(status)}")
+        detail = last_error_detail()
+        super().__init__(f"q4lin: {what}{STATUS.get(status, status)}: {status_string(status)}"
+                         + (f" [{detail}]" if detail else ""))
+
+
+def last_error_detail() -> str:
+    return load().q4lin_last_error_detail().decode(errors="replace")
 
 
 def load(path: str | None = None) -> ctypes.CDLL:
@@ -60,6 +67,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q4lin_device_status.restype = ctypes.c_int
     lib.q4lin_clear_device_status.argtypes = []
     lib.q4lin_clear_device_status.restype = ctypes.c_int
+    lib.q4lin_last_error_detail.argtypes = []
+    lib.q4lin_last_error_detail.restype = ctypes.c_char_p
     lib.q4lin_version.argtypes = []
     lib.q4lin_version.restype = ctypes.c_char_p
     if path is None:
@@ -89,7 +98,7 @@ def kernel_launches(N: int, K: int, T: int) -> int:
     return int(load().q4lin_kernel_launches(N, K, T))
 
 
-_IMPLEMENTED = (ROUTE_GEMV, ROUTE_TC)
+_IMPLEMENTED = (ROUTE_GEMV, ROUTE_TC_SPLITK, ROUTE_TC)
 
 
 def implemented_routes():
