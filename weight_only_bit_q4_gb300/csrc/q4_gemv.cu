@@ -14,8 +14,8 @@
 //     sum_k (q_k - 8) x_k  =  sum_k (128 + q_k) x_k  -  136 * sum_k x_k,
 // which costs one FMA per weight and token; the group scale multiplies the
 // chunk partial once.  All arithmetic is FP32.
-#include "q4_common.cuh"
 #include "q4_internal.h"
+#include "q4_sm100.cuh"
 
 namespace q4 {
 
@@ -124,13 +124,246 @@ q4_gemv_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict__ scal
   }
 }
 
+// ---------------------------------------------------------------------------
+// Single-token streaming GEMV.  One persistent CTA per SM owns a contiguous
+// range of rows (balanced to one row).  A producer warp streams the rows'
+// code bytes into a ring of shared-memory slots with 1-D bulk async copies
+// (4 rows per copy), so the CTA's share is in flight from the start.
+//
+// K is cut into column groups of 32 chunks (a chunk = 16 code bytes = 32
+// weights = half a scale group); warp j of a row stream owns column group j,
+// so lane l always handles chunk 32 j + l: its 32 x values (and their sum)
+// are loaded once from global memory and stay in registers for every row.
+// Per 4-row slot a warp reads one conflict-free 16-byte code chunk per row,
+// decodes it to (128 + q) floats with byte permutes, accumulates with packed
+// FP32 FMAs, applies (partial - 136 * sum x) * s, and reduces across the warp.
+// The NJ column-group partials of a row are summed in a fixed order at the end
+// (deterministic), then rounded to bf16.
+constexpr int kBulkThreads = 512;
+constexpr int kBulkConsumers = 15;   // warps 1..15
+constexpr int kBulkRows = 4;
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+struct StreamLayout {
+  uint32_t part_off, bar_off, slot_off, slot_bytes, bytes;
+};
+
+// partial sums [rows_cap][nj] fp32, then full/empty barriers, then the slots (128-byte aligned)
+__host__ __device__ inline StreamLayout stream_layout(int64_t K, int64_t rows_cap, int nj, int slots) {
+  StreamLayout L;
+  L.part_off = 0;
+  L.bar_off = (uint32_t)((rows_cap * nj * 4 + 15) / 16 * 16);
+  L.slot_off = (L.bar_off + (uint32_t)slots * 16 + 127) / 128 * 128;
+  L.slot_bytes = (uint32_t)(kBulkRows * (K / 2));
+  L.bytes = L.slot_off + (uint32_t)slots * L.slot_bytes;
+  return L;
+}
+
+__global__ void __launch_bounds__(kBulkThreads, 1)
+q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict__ scales,
+                      const uint16_t* __restrict__ x, uint16_t* __restrict__ y, int64_t N, int64_t K,
+                      int64_t rows_cap, int nj, int slots) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const StreamLayout L = stream_layout(K, rows_cap, nj, slots);
+  float* part = reinterpret_cast<float*>(smem + L.part_off);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t full0 = sbase + L.bar_off, empty0 = full0 + 8u * slots;
+  __shared__ int abort_word;
+  volatile int* abort_flag = &abort_word;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // 4-row blocks are dealt round-robin: CTA c owns global blocks c, c + G, c + 2G, ...
+  // so at any moment the whole GPU streams one contiguous window of the code plane.
+  const int64_t nblk = (N + kBulkRows - 1) / kBulkRows;
+  const int nb = (int)((nblk - blockIdx.x + gridDim.x - 1) / gridDim.x);
+  auto blk_row = [&](int b) { return ((int64_t)b * gridDim.x + blockIdx.x) * kBulkRows; };
+  auto blk_rows = [&](int b) { const int64_t ra = blk_row(b); return (int)((N - ra < kBulkRows) ? (N - ra) : kBulkRows); };
+  const int64_t row_bytes = K / 2, groups = K / 64, nchunk = K / 32;
+  const int streams = kBulkConsumers / nj;   // row streams; warp (j, stream) = 1 + stream * nj + j
+
+  // Barrier setup and the first copies are issued before the CTA-wide barrier,
+  // so the loads start while the other warps are still being set up.
+  const int first = nb < slots ? nb : slots;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < first; ++s) {
+      mbar_init(full0 + 8u * s, 1);
+      mbar_init(empty0 + 8u * s, nj);   // one arrival per column-group warp
+    }
+    abort_word = 0;
+    fence_mbar_init();
+    for (int b = 0; b < first; ++b) {
+      const int64_t ra = blk_row(b);
+      const uint32_t bytes = (uint32_t)(blk_rows(b) * row_bytes);
+      mbar_expect_tx(full0 + 8u * b, bytes);
+      bulk_g2s(sbase + L.slot_off + (uint32_t)b * L.slot_bytes, wq + ra * row_bytes, bytes, full0 + 8u * b);
+    }
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ---- producer (whole warp runs the loop; lane 0 issues): refill freed slots
+    int b = first;
+    for (; b < nb; ++b) {
+      const int s = b % slots;
+      if (!warp_wait(empty0 + 8u * s, ((b / slots) & 1) ^ 1, abort_flag, &g_gemv_status)) break;
+      if (lane == 0) {
+        const int64_t ra = blk_row(b);
+        const uint32_t bytes = (uint32_t)(blk_rows(b) * row_bytes);
+        mbar_expect_tx(full0 + 8u * s, bytes);
+        bulk_g2s(sbase + L.slot_off + (uint32_t)s * L.slot_bytes, wq + ra * row_bytes, bytes, full0 + 8u * s);
+      }
+      __syncwarp();
+    }
+    if (b < nb && lane == 0)  // aborted: let the copies already issued land before the CTA exits
+      for (int d = (b - slots > 0 ? b - slots : 0); d < b; ++d)
+        mbar_drain(full0 + 8u * (d % slots), (d / slots) & 1);
+    __syncwarp();
+  } else if (warp - 1 < streams * nj) {
+    const int j = (warp - 1) % nj, stream = (warp - 1) / nj;
+    const int64_t c = (int64_t)j * 32 + lane;     // this lane's chunk
+    const bool c_ok = c < nchunk;
+    // this lane's 32 x values and their sum, kept in registers for every row
+    float2 xv[16];
+    float xsum = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 v = c_ok ? ld_nc_u4(x + c * 32 + q * 8) : make_uint4(0, 0, 0, 0);
+      xv[4 * q + 0] = make_float2(bf16lo(v.x), bf16hi(v.x));
+      xv[4 * q + 1] = make_float2(bf16lo(v.y), bf16hi(v.y));
+      xv[4 * q + 2] = make_float2(bf16lo(v.z), bf16hi(v.z));
+      xv[4 * q + 3] = make_float2(bf16lo(v.w), bf16hi(v.w));
+    }
+#pragma unroll
+    for (int q = 0; q < 16; ++q) xsum += xv[q].x + xv[q].y;
+    const float bias = -136.f * xsum;
+
+    for (int b = stream; b < nb; b += streams) {
+      const int s = b % slots;
+      const int64_t ra = blk_row(b);
+      const int nr = blk_rows(b);
+      float sc[kBulkRows];
+#pragma unroll
+      for (int i = 0; i < kBulkRows; ++i)
+        sc[i] = (c_ok && i < nr) ? fp16_bits_to_float(scales[(ra + i) * groups + (c >> 1)]) : 0.f;
+      if (!warp_wait(full0 + 8u * s, (b / slots) & 1, abort_flag, &g_gemv_status)) break;
+      const uint32_t slot = sbase + L.slot_off + (uint32_t)s * L.slot_bytes;
+      float acc[kBulkRows];
+#pragma unroll
+      for (int i = 0; i < kBulkRows; ++i) {
+        acc[i] = 0.f;
+        if (i < nr && c_ok) {
+          const uint4 cw = ld_shared_v4(slot + (uint32_t)(i * row_bytes + c * 16));
+          const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+          float2 p2 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int wi = 0; wi < 4; ++wi) {
+            const uint32_t lo = words[wi] & 0x0F0F0F0Fu, hi = (words[wi] >> 4) & 0x0F0F0F0Fu;
+            p2 = ffma2(make_float2(f128_plus_byte<0>(lo), f128_plus_byte<0>(hi)), xv[4 * wi + 0], p2);
+            p2 = ffma2(make_float2(f128_plus_byte<1>(lo), f128_plus_byte<1>(hi)), xv[4 * wi + 1], p2);
+            p2 = ffma2(make_float2(f128_plus_byte<2>(lo), f128_plus_byte<2>(hi)), xv[4 * wi + 2], p2);
+            p2 = ffma2(make_float2(f128_plus_byte<3>(lo), f128_plus_byte<3>(hi)), xv[4 * wi + 3], p2);
+          }
+          acc[i] = sc[i] * ((p2.x + p2.y) + bias);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8u * s);
+#pragma unroll
+      for (int i = 0; i < kBulkRows; ++i) {
+        const float v = warp_sum(acc[i]);
+        if (lane == 0 && i < nr) part[(b * kBulkRows + i) * nj + j] = v;
+      }
+    }
+  }
+
+  // ---- final: y[row] = bf16(sum over column groups, in order).  Every warp
+  // reaches this barrier converged (all role loops are warp-uniform).
+  __syncthreads();
+  if (*abort_flag) return;
+  for (int64_t r = threadIdx.x; r < (int64_t)nb * kBulkRows; r += kBulkThreads) {
+    const int b = (int)(r / kBulkRows), i = (int)(r % kBulkRows);
+    if (i >= blk_rows(b)) continue;
+    float v = 0.f;
+    for (int jj = 0; jj < nj; ++jj) v += part[r * nj + jj];
+    y[blk_row(b) + i] = float_to_bf16_bits(v);
+  }
+}
+
 }  // namespace
 
 size_t gemv_workspace_bytes(int64_t, int64_t, int64_t) { return 0; }
 
-int gemv_launch_count(int64_t, int64_t, int64_t T) { return (int)((T + 3) / 4); }
+bool gemv_stream_ok(int64_t N, int64_t K, int64_t T);
+int gemv_launch_count(int64_t N, int64_t K, int64_t T) {
+  return gemv_stream_ok(N, K, T) ? 1 : (int)((T + 3) / 4);
+}
+
+struct StreamPlan {
+  int64_t grid, rows_cap;
+  int nj, slots;
+  uint32_t bytes;
+};
+
+static bool stream_plan(int64_t N, int64_t K, int nsm, StreamPlan* p) {
+  const int64_t nchunk = K / 32;
+  p->nj = (int)((nchunk + 31) / 32);
+  if (p->nj > kBulkConsumers) return false;
+  p->grid = (N + kBulkRows - 1) / kBulkRows;
+  if (p->grid > nsm) p->grid = nsm;
+  if (p->grid < 1) p->grid = 1;
+  p->rows_cap = ((N + kBulkRows - 1) / kBulkRows + p->grid - 1) / p->grid * kBulkRows;
+  const int64_t budget = 232448 - 1024;
+  const StreamLayout L0 = stream_layout(K, p->rows_cap, p->nj, 0);
+  const int64_t per = (int64_t)kBulkRows * (K / 2) + 16;
+  int64_t s = (budget - L0.slot_off - 128) / per;
+  if (s > 32) s = 32;
+  if (s < 4) return false;
+  p->slots = (int)s;
+  p->bytes = stream_layout(K, p->rows_cap, p->nj, p->slots).bytes;
+  return p->bytes <= budget;
+}
+
+static int device_sms() {
+  static int sms[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev < 64 && sms[dev]) return sms[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (dev < 64) sms[dev] = n;
+  return n;
+}
+
+static int gemv_stream_launch(const LinearArgs& a) {
+  static bool attr[64] = {};
+  int dev = 0;
+  if (cuda_check(cudaGetDevice(&dev), "cudaGetDevice")) return Q4LIN_ERR_CUDA;
+  StreamPlan pl;
+  if (!stream_plan(a.N, a.K, device_sms(), &pl)) return Q4LIN_ERR_INVALID_ARG;
+  if (dev >= 64 || !attr[dev]) {
+    if (cuda_check(cudaFuncSetAttribute(q4_gemv_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        232448 - 1024),
+                   "gemv: cudaFuncSetAttribute"))
+      return Q4LIN_ERR_CUDA;
+    if (dev < 64) attr[dev] = true;
+  }
+  q4_gemv_stream_kernel<<<(unsigned)pl.grid, kBulkThreads, pl.bytes, a.stream>>>(a.wq, a.scales, a.x, a.y, a.N, a.K,
+                                                                                 pl.rows_cap, pl.nj, pl.slots);
+  return cuda_check(cudaGetLastError(), "gemv: streaming kernel launch");
+}
+
+bool gemv_stream_ok(int64_t N, int64_t K, int64_t T) {
+  StreamPlan pl;
+  return T == 1 && stream_plan(N, K, 148, &pl);
+}
 
 int gemv_launch(const LinearArgs& a) {
+  if (gemv_stream_ok(a.N, a.K, a.T)) return gemv_stream_launch(a);
   const int64_t rows_per_cta = (int64_t)kRows * kWarps;
   const int64_t grid = (a.N + rows_per_cta - 1) / rows_per_cta;
   if (grid > 0x7fffffff) return Q4LIN_ERR_INVALID_ARG;

@@ -156,17 +156,17 @@ __host__ __device__ constexpr uint32_t idesc_kind_f16(int M, int N, uint32_t ab_
 }
 
 // ----------------------------------------------------------------- shared memory
+// Ordering against the mbarrier waits, fences and arrivals around them comes
+// from those (volatile, memory-clobbering) instructions; the accesses
+// themselves carry no compiler barrier so the scheduler can interleave them
+// with arithmetic.
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
-  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
 }
 
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr)
-               : "memory");
+  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
   return v;
 }
 
@@ -176,16 +176,19 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
 // in the low half and the byte shifted down by 4 in the high half; masking the
 // two low nibbles and OR-ing 0x4300 gives the exact bf16 pair (128 + q[2j],
 // 128 + q[2j+1]); subtracting 136 gives (q - 8) exactly.
+__device__ __forceinline__ uint32_t bf16x2_sub136(uint32_t v) {
+  uint32_t r;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(0x43084308u));  // 0x4308 = bf16 136
+  return r;
+}
+
 __device__ __forceinline__ uint4 decode_word_bf16(uint32_t w) {
   const uint32_t w4 = w >> 4;
-  const __nv_bfloat162 bias = __bfloat162bfloat162(__ushort_as_bfloat16((unsigned short)0x4308));  // 136
   uint32_t h[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const uint32_t t = __byte_perm(w, w4, (uint32_t)(j | ((4 + j) << 8)));
-    uint32_t v = (t & 0x000F000Fu) | 0x43004300u;
-    __nv_bfloat162 b = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&v), bias);
-    h[j] = *reinterpret_cast<uint32_t*>(&b);
+    h[j] = bf16x2_sub136((t & 0x000F000Fu) | 0x43004300u);
   }
   return make_uint4(h[0], h[1], h[2], h[3]);
 }
@@ -234,7 +237,13 @@ __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
 }
 
-// 8 consecutive 32-bit TMEM columns of this thread's lane (no wait).
+// 4 / 8 consecutive 32-bit TMEM columns of this thread's lane (no wait).
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])

@@ -16,7 +16,7 @@
 //     q - 8, written in the MMA's 128-byte-swizzled K-major A layout;
 //   * one thread issues 4 x tcgen05.mma (K = 16) per group into one of two
 //     TMEM buffers, D_g[n, t] = sum_{k in g} (q[n,k] - 8) x[t,k];
-//   * two accumulate warpgroups read D_g back (tcgen05.ld) and add
+//   * four accumulate warpgroups read D_g back (tcgen05.ld) and add
 //     s[n,g] * D_g[n,t] to FP32 registers, then round to bf16 and store Y[t, n].
 //
 // Every product (q - 8) * x is exact in FP32 and the group scale multiplies
@@ -47,21 +47,24 @@ struct TcParams {
   int splitk;  // CTAs of a cluster sharing one output tile along K (1 = no split)
 };
 
-// Warpgroup roles (setmaxnreg works per warpgroup):
-//   wg0: warp 0 TMA producer (X), warp 1 TMEM owner + MMA issuer,
+// Warpgroup roles (setmaxnreg works per warpgroup of 4 consecutive warps):
+//   wg0: warp 0 TMA producer (X tiles), warp 1 TMEM owner + MMA issuer,
 //        warp 2 TMA producer (code plane), warp 3 idle
-//   wg1: decode (one thread per tile row, one whole 64-wide group per step)
-//   wg2, wg3: FP32 accumulation of scaled group partials + epilogue
-//             (one thread per row and column half; warp % 4 = TMEM lane quadrant)
-constexpr int kThreads = 512;
+//   wg1: decode, one thread per tile row, one whole code stage per iteration
+//   wg2..wg5: FP32 accumulation of the scaled group partials and the
+//        epilogue; warp w reads TMEM lane quadrant w % 4 and column quarter
+//        (w - 8) / 4, one thread per (row, column quarter)
+constexpr int kThreads = 768;
+constexpr int kAccWarps = 16;
 constexpr int kTileM = 128;
 constexpr int kGroupsPerW = 4;               // code stage: 128 rows x 128 bytes = 4 groups
 constexpr uint32_t kABytes = kTileM * 128;   // one group of A: 128 rows x 64 bf16
 constexpr uint32_t kWBytes = kTileM * 128;   // one code stage
-constexpr int kRegsLow = 64;                 // wg0, wg1 after the split
-constexpr int kRegsHigh = 192;               // wg2, wg3 after the split
-static_assert((2 * kRegsLow + 2 * kRegsHigh) * 128 <= 65536, "register split exceeds the launch budget");
-static_assert((2 * kRegsLow + 2 * kRegsHigh) * 128 == (65536 / kThreads) * kThreads,
+constexpr int kRegsLaunch = 80;              // 65536 / 768, rounded down to a multiple of 8
+constexpr int kRegsCtl = 40;                 // wg0
+constexpr int kRegsDec = 56;                 // wg1
+constexpr int kRegsAcc = 96;                 // wg2..wg5
+static_assert(128 * (kRegsCtl + kRegsDec) + 512 * kRegsAcc == kThreads * kRegsLaunch,
               "register split must equal the launch allocation");
 
 template <int BN, int S, int SW>
@@ -71,8 +74,8 @@ struct TcSmem {
   static constexpr uint32_t b_off = a_off + S * kABytes;
   static constexpr uint32_t w_off = b_off + S * kB;
   static constexpr uint32_t bar_off = w_off + SW * kWBytes;
-  // full_a[S], full_b[S], empty[S], w_full[SW], w_empty[SW], mma_done[2], tmem_free[2]
-  static constexpr uint32_t n_bars = 3 * S + 2 * SW + 4;
+  // full[S], empty[S], w_full[SW], w_empty[SW], mma_done[2], tmem_free[2], done
+  static constexpr uint32_t n_bars = 2 * S + 2 * SW + 5;
   static constexpr uint32_t misc_off = bar_off + n_bars * 8;
   static constexpr uint32_t bytes = misc_off + 16;
   static constexpr uint32_t alloc = bytes + 1024;  // slack for 1024-byte alignment
@@ -86,21 +89,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_x,
              const TcParams p) {
   using L = TcSmem<BN, S, SW>;
-  constexpr int kCols = BN / 2;  // accumulator columns per accumulate thread
-  constexpr int kChunk = kCols >= 128 ? 16 : (kCols >= 32 ? 32 : kCols);  // TMEM columns per load
-  static_assert(kCols % 8 == 0 && kCols % kChunk == 0, "BN must be a multiple of 16");
+  constexpr int kCols = BN / 4;  // accumulator columns per accumulate thread
+  static_assert(kCols % 4 == 0, "BN must be a multiple of 16");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bars = sbase + L::bar_off;
-  auto full_a = [&](int s) { return bars + 8u * s; };
-  auto full_b = [&](int s) { return bars + 8u * (S + s); };
-  auto empty = [&](int s) { return bars + 8u * (2 * S + s); };
-  auto w_full = [&](int s) { return bars + 8u * (3 * S + s); };
-  auto w_empty = [&](int s) { return bars + 8u * (3 * S + SW + s); };
-  auto mma_done = [&](int b) { return bars + 8u * (3 * S + 2 * SW + b); };
-  auto tmem_free = [&](int b) { return bars + 8u * (3 * S + 2 * SW + 2 + b); };
+  auto full = [&](int s) { return bars + 8u * s; };
+  auto empty = [&](int s) { return bars + 8u * (S + s); };
+  auto w_full = [&](int s) { return bars + 8u * (2 * S + s); };
+  auto w_empty = [&](int s) { return bars + 8u * (2 * S + SW + s); };
+  auto mma_done = [&](int b) { return bars + 8u * (2 * S + 2 * SW + b); };
+  auto tmem_free = [&](int b) { return bars + 8u * (2 * S + 2 * SW + 2 + b); };
+  const uint32_t done_bar = bars + 8u * (2 * S + 2 * SW + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
 
@@ -123,8 +125,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full_a(s), 4);   // the 4 decode warps
-      mbar_init(full_b(s), 1);
+      mbar_init(full(s), 4 + 1);   // the 4 decode warps + the X producer's expect_tx arrival
       mbar_init(empty(s), 1);
     }
     for (int s = 0; s < SW; ++s) {
@@ -133,8 +134,9 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(mma_done(b), 1);
-      mbar_init(tmem_free(b), 8);  // the 8 accumulate warps
+      mbar_init(tmem_free(b), kAccWarps);
     }
+    mbar_init(done_bar, kAccWarps);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_codes);
@@ -147,25 +149,25 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
   const uint32_t tmem_base = *tmem_slot;
 
   if (wg == 0) {
-    setmaxnreg_dec<kRegsLow>();
+    setmaxnreg_dec<kRegsCtl>();
+    // single-lane role loops; the other lanes wait at the __syncwarp below
     if (warp == 0 && lane == 0) {
       // ----------------------------------------------------------- TMA producer: token tiles of X
-      int last_b = -1;
+      int last = -1;
       bool ok = true;
       for (int i = 0; i < ng; ++i) {
         const int s = i % S;
         if (!(ok = mbar_wait(empty(s), ((i / S) & 1) ^ 1, abort_flag, &g_tc_status))) break;
-        mbar_expect_tx(full_b(s), L::kB);
-        tma_load_2d(sbase + L::b_off + s * L::kB, &tm_x, full_b(s), (g_begin + i) * 64, (int32_t)t0);
-        last_b = i;
+        mbar_expect_tx(full(s), L::kB);
+        tma_load_2d(sbase + L::b_off + s * L::kB, &tm_x, full(s), (g_begin + i) * 64, (int32_t)t0);
+        last = i;
       }
       if (!ok)  // let every copy already issued land before shared memory is released
-        for (int i = (last_b - S + 1 > 0 ? last_b - S + 1 : 0); i <= last_b; ++i)
-          mbar_drain(full_b(i % S), (i / S) & 1);
+        for (int i = (last - S + 1 > 0 ? last - S + 1 : 0); i <= last; ++i) mbar_drain(full(i % S), (i / S) & 1);
     } else if (warp == 2 && lane == 0) {
       // ----------------------------------------------------------- TMA producer: code plane stages
       const int nws = (ng + kGroupsPerW - 1) / kGroupsPerW;
-      int last_w = -1;
+      int last = -1;
       bool ok = true;
       for (int ws = 0; ws < nws; ++ws) {
         const int slot = ws % SW;
@@ -173,61 +175,83 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
         mbar_expect_tx(w_full(slot), kWBytes);
         tma_load_2d(sbase + L::w_off + slot * kWBytes, &tm_codes, w_full(slot), (g_begin + ws * kGroupsPerW) * 32,
                     (int32_t)m0);
-        last_w = ws;
+        last = ws;
       }
       if (!ok)
-        for (int ws = (last_w - SW + 1 > 0 ? last_w - SW + 1 : 0); ws <= last_w; ++ws)
+        for (int ws = (last - SW + 1 > 0 ? last - SW + 1 : 0); ws <= last; ++ws)
           mbar_drain(w_full(ws % SW), (ws / SW) & 1);
     } else if (warp == 1 && lane == 0) {
       // ----------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc = idesc_kind_f16(kTileM, BN, 1);  // bf16 x bf16 -> f32
+      const uint64_t a_desc0 = sw128_desc(sbase + L::a_off), b_desc0 = sw128_desc(sbase + L::b_off);
       for (int i = 0; i < ng; ++i) {
         const int s = i % S, buf = i & 1;
-        const uint32_t par = (i / S) & 1;
-        if (!mbar_wait(full_a(s), par, abort_flag, &g_tc_status)) break;
-        if (!mbar_wait(full_b(s), par, abort_flag, &g_tc_status)) break;
+        if (!mbar_wait(full(s), (i / S) & 1, abort_flag, &g_tc_status)) break;
         if (i >= 2 && !mbar_wait(tmem_free(buf), ((i >> 1) - 1) & 1, abort_flag, &g_tc_status)) break;
         tc_fence_after();
-        const uint32_t a_addr = sbase + L::a_off + s * kABytes;
-        const uint32_t b_addr = sbase + L::b_off + s * L::kB;
+        // descriptor start address advances in 16-byte units: stage offsets and the 32-byte K steps
+        const uint64_t a_desc = a_desc0 + (uint64_t)((s * kABytes) >> 4);
+        const uint64_t b_desc = b_desc0 + (uint64_t)((s * L::kB) >> 4);
         const uint32_t d = tmem_base + (uint32_t)(buf * BN);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_f16(d, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32), idesc, kk != 0);
+        for (int kk = 0; kk < 4; ++kk) mma_f16(d, a_desc + 2 * kk, b_desc + 2 * kk, idesc, kk != 0);
         mma_commit(empty(s));
         mma_commit(mma_done(buf));
       }
     }
-    __syncwarp();  // reconverge lane 0 (producer / MMA) with the rest of its warp
+    __syncwarp();
     if (splitk > 1) {  // the accumulate warpgroups reduce between these two cluster barriers
       cluster_sync();
       cluster_sync();
     }
-  } else if (wg == 1) {
-    setmaxnreg_dec<kRegsLow>();
-    // ------------------------------------------------------------- decode
-    const int r = (warp - 4) * 32 + lane;  // tile row
-    for (int i = 0; i < ng; ++i) {
-      const int ws = i / kGroupsPerW, gi = i % kGroupsPerW, slot = ws % SW;
-      if (gi == 0 && !warp_wait(w_full(slot), (ws / SW) & 1, abort_flag, &g_tc_status)) break;
-      const int s = i % S;
-      if (!warp_wait(empty(s), ((i / S) & 1) ^ 1, abort_flag, &g_tc_status)) break;
-      const uint32_t csrc = sbase + L::w_off + slot * kWBytes + r * 128;
-      const uint4 c0 = ld_shared_v4(csrc + (((2 * gi) ^ (r & 7)) << 4));
-      const uint4 c1 = ld_shared_v4(csrc + (((2 * gi + 1) ^ (r & 7)) << 4));
-      const uint32_t adst = sbase + L::a_off + s * kABytes + r * 128;
-      const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-      uint4 dec[8];  // decode all eight words before storing: the stores are compiler barriers
-#pragma unroll
-      for (int j = 0; j < 8; ++j) dec[j] = decode_word_bf16(words[j]);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) st_shared_v4(adst + ((j ^ (r & 7)) << 4), dec[j]);
-      fence_proxy_async();
-      __syncwarp();
+    if (warp == 1) {
+      // ----------------------------------------------------------- teardown: release TMEM once the
+      // accumulate warps are done with it (they arrive on `done` after their last tcgen05.ld)
       if (lane == 0) {
-        mbar_arrive(full_a(s));
-        if (gi == kGroupsPerW - 1 || i == ng - 1) mbar_arrive(w_empty(slot));
+        mbar_drain(done_bar, 0);
+        if (*abort_flag) {  // MMAs in flight must finish before TMEM is released
+          mbar_drain(mma_done(0), 0);
+          mbar_drain(mma_done(1), 0);
+        }
       }
+      __syncwarp();
+      tc_fence_after();
+      tmem_dealloc(tmem_base, L::tmem_cols);
+    }
+  } else if (wg == 1) {
+    setmaxnreg_dec<kRegsDec>();
+    // ------------------------------------------------------------- decode
+    // One code stage (4 groups of this thread's row) per outer iteration; each
+    // group is released to the MMA as soon as it is written.
+    const int r = (warp - 4) * 32 + lane;  // tile row
+    const int nws = (ng + kGroupsPerW - 1) / kGroupsPerW;
+    bool ok = true;
+    for (int ws = 0; ws < nws && ok; ++ws) {
+      const int slot = ws % SW;
+      if (!(ok = warp_wait(w_full(slot), (ws / SW) & 1, abort_flag, &g_tc_status))) break;
+      const uint32_t csrc = sbase + L::w_off + slot * kWBytes + r * 128;
+      uint4 cw[2 * kGroupsPerW];
+#pragma unroll
+      for (int c = 0; c < 2 * kGroupsPerW; ++c) cw[c] = ld_shared_v4(csrc + ((c ^ (r & 7)) << 4));
+      const int gcount = (ng - ws * kGroupsPerW < kGroupsPerW) ? (ng - ws * kGroupsPerW) : kGroupsPerW;
+#pragma unroll
+      for (int gi = 0; gi < kGroupsPerW; ++gi) {
+        if (gi >= gcount) break;
+        const int i = ws * kGroupsPerW + gi, s = i % S;
+        if (!(ok = warp_wait(empty(s), ((i / S) & 1) ^ 1, abort_flag, &g_tc_status))) break;
+        const uint32_t adst = sbase + L::a_off + s * kABytes + r * 128;
+        const uint32_t words[8] = {cw[2 * gi].x,     cw[2 * gi].y,     cw[2 * gi].z,     cw[2 * gi].w,
+                                   cw[2 * gi + 1].x, cw[2 * gi + 1].y, cw[2 * gi + 1].z, cw[2 * gi + 1].w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) st_shared_v4(adst + ((j ^ (r & 7)) << 4), decode_word_bf16(words[j]));
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(full(s));
+      }
+      // Release the code stage only after its bytes were consumed: a TMA (async proxy) refill
+      // must not race the shared-memory reads above.
+      __syncwarp();
+      if (lane == 0) mbar_arrive(w_empty(slot));
     }
     __syncwarp();
     if (splitk > 1) {
@@ -235,11 +259,11 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
       cluster_sync();
     }
   } else {
-    setmaxnreg_inc<kRegsHigh>();
+    setmaxnreg_inc<kRegsAcc>();
     // ------------------------------------------------------------- accumulate
-    const int quad = warp & 3;            // TMEM lane quadrant
-    const int chalf = (warp - 8) >> 2;    // column half
-    const int r_acc = quad * 32 + lane;   // tile row
+    const int quad = warp & 3;                  // TMEM lane quadrant
+    const int cq = (warp - 8) >> 2;             // column quarter
+    const int r_acc = quad * 32 + lane;         // tile row
     float2 acc[kCols / 2];
 #pragma unroll
     for (int i = 0; i < kCols / 2; ++i) acc[i] = make_float2(0.f, 0.f);
@@ -253,7 +277,8 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
       s_cur[j] = 0;
       s_nxt[j] = (row_ok && j < ng) ? srow[g_begin + j] : (uint16_t)0;
     }
-    const uint32_t tlane = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(chalf * kCols);
+    const uint32_t tlane = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(cq * kCols);
+    constexpr int kLd = kCols >= 16 ? 16 : kCols;    // columns per tcgen05.ld
     for (int i = 0; i < ng; ++i) {
       const int buf = i & 1, gi = i % kGroupsPerW;
       if (gi == 0) {
@@ -272,14 +297,14 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
       if (!(acc_ok = warp_wait(mma_done(buf), (i >> 1) & 1, abort_flag, &g_tc_status))) break;
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < kCols; c += kChunk) {
-        uint32_t v[kChunk];
-        if constexpr (kChunk == 32) tmem_ld32(tlane + buf * BN + c, v);
-        else if constexpr (kChunk == 16) tmem_ld16(tlane + buf * BN + c, v);
-        else tmem_ld8(tlane + buf * BN + c, v);
+      for (int c = 0; c < kCols; c += kLd) {
+        uint32_t v[kLd];
+        if constexpr (kLd == 16) tmem_ld16(tlane + buf * BN + c, v);
+        else if constexpr (kLd == 8) tmem_ld8(tlane + buf * BN + c, v);
+        else tmem_ld4(tlane + buf * BN + c, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < kChunk; j += 2)
+        for (int j = 0; j < kLd; j += 2)
           acc[(c + j) / 2] =
               ffma2(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), s2, acc[(c + j) / 2]);
       }
@@ -296,7 +321,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
         const uint32_t remote0 = mapa_shared(sbase, 0);
 #pragma unroll
         for (int c = 0; c < kCols; c += 4) {
-          const uint32_t off = (((crank - 1) * (BN / 4) + (chalf * kCols + c) / 4) * kTileM + r_acc) * 16;
+          const uint32_t off = (((crank - 1) * (BN / 4) + (cq * kCols + c) / 4) * kTileM + r_acc) * 16;
           st_cluster_v4(remote0 + off, acc[c / 2].x, acc[c / 2].y, acc[c / 2 + 1].x, acc[c / 2 + 1].y);
         }
       }
@@ -306,7 +331,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
         for (int q = 1; q < splitk; ++q) {
 #pragma unroll
           for (int c = 0; c < kCols; c += 4) {
-            const uint32_t off = (((q - 1) * (BN / 4) + (chalf * kCols + c) / 4) * kTileM + r_acc) * 16;
+            const uint32_t off = (((q - 1) * (BN / 4) + (cq * kCols + c) / 4) * kTileM + r_acc) * 16;
             const float4 v = ld_shared_f4(sbase + off);
             acc[c / 2] = fadd2(acc[c / 2], make_float2(v.x, v.y));
             acc[c / 2 + 1] = fadd2(acc[c / 2 + 1], make_float2(v.z, v.w));
@@ -319,24 +344,14 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
     if (crank == 0 && acc_ok && !*abort_flag && row_ok) {
 #pragma unroll
       for (int j = 0; j < kCols; ++j) {
-        const int64_t t = t0 + chalf * kCols + j;
+        const int64_t t = t0 + cq * kCols + j;
         const float v = (j & 1) ? acc[j / 2].y : acc[j / 2].x;
         if (t < p.T) p.y[t * p.N + row] = float_to_bf16_bits(v);
       }
     }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    if (*abort_flag && lane == 0) {
-      // MMAs in flight must finish before TMEM is released: wait for the last commits.
-      mbar_drain(mma_done(0), 0);
-      mbar_drain(mma_done(1), 0);
-    }
+    tc_fence_before();
     __syncwarp();
-    tc_fence_after();
-    tmem_dealloc(tmem_base, L::tmem_cols);
+    if (lane == 0) mbar_arrive(done_bar);
   }
 }
 
