@@ -126,22 +126,23 @@ q4_gemv_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict__ scal
 
 // ---------------------------------------------------------------------------
 // Single-token streaming GEMV.  One persistent CTA per SM owns a contiguous
-// range of rows (balanced to one row).  A producer warp streams the rows'
-// code bytes into a ring of shared-memory slots with 1-D bulk async copies
-// (4 rows per copy), so the CTA's share is in flight from the start.
+// range of rows (balanced to one row).  Thread 0 first copies x into shared
+// memory (one bulk copy per CTA), then streams the rows' code bytes into a ring
+// of shared-memory slots with 1-D bulk async copies (8 rows per copy), so the
+// CTA's share is in flight from the start.
 //
 // K is cut into column groups of 32 chunks (a chunk = 16 code bytes = 32
 // weights = half a scale group); warp j of a row stream owns column group j,
 // so lane l always handles chunk 32 j + l: its 32 x values (and their sum)
-// are loaded once from global memory and stay in registers for every row.
-// Per 4-row slot a warp reads one conflict-free 16-byte code chunk per row,
+// are read once from the shared copy of x and stay in registers for every row.
+// Per 8-row slot a warp reads one conflict-free 16-byte code chunk per row,
 // decodes it to (128 + q) floats with byte permutes, accumulates with packed
 // FP32 FMAs, applies (partial - 136 * sum x) * s, and reduces across the warp.
 // The NJ column-group partials of a row are summed in a fixed order at the end
 // (deterministic), then rounded to bf16.
 constexpr int kBulkThreads = 512;
 constexpr int kBulkConsumers = 15;   // warps 1..15
-constexpr int kBulkRows = 4;
+constexpr int kBulkRows = 8;
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
@@ -150,15 +151,17 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 }
 
 struct StreamLayout {
-  uint32_t part_off, bar_off, slot_off, slot_bytes, bytes;
+  uint32_t x_off, part_off, bar_off, slot_off, slot_bytes, bytes;
 };
 
-// partial sums [rows_cap][nj] fp32, then full/empty barriers, then the slots (128-byte aligned)
+// x (bf16, K elements), partial sums [rows_cap][nj] fp32, the x barrier and the
+// full/empty barriers, then the slots (128-byte aligned)
 __host__ __device__ inline StreamLayout stream_layout(int64_t K, int64_t rows_cap, int nj, int slots) {
   StreamLayout L;
-  L.part_off = 0;
-  L.bar_off = (uint32_t)((rows_cap * nj * 4 + 15) / 16 * 16);
-  L.slot_off = (L.bar_off + (uint32_t)slots * 16 + 127) / 128 * 128;
+  L.x_off = 0;
+  L.part_off = (uint32_t)(K * 2);
+  L.bar_off = (uint32_t)((L.part_off + rows_cap * nj * 4 + 15) / 16 * 16);
+  L.slot_off = (L.bar_off + 8 + (uint32_t)slots * 16 + 127) / 128 * 128;
   L.slot_bytes = (uint32_t)(kBulkRows * (K / 2));
   L.bytes = L.slot_off + (uint32_t)slots * L.slot_bytes;
   return L;
@@ -172,17 +175,19 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
   const StreamLayout L = stream_layout(K, rows_cap, nj, slots);
   float* part = reinterpret_cast<float*>(smem + L.part_off);
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t full0 = sbase + L.bar_off, empty0 = full0 + 8u * slots;
+  const uint32_t xbar = sbase + L.bar_off;
+  const uint32_t full0 = xbar + 8, empty0 = full0 + 8u * slots;
   __shared__ int abort_word;
   volatile int* abort_flag = &abort_word;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // 4-row blocks are dealt round-robin: CTA c owns global blocks c, c + G, c + 2G, ...
-  // so at any moment the whole GPU streams one contiguous window of the code plane.
-  const int64_t nblk = (N + kBulkRows - 1) / kBulkRows;
-  const int nb = (int)((nblk - blockIdx.x + gridDim.x - 1) / gridDim.x);
-  auto blk_row = [&](int b) { return ((int64_t)b * gridDim.x + blockIdx.x) * kBulkRows; };
-  auto blk_rows = [&](int b) { const int64_t ra = blk_row(b); return (int)((N - ra < kBulkRows) ? (N - ra) : kBulkRows); };
+  // CTA c owns the contiguous rows [c N / G, (c+1) N / G), balanced to one row, in
+  // blocks of kBulkRows (the last one may be shorter).
+  const int64_t r0 = (int64_t)blockIdx.x * N / gridDim.x;
+  const int64_t r1 = (int64_t)(blockIdx.x + 1) * N / gridDim.x;
+  const int nb = (int)((r1 - r0 + kBulkRows - 1) / kBulkRows);
+  auto blk_row = [&](int b) { return r0 + (int64_t)b * kBulkRows; };
+  auto blk_rows = [&](int b) { const int64_t ra = blk_row(b); return (int)((r1 - ra < kBulkRows) ? (r1 - ra) : kBulkRows); };
   const int64_t row_bytes = K / 2, groups = K / 64, nchunk = K / 32;
   const int streams = kBulkConsumers / nj;   // row streams; warp (j, stream) = 1 + stream * nj + j
 
@@ -190,12 +195,17 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
   // so the loads start while the other warps are still being set up.
   const int first = nb < slots ? nb : slots;
   if (threadIdx.x == 0) {
+    mbar_init(xbar, 1);
     for (int s = 0; s < first; ++s) {
       mbar_init(full0 + 8u * s, 1);
       mbar_init(empty0 + 8u * s, nj);   // one arrival per column-group warp
     }
     abort_word = 0;
     fence_mbar_init();
+    // x first (one copy per CTA: every warp reading it from global memory would hammer
+    // the same few L2 lines from every SM at once), then the weight blocks
+    mbar_expect_tx(xbar, (uint32_t)(K * 2));
+    bulk_g2s(sbase + L.x_off, x, (uint32_t)(K * 2), xbar);
     for (int b = 0; b < first; ++b) {
       const int64_t ra = blk_row(b);
       const uint32_t bytes = (uint32_t)(blk_rows(b) * row_bytes);
@@ -219,9 +229,11 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
       }
       __syncwarp();
     }
-    if (b < nb && lane == 0)  // aborted: let the copies already issued land before the CTA exits
+    if (b < nb && lane == 0) {  // aborted: let the copies already issued land before the CTA exits
+      mbar_drain(xbar, 0);
       for (int d = (b - slots > 0 ? b - slots : 0); d < b; ++d)
         mbar_drain(full0 + 8u * (d % slots), (d / slots) & 1);
+    }
     __syncwarp();
   } else if (warp - 1 < streams * nj) {
     const int j = (warp - 1) % nj, stream = (warp - 1) / nj;
@@ -230,9 +242,11 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
     // this lane's 32 x values and their sum, kept in registers for every row
     float2 xv[16];
     float xsum = 0.f;
+    const bool x_ok = warp_wait(xbar, 0, abort_flag, &g_gemv_status);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const uint4 v = c_ok ? ld_nc_u4(x + c * 32 + q * 8) : make_uint4(0, 0, 0, 0);
+      const uint4 v = (c_ok && x_ok) ? ld_shared_v4(sbase + L.x_off + (uint32_t)(c * 64 + q * 16))
+                                     : make_uint4(0, 0, 0, 0);
       xv[4 * q + 0] = make_float2(bf16lo(v.x), bf16hi(v.x));
       xv[4 * q + 1] = make_float2(bf16lo(v.y), bf16hi(v.y));
       xv[4 * q + 2] = make_float2(bf16lo(v.z), bf16hi(v.z));
@@ -313,10 +327,10 @@ static bool stream_plan(int64_t N, int64_t K, int nsm, StreamPlan* p) {
   const int64_t nchunk = K / 32;
   p->nj = (int)((nchunk + 31) / 32);
   if (p->nj > kBulkConsumers) return false;
-  p->grid = (N + kBulkRows - 1) / kBulkRows;
+  p->grid = (N + 3) / 4;  // at least 4 rows per CTA
   if (p->grid > nsm) p->grid = nsm;
   if (p->grid < 1) p->grid = 1;
-  p->rows_cap = ((N + kBulkRows - 1) / kBulkRows + p->grid - 1) / p->grid * kBulkRows;
+  p->rows_cap = ((N + p->grid - 1) / p->grid + kBulkRows - 1) / kBulkRows * kBulkRows;
   const int64_t budget = 232448 - 1024;
   const StreamLayout L0 = stream_layout(K, p->rows_cap, p->nj, 0);
   const int64_t per = (int64_t)kBulkRows * (K / 2) + 16;

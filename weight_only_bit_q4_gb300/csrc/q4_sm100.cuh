@@ -52,11 +52,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   return false;
 }
 
-// Warp-uniform form of mbar_wait: every lane of the warp gets the same answer,
-// so warp-collective instructions after it stay convergent.
+// Warp-uniform form of mbar_wait: lane 0 polls (one barrier query instead of
+// 32), the warp reconverges and every lane gets lane 0's answer.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
-  const bool ok = mbar_wait(bar, parity, abort_flag, status);
-  return __all_sync(0xffffffffu, ok);
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, status);
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+// Named hardware barrier over `nthreads` threads (a multiple of 32): waiting
+// warps sleep in hardware instead of polling.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // Bounded wait used while tearing down after an abort (ignores the flag).
