@@ -48,8 +48,9 @@ struct TcParams {
 };
 
 // Warpgroup roles (setmaxnreg works per warpgroup of 4 consecutive warps):
-//   wg0: warp 0 TMA producer (X tiles), warp 1 TMEM owner + MMA issuer,
-//        warp 2 TMA producer (code plane), warp 3 idle
+//   wg0: warp 0 TMA producer (X tiles), warp 1 TMEM owner + MMA issuer of the
+//        even groups, warp 2 TMA producer (code plane), warp 3 MMA issuer of
+//        the odd groups
 //   wg1: decode, one thread per tile row, one whole code stage per iteration
 //   wg2..wg5: FP32 accumulation of the scaled group partials and the
 //        epilogue; warp w reads TMEM lane quadrant w % 4 and column quarter
@@ -74,8 +75,8 @@ struct TcSmem {
   static constexpr uint32_t b_off = a_off + S * kABytes;
   static constexpr uint32_t w_off = b_off + S * kB;
   static constexpr uint32_t bar_off = w_off + SW * kWBytes;
-  // full[S], empty[S], w_full[SW], w_empty[SW], mma_done[2], tmem_free[2], done
-  static constexpr uint32_t n_bars = 2 * S + 2 * SW + 5;
+  // full[S], empty[S], w_full[SW], w_empty[SW], mma_done[2], tmem_free[2], done, mma_fin
+  static constexpr uint32_t n_bars = 2 * S + 2 * SW + 6;
   static constexpr uint32_t misc_off = bar_off + n_bars * 8;
   static constexpr uint32_t bytes = misc_off + 16;
   static constexpr uint32_t alloc = bytes + 1024;  // slack for 1024-byte alignment
@@ -103,6 +104,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
   auto mma_done = [&](int b) { return bars + 8u * (2 * S + 2 * SW + b); };
   auto tmem_free = [&](int b) { return bars + 8u * (2 * S + 2 * SW + 2 + b); };
   const uint32_t done_bar = bars + 8u * (2 * S + 2 * SW + 4);
+  const uint32_t fin_bar = bars + 8u * (2 * S + 2 * SW + 5);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
 
@@ -137,6 +139,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
       mbar_init(tmem_free(b), kAccWarps);
     }
     mbar_init(done_bar, kAccWarps);
+    mbar_init(fin_bar, 2);  // one final commit per MMA issuer
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_codes);
@@ -180,12 +183,18 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
       if (!ok)
         for (int ws = (last - SW + 1 > 0 ? last - SW + 1 : 0); ws <= last; ++ws)
           mbar_drain(w_full(ws % SW), (ws / SW) & 1);
-    } else if (warp == 1 && lane == 0) {
-      // ----------------------------------------------------------- MMA issuer
+    } else if ((warp == 1 || warp == 3) && lane == 0) {
+      // ----------------------------------------------------------- MMA issuers
+      // Group i goes to TMEM buffer i & 1 and is issued by warp 1 (even i) or warp 3
+      // (odd i).  A thread's first shared-memory access after a tcgen05.commit waits
+      // for the MMAs that commit covers, so one thread issuing every group would
+      // leave the tensor pipe idle for the completion latency of each group; with
+      // two issuers the next group is already queued while the current one drains.
       constexpr uint32_t idesc = idesc_kind_f16(kTileM, BN, 1);  // bf16 x bf16 -> f32
       const uint64_t a_desc0 = sw128_desc(sbase + L::a_off), b_desc0 = sw128_desc(sbase + L::b_off);
-      for (int i = 0; i < ng; ++i) {
-        const int s = i % S, buf = i & 1;
+      const int buf = warp == 1 ? 0 : 1;
+      for (int i = buf; i < ng; i += 2) {
+        const int s = i % S;
         if (!mbar_wait(full(s), (i / S) & 1, abort_flag, &g_tc_status)) break;
         if (i >= 2 && !mbar_wait(tmem_free(buf), ((i >> 1) - 1) & 1, abort_flag, &g_tc_status)) break;
         tc_fence_after();
@@ -198,6 +207,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
         mma_commit(empty(s));
         mma_commit(mma_done(buf));
       }
+      mma_commit(fin_bar);  // arrives once every MMA this thread issued has completed
     }
     __syncwarp();
     if (splitk > 1) {  // the accumulate warpgroups reduce between these two cluster barriers
@@ -209,10 +219,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
       // accumulate warps are done with it (they arrive on `done` after their last tcgen05.ld)
       if (lane == 0) {
         mbar_drain(done_bar, 0);
-        if (*abort_flag) {  // MMAs in flight must finish before TMEM is released
-          mbar_drain(mma_done(0), 0);
-          mbar_drain(mma_done(1), 0);
-        }
+        mbar_drain(fin_bar, 0);  // no MMA may still be writing TMEM when it is released
       }
       __syncwarp();
       tc_fence_after();
@@ -388,6 +395,54 @@ bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint6
 }
 
 template <int BN, int S, int SW>
+int set_kernel_attrs() {
+  using L = TcSmem<BN, S, SW>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  if (cuda_check(cudaGetDevice(&dev), "cudaGetDevice")) return Q4LIN_ERR_CUDA;
+  if (dev < 64 && attr_set[dev]) return Q4LIN_OK;
+  if (cuda_check(cudaFuncSetAttribute(q4_tc_kernel<BN, S, SW>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc),
+                 "tc: cudaFuncSetAttribute(max dynamic shared memory)"))
+    return Q4LIN_ERR_CUDA;
+  if (cuda_check(cudaFuncSetAttribute(q4_tc_kernel<BN, S, SW>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+                 "tc: cudaFuncSetAttribute(cluster size)"))
+    return Q4LIN_ERR_CUDA;
+  if (dev < 64) attr_set[dev] = true;
+  return Q4LIN_OK;
+}
+
+// How many clusters of `size` CTAs of this kernel can be resident at once (0 on
+// error).  Clusters are placed within one GPC, so this is below sms / size when
+// the GPCs' SM counts are not multiples of the cluster size.
+template <int BN, int S, int SW>
+int resident_clusters(int size) {
+  using L = TcSmem<BN, S, SW>;
+  static int cache[64][9] = {};
+  int dev = 0;
+  if (size < 1 || size > 8 || cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < 64 && cache[dev][size]) return cache[dev][size];
+  if (set_kernel_attrs<BN, S, SW>() != Q4LIN_OK) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, 1, (unsigned)size);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = L::alloc;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = (unsigned)size;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, q4_tc_kernel<BN, S, SW>, &cfg) != cudaSuccess || n < 0) {
+    cudaGetLastError();
+    n = 0;
+  }
+  if (dev < 64 && n > 0) cache[dev][size] = n;
+  return n;
+}
+
+template <int BN, int S, int SW>
 int launch_tile(const LinearArgs& a, int splitk) {
   using L = TcSmem<BN, S, SW>;
   static_assert(L::alloc <= 232448, "shared memory budget");
@@ -395,19 +450,7 @@ int launch_tile(const LinearArgs& a, int splitk) {
     set_error_detail("tc: split-K factor out of range for this tile");
     return Q4LIN_ERR_INVALID_ARG;
   }
-  static bool attr_set[64] = {};
-  int dev = 0;
-  if (cuda_check(cudaGetDevice(&dev), "cudaGetDevice")) return Q4LIN_ERR_CUDA;
-  if (dev >= 64 || !attr_set[dev]) {
-    if (cuda_check(cudaFuncSetAttribute(q4_tc_kernel<BN, S, SW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        L::alloc),
-                   "tc: cudaFuncSetAttribute(max dynamic shared memory)"))
-      return Q4LIN_ERR_CUDA;
-    if (cuda_check(cudaFuncSetAttribute(q4_tc_kernel<BN, S, SW>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0),
-                   "tc: cudaFuncSetAttribute(cluster size)"))
-      return Q4LIN_ERR_CUDA;
-    if (dev < 64) attr_set[dev] = true;
-  }
+  if (const int rc = set_kernel_attrs<BN, S, SW>()) return rc;
   CUtensorMap tm_codes, tm_x;
   if (!make_map_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.wq, (uint64_t)(a.K / 2), (uint64_t)a.N,
                    (uint64_t)(a.K / 2), 128, kTileM) ||
@@ -442,6 +485,16 @@ int max_splitk_for(int bn) {
   }
 }
 
+int resident_clusters_for(int bn, int size) {
+  switch (bn) {
+    case 256: return resident_clusters<256, 4, 2>(size);
+    case 128: return resident_clusters<128, 5, 3>(size);
+    case 64: return resident_clusters<64, 6, 4>(size);
+    case 32: return resident_clusters<32, 6, 6>(size);
+    default: return resident_clusters<16, 6, 6>(size);
+  }
+}
+
 int sm_count() {
   static int cached[64] = {};
   int dev = 0;
@@ -465,17 +518,26 @@ TcPlan tc_plan(int route, int64_t N, int64_t K, int64_t T, int sms) {
   else pl.bn = 16;
   pl.splitk = 1;
   if (route == Q4LIN_ROUTE_TC_SPLITK) {
-    // split K across a cluster until the CTA count fills whole waves of the GPU
+    // Split K across a cluster so that the CTAs fill the GPU in as few, as full
+    // waves as possible.  A wave holds as many clusters as can be resident at
+    // once (queried; without a device, sms / size).
     const int64_t tiles = ((N + kTileM - 1) / kTileM) * ((T + pl.bn - 1) / pl.bn);
     const int64_t nk = K / 64;
     double best = -1.0;
     const int smax = max_splitk_for(pl.bn) < 8 ? max_splitk_for(pl.bn) : 8;
     for (int s = 1; s <= smax && s <= nk; ++s) {
-      const int64_t ctas = tiles * s;
-      const int64_t waves = (ctas + sms - 1) / sms;
-      const double eff = (double)ctas / (double)(waves * sms);
-      if (eff > best + 1e-9) {
-        best = eff;
+      int64_t per_wave = sms / s;
+      if (s > 1) {
+        const int q = resident_clusters_for(pl.bn, s);
+        if (q > 0 && q < per_wave) per_wave = q;
+      }
+      if (per_wave < 1) continue;
+      const int64_t waves = (tiles + per_wave - 1) / per_wave;
+      // time ~ waves x (K share of one CTA + a fixed cost per CTA of about six
+      // groups: launch, first loads, epilogue); prefer fewer splits on ties
+      const double cost = (double)waves * ((double)nk / (double)s + 6.0);
+      if (best < 0 || cost < best - 1e-9) {
+        best = cost;
         pl.splitk = s;
       }
     }
