@@ -1,6 +1,6 @@
 // Tensor-core route of the Q4_G64_FP16 linear layer: TMA -> on-chip decode ->
-// tcgen05.mma (kind::f16, bf16 operands) with per-group accumulators in tensor
-// memory and the group scales applied in FP32.
+// tcgen05.mma (kind::f16, bf16 operands) with per-group accumulators in
+// tensor memory and the group scales applied in FP32.
 //
 // This is the tiled-MMA route of the Q4 linear measurement report
 // (q4-linear.md, route notes: BF16 input, FP32-accumulating dense MMA for the
@@ -12,11 +12,15 @@
 //   * two TMA producer threads stream the packed code plane (128-byte swizzle,
 //     4 groups per stage) and the bf16 token tile of X straight from the
 //     caller's buffer (128-byte swizzle, one 64-wide group per stage);
-//   * a decode warpgroup turns each group's codes into the exact bf16 values
-//     q - 8, written in the MMA's 128-byte-swizzled K-major A layout;
-//   * one thread issues 4 x tcgen05.mma (K = 16) per group into one of two
-//     TMEM buffers, D_g[n, t] = sum_{k in g} (q[n,k] - 8) x[t,k];
-//   * four accumulate warpgroups read D_g back (tcgen05.ld) and add
+//   * two decode warpgroups ("teams") take alternate groups and turn each
+//     group's codes into the exact bf16 values q - 8: written into a
+//     tensor-memory A stage with tcgen05.st where tensor memory has room
+//     (token tiles up to 128 wide), else into a 128-byte-swizzled
+//     shared-memory A stage;
+//   * one MMA issuer thread issues 4 x tcgen05.mma (K = 16) per group into a
+//     tensor-memory accumulator buffer,
+//     D_g[n, t] = sum_{k in g} (q[n,k] - 8) x[t,k];
+//   * the accumulate warpgroups read D_g back (tcgen05.ld) and add
 //     s[n,g] * D_g[n,t] to FP32 registers, then round to bf16 and store Y[t, n].
 //
 // Every product (q - 8) * x is exact in FP32 and the group scale multiplies
@@ -25,9 +29,30 @@
 // (q - 8) * s to 11 bits -- about 2e-4 of rms(y) -- which brushes the layer's
 // 1e-3 rms accuracy floor on large outputs; bf16 folding misses it outright.)
 //
+// Synchronisation, shaped by what the hardware charges for it:
+//   * while the tensor core streams its shared-memory operands an mbarrier
+//     wait costs a few hundred cycles even when the phase has long completed,
+//     and a thread with tcgen05.mma operations in flight pays that on every
+//     shared-memory access; so the issuer never touches shared memory.  The
+//     decode team of group i (after writing its A stage and seeing its X tile
+//     land) and every accumulate warp (after reading back the accumulator
+//     buffer that group i will overwrite) arrive on a hardware named barrier,
+//     on which the issuer waits;
+//   * tcgen05.mma is issued by that one thread only (concurrent issue from two
+//     threads corrupted results);
+//   * one tcgen05.commit per group, into a ring of mbarriers that everything
+//     downstream waits on: the X producer and the decode team (the group's X
+//     and A stages are free again) and the accumulate warps (D_i is ready);
+//   * a parity wait cannot tell phase k from phase k + 2, so no waiter may fall
+//     two phases behind: the rings cover every buffer ring, and the A and X
+//     rings have even depths so that each slot belongs to one decode team;
+//   * named barriers cannot time out, so every role keeps arriving on them for
+//     every group even after an abort: the issuer always runs to completion.
+//
 // Every mbarrier wait is bounded: on expiry the kernel records
-// Q4LIN_ERR_TIMEOUT in its device error word, drains what it issued (again
-// bounded) and exits instead of hanging.
+// Q4LIN_ERR_TIMEOUT in its device error word, skips the remaining work
+// (still arriving where others wait), drains what it issued (again bounded)
+// and exits instead of hanging.
 #include <mutex>
 
 #include "q4_internal.h"
@@ -47,64 +72,98 @@ struct TcParams {
   int splitk;  // CTAs of a cluster sharing one output tile along K (1 = no split)
 };
 
-// Warpgroup roles (setmaxnreg works per warpgroup of 4 consecutive warps):
-//   wg0: warp 0 TMA producer (X tiles), warp 1 TMEM owner + MMA issuer of the
-//        even groups, warp 2 TMA producer (code plane), warp 3 MMA issuer of
-//        the odd groups
-//   wg1: decode, one thread per tile row, one whole code stage per iteration
-//   wg2..wg5: FP32 accumulation of the scaled group partials and the
-//        epilogue; warp w reads TMEM lane quadrant w % 4 and column quarter
-//        (w - 8) / 4, one thread per (row, column quarter)
-constexpr int kThreads = 768;
-constexpr int kAccWarps = 16;
 constexpr int kTileM = 128;
-constexpr int kGroupsPerW = 4;               // code stage: 128 rows x 128 bytes = 4 groups
-constexpr uint32_t kABytes = kTileM * 128;   // one group of A: 128 rows x 64 bf16
-constexpr uint32_t kWBytes = kTileM * 128;   // one code stage
-constexpr int kRegsLaunch = 80;              // 65536 / 768, rounded down to a multiple of 8
-constexpr int kRegsCtl = 40;                 // wg0
-constexpr int kRegsDec = 56;                 // wg1
-constexpr int kRegsAcc = 96;                 // wg2..wg5
-static_assert(128 * (kRegsCtl + kRegsDec) + 512 * kRegsAcc == kThreads * kRegsLaunch,
-              "register split must equal the launch allocation");
+constexpr int kGroupsPerW = 4;              // code stage: 128 rows x 128 bytes = 4 groups
+constexpr uint32_t kWBytes = kTileM * 128;  // one code stage
+constexpr uint32_t kABytes = kTileM * 128;  // one shared-memory A stage: 128 rows x 64 bf16
+constexpr int kRing = 8;                    // depth of the per-group MMA-done / issue rings
+constexpr uint32_t kIssueBar0 = 1;          // named barriers kIssueBar0 .. kIssueBar0 + kRing - 1
 
-template <int BN, int S, int SW>
+// Per token-tile width: X stages, A stages, accumulator buffers, accumulate
+// warpgroups, code stages and where A lives.  Tensor memory holds NB * BN
+// accumulator columns, followed (A in tensor memory) by SA * 32 A columns.
+template <int BN> struct TcCfg;
+template <> struct TcCfg<256> { static constexpr int SX = 4, SA = 4, NB = 2, NACC = 4, SW = 2; static constexpr bool kATmem = false; };
+template <> struct TcCfg<128> { static constexpr int SX = 8, SA = 8, NB = 2, NACC = 4, SW = 4; static constexpr bool kATmem = true; };
+template <> struct TcCfg<64> { static constexpr int SX = 8, SA = 8, NB = 4, NACC = 1, SW = 4; static constexpr bool kATmem = true; };
+template <> struct TcCfg<32> { static constexpr int SX = 8, SA = 8, NB = 8, NACC = 1, SW = 4; static constexpr bool kATmem = true; };
+template <> struct TcCfg<16> { static constexpr int SX = 8, SA = 8, NB = 8, NACC = 1, SW = 4; static constexpr bool kATmem = true; };
+
+// Warpgroup roles (setmaxnreg works per warpgroup of 4 consecutive warps):
+//   wg0: warp 0 TMA producer (X tiles), warp 1 TMA producer (code stages) and
+//        tensor-memory owner, warp 3 MMA issuer (warp 2 idles)
+//   wg1 / wg2: decode teams of the even / odd groups, one thread per tile row
+//   wg3..: FP32 accumulation of the scaled group partials and the epilogue;
+//        warp w reads TMEM lane quadrant w % 4 and column chunk (w - 12) / 4
+template <int BN>
 struct TcSmem {
+  using C = TcCfg<BN>;
+  static constexpr int SX = C::SX, SA = C::SA, NB = C::NB, NACC = C::NACC, SW = C::SW;
+  static constexpr bool kATmem = C::kATmem;
+  static_assert(SA % 2 == 0 && SX % 2 == 0, "the A and X ring depths must be even (one decode team per slot)");
+  static_assert(kRing % 2 == 0 && kRing >= SX && kRing >= SA && kRing >= NB,
+                "the barrier rings must cover every buffer ring (no waiter two phases behind)");
+  static_assert(NB * BN + (kATmem ? SA * 32 : 0) <= 512, "tensor memory budget");
+  static constexpr int threads = 128 * (3 + NACC);
+  static constexpr uint32_t issue_threads = 128 + 128 * NACC + 32;  // decode team + accumulate + issuer
   static constexpr uint32_t kB = BN * 128;  // one group of X: BN rows x 64 bf16
-  static constexpr uint32_t a_off = 0;
-  static constexpr uint32_t b_off = a_off + S * kABytes;
-  static constexpr uint32_t w_off = b_off + S * kB;
-  static constexpr uint32_t bar_off = w_off + SW * kWBytes;
-  // full[S], empty[S], w_full[SW], w_empty[SW], mma_done[2], tmem_free[2], done, mma_fin
-  static constexpr uint32_t n_bars = 2 * S + 2 * SW + 6;
+  static constexpr uint32_t x_off = 0;
+  static constexpr uint32_t a_off = x_off + SX * kB;  // shared-memory A stages (A not in tensor memory)
+  static constexpr uint32_t c_off = a_off + (kATmem ? 0 : SA * kABytes);
+  static constexpr uint32_t bar_off = c_off + SW * kWBytes;
+  // x_full[SX], c_full[SW], c_empty[SW], mma_done[kRing], done, fin
+  static constexpr uint32_t n_bars = SX + 2 * SW + kRing + 2;
   static constexpr uint32_t misc_off = bar_off + n_bars * 8;
   static constexpr uint32_t bytes = misc_off + 16;
   static constexpr uint32_t alloc = bytes + 1024;  // slack for 1024-byte alignment
-  static constexpr uint32_t tmem_cols = 2 * BN < 32 ? 32 : 2 * BN;
+  static constexpr uint32_t a_col = NB * BN;       // first A column in tensor memory
+  static constexpr uint32_t tmem_cols = 512;
   // split-K partial sums of the other CTAs of the cluster reuse the pipeline buffers
   static constexpr int max_splitk = 1 + (int)(bar_off / (kTileM * BN * 4));
 };
 
-template <int BN, int S, int SW>
-__global__ void __launch_bounds__(kThreads, 1)
+// Registers per thread after the split (four accumulate warpgroups only; with
+// one, the launch allocation of 128 per thread covers every role).  The split
+// sums to at most the launch allocation: 896 threads x 72.
+template <bool kATmem> struct TcRegs;
+template <> struct TcRegs<true> { static constexpr int ctl = 32, dec = 64, acc = 80; };
+template <> struct TcRegs<false> { static constexpr int ctl = 40, dec = 40, acc = 96; };
+static_assert(128 * TcRegs<true>::ctl + 256 * TcRegs<true>::dec + 512 * TcRegs<true>::acc <= 896 * 72, "register split");
+static_assert(128 * TcRegs<false>::ctl + 256 * TcRegs<false>::dec + 512 * TcRegs<false>::acc <= 896 * 72, "register split");
+
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* v) {
+  if constexpr (N == 16) tmem_ld16(taddr, *reinterpret_cast<uint32_t(*)[16]>(v));
+  else if constexpr (N == 8) tmem_ld8(taddr, *reinterpret_cast<uint32_t(*)[8]>(v));
+  else tmem_ld4(taddr, *reinterpret_cast<uint32_t(*)[4]>(v));
+}
+
+template <int BN>
+__global__ void __launch_bounds__(TcSmem<BN>::threads, 1)
 q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_x,
              const TcParams p) {
-  using L = TcSmem<BN, S, SW>;
-  constexpr int kCols = BN / 4;  // accumulator columns per accumulate thread
-  static_assert(kCols % 4 == 0, "BN must be a multiple of 16");
+  using L = TcSmem<BN>;
+  using R = TcRegs<L::kATmem>;
+  constexpr int SX = L::SX, SA = L::SA, NB = L::NB, NACC = L::NACC, SW = L::SW;
+  constexpr int kAccWarps = 4 * NACC;
+  constexpr int kCols = BN / NACC;  // accumulator columns per accumulate thread
+  static_assert(kCols % 4 == 0, "column chunk must be a multiple of 4");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bars = sbase + L::bar_off;
-  auto full = [&](int s) { return bars + 8u * s; };
-  auto empty = [&](int s) { return bars + 8u * (S + s); };
-  auto w_full = [&](int s) { return bars + 8u * (2 * S + s); };
-  auto w_empty = [&](int s) { return bars + 8u * (2 * S + SW + s); };
-  auto mma_done = [&](int b) { return bars + 8u * (2 * S + 2 * SW + b); };
-  auto tmem_free = [&](int b) { return bars + 8u * (2 * S + 2 * SW + 2 + b); };
-  const uint32_t done_bar = bars + 8u * (2 * S + 2 * SW + 4);
-  const uint32_t fin_bar = bars + 8u * (2 * S + 2 * SW + 5);
+  // Group i uses X slot i % SX, A slot i % SA, accumulator buffer i % NB, named
+  // barrier kIssueBar0 + i % kRing and mma_done entry i % kRing (one commit per
+  // group: its X and A slots are free again and its accumulator buffer holds D_i).
+  auto x_full = [&](int s) { return bars + 8u * s; };
+  auto c_full = [&](int s) { return bars + 8u * (SX + s); };
+  auto c_empty = [&](int s) { return bars + 8u * (SX + SW + s); };
+  auto mma_done = [&](int i) { return bars + 8u * (SX + 2 * SW + i % kRing); };
+  auto ring_par = [](int i) { return (uint32_t)((i / kRing) & 1); };
+  auto issue_bar = [](int i) { return kIssueBar0 + (uint32_t)(i % kRing); };
+  const uint32_t done_bar = bars + 8u * (SX + 2 * SW + kRing);
+  const uint32_t fin_bar = done_bar + 8u;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
 
@@ -124,22 +183,17 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
     g_end = (int)(((int64_t)p.nk * (crank + 1)) / splitk);
   }
   const int ng = g_end - g_begin;
+  const int nws = (ng + kGroupsPerW - 1) / kGroupsPerW;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(full(s), 4 + 1);   // the 4 decode warps + the X producer's expect_tx arrival
-      mbar_init(empty(s), 1);
-    }
+    for (int s = 0; s < SX; ++s) mbar_init(x_full(s), 1);
     for (int s = 0; s < SW; ++s) {
-      mbar_init(w_full(s), 1);
-      mbar_init(w_empty(s), 4);
+      mbar_init(c_full(s), 1);
+      mbar_init(c_empty(s), 8);  // every code stage is read by both teams' 4 warps
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(mma_done(b), 1);
-      mbar_init(tmem_free(b), kAccWarps);
-    }
+    for (int r = 0; r < kRing; ++r) mbar_init(mma_done(r), 1);
     mbar_init(done_bar, kAccWarps);
-    mbar_init(fin_bar, 2);  // one final commit per MMA issuer
+    mbar_init(fin_bar, 1);  // the issuer's final commit
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_codes);
@@ -152,62 +206,66 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
   const uint32_t tmem_base = *tmem_slot;
 
   if (wg == 0) {
-    setmaxnreg_dec<kRegsCtl>();
-    // single-lane role loops; the other lanes wait at the __syncwarp below
+    if constexpr (NACC == 4) setmaxnreg_dec<R::ctl>();
+    // the producers run on one lane (the others wait at the __syncwarp below);
+    // the issuer loop is warp-uniform
     if (warp == 0 && lane == 0) {
       // ----------------------------------------------------------- TMA producer: token tiles of X
       int last = -1;
       bool ok = true;
       for (int i = 0; i < ng; ++i) {
-        const int s = i % S;
-        if (!(ok = mbar_wait(empty(s), ((i / S) & 1) ^ 1, abort_flag, &g_tc_status))) break;
-        mbar_expect_tx(full(s), L::kB);
-        tma_load_2d(sbase + L::b_off + s * L::kB, &tm_x, full(s), (g_begin + i) * 64, (int32_t)t0);
+        const int s = i % SX;
+        if (i >= SX && !(ok = mbar_wait(mma_done(i - SX), ring_par(i - SX), abort_flag, &g_tc_status))) break;
+        mbar_expect_tx(x_full(s), L::kB);
+        tma_load_2d(sbase + L::x_off + s * L::kB, &tm_x, x_full(s), (g_begin + i) * 64, (int32_t)t0);
         last = i;
       }
       if (!ok)  // let every copy already issued land before shared memory is released
-        for (int i = (last - S + 1 > 0 ? last - S + 1 : 0); i <= last; ++i) mbar_drain(full(i % S), (i / S) & 1);
-    } else if (warp == 2 && lane == 0) {
+        for (int i = (last - SX + 1 > 0 ? last - SX + 1 : 0); i <= last; ++i) mbar_drain(x_full(i % SX), (i / SX) & 1);
+    } else if (warp == 1 && lane == 0) {
       // ----------------------------------------------------------- TMA producer: code plane stages
-      const int nws = (ng + kGroupsPerW - 1) / kGroupsPerW;
       int last = -1;
       bool ok = true;
       for (int ws = 0; ws < nws; ++ws) {
         const int slot = ws % SW;
-        if (!(ok = mbar_wait(w_empty(slot), ((ws / SW) & 1) ^ 1, abort_flag, &g_tc_status))) break;
-        mbar_expect_tx(w_full(slot), kWBytes);
-        tma_load_2d(sbase + L::w_off + slot * kWBytes, &tm_codes, w_full(slot), (g_begin + ws * kGroupsPerW) * 32,
+        if (!(ok = mbar_wait(c_empty(slot), ((ws / SW) & 1) ^ 1, abort_flag, &g_tc_status))) break;
+        mbar_expect_tx(c_full(slot), kWBytes);
+        tma_load_2d(sbase + L::c_off + slot * kWBytes, &tm_codes, c_full(slot), (g_begin + ws * kGroupsPerW) * 32,
                     (int32_t)m0);
         last = ws;
       }
       if (!ok)
         for (int ws = (last - SW + 1 > 0 ? last - SW + 1 : 0); ws <= last; ++ws)
-          mbar_drain(w_full(ws % SW), (ws / SW) & 1);
-    } else if ((warp == 1 || warp == 3) && lane == 0) {
-      // ----------------------------------------------------------- MMA issuers
-      // Group i goes to TMEM buffer i & 1 and is issued by warp 1 (even i) or warp 3
-      // (odd i).  A thread's first shared-memory access after a tcgen05.commit waits
-      // for the MMAs that commit covers, so one thread issuing every group would
-      // leave the tensor pipe idle for the completion latency of each group; with
-      // two issuers the next group is already queued while the current one drains.
+          mbar_drain(c_full(ws % SW), (ws / SW) & 1);
+    } else if (warp == 3) {
+      // ----------------------------------------------------------- MMA issuer (no shared-memory access)
       constexpr uint32_t idesc = idesc_kind_f16(kTileM, BN, 1);  // bf16 x bf16 -> f32
-      const uint64_t a_desc0 = sw128_desc(sbase + L::a_off), b_desc0 = sw128_desc(sbase + L::b_off);
-      const int buf = warp == 1 ? 0 : 1;
-      for (int i = buf; i < ng; i += 2) {
-        const int s = i % S;
-        if (!mbar_wait(full(s), (i / S) & 1, abort_flag, &g_tc_status)) break;
-        if (i >= 2 && !mbar_wait(tmem_free(buf), ((i >> 1) - 1) & 1, abort_flag, &g_tc_status)) break;
+      // descriptors as 32-bit halves: the start address (low half) advances in 16-byte
+      // units by the stage offset and by 2 per 32-byte K step
+      const uint64_t bd = sw128_desc(sbase + L::x_off), ad = sw128_desc(sbase + L::a_off);
+      const uint32_t b_lo0 = (uint32_t)bd, b_hi = (uint32_t)(bd >> 32);
+      const uint32_t a_lo0 = (uint32_t)ad, a_hi = (uint32_t)(ad >> 32);
+      for (int i = 0; i < ng; ++i) {
+        named_bar_sync(issue_bar(i), L::issue_threads);  // A stage written, X landed, buffer free
         tc_fence_after();
-        // descriptor start address advances in 16-byte units: stage offsets and the 32-byte K steps
-        const uint64_t a_desc = a_desc0 + (uint64_t)((s * kABytes) >> 4);
-        const uint64_t b_desc = b_desc0 + (uint64_t)((s * L::kB) >> 4);
-        const uint32_t d = tmem_base + (uint32_t)(buf * BN);
+        if (lane == 0) {
+          const int s = i % SX, sa = i % SA, b = i % NB;
+          const uint32_t b_lo = b_lo0 + ((uint32_t)(s * L::kB) >> 4);
+          const uint32_t d = tmem_base + (uint32_t)(b * BN);
+          if constexpr (L::kATmem) {
+            const uint32_t a = tmem_base + L::a_col + (uint32_t)(sa * 32);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_f16(d, a_desc + 2 * kk, b_desc + 2 * kk, idesc, kk != 0);
-        mma_commit(empty(s));
-        mma_commit(mma_done(buf));
+            for (int kk = 0; kk < 4; ++kk) mma_f16_ts32(d, a + 8 * kk, b_lo + 2 * kk, b_hi, idesc, kk != 0);
+          } else {
+            const uint32_t a_lo = a_lo0 + ((uint32_t)(sa * kABytes) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) mma_f16_ss(d, a_lo + 2 * kk, a_hi, b_lo + 2 * kk, b_hi, idesc, kk != 0);
+          }
+          mma_commit(mma_done(i));
+        }
+        __syncwarp();
       }
-      mma_commit(fin_bar);  // arrives once every MMA this thread issued has completed
+      if (lane == 0) mma_commit(fin_bar);  // arrives once every MMA issued here has completed
     }
     __syncwarp();
     if (splitk > 1) {  // the accumulate warpgroups reduce between these two cluster barriers
@@ -215,50 +273,77 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
       cluster_sync();
     }
     if (warp == 1) {
-      // ----------------------------------------------------------- teardown: release TMEM once the
-      // accumulate warps are done with it (they arrive on `done` after their last tcgen05.ld)
+      // ----------------------------------------------------------- teardown: release tensor memory once
+      // the accumulate warps are done with it and no MMA is still running
       if (lane == 0) {
         mbar_drain(done_bar, 0);
-        mbar_drain(fin_bar, 0);  // no MMA may still be writing TMEM when it is released
+        mbar_drain(fin_bar, 0);
       }
       __syncwarp();
       tc_fence_after();
       tmem_dealloc(tmem_base, L::tmem_cols);
     }
-  } else if (wg == 1) {
-    setmaxnreg_dec<kRegsDec>();
-    // ------------------------------------------------------------- decode
-    // One code stage (4 groups of this thread's row) per outer iteration; each
-    // group is released to the MMA as soon as it is written.
-    const int r = (warp - 4) * 32 + lane;  // tile row
-    const int nws = (ng + kGroupsPerW - 1) / kGroupsPerW;
+  } else if (wg == 1 || wg == 2) {
+    if constexpr (NACC == 4) setmaxnreg_dec<R::dec>();
+    // ------------------------------------------------------------- decode (team = wg - 1)
+    // Team t decodes groups 4 ws + t and 4 ws + t + 2 of every code stage ws,
+    // one tile row per thread, into the A stage of the group's ring slot.
+    const int team = wg - 1;
+    const int q = warp & 3;
+    const int r = q * 32 + lane;  // tile row = tensor-memory lane
+    const uint32_t a_lane = tmem_base + ((uint32_t)(q * 32) << 16) + L::a_col;
     bool ok = true;
-    for (int ws = 0; ws < nws && ok; ++ws) {
+    for (int ws = 0; ws < nws; ++ws) {
       const int slot = ws % SW;
-      if (!(ok = warp_wait(w_full(slot), (ws / SW) & 1, abort_flag, &g_tc_status))) break;
-      const uint32_t csrc = sbase + L::w_off + slot * kWBytes + r * 128;
-      uint4 cw[2 * kGroupsPerW];
+      ok = ok && warp_wait(c_full(slot), (ws / SW) & 1, abort_flag, &g_tc_status);
+      const uint32_t csrc = sbase + L::c_off + slot * kWBytes + r * 128;
+      uint4 cw[4];
 #pragma unroll
-      for (int c = 0; c < 2 * kGroupsPerW; ++c) cw[c] = ld_shared_v4(csrc + ((c ^ (r & 7)) << 4));
-      const int gcount = (ng - ws * kGroupsPerW < kGroupsPerW) ? (ng - ws * kGroupsPerW) : kGroupsPerW;
-#pragma unroll
-      for (int gi = 0; gi < kGroupsPerW; ++gi) {
-        if (gi >= gcount) break;
-        const int i = ws * kGroupsPerW + gi, s = i % S;
-        if (!(ok = warp_wait(empty(s), ((i / S) & 1) ^ 1, abort_flag, &g_tc_status))) break;
-        const uint32_t adst = sbase + L::a_off + s * kABytes + r * 128;
-        const uint32_t words[8] = {cw[2 * gi].x,     cw[2 * gi].y,     cw[2 * gi].z,     cw[2 * gi].w,
-                                   cw[2 * gi + 1].x, cw[2 * gi + 1].y, cw[2 * gi + 1].z, cw[2 * gi + 1].w};
-#pragma unroll
-        for (int j = 0; j < 8; ++j) st_shared_v4(adst + ((j ^ (r & 7)) << 4), decode_word_bf16(words[j]));
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(full(s));
+      for (int h = 0; h < 2; ++h) {
+        const int c0 = 2 * (team + 2 * h);  // first 16-byte chunk of group team + 2h
+        cw[2 * h] = ok ? ld_shared_v4(csrc + ((c0 ^ (r & 7)) << 4)) : make_uint4(0, 0, 0, 0);
+        cw[2 * h + 1] = ok ? ld_shared_v4(csrc + (((c0 + 1) ^ (r & 7)) << 4)) : make_uint4(0, 0, 0, 0);
       }
-      // Release the code stage only after its bytes were consumed: a TMA (async proxy) refill
-      // must not race the shared-memory reads above.
+      // The code slot is free once both teams have their chunks in registers (a TMA
+      // refill must not race the reads above).
       __syncwarp();
-      if (lane == 0) mbar_arrive(w_empty(slot));
+      if (lane == 0) mbar_arrive(c_empty(slot));
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int i = ws * kGroupsPerW + team + 2 * h;
+        if (i >= ng) break;
+        const int sa = i % SA;
+        // the slot's previous group (i - SA, same team) must have been consumed by its MMA
+        if (i >= SA) ok = ok && warp_wait(mma_done(i - SA), ring_par(i - SA), abort_flag, &g_tc_status);
+        if (ok) {
+          tc_fence_after();
+          const uint32_t words[8] = {cw[2 * h].x,     cw[2 * h].y,     cw[2 * h].z,     cw[2 * h].w,
+                                     cw[2 * h + 1].x, cw[2 * h + 1].y, cw[2 * h + 1].z, cw[2 * h + 1].w};
+          if constexpr (L::kATmem) {
+            uint32_t v[32];  // column j = code byte j = (k = 2j, k = 2j + 1)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint4 d4 = decode_word_bf16(words[j]);
+              v[4 * j + 0] = d4.x;
+              v[4 * j + 1] = d4.y;
+              v[4 * j + 2] = d4.z;
+              v[4 * j + 3] = d4.w;
+            }
+            tmem_st32(a_lane + (uint32_t)(sa * 32), v);
+            tmem_st_wait();
+          } else {
+            // row r of the 128-byte-swizzled K-major A stage: 16-byte chunk j holds k = 8j .. 8j + 7
+            const uint32_t adst = sbase + L::a_off + sa * kABytes + r * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) st_shared_v4(adst + ((j ^ (r & 7)) << 4), decode_word_bf16(words[j]));
+            fence_proxy_async();  // generic-proxy stores -> the tensor core's (async-proxy) reads
+          }
+        }
+        ok = ok && warp_wait(x_full(i % SX), (i / SX) & 1, abort_flag, &g_tc_status);
+        tc_fence_before();
+        __syncwarp();
+        named_bar_arrive(issue_bar(i), L::issue_threads);  // always: the issuer must never wait forever
+      }
     }
     __syncwarp();
     if (splitk > 1) {
@@ -266,10 +351,10 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
       cluster_sync();
     }
   } else {
-    setmaxnreg_inc<kRegsAcc>();
+    if constexpr (NACC == 4) setmaxnreg_inc<R::acc>();
     // ------------------------------------------------------------- accumulate
     const int quad = warp & 3;                  // TMEM lane quadrant
-    const int cq = (warp - 8) >> 2;             // column quarter
+    const int cq = (warp - 12) >> 2;            // column chunk
     const int r_acc = quad * 32 + lane;         // tile row
     float2 acc[kCols / 2];
 #pragma unroll
@@ -277,47 +362,64 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
     bool acc_ok = true;
     const int64_t row = m0 + r_acc;
     const bool row_ok = row < p.N;
-    const uint16_t* srow = p.scales + (row_ok ? row : 0) * (p.K >> 6);
-    uint16_t s_cur[kGroupsPerW], s_nxt[kGroupsPerW];
-#pragma unroll
-    for (int j = 0; j < kGroupsPerW; ++j) {
-      s_cur[j] = 0;
-      s_nxt[j] = (row_ok && j < ng) ? srow[g_begin + j] : (uint16_t)0;
-    }
+    // Scales are read as pairs of groups (K / 64 is even, so every row starts on a
+    // 4-byte boundary); the next pair is fetched as soon as the current one is used.
+    const uint32_t* srow = reinterpret_cast<const uint32_t*>(p.scales + (row_ok ? row : 0) * (p.K >> 6));
+    int pcur = g_begin >> 1;
+    uint32_t s_cur = row_ok ? __ldg(srow + pcur) : 0u;
+    uint32_t s_nxt = (row_ok && 2 * (pcur + 1) < p.nk) ? __ldg(srow + pcur + 1) : 0u;
     const uint32_t tlane = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(cq * kCols);
-    constexpr int kLd = kCols >= 16 ? 16 : kCols;    // columns per tcgen05.ld
+    // the first NB groups find their accumulator buffers free
+    for (int i = 0; i < NB && i < ng; ++i) named_bar_arrive(issue_bar(i), L::issue_threads);
     for (int i = 0; i < ng; ++i) {
-      const int buf = i & 1, gi = i % kGroupsPerW;
-      if (gi == 0) {
-#pragma unroll
-        for (int j = 0; j < kGroupsPerW; ++j) {
-          s_cur[j] = s_nxt[j];
-          const int ii = i + kGroupsPerW + j;
-          s_nxt[j] = (row_ok && ii < ng) ? srow[g_begin + ii] : (uint16_t)0;
-        }
+      const int b = i % NB, ga = g_begin + i;
+      if ((ga >> 1) != pcur) {
+        ++pcur;
+        s_cur = s_nxt;
+        s_nxt = (row_ok && 2 * (pcur + 1) < p.nk) ? __ldg(srow + pcur + 1) : 0u;
       }
-      uint16_t sb = s_cur[0];
-#pragma unroll
-      for (int j = 1; j < kGroupsPerW; ++j) sb = (gi == j) ? s_cur[j] : sb;
-      const float sf = fp16_bits_to_float(sb);
+      const float sf = fp16_bits_to_float((uint16_t)((ga & 1) ? (s_cur >> 16) : (s_cur & 0xFFFFu)));
       const float2 s2 = make_float2(sf, sf);
-      if (!(acc_ok = warp_wait(mma_done(buf), (i >> 1) & 1, abort_flag, &g_tc_status))) break;
-      tc_fence_after();
+      acc_ok = acc_ok && warp_wait(mma_done(i), ring_par(i), abort_flag, &g_tc_status);
+      if (acc_ok) {
+        tc_fence_after();
+        const uint32_t dcol = tlane + (uint32_t)(b * BN);
 #pragma unroll
-      for (int c = 0; c < kCols; c += kLd) {
-        uint32_t v[kLd];
-        if constexpr (kLd == 16) tmem_ld16(tlane + buf * BN + c, v);
-        else if constexpr (kLd == 8) tmem_ld8(tlane + buf * BN + c, v);
-        else tmem_ld4(tlane + buf * BN + c, v);
-        tmem_ld_wait();
+        for (int c = 0; c < kCols; c += 16) {
+          constexpr int kRest = kCols % 16;
+          if (c + 16 <= kCols) {
+            uint32_t v[16];
+            tmem_ld_cols<16>(dcol + c, v);
+            tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < kLd; j += 2)
-          acc[(c + j) / 2] =
-              ffma2(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), s2, acc[(c + j) / 2]);
+            for (int j = 0; j < 16; j += 2)
+              acc[(c + j) / 2] = ffma2(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), s2, acc[(c + j) / 2]);
+          } else {
+            // remainder of 4, 8 or 12 columns
+            if constexpr (kRest >= 8) {
+              uint32_t v[8];
+              tmem_ld_cols<8>(dcol + c, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 8; j += 2)
+                acc[(c + j) / 2] = ffma2(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), s2, acc[(c + j) / 2]);
+            }
+            if constexpr (kRest % 8 == 4) {
+              constexpr int c4 = (kRest >= 8) ? 8 : 0;
+              uint32_t v[4];
+              tmem_ld_cols<4>(dcol + c + c4, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 4; j += 2)
+                acc[(c + c4 + j) / 2] =
+                    ffma2(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), s2, acc[(c + c4 + j) / 2]);
+            }
+          }
+        }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tmem_free(buf));
+      if (i + NB < ng) named_bar_arrive(issue_bar(i + NB), L::issue_threads);  // buffer b is free for group i + NB
     }
 
     // ----------------------------------------------------------- split-K reduction across the cluster
@@ -394,17 +496,17 @@ bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint6
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int S, int SW>
+template <int BN>
 int set_kernel_attrs() {
-  using L = TcSmem<BN, S, SW>;
+  using L = TcSmem<BN>;
   static bool attr_set[64] = {};
   int dev = 0;
   if (cuda_check(cudaGetDevice(&dev), "cudaGetDevice")) return Q4LIN_ERR_CUDA;
   if (dev < 64 && attr_set[dev]) return Q4LIN_OK;
-  if (cuda_check(cudaFuncSetAttribute(q4_tc_kernel<BN, S, SW>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc),
+  if (cuda_check(cudaFuncSetAttribute(q4_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc),
                  "tc: cudaFuncSetAttribute(max dynamic shared memory)"))
     return Q4LIN_ERR_CUDA;
-  if (cuda_check(cudaFuncSetAttribute(q4_tc_kernel<BN, S, SW>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+  if (cuda_check(cudaFuncSetAttribute(q4_tc_kernel<BN>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
                  "tc: cudaFuncSetAttribute(cluster size)"))
     return Q4LIN_ERR_CUDA;
   if (dev < 64) attr_set[dev] = true;
@@ -414,17 +516,17 @@ int set_kernel_attrs() {
 // How many clusters of `size` CTAs of this kernel can be resident at once (0 on
 // error).  Clusters are placed within one GPC, so this is below sms / size when
 // the GPCs' SM counts are not multiples of the cluster size.
-template <int BN, int S, int SW>
+template <int BN>
 int resident_clusters(int size) {
-  using L = TcSmem<BN, S, SW>;
+  using L = TcSmem<BN>;
   static int cache[64][9] = {};
   int dev = 0;
   if (size < 1 || size > 8 || cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (dev < 64 && cache[dev][size]) return cache[dev][size];
-  if (set_kernel_attrs<BN, S, SW>() != Q4LIN_OK) return 0;
+  if (set_kernel_attrs<BN>() != Q4LIN_OK) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1, 1, (unsigned)size);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(L::threads, 1, 1);
   cfg.dynamicSmemBytes = L::alloc;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -434,7 +536,7 @@ int resident_clusters(int size) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, q4_tc_kernel<BN, S, SW>, &cfg) != cudaSuccess || n < 0) {
+  if (cudaOccupancyMaxActiveClusters(&n, q4_tc_kernel<BN>, &cfg) != cudaSuccess || n < 0) {
     cudaGetLastError();
     n = 0;
   }
@@ -442,15 +544,15 @@ int resident_clusters(int size) {
   return n;
 }
 
-template <int BN, int S, int SW>
+template <int BN>
 int launch_tile(const LinearArgs& a, int splitk) {
-  using L = TcSmem<BN, S, SW>;
+  using L = TcSmem<BN>;
   static_assert(L::alloc <= 232448, "shared memory budget");
   if (splitk < 1 || splitk > 8 || splitk > L::max_splitk) {
     set_error_detail("tc: split-K factor out of range for this tile");
     return Q4LIN_ERR_INVALID_ARG;
   }
-  if (const int rc = set_kernel_attrs<BN, S, SW>()) return rc;
+  if (const int rc = set_kernel_attrs<BN>()) return rc;
   CUtensorMap tm_codes, tm_x;
   if (!make_map_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.wq, (uint64_t)(a.K / 2), (uint64_t)a.N,
                    (uint64_t)(a.K / 2), 128, kTileM) ||
@@ -462,7 +564,7 @@ int launch_tile(const LinearArgs& a, int splitk) {
   const TcParams p{a.scales, a.y, a.N, a.K, a.T, (int)(a.K / 64), splitk};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((a.N + kTileM - 1) / kTileM), (unsigned)((a.T + BN - 1) / BN), (unsigned)splitk);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(L::threads, 1, 1);
   cfg.dynamicSmemBytes = L::alloc;
   cfg.stream = a.stream;
   cudaLaunchAttribute attr[1];
@@ -472,26 +574,26 @@ int launch_tile(const LinearArgs& a, int splitk) {
   attr[0].val.clusterDim.z = (unsigned)splitk;
   cfg.attrs = attr;
   cfg.numAttrs = splitk > 1 ? 1 : 0;
-  return cuda_check(cudaLaunchKernelEx(&cfg, q4_tc_kernel<BN, S, SW>, tm_codes, tm_x, p), "tc: kernel launch");
+  return cuda_check(cudaLaunchKernelEx(&cfg, q4_tc_kernel<BN>, tm_codes, tm_x, p), "tc: kernel launch");
 }
 
 int max_splitk_for(int bn) {
   switch (bn) {
-    case 256: return TcSmem<256, 4, 2>::max_splitk;
-    case 128: return TcSmem<128, 5, 3>::max_splitk;
-    case 64: return TcSmem<64, 6, 4>::max_splitk;
-    case 32: return TcSmem<32, 6, 6>::max_splitk;
-    default: return TcSmem<16, 6, 6>::max_splitk;
+    case 256: return TcSmem<256>::max_splitk;
+    case 128: return TcSmem<128>::max_splitk;
+    case 64: return TcSmem<64>::max_splitk;
+    case 32: return TcSmem<32>::max_splitk;
+    default: return TcSmem<16>::max_splitk;
   }
 }
 
 int resident_clusters_for(int bn, int size) {
   switch (bn) {
-    case 256: return resident_clusters<256, 4, 2>(size);
-    case 128: return resident_clusters<128, 5, 3>(size);
-    case 64: return resident_clusters<64, 6, 4>(size);
-    case 32: return resident_clusters<32, 6, 6>(size);
-    default: return resident_clusters<16, 6, 6>(size);
+    case 256: return resident_clusters<256>(size);
+    case 128: return resident_clusters<128>(size);
+    case 64: return resident_clusters<64>(size);
+    case 32: return resident_clusters<32>(size);
+    default: return resident_clusters<16>(size);
   }
 }
 
@@ -509,40 +611,49 @@ int sm_count() {
 }  // namespace
 
 TcPlan tc_plan(int route, int64_t N, int64_t K, int64_t T, int sms) {
-  TcPlan pl{};
-  // token tile: the smallest MMA N (multiple of 16, <= 256) covering T, else 256
-  if (T > 128) pl.bn = 256;
-  else if (T > 64) pl.bn = 128;
-  else if (T > 32) pl.bn = 64;
-  else if (T > 16) pl.bn = 32;
-  else pl.bn = 16;
-  pl.splitk = 1;
-  if (route == Q4LIN_ROUTE_TC_SPLITK) {
-    // Split K across a cluster so that the CTAs fill the GPU in as few, as full
-    // waves as possible.  A wave holds as many clusters as can be resident at
-    // once (queried; without a device, sms / size).
-    const int64_t tiles = ((N + kTileM - 1) / kTileM) * ((T + pl.bn - 1) / pl.bn);
-    const int64_t nk = K / 64;
-    double best = -1.0;
-    const int smax = max_splitk_for(pl.bn) < 8 ? max_splitk_for(pl.bn) : 8;
+  // Token-tile width candidates: the smallest MMA N covering T up to 128
+  // tokens; above that 256 or 128.  For each candidate and split factor the
+  // cost is waves x per-CTA time, with a per-group time of max(MMA time, the
+  // synchronisation floor of a group) and a fixed per-CTA cost; a wave holds as
+  // many CTAs (clusters) as can be resident at once (queried; without a
+  // device, sms / size).
+  int cand[2] = {0, 0};
+  int ncand = 0;
+  if (T > 128) {
+    cand[0] = 256;
+    cand[1] = 128;
+    ncand = 2;
+  } else {
+    cand[0] = T > 64 ? 128 : T > 32 ? 64 : T > 16 ? 32 : 16;
+    ncand = 1;
+  }
+  constexpr double kGroupFloor = 650.0;   // clocks per group the pipeline sustains at best
+  constexpr double kCtaFixed = 3000.0;    // launch, first loads, epilogue
+  const int64_t nk = K / 64;
+  TcPlan best_pl{cand[0], 1};
+  double best = -1.0;
+  for (int c = 0; c < ncand; ++c) {
+    const int bn = cand[c];
+    const int64_t tiles = ((N + kTileM - 1) / kTileM) * ((T + bn - 1) / bn);
+    const double t_group = (2.0 * bn + 150.0) > kGroupFloor ? (2.0 * bn + 150.0) : kGroupFloor;
+    const int smax = route == Q4LIN_ROUTE_TC_SPLITK ? (max_splitk_for(bn) < 8 ? max_splitk_for(bn) : 8) : 1;
     for (int s = 1; s <= smax && s <= nk; ++s) {
       int64_t per_wave = sms / s;
       if (s > 1) {
-        const int q = resident_clusters_for(pl.bn, s);
+        const int q = resident_clusters_for(bn, s);
         if (q > 0 && q < per_wave) per_wave = q;
       }
       if (per_wave < 1) continue;
       const int64_t waves = (tiles + per_wave - 1) / per_wave;
-      // time ~ waves x (K share of one CTA + a fixed cost per CTA of about six
-      // groups: launch, first loads, epilogue); prefer fewer splits on ties
-      const double cost = (double)waves * ((double)nk / (double)s + 6.0);
-      if (best < 0 || cost < best - 1e-9) {
+      const double cost = (double)waves * ((double)((nk + s - 1) / s) * t_group + kCtaFixed);
+      if (best < 0 || cost < best - 1e-9) {  // ties keep the earlier (fewer splits, preferred width)
         best = cost;
-        pl.splitk = s;
+        best_pl.bn = bn;
+        best_pl.splitk = s;
       }
     }
   }
-  return pl;
+  return best_pl;
 }
 
 size_t tc_workspace_bytes(int64_t, int64_t, int64_t) { return 0; }
@@ -561,11 +672,11 @@ int tc_launch(const LinearArgs& a, int route) {
   }
   const TcPlan pl = tc_plan(route, a.N, a.K, a.T, sm_count());
   switch (pl.bn) {
-    case 256: return launch_tile<256, 4, 2>(a, pl.splitk);
-    case 128: return launch_tile<128, 5, 3>(a, pl.splitk);
-    case 64: return launch_tile<64, 6, 4>(a, pl.splitk);
-    case 32: return launch_tile<32, 6, 6>(a, pl.splitk);
-    default: return launch_tile<16, 6, 6>(a, pl.splitk);
+    case 256: return launch_tile<256>(a, pl.splitk);
+    case 128: return launch_tile<128>(a, pl.splitk);
+    case 64: return launch_tile<64>(a, pl.splitk);
+    case 32: return launch_tile<32>(a, pl.splitk);
+    default: return launch_tile<16>(a, pl.splitk);
   }
 }
 

@@ -75,8 +75,7 @@ int check_device() {
 
 int route_for(int64_t N, int64_t K, int64_t T) {
   if (T <= 4 || !q4::tc_supported(N, K, T)) return Q4LIN_ROUTE_GEMV;
-  if (T <= 64) return Q4LIN_ROUTE_TC_SPLITK;
-  return Q4LIN_ROUTE_TC;
+  return Q4LIN_ROUTE_TC_SPLITK;  // the tile planner splits K only where that fills the GPU better
 }
 
 size_t round256(size_t b) { return (b + 255) / 256 * 256; }
