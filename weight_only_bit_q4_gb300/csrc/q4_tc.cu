@@ -629,6 +629,8 @@ TcPlan tc_plan(int route, int64_t N, int64_t K, int64_t T, int sms) {
   }
   constexpr double kGroupFloor = 650.0;   // clocks per group the pipeline sustains at best
   constexpr double kCtaFixed = 3000.0;    // launch, first loads, epilogue
+  // cluster barriers and the distributed-shared-memory reduction of a 128 x BN FP32 tile
+  constexpr double kSplitPerColumn = 20.0;
   const int64_t nk = K / 64;
   TcPlan best_pl{cand[0], 1};
   double best = -1.0;
@@ -645,7 +647,8 @@ TcPlan tc_plan(int route, int64_t N, int64_t K, int64_t T, int sms) {
       }
       if (per_wave < 1) continue;
       const int64_t waves = (tiles + per_wave - 1) / per_wave;
-      const double cost = (double)waves * ((double)((nk + s - 1) / s) * t_group + kCtaFixed);
+      const double cost =
+          (double)waves * ((double)((nk + s - 1) / s) * t_group + kCtaFixed + (s > 1 ? kSplitPerColumn * bn : 0.0));
       if (best < 0 || cost < best - 1e-9) {  // ties keep the earlier (fewer splits, preferred width)
         best = cost;
         best_pl.bn = bn;
