@@ -142,12 +142,19 @@ q4_gemv_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict__ scal
 // (deterministic), then rounded to bf16.
 constexpr int kBulkThreads = 512;
 constexpr int kBulkConsumers = 15;   // warps 1..15
+constexpr int64_t kBulkSmemBudget = 232448 - 1024;
 constexpr int kBulkRows = 8;
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
                : "memory");
+}
+
+// Pull global bytes into L2 (no destination, no completion): a hint that never
+// changes what a later load returns -- L2 is where every SM's view meets.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 struct StreamLayout {
@@ -172,6 +179,22 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
                       const uint16_t* __restrict__ x, uint16_t* __restrict__ y, int64_t N, int64_t K,
                       int64_t rows_cap, int nj, int slots) {
   extern __shared__ __align__(128) uint8_t smem[];
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    // While the previous kernel finishes, start this CTA's rows on their way into L2
+    // (codes and scales, 16-byte granules, 32 KB per prefetch).
+    const int64_t p0 = (int64_t)blockIdx.x * N / gridDim.x, p1 = (int64_t)(blockIdx.x + 1) * N / gridDim.x;
+    const uint8_t* cb = wq + p0 * (K / 2);
+    for (int64_t off = 0, len = (p1 - p0) * (K / 2); off < len; off += 32768)
+      bulk_prefetch_l2(cb + off, (uint32_t)(len - off < 32768 ? len - off : 32768));
+    // scales: the 16-byte-aligned interior of this CTA's rows only (never past them)
+    const uintptr_t s0 = reinterpret_cast<uintptr_t>(scales + p0 * (K / 64));
+    const uintptr_t s1 = reinterpret_cast<uintptr_t>(scales + p1 * (K / 64));
+    const uintptr_t a0 = (s0 + 15) & ~uintptr_t(15), a1 = s1 & ~uintptr_t(15);
+    for (uintptr_t a = a0; a < a1; a += 32768)
+      bulk_prefetch_l2(reinterpret_cast<const void*>(a), (uint32_t)(a1 - a < 32768 ? a1 - a : 32768));
+  }
+  pdl_wait_previous();  // before any global-memory read that must see the previous kernel's writes
   const StreamLayout L = stream_layout(K, rows_cap, nj, slots);
   float* part = reinterpret_cast<float*>(smem + L.part_off);
   const uint32_t sbase = smem_u32(smem);
@@ -331,7 +354,7 @@ static bool stream_plan(int64_t N, int64_t K, int nsm, StreamPlan* p) {
   if (p->grid > nsm) p->grid = nsm;
   if (p->grid < 1) p->grid = 1;
   p->rows_cap = ((N + p->grid - 1) / p->grid + kBulkRows - 1) / kBulkRows * kBulkRows;
-  const int64_t budget = 232448 - 1024;
+  const int64_t budget = kBulkSmemBudget;
   const StreamLayout L0 = stream_layout(K, p->rows_cap, p->nj, 0);
   const int64_t per = (int64_t)kBulkRows * (K / 2) + 16;
   int64_t s = (budget - L0.slot_off - 128) / per;
@@ -361,14 +384,25 @@ static int gemv_stream_launch(const LinearArgs& a) {
   if (!stream_plan(a.N, a.K, device_sms(), &pl)) return Q4LIN_ERR_INVALID_ARG;
   if (dev >= 64 || !attr[dev]) {
     if (cuda_check(cudaFuncSetAttribute(q4_gemv_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        232448 - 1024),
+                                        (int)kBulkSmemBudget),
                    "gemv: cudaFuncSetAttribute"))
       return Q4LIN_ERR_CUDA;
     if (dev < 64) attr[dev] = true;
   }
-  q4_gemv_stream_kernel<<<(unsigned)pl.grid, kBulkThreads, pl.bytes, a.stream>>>(a.wq, a.scales, a.x, a.y, a.N, a.K,
-                                                                                 pl.rows_cap, pl.nj, pl.slots);
-  return cuda_check(cudaGetLastError(), "gemv: streaming kernel launch");
+  // programmatic dependent launch: the kernel waits for its predecessor before touching memory
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)pl.grid, 1, 1);
+  cfg.blockDim = dim3(kBulkThreads, 1, 1);
+  cfg.dynamicSmemBytes = pl.bytes;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cuda_check(cudaLaunchKernelEx(&cfg, q4_gemv_stream_kernel, a.wq, a.scales, a.x, a.y, a.N, a.K, pl.rows_cap,
+                                       pl.nj, pl.slots),
+                    "gemv: streaming kernel launch");
 }
 
 bool gemv_stream_ok(int64_t N, int64_t K, int64_t T) {

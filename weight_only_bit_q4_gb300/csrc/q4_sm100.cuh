@@ -89,6 +89,14 @@ __device__ __forceinline__ bool named_bar_red_or(bool pred, uint32_t id, uint32_
   return out != 0;
 }
 
+// Programmatic dependent launch: let the next kernel in the stream begin
+// launching, then wait until the previous kernel has completed and its memory
+// operations are visible.  Called before any global-memory access, so the
+// ordering with every producer and consumer in the stream is unchanged; only
+// the launch latency overlaps the previous kernel's tail.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_previous() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Bounded wait used while tearing down after an abort (ignores the flag).
 __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
   for (uint32_t i = 0; i < kSpinLimit; ++i)
