@@ -98,3 +98,25 @@ def test_valid_call_without_gpu_reports_error_not_crash(lib):
         pytest.skip("a GPU is present")
     st = _call(4, 128, 1)
     assert st in (5, 6)   # device unsupported / CUDA error: no device here
+
+
+def test_tile_plan_query(lib):
+    # Host-only: the planner reads device attributes when there is a device and
+    # falls back to a nominal SM count when there is none.
+    assert q4lin.tile_plan(6144, 5120, 1) == (0, 1)                      # GEMV route
+    assert q4lin.tile_plan(6144, 5120, 64, q4lin.ROUTE_GEMV) == (0, 1)
+    assert q4lin.tile_plan(6144, 5120, 0) == (0, 1)                      # empty problem
+    for T, widths in ((8, {16}), (24, {32}), (48, {64}), (100, {128}), (1024, {128, 256})):
+        bn, sk = q4lin.tile_plan(6144, 5120, T)
+        assert bn in widths and 1 <= sk <= 8, (T, bn, sk)
+        bn, sk = q4lin.tile_plan(6144, 5120, T, q4lin.ROUTE_TC)
+        assert bn in widths and sk == 1, (T, bn, sk)
+    # a deep K with few row tiles is split; a long N that fills the GPU is not
+    assert q4lin.tile_plan(1024, 65536, 16)[1] > 1
+    assert q4lin.tile_plan(65536, 1024, 16)[1] == 1
+    with pytest.raises(q4lin.Q4LinError):
+        q4lin.tile_plan(6144, 100, 8)
+    with pytest.raises(q4lin.Q4LinError):
+        q4lin.tile_plan(6144, 5120, 8, route=9)
+    bn = ctypes.c_int(0)
+    assert lib.q4lin_tile_plan(0, 6144, 5120, 8, ctypes.byref(bn), None) == 1

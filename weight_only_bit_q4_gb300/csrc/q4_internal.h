@@ -33,6 +33,7 @@ struct TcPlan {
   int splitk;  // cluster size along K
 };
 TcPlan tc_plan(int route, int64_t N, int64_t K, int64_t T, int sms);
+TcPlan tc_plan_current_device(int route, int64_t N, int64_t K, int64_t T);
 int tc_launch(const LinearArgs& a, int route);
 size_t tc_workspace_bytes(int64_t N, int64_t K, int64_t T);
 int tc_launch_count(int64_t N, int64_t K, int64_t T);

@@ -19,7 +19,7 @@ ROUTE_AUTO, ROUTE_GEMV, ROUTE_TC_SPLITK, ROUTE_TC = 0, 1, 2, 3
 ROUTE_NAMES = {ROUTE_AUTO: "auto", ROUTE_GEMV: "gemv", ROUTE_TC_SPLITK: "tc_splitk", ROUTE_TC: "tc"}
 
 EXPORTS = ("q4lin_workspace_bytes", "q4lin_linear", "q4lin_linear_route",
-           "q4lin_route_workspace_bytes", "q4lin_select_route", "q4lin_kernel_launches",
+           "q4lin_route_workspace_bytes", "q4lin_select_route", "q4lin_tile_plan", "q4lin_kernel_launches",
            "q4lin_status_string",
            "q4lin_device_status", "q4lin_clear_device_status", "q4lin_last_error_detail",
            "q4lin_version")
@@ -59,6 +59,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q4lin_linear_route.restype = ctypes.c_int
     lib.q4lin_select_route.argtypes = [i64, i64, i64]
     lib.q4lin_select_route.restype = ctypes.c_int
+    lib.q4lin_tile_plan.argtypes = [ctypes.c_int, i64, i64, i64, ctypes.POINTER(ctypes.c_int),
+                                    ctypes.POINTER(ctypes.c_int)]
+    lib.q4lin_tile_plan.restype = ctypes.c_int
     lib.q4lin_kernel_launches.argtypes = [i64, i64, i64]
     lib.q4lin_kernel_launches.restype = ctypes.c_int
     lib.q4lin_status_string.argtypes = [ctypes.c_int]
@@ -92,6 +95,15 @@ def workspace_bytes(N: int, K: int, T: int, route: int = ROUTE_AUTO) -> int:
 
 def select_route(N: int, K: int, T: int) -> int:
     return int(load().q4lin_select_route(N, K, T))
+
+
+def tile_plan(N: int, K: int, T: int, route: int = ROUTE_AUTO) -> tuple:
+    """(token-tile width, split-K cluster size) the tensor-core route runs; (0, 1) for the GEMV."""
+    bn, sk = ctypes.c_int(0), ctypes.c_int(0)
+    st = load().q4lin_tile_plan(route, N, K, T, ctypes.byref(bn), ctypes.byref(sk))
+    if st != OK:
+        raise Q4LinError(st, "tile plan: ")
+    return int(bn.value), int(sk.value)
 
 
 def kernel_launches(N: int, K: int, T: int) -> int:
