@@ -126,24 +126,30 @@ q4_gemv_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict__ scal
 
 // ---------------------------------------------------------------------------
 // Single-token streaming GEMV.  One persistent CTA per SM owns a contiguous
-// range of rows (balanced to one row).  Thread 0 first copies x into shared
-// memory (one bulk copy per CTA), then streams the rows' code bytes into a ring
-// of shared-memory slots with 1-D bulk async copies (8 rows per copy), so the
-// CTA's share is in flight from the start.
+// range of rows (balanced to one row), cut into blocks of RB rows.  Thread 0
+// copies x into shared memory (one bulk copy per CTA), then streams every
+// block's code bytes and its scales (a block's scales are one contiguous run
+// of the scale plane) into a ring of shared-memory slots with 1-D bulk async
+// copies, so the CTA's share is in flight from the start and no consumer ever
+// waits on a global load.
 //
 // K is cut into column groups of 32 chunks (a chunk = 16 code bytes = 32
-// weights = half a scale group); warp j of a row stream owns column group j,
-// so lane l always handles chunk 32 j + l: its 32 x values (and their sum)
-// are read once from the shared copy of x and stay in registers for every row.
-// Per 8-row slot a warp reads one conflict-free 16-byte code chunk per row,
-// decodes it to (128 + q) floats with byte permutes, accumulates with packed
-// FP32 FMAs, applies (partial - 136 * sum x) * s, and reduces across the warp.
-// The NJ column-group partials of a row are summed in a fixed order at the end
-// (deterministic), then rounded to bf16.
-constexpr int kBulkThreads = 512;
-constexpr int kBulkConsumers = 15;   // warps 1..15
-constexpr int64_t kBulkSmemBudget = 232448 - 1024;
-constexpr int kBulkRows = 8;
+// weights = half a scale group).  A work item is one (block, column group)
+// pair; the W consumer warps take the items in block-major order, warp w the
+// items w, w + W, w + 2W, ...  Where a multiple of the group count between 12
+// and 15 exists, W is that multiple, so a warp keeps one column group and its
+// 32 x values per lane in registers for the whole kernel; otherwise W = 15 and
+// a warp reloads its x values from shared memory whenever its group changes.  Per item a lane decodes one conflict-free 16-byte code chunk
+// per row into (128 + q) floats with byte permutes, accumulates with packed
+// FP32 FMAs, applies (partial - 136 * sum x) * s, and the warp reduces the RB
+// row partials with a halving butterfly (each exchange hands half of the
+// remaining rows to the partner lane, so RB rows cost log2(RB) + 5 shuffle
+// rounds instead of 5 RB).  The column-group partials of a row are summed in a
+// fixed order at the end (deterministic), then rounded to bf16.
+constexpr int kStreamThreads = 512;
+constexpr int kStreamConsumers = 15;   // warps 1..15
+constexpr int64_t kStreamSmemBudget = 232448 - 1024;
+constexpr int64_t kPrefetchCapBytes = 512 * 1024;   // L2 prefetch of one CTA's codes, at most
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
@@ -157,45 +163,112 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+__device__ __forceinline__ uint16_t ld_shared_u16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
 struct StreamLayout {
-  uint32_t x_off, part_off, bar_off, slot_off, slot_bytes, bytes;
+  uint32_t x_off, part_off, bar_off, code_off, code_stride, sc_off, sc_stride, bytes;
 };
 
 // x (bf16, K elements), partial sums [rows_cap][nj] fp32, the x barrier and the
-// full/empty barriers, then the slots (128-byte aligned)
-__host__ __device__ inline StreamLayout stream_layout(int64_t K, int64_t rows_cap, int nj, int slots) {
+// full/empty barriers, the code slots (128-byte aligned) and the scale slots
+// (16-byte aligned; a block's run of scales plus up to 15 bytes of alignment
+// slack on either side).
+__host__ __device__ inline StreamLayout stream_layout(int64_t K, int rb, int64_t rows_cap, int nj, int slots) {
   StreamLayout L;
   L.x_off = 0;
   L.part_off = (uint32_t)(K * 2);
   L.bar_off = (uint32_t)((L.part_off + rows_cap * nj * 4 + 15) / 16 * 16);
-  L.slot_off = (L.bar_off + 8 + (uint32_t)slots * 16 + 127) / 128 * 128;
-  L.slot_bytes = (uint32_t)(kBulkRows * (K / 2));
-  L.bytes = L.slot_off + (uint32_t)slots * L.slot_bytes;
+  L.code_off = (L.bar_off + 8 + (uint32_t)slots * 16 + 127) / 128 * 128;
+  L.code_stride = (uint32_t)((rb * (K / 2) + 127) / 128 * 128);
+  L.sc_off = L.code_off + (uint32_t)slots * L.code_stride;
+  L.sc_stride = (uint32_t)((rb * (K / 32) + 32 + 15) / 16 * 16);
+  L.bytes = L.sc_off + (uint32_t)slots * L.sc_stride;
   return L;
 }
 
-__global__ void __launch_bounds__(kBulkThreads, 1)
+// Queue block b (rows [ra, ra + nr)) into slot s: its code rows, and the
+// 16-byte granules of the scale plane that cover its scale run [st, en) (the
+// plane starts 16-byte aligned; a granule past the plane's last full one is
+// never copied -- the at most 7 scales there are read with plain loads and
+// stored before the barrier arrival that publishes them).
+__device__ __forceinline__ void stream_issue(const uint8_t* wq, const uint8_t* sc_plane, int64_t plane_bytes,
+                                             int64_t row_bytes, int64_t sc_row_bytes, int64_t ra, int nr,
+                                             uint32_t code_dst, uint32_t sc_dst, uint32_t full_bar) {
+  const uint32_t cbytes = (uint32_t)(nr * row_bytes);
+  const int64_t st = ra * sc_row_bytes, en = (ra + nr) * sc_row_bytes;
+  const int64_t a = st & ~(int64_t)15;
+  const int64_t e_up = (en + 15) & ~(int64_t)15, e_cap = plane_bytes & ~(int64_t)15;
+  const int64_t e = e_up < e_cap ? e_up : e_cap;  // >= a, since st < plane_bytes
+  for (int64_t t = (e > st ? e : st); t < en; t += 2)
+    st_shared_u16(sc_dst + (uint32_t)(t - a), *reinterpret_cast<const uint16_t*>(sc_plane + t));
+  const uint32_t sbytes = (uint32_t)(e - a);
+  mbar_expect_tx(full_bar, cbytes + sbytes);
+  bulk_g2s(code_dst, wq + ra * row_bytes, cbytes, full_bar);
+  if (sbytes > 0) bulk_g2s(sc_dst, sc_plane + a, sbytes, full_bar);
+}
+
+// Sum each of the RB per-lane row partials over the warp.  Round r (offset
+// 16 >> r) swaps half of the rows still held with lane ^ offset, so afterwards
+// a lane holds one row whose index is read from lane bits 4, 3, ... (most
+// significant first); the remaining rounds are a plain butterfly.
+template <int RB>
+__device__ __forceinline__ float reduce_rows(const float (&acc)[RB], int lane, int* row) {
+  float a[RB];
+#pragma unroll
+  for (int i = 0; i < RB; ++i) a[i] = acc[i];
+  int r = 0;
+#pragma unroll
+  for (int n = RB, off = 16; n > 1; n >>= 1, off >>= 1) {
+    const bool h = (lane & off) != 0;
+#pragma unroll
+    for (int q = 0; q < n / 2; ++q) {
+      const float send = h ? a[q] : a[q + n / 2];
+      const float keep = h ? a[q + n / 2] : a[q];
+      a[q] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+    r = 2 * r + (h ? 1 : 0);
+  }
+#pragma unroll
+  for (int off = 16 / RB; off >= 1; off >>= 1) a[0] += __shfl_xor_sync(0xffffffffu, a[0], off);
+  *row = r;
+  return a[0];
+}
+
+template <int RB>
+__global__ void __launch_bounds__(kStreamThreads, 1)
 q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict__ scales,
                       const uint16_t* __restrict__ x, uint16_t* __restrict__ y, int64_t N, int64_t K,
-                      int64_t rows_cap, int nj, int slots) {
+                      int64_t rows_cap, int nj, int nw, int slots) {
   extern __shared__ __align__(128) uint8_t smem[];
   pdl_launch_dependents();
+  const int64_t r0 = (int64_t)blockIdx.x * N / gridDim.x;
+  const int64_t r1 = (int64_t)(blockIdx.x + 1) * N / gridDim.x;
+  const int64_t row_bytes = K / 2, sc_row_bytes = K / 32, nchunk = K / 32;
+  const int64_t plane_bytes = N * sc_row_bytes;
+  const uint8_t* sc_plane = reinterpret_cast<const uint8_t*>(scales);
   if (threadIdx.x == 0) {
-    // While the previous kernel finishes, start this CTA's rows on their way into L2
-    // (codes and scales, 16-byte granules, 32 KB per prefetch).
-    const int64_t p0 = (int64_t)blockIdx.x * N / gridDim.x, p1 = (int64_t)(blockIdx.x + 1) * N / gridDim.x;
-    const uint8_t* cb = wq + p0 * (K / 2);
-    for (int64_t off = 0, len = (p1 - p0) * (K / 2); off < len; off += 32768)
+    // While the previous kernel finishes, start this CTA's rows on their way into L2:
+    // the first kPrefetchCapBytes of its codes, and the 16-byte-aligned interior of its
+    // scale run (never past it), 32 KB per prefetch.
+    const uint8_t* cb = wq + r0 * row_bytes;
+    int64_t len = (r1 - r0) * row_bytes;
+    if (len > kPrefetchCapBytes) len = kPrefetchCapBytes;
+    for (int64_t off = 0; off < len; off += 32768)
       bulk_prefetch_l2(cb + off, (uint32_t)(len - off < 32768 ? len - off : 32768));
-    // scales: the 16-byte-aligned interior of this CTA's rows only (never past them)
-    const uintptr_t s0 = reinterpret_cast<uintptr_t>(scales + p0 * (K / 64));
-    const uintptr_t s1 = reinterpret_cast<uintptr_t>(scales + p1 * (K / 64));
-    const uintptr_t a0 = (s0 + 15) & ~uintptr_t(15), a1 = s1 & ~uintptr_t(15);
-    for (uintptr_t a = a0; a < a1; a += 32768)
-      bulk_prefetch_l2(reinterpret_cast<const void*>(a), (uint32_t)(a1 - a < 32768 ? a1 - a : 32768));
+    const int64_t a0 = (r0 * sc_row_bytes + 15) & ~(int64_t)15, a1 = (r1 * sc_row_bytes) & ~(int64_t)15;
+    for (int64_t off = a0; off < a1; off += 32768)
+      bulk_prefetch_l2(sc_plane + off, (uint32_t)(a1 - off < 32768 ? a1 - off : 32768));
   }
   pdl_wait_previous();  // before any global-memory read that must see the previous kernel's writes
-  const StreamLayout L = stream_layout(K, rows_cap, nj, slots);
+  const StreamLayout L = stream_layout(K, RB, rows_cap, nj, slots);
   float* part = reinterpret_cast<float*>(smem + L.part_off);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t xbar = sbase + L.bar_off;
@@ -204,15 +277,8 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
   volatile int* abort_flag = &abort_word;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // CTA c owns the contiguous rows [c N / G, (c+1) N / G), balanced to one row, in
-  // blocks of kBulkRows (the last one may be shorter).
-  const int64_t r0 = (int64_t)blockIdx.x * N / gridDim.x;
-  const int64_t r1 = (int64_t)(blockIdx.x + 1) * N / gridDim.x;
-  const int nb = (int)((r1 - r0 + kBulkRows - 1) / kBulkRows);
-  auto blk_row = [&](int b) { return r0 + (int64_t)b * kBulkRows; };
-  auto blk_rows = [&](int b) { const int64_t ra = blk_row(b); return (int)((r1 - ra < kBulkRows) ? (r1 - ra) : kBulkRows); };
-  const int64_t row_bytes = K / 2, groups = K / 64, nchunk = K / 32;
-  const int streams = kBulkConsumers / nj;   // row streams; warp (j, stream) = 1 + stream * nj + j
+  const int nb = (int)((r1 - r0 + RB - 1) / RB);
+  const int64_t last_rows = (r1 - r0) - (int64_t)(nb - 1) * RB;   // rows of the last block
 
   // Barrier setup and the first copies are issued before the CTA-wide barrier,
   // so the loads start while the other warps are still being set up.
@@ -221,20 +287,18 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
     mbar_init(xbar, 1);
     for (int s = 0; s < first; ++s) {
       mbar_init(full0 + 8u * s, 1);
-      mbar_init(empty0 + 8u * s, nj);   // one arrival per column-group warp
+      mbar_init(empty0 + 8u * s, nj);   // one arrival per work item of the block
     }
     abort_word = 0;
     fence_mbar_init();
     // x first (one copy per CTA: every warp reading it from global memory would hammer
-    // the same few L2 lines from every SM at once), then the weight blocks
+    // the same few L2 lines from every SM at once), then the first blocks
     mbar_expect_tx(xbar, (uint32_t)(K * 2));
     bulk_g2s(sbase + L.x_off, x, (uint32_t)(K * 2), xbar);
-    for (int b = 0; b < first; ++b) {
-      const int64_t ra = blk_row(b);
-      const uint32_t bytes = (uint32_t)(blk_rows(b) * row_bytes);
-      mbar_expect_tx(full0 + 8u * b, bytes);
-      bulk_g2s(sbase + L.slot_off + (uint32_t)b * L.slot_bytes, wq + ra * row_bytes, bytes, full0 + 8u * b);
-    }
+    for (int b = 0; b < first; ++b)
+      stream_issue(wq, sc_plane, plane_bytes, row_bytes, sc_row_bytes, r0 + (int64_t)b * RB,
+                   b == nb - 1 ? (int)last_rows : RB, sbase + L.code_off + (uint32_t)b * L.code_stride,
+                   sbase + L.sc_off + (uint32_t)b * L.sc_stride, full0 + 8u * b);
   }
   __syncthreads();
 
@@ -244,12 +308,10 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
     for (; b < nb; ++b) {
       const int s = b % slots;
       if (!warp_wait(empty0 + 8u * s, ((b / slots) & 1) ^ 1, abort_flag, &g_gemv_status)) break;
-      if (lane == 0) {
-        const int64_t ra = blk_row(b);
-        const uint32_t bytes = (uint32_t)(blk_rows(b) * row_bytes);
-        mbar_expect_tx(full0 + 8u * s, bytes);
-        bulk_g2s(sbase + L.slot_off + (uint32_t)s * L.slot_bytes, wq + ra * row_bytes, bytes, full0 + 8u * s);
-      }
+      if (lane == 0)
+        stream_issue(wq, sc_plane, plane_bytes, row_bytes, sc_row_bytes, r0 + (int64_t)b * RB,
+                     b == nb - 1 ? (int)last_rows : RB, sbase + L.code_off + (uint32_t)s * L.code_stride,
+                     sbase + L.sc_off + (uint32_t)s * L.sc_stride, full0 + 8u * s);
       __syncwarp();
     }
     if (b < nb && lane == 0) {  // aborted: let the copies already issued land before the CTA exits
@@ -258,43 +320,46 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
         mbar_drain(full0 + 8u * (d % slots), (d / slots) & 1);
     }
     __syncwarp();
-  } else if (warp - 1 < streams * nj) {
-    const int j = (warp - 1) % nj, stream = (warp - 1) / nj;
-    const int64_t c = (int64_t)j * 32 + lane;     // this lane's chunk
-    const bool c_ok = c < nchunk;
-    // this lane's 32 x values and their sum, kept in registers for every row
+  } else if (warp - 1 < nw) {
+    const int w = warp - 1;
+    const int items = nb * nj;
     float2 xv[16];
-    float xsum = 0.f;
-    const bool x_ok = warp_wait(xbar, 0, abort_flag, &g_gemv_status);
+    float bias = 0.f;
+    int cur_j = -1;
+    bool ok = warp_wait(xbar, 0, abort_flag, &g_gemv_status);
+    for (int it = w; ok && it < items; it += nw) {
+      const int b = it / nj, j = it - b * nj;
+      const int64_t c = (int64_t)j * 32 + lane;     // this lane's chunk
+      const bool c_ok = c < nchunk;
+      if (j != cur_j) {
+        // this lane's 32 x values and their sum, kept in registers while the group stays
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 v = (c_ok && x_ok) ? ld_shared_v4(sbase + L.x_off + (uint32_t)(c * 64 + q * 16))
-                                     : make_uint4(0, 0, 0, 0);
-      xv[4 * q + 0] = make_float2(bf16lo(v.x), bf16hi(v.x));
-      xv[4 * q + 1] = make_float2(bf16lo(v.y), bf16hi(v.y));
-      xv[4 * q + 2] = make_float2(bf16lo(v.z), bf16hi(v.z));
-      xv[4 * q + 3] = make_float2(bf16lo(v.w), bf16hi(v.w));
-    }
+        for (int q = 0; q < 4; ++q) {
+          const uint4 v = c_ok ? ld_shared_v4(sbase + L.x_off + (uint32_t)(c * 64 + q * 16)) : make_uint4(0, 0, 0, 0);
+          xv[4 * q + 0] = make_float2(bf16lo(v.x), bf16hi(v.x));
+          xv[4 * q + 1] = make_float2(bf16lo(v.y), bf16hi(v.y));
+          xv[4 * q + 2] = make_float2(bf16lo(v.z), bf16hi(v.z));
+          xv[4 * q + 3] = make_float2(bf16lo(v.w), bf16hi(v.w));
+        }
+        float2 xs2 = xv[0];
 #pragma unroll
-    for (int q = 0; q < 16; ++q) xsum += xv[q].x + xv[q].y;
-    const float bias = -136.f * xsum;
-
-    for (int b = stream; b < nb; b += streams) {
+        for (int q = 1; q < 16; ++q) xs2 = fadd2(xs2, xv[q]);
+        bias = -136.f * (xs2.x + xs2.y);
+        cur_j = j;
+      }
       const int s = b % slots;
-      const int64_t ra = blk_row(b);
-      const int nr = blk_rows(b);
-      float sc[kBulkRows];
-#pragma unroll
-      for (int i = 0; i < kBulkRows; ++i)
-        sc[i] = (c_ok && i < nr) ? fp16_bits_to_float(scales[(ra + i) * groups + (c >> 1)]) : 0.f;
       if (!warp_wait(full0 + 8u * s, (b / slots) & 1, abort_flag, &g_gemv_status)) break;
-      const uint32_t slot = sbase + L.slot_off + (uint32_t)s * L.slot_bytes;
-      float acc[kBulkRows];
+      const int nr = b == nb - 1 ? (int)last_rows : RB;
+      const uint32_t cslot = sbase + L.code_off + (uint32_t)s * L.code_stride;
+      const uint32_t sslot = sbase + L.sc_off + (uint32_t)s * L.sc_stride +
+                             (uint32_t)(((r0 + (int64_t)b * RB) * sc_row_bytes) & 15);
+      float acc[RB];
 #pragma unroll
-      for (int i = 0; i < kBulkRows; ++i) {
+      for (int i = 0; i < RB; ++i) {
         acc[i] = 0.f;
         if (i < nr && c_ok) {
-          const uint4 cw = ld_shared_v4(slot + (uint32_t)(i * row_bytes + c * 16));
+          const uint4 cw = ld_shared_v4(cslot + (uint32_t)(i * row_bytes + c * 16));
+          const float sc = fp16_bits_to_float(ld_shared_u16(sslot + (uint32_t)(i * sc_row_bytes + (c >> 1) * 2)));
           const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
           float2 p2 = make_float2(0.f, 0.f);
 #pragma unroll
@@ -305,16 +370,14 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
             p2 = ffma2(make_float2(f128_plus_byte<2>(lo), f128_plus_byte<2>(hi)), xv[4 * wi + 2], p2);
             p2 = ffma2(make_float2(f128_plus_byte<3>(lo), f128_plus_byte<3>(hi)), xv[4 * wi + 3], p2);
           }
-          acc[i] = sc[i] * ((p2.x + p2.y) + bias);
+          acc[i] = sc * ((p2.x + p2.y) + bias);
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8u * s);
-#pragma unroll
-      for (int i = 0; i < kBulkRows; ++i) {
-        const float v = warp_sum(acc[i]);
-        if (lane == 0 && i < nr) part[(b * kBulkRows + i) * nj + j] = v;
-      }
+      int row = 0;
+      const float v = reduce_rows<RB>(acc, lane, &row);
+      if ((lane & (32 / RB - 1)) == 0 && row < nr) part[((int64_t)b * RB + row) * nj + j] = v;
     }
   }
 
@@ -322,12 +385,10 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
   // reaches this barrier converged (all role loops are warp-uniform).
   __syncthreads();
   if (*abort_flag) return;
-  for (int64_t r = threadIdx.x; r < (int64_t)nb * kBulkRows; r += kBulkThreads) {
-    const int b = (int)(r / kBulkRows), i = (int)(r % kBulkRows);
-    if (i >= blk_rows(b)) continue;
+  for (int64_t r = threadIdx.x; r < r1 - r0; r += kStreamThreads) {
     float v = 0.f;
     for (int jj = 0; jj < nj; ++jj) v += part[r * nj + jj];
-    y[blk_row(b) + i] = float_to_bf16_bits(v);
+    y[r0 + r] = float_to_bf16_bits(v);
   }
 }
 
@@ -342,26 +403,34 @@ int gemv_launch_count(int64_t N, int64_t K, int64_t T) {
 
 struct StreamPlan {
   int64_t grid, rows_cap;
-  int nj, slots;
+  int rb, nj, nw, slots;
   uint32_t bytes;
 };
 
+// Rows per block: 8 if their code rows fit 32 KB, else 4 if they fit 40 KB, else 2;
+// the ring gets as many slots as the shared-memory budget holds (at least 2).
 static bool stream_plan(int64_t N, int64_t K, int nsm, StreamPlan* p) {
+  if (N < 1 || K < 128) return false;
   const int64_t nchunk = K / 32;
   p->nj = (int)((nchunk + 31) / 32);
-  if (p->nj > kBulkConsumers) return false;
+  // consumer warps: a multiple of the group count (no x reloads) unless that idles
+  // more than 3 of the 15, then all 15 (a warp reloads x when its group changes)
+  const int whole = p->nj <= kStreamConsumers ? (kStreamConsumers / p->nj) * p->nj : 0;
+  p->nw = whole >= kStreamConsumers - 3 ? whole : kStreamConsumers;
+  p->rb = 8 * (K / 2) <= 32768 ? 8 : 4 * (K / 2) <= 40960 ? 4 : 2;
   p->grid = (N + 3) / 4;  // at least 4 rows per CTA
   if (p->grid > nsm) p->grid = nsm;
   if (p->grid < 1) p->grid = 1;
-  p->rows_cap = ((N + p->grid - 1) / p->grid + kBulkRows - 1) / kBulkRows * kBulkRows;
-  const int64_t budget = kBulkSmemBudget;
-  const StreamLayout L0 = stream_layout(K, p->rows_cap, p->nj, 0);
-  const int64_t per = (int64_t)kBulkRows * (K / 2) + 16;
-  int64_t s = (budget - L0.slot_off - 128) / per;
+  p->rows_cap = ((N + p->grid - 1) / p->grid + p->rb - 1) / p->rb * p->rb;
+  const int64_t budget = kStreamSmemBudget;
+  const StreamLayout L0 = stream_layout(K, p->rb, p->rows_cap, p->nj, 0);
+  const int64_t per = (int64_t)L0.code_stride + L0.sc_stride + 16;
+  if ((int64_t)L0.code_off + 128 > budget) return false;
+  int64_t s = (budget - L0.code_off - 128) / per;
   if (s > 32) s = 32;
-  if (s < 4) return false;
+  if (s < 2) return false;
   p->slots = (int)s;
-  p->bytes = stream_layout(K, p->rows_cap, p->nj, p->slots).bytes;
+  p->bytes = stream_layout(K, p->rb, p->rows_cap, p->nj, p->slots).bytes;
   return p->bytes <= budget;
 }
 
@@ -376,15 +445,14 @@ static int device_sms() {
   return n;
 }
 
-static int gemv_stream_launch(const LinearArgs& a) {
+template <int RB>
+static int gemv_stream_launch_rb(const LinearArgs& a, const StreamPlan& pl) {
   static bool attr[64] = {};
   int dev = 0;
   if (cuda_check(cudaGetDevice(&dev), "cudaGetDevice")) return Q4LIN_ERR_CUDA;
-  StreamPlan pl;
-  if (!stream_plan(a.N, a.K, device_sms(), &pl)) return Q4LIN_ERR_INVALID_ARG;
   if (dev >= 64 || !attr[dev]) {
-    if (cuda_check(cudaFuncSetAttribute(q4_gemv_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)kBulkSmemBudget),
+    if (cuda_check(cudaFuncSetAttribute(q4_gemv_stream_kernel<RB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)kStreamSmemBudget),
                    "gemv: cudaFuncSetAttribute"))
       return Q4LIN_ERR_CUDA;
     if (dev < 64) attr[dev] = true;
@@ -392,7 +460,7 @@ static int gemv_stream_launch(const LinearArgs& a) {
   // programmatic dependent launch: the kernel waits for its predecessor before touching memory
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)pl.grid, 1, 1);
-  cfg.blockDim = dim3(kBulkThreads, 1, 1);
+  cfg.blockDim = dim3(kStreamThreads, 1, 1);
   cfg.dynamicSmemBytes = pl.bytes;
   cfg.stream = a.stream;
   cudaLaunchAttribute at[1];
@@ -400,9 +468,19 @@ static int gemv_stream_launch(const LinearArgs& a) {
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cuda_check(cudaLaunchKernelEx(&cfg, q4_gemv_stream_kernel, a.wq, a.scales, a.x, a.y, a.N, a.K, pl.rows_cap,
-                                       pl.nj, pl.slots),
+  return cuda_check(cudaLaunchKernelEx(&cfg, q4_gemv_stream_kernel<RB>, a.wq, a.scales, a.x, a.y, a.N, a.K,
+                                       pl.rows_cap, pl.nj, pl.nw, pl.slots),
                     "gemv: streaming kernel launch");
+}
+
+static int gemv_stream_launch(const LinearArgs& a) {
+  StreamPlan pl;
+  if (!stream_plan(a.N, a.K, device_sms(), &pl)) return Q4LIN_ERR_INVALID_ARG;
+  switch (pl.rb) {
+    case 8: return gemv_stream_launch_rb<8>(a, pl);
+    case 4: return gemv_stream_launch_rb<4>(a, pl);
+    default: return gemv_stream_launch_rb<2>(a, pl);
+  }
 }
 
 bool gemv_stream_ok(int64_t N, int64_t K, int64_t T) {
