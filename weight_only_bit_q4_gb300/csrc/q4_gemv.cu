@@ -177,16 +177,17 @@ struct StreamLayout {
   uint32_t x_off, part_off, bar_off, code_off, code_stride, sc_off, sc_stride, bytes;
 };
 
-// x (bf16, K elements), partial sums [rows_cap][nj] fp32, the x barrier and the
-// full/empty barriers, the code slots (128-byte aligned) and the scale slots
-// (16-byte aligned; a block's run of scales plus up to 15 bytes of alignment
-// slack on either side).
-__host__ __device__ inline StreamLayout stream_layout(int64_t K, int rb, int64_t rows_cap, int nj, int slots) {
+// x (bf16, K elements), partial sums [rows_cap][nj] fp32, the x barrier, nfull
+// "block landed" barriers and `slots` "slot free" barriers, the code slots
+// (128-byte aligned) and the scale slots (16-byte aligned; a block's run of
+// scales plus up to 15 bytes of alignment slack on either side).
+__host__ __device__ inline StreamLayout stream_layout(int64_t K, int rb, int64_t rows_cap, int nj, int slots,
+                                                      int nfull) {
   StreamLayout L;
   L.x_off = 0;
   L.part_off = (uint32_t)(K * 2);
   L.bar_off = (uint32_t)((L.part_off + rows_cap * nj * 4 + 15) / 16 * 16);
-  L.code_off = (L.bar_off + 8 + (uint32_t)slots * 16 + 127) / 128 * 128;
+  L.code_off = (L.bar_off + 8 + (uint32_t)(nfull + slots) * 8 + 127) / 128 * 128;
   L.code_stride = (uint32_t)((rb * (K / 2) + 127) / 128 * 128);
   L.sc_off = L.code_off + (uint32_t)slots * L.code_stride;
   L.sc_stride = (uint32_t)((rb * (K / 32) + 32 + 15) / 16 * 16);
@@ -246,7 +247,7 @@ template <int RB>
 __global__ void __launch_bounds__(kStreamThreads, 1)
 q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict__ scales,
                       const uint16_t* __restrict__ x, uint16_t* __restrict__ y, int64_t N, int64_t K,
-                      int64_t rows_cap, int nj, int nw, int slots) {
+                      int64_t rows_cap, int nj, int nw, int slots, int nfull) {
   extern __shared__ __align__(128) uint8_t smem[];
   pdl_launch_dependents();
   const int64_t r0 = (int64_t)blockIdx.x * N / gridDim.x;
@@ -268,11 +269,11 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
       bulk_prefetch_l2(sc_plane + off, (uint32_t)(a1 - off < 32768 ? a1 - off : 32768));
   }
   pdl_wait_previous();  // before any global-memory read that must see the previous kernel's writes
-  const StreamLayout L = stream_layout(K, RB, rows_cap, nj, slots);
+  const StreamLayout L = stream_layout(K, RB, rows_cap, nj, slots, nfull);
   float* part = reinterpret_cast<float*>(smem + L.part_off);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t xbar = sbase + L.bar_off;
-  const uint32_t full0 = xbar + 8, empty0 = full0 + 8u * slots;
+  const uint32_t full0 = xbar + 8, empty0 = full0 + 8u * nfull;
   __shared__ int abort_word;
   volatile int* abort_flag = &abort_word;
 
@@ -285,10 +286,8 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
   const int first = nb < slots ? nb : slots;
   if (threadIdx.x == 0) {
     mbar_init(xbar, 1);
-    for (int s = 0; s < first; ++s) {
-      mbar_init(full0 + 8u * s, 1);
-      mbar_init(empty0 + 8u * s, nj);   // one arrival per work item of the block
-    }
+    for (int f = 0; f < nfull; ++f) mbar_init(full0 + 8u * f, 1);
+    for (int s = 0; s < slots; ++s) mbar_init(empty0 + 8u * s, nj);   // one arrival per work item
     abort_word = 0;
     fence_mbar_init();
     // x first (one copy per CTA: every warp reading it from global memory would hammer
@@ -311,31 +310,39 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
       if (lane == 0)
         stream_issue(wq, sc_plane, plane_bytes, row_bytes, sc_row_bytes, r0 + (int64_t)b * RB,
                      b == nb - 1 ? (int)last_rows : RB, sbase + L.code_off + (uint32_t)s * L.code_stride,
-                     sbase + L.sc_off + (uint32_t)s * L.sc_stride, full0 + 8u * s);
+                     sbase + L.sc_off + (uint32_t)s * L.sc_stride, full0 + 8u * (b % nfull));
       __syncwarp();
     }
     if (b < nb && lane == 0) {  // aborted: let the copies already issued land before the CTA exits
       mbar_drain(xbar, 0);
       for (int d = (b - slots > 0 ? b - slots : 0); d < b; ++d)
-        mbar_drain(full0 + 8u * (d % slots), (d / slots) & 1);
+        mbar_drain(full0 + 8u * (d % nfull), (d / nfull) & 1);
     }
     __syncwarp();
   } else if (warp - 1 < nw) {
     const int w = warp - 1;
     const int items = nb * nj;
+    const uint32_t rowb = (uint32_t)row_bytes, scrb = (uint32_t)sc_row_bytes;
+    // alignment slack of block 0's scale run in its slot; block b's is (d0 + b RB scrb) mod 16
+    const uint32_t d0 = (uint32_t)((r0 * sc_row_bytes) & 15);
     float2 xv[16];
     float bias = 0.f;
     int cur_j = -1;
+    // item it = w, w + nw, ...: block b = it / nj and group j = it % nj, the block's slot
+    // s = b % slots, and its "landed" barrier fb = b % nfull with phase parity
+    // fph = (b / nfull) & 1, all advanced incrementally
+    int b = w / nj, j = w - (w / nj) * nj;
+    const int db = nw / nj, dj = nw - (nw / nj) * nj;
+    int s = b % slots, fb = b % nfull, fph = (b / nfull) & 1;
     bool ok = warp_wait(xbar, 0, abort_flag, &g_gemv_status);
     for (int it = w; ok && it < items; it += nw) {
-      const int b = it / nj, j = it - b * nj;
-      const int64_t c = (int64_t)j * 32 + lane;     // this lane's chunk
-      const bool c_ok = c < nchunk;
+      const uint32_t c = (uint32_t)j * 32u + (uint32_t)lane;     // this lane's chunk
+      const bool c_ok = c < (uint32_t)nchunk;
       if (j != cur_j) {
         // this lane's 32 x values and their sum, kept in registers while the group stays
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const uint4 v = c_ok ? ld_shared_v4(sbase + L.x_off + (uint32_t)(c * 64 + q * 16)) : make_uint4(0, 0, 0, 0);
+          const uint4 v = c_ok ? ld_shared_v4(sbase + L.x_off + c * 64u + (uint32_t)q * 16u) : make_uint4(0, 0, 0, 0);
           xv[4 * q + 0] = make_float2(bf16lo(v.x), bf16hi(v.x));
           xv[4 * q + 1] = make_float2(bf16lo(v.y), bf16hi(v.y));
           xv[4 * q + 2] = make_float2(bf16lo(v.z), bf16hi(v.z));
@@ -347,19 +354,18 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
         bias = -136.f * (xs2.x + xs2.y);
         cur_j = j;
       }
-      const int s = b % slots;
-      if (!warp_wait(full0 + 8u * s, (b / slots) & 1, abort_flag, &g_gemv_status)) break;
+      if (!warp_wait(full0 + 8u * fb, fph, abort_flag, &g_gemv_status)) break;
       const int nr = b == nb - 1 ? (int)last_rows : RB;
-      const uint32_t cslot = sbase + L.code_off + (uint32_t)s * L.code_stride;
-      const uint32_t sslot = sbase + L.sc_off + (uint32_t)s * L.sc_stride +
-                             (uint32_t)(((r0 + (int64_t)b * RB) * sc_row_bytes) & 15);
+      const uint32_t crow = sbase + L.code_off + (uint32_t)s * L.code_stride + c * 16u;
+      const uint32_t srow = sbase + L.sc_off + (uint32_t)s * L.sc_stride +
+                            ((d0 + (uint32_t)b * (uint32_t)RB * scrb) & 15u) + (c >> 1) * 2u;
       float acc[RB];
 #pragma unroll
       for (int i = 0; i < RB; ++i) {
         acc[i] = 0.f;
         if (i < nr && c_ok) {
-          const uint4 cw = ld_shared_v4(cslot + (uint32_t)(i * row_bytes + c * 16));
-          const float sc = fp16_bits_to_float(ld_shared_u16(sslot + (uint32_t)(i * sc_row_bytes + (c >> 1) * 2)));
+          const uint4 cw = ld_shared_v4(crow + (uint32_t)i * rowb);
+          const float sc = fp16_bits_to_float(ld_shared_u16(srow + (uint32_t)i * scrb));
           const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
           float2 p2 = make_float2(0.f, 0.f);
 #pragma unroll
@@ -377,7 +383,22 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
       if (lane == 0) mbar_arrive(empty0 + 8u * s);
       int row = 0;
       const float v = reduce_rows<RB>(acc, lane, &row);
-      if ((lane & (32 / RB - 1)) == 0 && row < nr) part[((int64_t)b * RB + row) * nj + j] = v;
+      if ((lane & (32 / RB - 1)) == 0 && row < nr) part[(b * RB + row) * nj + j] = v;
+      // next item
+      int nb_step = db;
+      j += dj;
+      if (j >= nj) {
+        j -= nj;
+        ++nb_step;
+      }
+      b += nb_step;
+      s += nb_step;
+      while (s >= slots) s -= slots;
+      fb += nb_step;
+      while (fb >= nfull) {
+        fb -= nfull;
+        fph ^= 1;
+      }
     }
   }
 
@@ -403,7 +424,7 @@ int gemv_launch_count(int64_t N, int64_t K, int64_t T) {
 
 struct StreamPlan {
   int64_t grid, rows_cap;
-  int rb, nj, nw, slots;
+  int rb, nj, nw, slots, nfull;
   uint32_t bytes;
 };
 
@@ -422,15 +443,22 @@ static bool stream_plan(int64_t N, int64_t K, int nsm, StreamPlan* p) {
   if (p->grid > nsm) p->grid = nsm;
   if (p->grid < 1) p->grid = 1;
   p->rows_cap = ((N + p->grid - 1) / p->grid + p->rb - 1) / p->rb * p->rb;
+  // A consumer waiting for block b has consumed its previous block, at most `lead`
+  // blocks earlier, so every block up to lead + slots before b has landed (the
+  // producer refills a slot only after its block was consumed).  With
+  // slots + lead "landed" barriers, block b's barrier was last used by a block
+  // that has landed, so a parity wait can never match a phase two behind.
+  const int lead = p->nw / p->nj + (p->nw % p->nj != 0 ? 1 : 0);
   const int64_t budget = kStreamSmemBudget;
-  const StreamLayout L0 = stream_layout(K, p->rb, p->rows_cap, p->nj, 0);
+  const StreamLayout L0 = stream_layout(K, p->rb, p->rows_cap, p->nj, 0, lead);
   const int64_t per = (int64_t)L0.code_stride + L0.sc_stride + 16;
   if ((int64_t)L0.code_off + 128 > budget) return false;
   int64_t s = (budget - L0.code_off - 128) / per;
   if (s > 32) s = 32;
   if (s < 2) return false;
   p->slots = (int)s;
-  p->bytes = stream_layout(K, p->rb, p->rows_cap, p->nj, p->slots).bytes;
+  p->nfull = p->slots + lead;
+  p->bytes = stream_layout(K, p->rb, p->rows_cap, p->nj, p->slots, p->nfull).bytes;
   return p->bytes <= budget;
 }
 
@@ -469,7 +497,7 @@ static int gemv_stream_launch_rb(const LinearArgs& a, const StreamPlan& pl) {
   cfg.attrs = at;
   cfg.numAttrs = 1;
   return cuda_check(cudaLaunchKernelEx(&cfg, q4_gemv_stream_kernel<RB>, a.wq, a.scales, a.x, a.y, a.N, a.K,
-                                       pl.rows_cap, pl.nj, pl.nw, pl.slots),
+                                       pl.rows_cap, pl.nj, pl.nw, pl.slots, pl.nfull),
                     "gemv: streaming kernel launch");
 }
 
