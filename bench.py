@@ -48,6 +48,8 @@ WORKLOADS = {
     "q4_14336x5120": (14336, 5120, None, "lognormal", True, 0, None),       # --t in {1,16,128,1024}
     "q4_34816x5120_t1024": (34816, 5120, 1024, "halfnormal", False, 0, 0),
     "q4_5120x17408_t1024": (5120, 17408, 1024, "halfnormal", False, 0, 0),
+    "q4_34816x5120": (34816, 5120, None, "halfnormal", False, 0, None),      # --t (profiling long weights)
+    "q4_5120x17408": (5120, 17408, None, "halfnormal", False, 0, None),      # --t (profiling deep K)
 }
 DEFAULT_WORKLOAD = "q4_6144x5120_t1"
 
@@ -354,6 +356,7 @@ def measure_ours(args, wl, rank, world, local):
 
     return dict(per_call_us=per_call_us, total_ms=total_ms, calls=calls, copies=R, cold_us=cold_us,
                 clocks=clocks, route=q4lin.ROUTE_NAMES.get(route, str(route)), launches=launches, e2e=e2e,
+                tile=dict(zip(("n", "split_k"), q4lin.tile_plan(N, K, T))),
                 ws_bytes=ws_n)
 
 
@@ -504,6 +507,7 @@ def main(argv=None):
         "dtype": "f32" if res["route"] == "gemv" else "bf16xbf16->f32",
         "data": "synthetic",
         "config": {"workload": wl["name"], "N": N, "K": K, "T": T, "route": res["route"],
+                   "tile": res["tile"],
                    "timing": f"steady state: CUDA graph of {res['copies']} back-to-back calls replayed, events per replay",
                    "l2": f"inputs larger than L2: {res['copies']} rotating copies of weights, X and Y "
                          f"({res['copies'] * mb / 1e6:.0f} MB)",

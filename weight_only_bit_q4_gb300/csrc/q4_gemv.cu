@@ -139,17 +139,22 @@ q4_gemv_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict__ scal
 // items w, w + W, w + 2W, ...  Where a multiple of the group count between 12
 // and 15 exists, W is that multiple, so a warp keeps one column group and its
 // 32 x values per lane in registers for the whole kernel; otherwise W = 15 and
-// a warp reloads its x values from shared memory whenever its group changes.  Per item a lane decodes one conflict-free 16-byte code chunk
-// per row into (128 + q) floats with byte permutes, accumulates with packed
-// FP32 FMAs, applies (partial - 136 * sum x) * s, and the warp reduces the RB
-// row partials with a halving butterfly (each exchange hands half of the
-// remaining rows to the partner lane, so RB rows cost log2(RB) + 5 shuffle
-// rounds instead of 5 RB).  The column-group partials of a row are summed in a
-// fixed order at the end (deterministic), then rounded to bf16.
+// a warp reloads its x values from shared memory whenever its group changes.
+// Per item a lane decodes one conflict-free 16-byte code chunk per row into
+// (128 + q) floats with byte permutes, accumulates with packed FP32 FMAs,
+// applies (partial - 136 * sum x) * s, and the warp reduces the RB row partials
+// with a halving butterfly (each exchange hands half of the remaining rows to
+// the partner lane, so 8 rows take 9 shuffles instead of 40).  The
+// column-group partials of a row are summed in a fixed order at the end
+// (deterministic), then rounded to bf16.
 constexpr int kStreamThreads = 512;
 constexpr int kStreamConsumers = 15;   // warps 1..15
 constexpr int64_t kStreamSmemBudget = 232448 - 1024;
-constexpr int64_t kPrefetchCapBytes = 512 * 1024;   // L2 prefetch of one CTA's codes, at most
+// L2 prefetch of one CTA's codes before the dependency wait, at most.  Enough to
+// cover the start of the CTA's stream; prefetching a whole large share competes
+// with the ring's own copies (measured: 34816 x 5120 takes 31.8 us with 512 KB,
+// 27.7 us with 64 KB; the 6144 x 5120 decode call is 7.8 us either way).
+constexpr int64_t kPrefetchCapBytes = 64 * 1024;
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
@@ -256,15 +261,16 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
   const int64_t plane_bytes = N * sc_row_bytes;
   const uint8_t* sc_plane = reinterpret_cast<const uint8_t*>(scales);
   if (threadIdx.x == 0) {
-    // While the previous kernel finishes, start this CTA's rows on their way into L2:
-    // the first kPrefetchCapBytes of its codes, and the 16-byte-aligned interior of its
-    // scale run (never past it), 32 KB per prefetch.
+    // While the previous kernel finishes, start the head of this CTA's rows on their way
+    // into L2: the first kPrefetchCapBytes of its codes, and the 16-byte-aligned interior
+    // of those rows' scale run (never past it), 32 KB per prefetch.
     const uint8_t* cb = wq + r0 * row_bytes;
     int64_t len = (r1 - r0) * row_bytes;
     if (len > kPrefetchCapBytes) len = kPrefetchCapBytes;
     for (int64_t off = 0; off < len; off += 32768)
       bulk_prefetch_l2(cb + off, (uint32_t)(len - off < 32768 ? len - off : 32768));
-    const int64_t a0 = (r0 * sc_row_bytes + 15) & ~(int64_t)15, a1 = (r1 * sc_row_bytes) & ~(int64_t)15;
+    const int64_t pf_end = r0 + (len + row_bytes - 1) / row_bytes;   // <= r1
+    const int64_t a0 = (r0 * sc_row_bytes + 15) & ~(int64_t)15, a1 = (pf_end * sc_row_bytes) & ~(int64_t)15;
     for (int64_t off = a0; off < a1; off += 32768)
       bulk_prefetch_l2(sc_plane + off, (uint32_t)(a1 - off < 32768 ? a1 - off : 32768));
   }
