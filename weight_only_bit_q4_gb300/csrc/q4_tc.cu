@@ -356,6 +356,10 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
     const int quad = warp & 3;                  // TMEM lane quadrant
     const int cq = (warp - 12) >> 2;            // column chunk
     const int r_acc = quad * 32 + lane;         // tile row
+    // Release an accumulator buffer as soon as its last 16-column chunk is read
+    // (before that chunk's FMAs) where a thread reads 64 columns per group: measured
+    // 10 % faster at BN = 256 and BN = 64, 3 % slower at BN = 128 (32 columns).
+    constexpr bool kEarlyRelease = kCols >= 64 && kCols % 16 == 0;
     float2 acc[kCols / 2];
 #pragma unroll
     for (int i = 0; i < kCols / 2; ++i) acc[i] = make_float2(0.f, 0.f);
@@ -381,6 +385,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
       const float sf = fp16_bits_to_float((uint16_t)((ga & 1) ? (s_cur >> 16) : (s_cur & 0xFFFFu)));
       const float2 s2 = make_float2(sf, sf);
       acc_ok = acc_ok && warp_wait(mma_done(i), ring_par(i), abort_flag, &g_tc_status);
+      bool released = false;
       if (acc_ok) {
         tc_fence_after();
         const uint32_t dcol = tlane + (uint32_t)(b * BN);
@@ -391,6 +396,14 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
             uint32_t v[16];
             tmem_ld_cols<16>(dcol + c, v);
             tmem_ld_wait();
+            if (kEarlyRelease && c + 16 == kCols) {
+              // the whole partial is in registers: hand buffer b back to the MMA
+              // before the last chunk's FMAs
+              tc_fence_before();
+              __syncwarp();
+              if (i + NB < ng) named_bar_arrive(issue_bar(i + NB), L::issue_threads);
+              released = true;
+            }
 #pragma unroll
             for (int j = 0; j < 16; j += 2)
               acc[(c + j) / 2] = ffma2(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), s2, acc[(c + j) / 2]);
@@ -417,9 +430,11 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (i + NB < ng) named_bar_arrive(issue_bar(i + NB), L::issue_threads);  // buffer b is free for group i + NB
+      if (!released) {
+        tc_fence_before();
+        __syncwarp();
+        if (i + NB < ng) named_bar_arrive(issue_bar(i + NB), L::issue_threads);  // buffer b is free for group i + NB
+      }
     }
 
     // ----------------------------------------------------------- split-K reduction across the cluster
@@ -621,7 +636,7 @@ struct TileCost {
   double fixed_ns;
 };
 constexpr TileCost kTileCost[] = {
-    {16, 310.0, 4300.0}, {32, 330.0, 4400.0}, {64, 380.0, 4700.0}, {128, 440.0, 5300.0}, {256, 700.0, 8300.0}};
+    {16, 310.0, 4300.0}, {32, 330.0, 4400.0}, {64, 335.0, 6500.0}, {128, 440.0, 5300.0}, {256, 615.0, 7800.0}};
 constexpr double kSplitNsPerColumn = 22.0;
 
 const TileCost& tile_cost(int bn) {
