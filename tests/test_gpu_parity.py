@@ -105,17 +105,20 @@ def test_ragged_shapes(route, N, K, T):
     assert_close(run(*to_dev(wq, s, x), route), y_ref, f"{q4lin.ROUTE_NAMES[route]} {N}x{K} T={T}")
 
 
+@pytest.mark.parametrize("T", [1, 2, 3, 4])
 @pytest.mark.parametrize("N,K", [(1, 128), (3, 128), (5, 128), (607, 384), (153, 1152), (1001, 4096),
                                  (999, 8192), (333, 8320), (150, 14336), (257, 17408), (77, 28672),
                                  (61, 49152), (10, 65536)])
-def test_decode_gemv_shapes(N, K):
-    """T = 1 across K: 8-, 4- and 2-row blocks, warps that keep or reload their x
-    values, scale runs that end inside the plane's last 16-byte granule (N K / 32
-    not a multiple of 16), one row per CTA, and a K beyond the streaming kernel."""
-    wq, s, x = synth.make_problem(N, K, 1, w_seed=N + K, x_seed=K)
+def test_decode_gemv_shapes(N, K, T):
+    """T = 1..4 on the GEMV route across K: 8-, 4- and 2-row blocks, 32- and
+    16-weight lane chunks, warps that keep or reload their x values, scale runs
+    that end inside the plane's last 16-byte granule (N K / 32 not a multiple of
+    16), one row per CTA, and shapes beyond the streaming kernel's shared memory."""
+    wq, s, x = synth.make_problem(N, K, T, w_seed=N + K, x_seed=K + T)
     y_ref = oracle.linear(wq, s, x)
-    assert_close(run(*to_dev(wq, s, x)), y_ref, f"decode {N}x{K}")
-    assert_close(run(*to_dev(wq, s, x), q4lin.ROUTE_GEMV), y_ref, f"decode gemv {N}x{K}")
+    assert_close(run(*to_dev(wq, s, x), q4lin.ROUTE_GEMV), y_ref, f"decode gemv {N}x{K} T={T}")
+    if T == 1:
+        assert_close(run(*to_dev(wq, s, x)), y_ref, f"decode {N}x{K}")
 
 
 # ------------------------------------------------------------ edge cases and guards

@@ -168,6 +168,12 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+__device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ uint16_t ld_shared_u16(uint32_t addr) {
   uint16_t v;
   asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
@@ -182,16 +188,16 @@ struct StreamLayout {
   uint32_t x_off, part_off, bar_off, code_off, code_stride, sc_off, sc_stride, bytes;
 };
 
-// x (bf16, K elements), partial sums [rows_cap][nj] fp32, the x barrier, nfull
+// x (bf16, TT rows of K), partial sums [rows_cap][nj][TT] fp32, the x barrier, nfull
 // "block landed" barriers and `slots` "slot free" barriers, the code slots
 // (128-byte aligned) and the scale slots (16-byte aligned; a block's run of
 // scales plus up to 15 bytes of alignment slack on either side).
-__host__ __device__ inline StreamLayout stream_layout(int64_t K, int rb, int64_t rows_cap, int nj, int slots,
+__host__ __device__ inline StreamLayout stream_layout(int64_t K, int tt, int rb, int64_t rows_cap, int nj, int slots,
                                                       int nfull) {
   StreamLayout L;
   L.x_off = 0;
-  L.part_off = (uint32_t)(K * 2);
-  L.bar_off = (uint32_t)((L.part_off + rows_cap * nj * 4 + 15) / 16 * 16);
+  L.part_off = (uint32_t)(tt * K * 2);
+  L.bar_off = (uint32_t)((L.part_off + rows_cap * nj * tt * 4 + 15) / 16 * 16);
   L.code_off = (L.bar_off + 8 + (uint32_t)(nfull + slots) * 8 + 127) / 128 * 128;
   L.code_stride = (uint32_t)((rb * (K / 2) + 127) / 128 * 128);
   L.sc_off = L.code_off + (uint32_t)slots * L.code_stride;
@@ -248,16 +254,23 @@ __device__ __forceinline__ float reduce_rows(const float (&acc)[RB], int lane, i
   return a[0];
 }
 
-template <int RB>
+template <int RB, int TT>
 __global__ void __launch_bounds__(kStreamThreads, 1)
 q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict__ scales,
                       const uint16_t* __restrict__ x, uint16_t* __restrict__ y, int64_t N, int64_t K,
                       int64_t rows_cap, int nj, int nw, int slots, int nfull) {
+  // A lane's chunk: 16 code bytes (32 weights) for one token, 8 code bytes (16
+  // weights) for several, so the x values of every token fit in registers.
+  constexpr int kCW = TT == 1 ? 16 : 8;           // code bytes per lane chunk
+  constexpr int kCV = 2 * kCW;                    // weights per lane chunk
+  constexpr int kWords = kCW / 4;                 // 32-bit code words per chunk
+  constexpr int kTP = TT == 1 ? 1 : TT == 2 ? 2 : 4;   // tokens padded to a power of two
+  static_assert(RB * kTP <= 32, "one butterfly reduces at most 32 partials");
   extern __shared__ __align__(128) uint8_t smem[];
   pdl_launch_dependents();
   const int64_t r0 = (int64_t)blockIdx.x * N / gridDim.x;
   const int64_t r1 = (int64_t)(blockIdx.x + 1) * N / gridDim.x;
-  const int64_t row_bytes = K / 2, sc_row_bytes = K / 32, nchunk = K / 32;
+  const int64_t row_bytes = K / 2, sc_row_bytes = K / 32, nchunk = K / kCV;
   const int64_t plane_bytes = N * sc_row_bytes;
   const uint8_t* sc_plane = reinterpret_cast<const uint8_t*>(scales);
   if (threadIdx.x == 0) {
@@ -275,7 +288,7 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
       bulk_prefetch_l2(sc_plane + off, (uint32_t)(a1 - off < 32768 ? a1 - off : 32768));
   }
   pdl_wait_previous();  // before any global-memory read that must see the previous kernel's writes
-  const StreamLayout L = stream_layout(K, RB, rows_cap, nj, slots, nfull);
+  const StreamLayout L = stream_layout(K, TT, RB, rows_cap, nj, slots, nfull);
   float* part = reinterpret_cast<float*>(smem + L.part_off);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t xbar = sbase + L.bar_off;
@@ -298,8 +311,8 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
     fence_mbar_init();
     // x first (one copy per CTA: every warp reading it from global memory would hammer
     // the same few L2 lines from every SM at once), then the first blocks
-    mbar_expect_tx(xbar, (uint32_t)(K * 2));
-    bulk_g2s(sbase + L.x_off, x, (uint32_t)(K * 2), xbar);
+    mbar_expect_tx(xbar, (uint32_t)(TT * K * 2));
+    bulk_g2s(sbase + L.x_off, x, (uint32_t)(TT * K * 2), xbar);
     for (int b = 0; b < first; ++b)
       stream_issue(wq, sc_plane, plane_bytes, row_bytes, sc_row_bytes, r0 + (int64_t)b * RB,
                    b == nb - 1 ? (int)last_rows : RB, sbase + L.code_off + (uint32_t)b * L.code_stride,
@@ -331,8 +344,8 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
     const uint32_t rowb = (uint32_t)row_bytes, scrb = (uint32_t)sc_row_bytes;
     // alignment slack of block 0's scale run in its slot; block b's is (d0 + b RB scrb) mod 16
     const uint32_t d0 = (uint32_t)((r0 * sc_row_bytes) & 15);
-    float2 xv[16];
-    float bias = 0.f;
+    float2 xv[TT][kCV / 2];
+    float bias[TT];
     int cur_j = -1;
     // item it = w, w + nw, ...: block b = it / nj and group j = it % nj, the block's slot
     // s = b % slots, and its "landed" barrier fb = b % nfull with phase parity
@@ -345,51 +358,76 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
       const uint32_t c = (uint32_t)j * 32u + (uint32_t)lane;     // this lane's chunk
       const bool c_ok = c < (uint32_t)nchunk;
       if (j != cur_j) {
-        // this lane's 32 x values and their sum, kept in registers while the group stays
+        // this lane's x values of every token and their sums, kept in registers while the
+        // group stays
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint4 v = c_ok ? ld_shared_v4(sbase + L.x_off + c * 64u + (uint32_t)q * 16u) : make_uint4(0, 0, 0, 0);
-          xv[4 * q + 0] = make_float2(bf16lo(v.x), bf16hi(v.x));
-          xv[4 * q + 1] = make_float2(bf16lo(v.y), bf16hi(v.y));
-          xv[4 * q + 2] = make_float2(bf16lo(v.z), bf16hi(v.z));
-          xv[4 * q + 3] = make_float2(bf16lo(v.w), bf16hi(v.w));
+        for (int t = 0; t < TT; ++t) {
+#pragma unroll
+          for (int q = 0; q < kCV / 8; ++q) {
+            const uint4 v = c_ok ? ld_shared_v4(sbase + L.x_off + (uint32_t)t * (uint32_t)(K * 2) + c * (uint32_t)(kCV * 2) +
+                                                (uint32_t)q * 16u)
+                                 : make_uint4(0, 0, 0, 0);
+            xv[t][4 * q + 0] = make_float2(bf16lo(v.x), bf16hi(v.x));
+            xv[t][4 * q + 1] = make_float2(bf16lo(v.y), bf16hi(v.y));
+            xv[t][4 * q + 2] = make_float2(bf16lo(v.z), bf16hi(v.z));
+            xv[t][4 * q + 3] = make_float2(bf16lo(v.w), bf16hi(v.w));
+          }
+          float2 xs2 = xv[t][0];
+#pragma unroll
+          for (int q = 1; q < kCV / 2; ++q) xs2 = fadd2(xs2, xv[t][q]);
+          bias[t] = -136.f * (xs2.x + xs2.y);
         }
-        float2 xs2 = xv[0];
-#pragma unroll
-        for (int q = 1; q < 16; ++q) xs2 = fadd2(xs2, xv[q]);
-        bias = -136.f * (xs2.x + xs2.y);
         cur_j = j;
       }
       if (!warp_wait(full0 + 8u * fb, fph, abort_flag, &g_gemv_status)) break;
       const int nr = b == nb - 1 ? (int)last_rows : RB;
-      const uint32_t crow = sbase + L.code_off + (uint32_t)s * L.code_stride + c * 16u;
+      const uint32_t crow = sbase + L.code_off + (uint32_t)s * L.code_stride + c * (uint32_t)kCW;
       const uint32_t srow = sbase + L.sc_off + (uint32_t)s * L.sc_stride +
-                            ((d0 + (uint32_t)b * (uint32_t)RB * scrb) & 15u) + (c >> 1) * 2u;
-      float acc[RB];
+                            ((d0 + (uint32_t)b * (uint32_t)RB * scrb) & 15u) + (c * (uint32_t)kCV / 64u) * 2u;
+      float acc[RB * kTP];
+#pragma unroll
+      for (int i = 0; i < RB * kTP; ++i) acc[i] = 0.f;
 #pragma unroll
       for (int i = 0; i < RB; ++i) {
-        acc[i] = 0.f;
         if (i < nr && c_ok) {
-          const uint4 cw = ld_shared_v4(crow + (uint32_t)i * rowb);
-          const float sc = fp16_bits_to_float(ld_shared_u16(srow + (uint32_t)i * scrb));
-          const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-          float2 p2 = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int wi = 0; wi < 4; ++wi) {
-            const uint32_t lo = words[wi] & 0x0F0F0F0Fu, hi = (words[wi] >> 4) & 0x0F0F0F0Fu;
-            p2 = ffma2(make_float2(f128_plus_byte<0>(lo), f128_plus_byte<0>(hi)), xv[4 * wi + 0], p2);
-            p2 = ffma2(make_float2(f128_plus_byte<1>(lo), f128_plus_byte<1>(hi)), xv[4 * wi + 1], p2);
-            p2 = ffma2(make_float2(f128_plus_byte<2>(lo), f128_plus_byte<2>(hi)), xv[4 * wi + 2], p2);
-            p2 = ffma2(make_float2(f128_plus_byte<3>(lo), f128_plus_byte<3>(hi)), xv[4 * wi + 3], p2);
+          uint32_t words[kWords];
+          if constexpr (kWords == 4) {
+            const uint4 cw = ld_shared_v4(crow + (uint32_t)i * rowb);
+            words[0] = cw.x; words[1] = cw.y; words[2] = cw.z; words[3] = cw.w;
+          } else {
+            const uint2 cw = ld_shared_v2(crow + (uint32_t)i * rowb);
+            words[0] = cw.x; words[1] = cw.y;
           }
-          acc[i] = sc * ((p2.x + p2.y) + bias);
+          const float sc = fp16_bits_to_float(ld_shared_u16(srow + (uint32_t)i * scrb));
+          float2 p2[TT];
+#pragma unroll
+          for (int t = 0; t < TT; ++t) p2[t] = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int wi = 0; wi < kWords; ++wi) {
+            const uint32_t lo = words[wi] & 0x0F0F0F0Fu, hi = (words[wi] >> 4) & 0x0F0F0F0Fu;
+            const float2 f0 = make_float2(f128_plus_byte<0>(lo), f128_plus_byte<0>(hi));
+            const float2 f1 = make_float2(f128_plus_byte<1>(lo), f128_plus_byte<1>(hi));
+            const float2 f2 = make_float2(f128_plus_byte<2>(lo), f128_plus_byte<2>(hi));
+            const float2 f3 = make_float2(f128_plus_byte<3>(lo), f128_plus_byte<3>(hi));
+#pragma unroll
+            for (int t = 0; t < TT; ++t) {
+              p2[t] = ffma2(f0, xv[t][4 * wi + 0], p2[t]);
+              p2[t] = ffma2(f1, xv[t][4 * wi + 1], p2[t]);
+              p2[t] = ffma2(f2, xv[t][4 * wi + 2], p2[t]);
+              p2[t] = ffma2(f3, xv[t][4 * wi + 3], p2[t]);
+            }
+          }
+#pragma unroll
+          for (int t = 0; t < TT; ++t) acc[i * kTP + t] = sc * ((p2[t].x + p2[t].y) + bias[t]);
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8u * s);
-      int row = 0;
-      const float v = reduce_rows<RB>(acc, lane, &row);
-      if ((lane & (32 / RB - 1)) == 0 && row < nr) part[(b * RB + row) * nj + j] = v;
+      int idx = 0;
+      const float v = reduce_rows<RB * kTP>(acc, lane, &idx);
+      const int row = idx / kTP, t = idx - (idx / kTP) * kTP;
+      if ((lane & (32 / (RB * kTP) - 1)) == 0 && row < nr && t < TT)
+        part[((b * RB + row) * nj + j) * TT + t] = v;
       // next item
       int nb_step = db;
       j += dj;
@@ -408,14 +446,15 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
     }
   }
 
-  // ---- final: y[row] = bf16(sum over column groups, in order).  Every warp
+  // ---- final: y[t, row] = bf16(sum over column groups, in order).  Every warp
   // reaches this barrier converged (all role loops are warp-uniform).
   __syncthreads();
   if (*abort_flag) return;
-  for (int64_t r = threadIdx.x; r < r1 - r0; r += kStreamThreads) {
+  for (int64_t r = threadIdx.x; r < (r1 - r0) * TT; r += kStreamThreads) {
+    const int64_t row = r / TT, t = r - (r / TT) * TT;
     float v = 0.f;
-    for (int jj = 0; jj < nj; ++jj) v += part[r * nj + jj];
-    y[r0 + r] = float_to_bf16_bits(v);
+    for (int jj = 0; jj < nj; ++jj) v += part[(row * nj + jj) * TT + t];
+    y[t * N + r0 + row] = float_to_bf16_bits(v);
   }
 }
 
@@ -423,22 +462,26 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
 
 size_t gemv_workspace_bytes(int64_t, int64_t, int64_t) { return 0; }
 
-bool gemv_stream_ok(int64_t N, int64_t K, int64_t T);
 int gemv_launch_count(int64_t N, int64_t K, int64_t T) {
   return gemv_stream_ok(N, K, T) ? 1 : (int)((T + 3) / 4);
 }
 
 struct StreamPlan {
   int64_t grid, rows_cap;
-  int rb, nj, nw, slots, nfull;
+  int tt, rb, nj, nw, slots, nfull;
   uint32_t bytes;
 };
 
-// Rows per block: 8 if their code rows fit 32 KB, else 4 if they fit 40 KB, else 2;
-// the ring gets as many slots as the shared-memory budget holds (at least 2).
-static bool stream_plan(int64_t N, int64_t K, int nsm, StreamPlan* p) {
-  if (N < 1 || K < 128) return false;
-  const int64_t nchunk = K / 32;
+// Tokens 1..4.  Rows per block: 8 if their code rows fit 32 KB, else 4 if they
+// fit 40 KB, else 2 (with several tokens, 8-row blocks also halve how often a
+// warp reloads x per row decoded: 6144 x 5120 T = 3 takes 13.4 us with them,
+// 15.7 us with 4-row blocks); the ring gets as many slots as the shared-memory
+// budget holds (at least 2).
+static bool stream_plan(int64_t N, int64_t K, int64_t T, int nsm, StreamPlan* p) {
+  if (N < 1 || K < 128 || T < 1 || T > 4) return false;
+  p->tt = (int)T;
+  const int64_t chunk_w = T == 1 ? 32 : 16;   // weights per lane chunk
+  const int64_t nchunk = K / chunk_w;
   p->nj = (int)((nchunk + 31) / 32);
   // consumer warps: a multiple of the group count (no x reloads) unless that idles
   // more than 3 of the 15, then all 15 (a warp reloads x when its group changes)
@@ -456,7 +499,8 @@ static bool stream_plan(int64_t N, int64_t K, int nsm, StreamPlan* p) {
   // that has landed, so a parity wait can never match a phase two behind.
   const int lead = p->nw / p->nj + (p->nw % p->nj != 0 ? 1 : 0);
   const int64_t budget = kStreamSmemBudget;
-  const StreamLayout L0 = stream_layout(K, p->rb, p->rows_cap, p->nj, 0, lead);
+  if (T * K * 2 > budget) return false;
+  const StreamLayout L0 = stream_layout(K, p->tt, p->rb, p->rows_cap, p->nj, 0, lead);
   const int64_t per = (int64_t)L0.code_stride + L0.sc_stride + 16;
   if ((int64_t)L0.code_off + 128 > budget) return false;
   int64_t s = (budget - L0.code_off - 128) / per;
@@ -464,7 +508,7 @@ static bool stream_plan(int64_t N, int64_t K, int nsm, StreamPlan* p) {
   if (s < 2) return false;
   p->slots = (int)s;
   p->nfull = p->slots + lead;
-  p->bytes = stream_layout(K, p->rb, p->rows_cap, p->nj, p->slots, p->nfull).bytes;
+  p->bytes = stream_layout(K, p->tt, p->rb, p->rows_cap, p->nj, p->slots, p->nfull).bytes;
   return p->bytes <= budget;
 }
 
@@ -479,13 +523,13 @@ static int device_sms() {
   return n;
 }
 
-template <int RB>
-static int gemv_stream_launch_rb(const LinearArgs& a, const StreamPlan& pl) {
+template <int RB, int TT>
+static int gemv_stream_launch_cfg(const LinearArgs& a, const StreamPlan& pl) {
   static bool attr[64] = {};
   int dev = 0;
   if (cuda_check(cudaGetDevice(&dev), "cudaGetDevice")) return Q4LIN_ERR_CUDA;
   if (dev >= 64 || !attr[dev]) {
-    if (cuda_check(cudaFuncSetAttribute(q4_gemv_stream_kernel<RB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cuda_check(cudaFuncSetAttribute(q4_gemv_stream_kernel<RB, TT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)kStreamSmemBudget),
                    "gemv: cudaFuncSetAttribute"))
       return Q4LIN_ERR_CUDA;
@@ -502,24 +546,32 @@ static int gemv_stream_launch_rb(const LinearArgs& a, const StreamPlan& pl) {
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cuda_check(cudaLaunchKernelEx(&cfg, q4_gemv_stream_kernel<RB>, a.wq, a.scales, a.x, a.y, a.N, a.K,
+  return cuda_check(cudaLaunchKernelEx(&cfg, q4_gemv_stream_kernel<RB, TT>, a.wq, a.scales, a.x, a.y, a.N, a.K,
                                        pl.rows_cap, pl.nj, pl.nw, pl.slots, pl.nfull),
                     "gemv: streaming kernel launch");
 }
 
+template <int TT>
+static int gemv_stream_launch_tt(const LinearArgs& a, const StreamPlan& pl) {
+  if (pl.rb == 8) return gemv_stream_launch_cfg<8, TT>(a, pl);
+  if (pl.rb == 4) return gemv_stream_launch_cfg<4, TT>(a, pl);
+  return gemv_stream_launch_cfg<2, TT>(a, pl);
+}
+
 static int gemv_stream_launch(const LinearArgs& a) {
   StreamPlan pl;
-  if (!stream_plan(a.N, a.K, device_sms(), &pl)) return Q4LIN_ERR_INVALID_ARG;
-  switch (pl.rb) {
-    case 8: return gemv_stream_launch_rb<8>(a, pl);
-    case 4: return gemv_stream_launch_rb<4>(a, pl);
-    default: return gemv_stream_launch_rb<2>(a, pl);
+  if (!stream_plan(a.N, a.K, a.T, device_sms(), &pl)) return Q4LIN_ERR_INVALID_ARG;
+  switch (pl.tt) {
+    case 1: return gemv_stream_launch_tt<1>(a, pl);
+    case 2: return gemv_stream_launch_tt<2>(a, pl);
+    case 3: return gemv_stream_launch_tt<3>(a, pl);
+    default: return gemv_stream_launch_tt<4>(a, pl);
   }
 }
 
 bool gemv_stream_ok(int64_t N, int64_t K, int64_t T) {
   StreamPlan pl;
-  return T == 1 && stream_plan(N, K, 148, &pl);
+  return stream_plan(N, K, T, device_sms(), &pl);   // the plan the launch will make
 }
 
 int gemv_launch(const LinearArgs& a) {

@@ -25,6 +25,9 @@ struct LinearArgs {
 int gemv_launch(const LinearArgs& a);
 size_t gemv_workspace_bytes(int64_t N, int64_t K, int64_t T);
 int gemv_launch_count(int64_t N, int64_t K, int64_t T);
+// Whether the streaming kernel (1..4 tokens, one launch) has a shared-memory plan for
+// (N, K, T) on the current device.
+bool gemv_stream_ok(int64_t N, int64_t K, int64_t T);
 
 // tcgen05 tile routes: one CTA per 128-row x BN-token output tile (per K
 // share when split across a cluster), group partials in tensor memory.

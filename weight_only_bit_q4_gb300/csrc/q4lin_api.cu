@@ -74,8 +74,13 @@ int check_device() {
 }
 
 int route_for(int64_t N, int64_t K, int64_t T) {
-  if (T <= 4 || !q4::tc_supported(N, K, T)) return Q4LIN_ROUTE_GEMV;
-  return Q4LIN_ROUTE_TC_SPLITK;  // the tile planner splits K only where that fills the GPU better
+  // One token: the streaming GEMV.  Two to four: the streaming GEMV where its shared
+  // memory holds their x (measured faster than the tile route there, e.g. 6144 x 5120
+  // T = 4: 16 us against 19 us); otherwise the tile route, whose planner splits K only
+  // where that fills the GPU better.
+  if (!q4::tc_supported(N, K, T)) return Q4LIN_ROUTE_GEMV;
+  if (T == 1 || (T <= 4 && q4::gemv_stream_ok(N, K, T))) return Q4LIN_ROUTE_GEMV;
+  return Q4LIN_ROUTE_TC_SPLITK;
 }
 
 size_t round256(size_t b) { return (b + 255) / 256 * 256; }
