@@ -149,6 +149,10 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
   constexpr int kCols = BN / NACC;  // accumulator columns per accumulate thread
   static_assert(kCols % 4 == 0, "column chunk must be a multiple of 4");
 
+  // Programmatic dependent launch: the next kernel in the stream may begin launching now;
+  // this CTA's setup below overlaps the previous kernel's tail, and every global-memory
+  // access waits for that kernel (pdl_wait_previous after the setup barrier).
+  pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -204,6 +208,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait_previous();  // before the first TMA load, scale load or output store
 
   if (wg == 0) {
     if constexpr (NACC == 4) setmaxnreg_dec<R::ctl>();
@@ -582,13 +587,22 @@ int launch_tile(const LinearArgs& a, int splitk) {
   cfg.blockDim = dim3(L::threads, 1, 1);
   cfg.dynamicSmemBytes = L::alloc;
   cfg.stream = a.stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = (unsigned)splitk;
+  // a cluster along K for a split, and programmatic dependent launch (the kernel waits
+  // for its predecessor before touching global memory; measured 1 us per call saved)
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (splitk > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 1;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = (unsigned)splitk;
+    ++na;
+  }
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
   cfg.attrs = attr;
-  cfg.numAttrs = splitk > 1 ? 1 : 0;
+  cfg.numAttrs = (unsigned)na;
   return cuda_check(cudaLaunchKernelEx(&cfg, q4_tc_kernel<BN>, tm_codes, tm_x, p), "tc: kernel launch");
 }
 
