@@ -50,6 +50,12 @@ WORKLOADS = {
     "q4_5120x17408_t1024": (5120, 17408, 1024, "halfnormal", False, 0, 0),
     "q4_34816x5120": (34816, 5120, None, "halfnormal", False, 0, None),      # --t (profiling long weights)
     "q4_5120x17408": (5120, 17408, None, "halfnormal", False, 0, None),      # --t (profiling deep K)
+    # the suites' other Q4 geometries: draft heads (T class 1, 16, 128, 1024) and
+    # vision projections (T class 4, 128, 1024)
+    "q4_131072x5120": (131072, 5120, None, "halfnormal", False, 0, None),
+    "q4_131072x2048": (131072, 2048, None, "halfnormal", False, 0, None),
+    "q4_3456x1152": (3456, 1152, None, "halfnormal", False, 0, None),
+    "q4_4304x1152": (4304, 1152, None, "halfnormal", False, 0, None),
 }
 DEFAULT_WORKLOAD = "q4_6144x5120_t1"
 
