@@ -362,7 +362,7 @@ def measure_ours(args, wl, rank, world, local):
 
     return dict(per_call_us=per_call_us, total_ms=total_ms, calls=calls, copies=R, cold_us=cold_us,
                 clocks=clocks, route=q4lin.ROUTE_NAMES.get(route, str(route)), launches=launches, e2e=e2e,
-                tile=dict(zip(("n", "split_k"), q4lin.tile_plan(N, K, T))),
+                tile=q4lin.tile_plan_full(N, K, T),
                 ws_bytes=ws_n)
 
 

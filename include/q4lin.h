@@ -100,15 +100,22 @@ int q4lin_select_route(int64_t N, int64_t K, int64_t T);
 
 /*
  * The tile plan a tensor-core route runs for (N, K, T) on the current device:
- *   *tile_n   token-tile width of one CTA (the MMA N: 16, 32, 64, 128 or 256)
- *   *split_k  CTAs of one thread-block cluster that share the K range of a tile
+ *   *tile_n        token-tile width of one CTA (the MMA N: 16, 32, 64, 128 or 256)
+ *   *split_k       CTAs of one thread-block cluster that share the K range of a
+ *                  tile in the main launch
+ *   *main_tiles    output tiles (128 rows x tile_n tokens, numbered with the row
+ *                  tile fastest) covered by the main launch; may be NULL
+ *   *tail_split_k  cluster size of a second launch over the remaining tiles
+ *                  (whole waves run unsplit, the partial last wave split along
+ *                  K), 0 when there is none; may be NULL
  * route Q4LIN_ROUTE_AUTO resolves as q4lin_linear does; the GEMV route (or an
- * empty problem) gives *tile_n = 0, *split_k = 1.  Host-only logic: reads
- * device attributes and occupancy, launches nothing.  Returns Q4LIN_OK, or
- * Q4LIN_ERR_INVALID_ARG for NULL outputs, an unknown route or invalid sizes
- * (outputs untouched).
+ * empty problem) gives *tile_n = 0, *split_k = 1, *main_tiles = 0,
+ * *tail_split_k = 0.  Host-only logic: reads device attributes and occupancy,
+ * launches nothing.  Returns Q4LIN_OK, or Q4LIN_ERR_INVALID_ARG for NULL
+ * tile_n / split_k, an unknown route or invalid sizes (outputs untouched).
  */
-int q4lin_tile_plan(int route, int64_t N, int64_t K, int64_t T, int* tile_n, int* split_k);
+int q4lin_tile_plan(int route, int64_t N, int64_t K, int64_t T, int* tile_n, int* split_k, int64_t* main_tiles,
+                    int* tail_split_k);
 
 /* Number of kernel launches one q4lin_linear call issues for (N, K, T) (host-only logic; 0 for
  * an empty problem or invalid sizes). */

@@ -119,4 +119,17 @@ def test_tile_plan_query(lib):
     with pytest.raises(q4lin.Q4LinError):
         q4lin.tile_plan(6144, 5120, 8, route=9)
     bn = ctypes.c_int(0)
-    assert lib.q4lin_tile_plan(0, 6144, 5120, 8, ctypes.byref(bn), None) == 1
+    assert lib.q4lin_tile_plan(0, 6144, 5120, 8, ctypes.byref(bn), None, None, None) == 1
+    sk = ctypes.c_int(0)
+    assert lib.q4lin_tile_plan(0, 6144, 5120, 8, ctypes.byref(bn), ctypes.byref(sk), None, None) == 0
+    # a tail launch covers exactly the tiles the main launch leaves, split along K
+    for N, K, T in ((6144, 5120, 1024), (5120, 17408, 1024), (34816, 5120, 1024), (6144, 5120, 8)):
+        p = q4lin.tile_plan_full(N, K, T)
+        tiles = -(-N // 128) * -(-T // p["n"])
+        assert 0 < p["main_tiles"] <= tiles
+        if p["main_tiles"] < tiles:
+            assert p["split_k"] == 1 and p["tail_split_k"] >= 2
+            assert q4lin.kernel_launches(N, K, T) == 2
+        else:
+            assert p["tail_split_k"] == 0 and q4lin.kernel_launches(N, K, T) == 1
+    assert q4lin.tile_plan_full(6144, 5120, 1) == {"n": 0, "split_k": 1, "main_tiles": 0, "tail_split_k": 0}

@@ -32,8 +32,10 @@ bool gemv_stream_ok(int64_t N, int64_t K, int64_t T);
 // tcgen05 tile routes: one CTA per 128-row x BN-token output tile (per K
 // share when split across a cluster), group partials in tensor memory.
 struct TcPlan {
-  int bn;      // token tile (MMA N)
-  int splitk;  // cluster size along K
+  int bn;              // token tile (MMA N)
+  int splitk;          // cluster size along K of the main launch
+  int64_t main_tiles;  // output tiles of the main launch (all of them without a tail launch)
+  int tail_splitk;     // cluster size along K of the tail launch over the other tiles (0 = none)
 };
 TcPlan tc_plan(int route, int64_t N, int64_t K, int64_t T, int sms);
 TcPlan tc_plan_current_device(int route, int64_t N, int64_t K, int64_t T);

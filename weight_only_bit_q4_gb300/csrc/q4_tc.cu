@@ -70,6 +70,8 @@ struct TcParams {
   int64_t N, K, T;
   int nk;      // groups (K-steps of 64)
   int splitk;  // CTAs of a cluster sharing one output tile along K (1 = no split)
+  uint32_t tile_base;  // first output tile of this launch (tiles are numbered m-major)
+  uint32_t tiles_m;    // row tiles, ceil(N / 128)
 };
 
 constexpr int kTileM = 128;
@@ -174,8 +176,12 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int wg = warp >> 2;
-  const int64_t m0 = (int64_t)blockIdx.x * kTileM;
-  const int64_t t0 = (int64_t)blockIdx.y * BN;
+  // Output tile of this CTA (cluster): tiles are numbered m-major, so consecutive
+  // CTAs share a token tile and its X stays in L2.  32-bit arithmetic (the host
+  // keeps tile numbers below 2^31): a 64-bit division would be a subroutine call.
+  const uint32_t tile = p.tile_base + blockIdx.x;
+  const int64_t m0 = (int64_t)(tile % p.tiles_m) * kTileM;
+  const int64_t t0 = (int64_t)(tile / p.tiles_m) * BN;
 
   // This CTA's share of the K groups (the whole K without a split).
   const int splitk = p.splitk;
@@ -565,7 +571,7 @@ int resident_clusters(int size) {
 }
 
 template <int BN>
-int launch_tile(const LinearArgs& a, int splitk) {
+int launch_tile(const LinearArgs& a, int splitk, int64_t tile_base, int64_t n_tiles) {
   using L = TcSmem<BN>;
   static_assert(L::alloc <= 232448, "shared memory budget");
   if (splitk < 1 || splitk > 8 || splitk > L::max_splitk) {
@@ -581,9 +587,10 @@ int launch_tile(const LinearArgs& a, int splitk) {
     set_error_detail("tc: cuTensorMapEncodeTiled failed (or is unavailable)");
     return Q4LIN_ERR_CUDA;
   }
-  const TcParams p{a.scales, a.y, a.N, a.K, a.T, (int)(a.K / 64), splitk};
+  const TcParams p{a.scales, a.y, a.N, a.K, a.T, (int)(a.K / 64), splitk, (uint32_t)tile_base,
+                   (uint32_t)((a.N + kTileM - 1) / kTileM)};
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((a.N + kTileM - 1) / kTileM), (unsigned)((a.T + BN - 1) / BN), (unsigned)splitk);
+  cfg.gridDim = dim3((unsigned)n_tiles, 1, (unsigned)splitk);
   cfg.blockDim = dim3(L::threads, 1, 1);
   cfg.dynamicSmemBytes = L::alloc;
   cfg.stream = a.stream;
@@ -659,11 +666,22 @@ const TileCost& tile_cost(int bn) {
   return kTileCost[0];
 }
 
+// The second launch of a tail plan: launch latency not hidden behind a previous kernel.
+constexpr double kTailLaunchNs = 1500.0;
+constexpr double kTailGroupFactor = 1.3;
+
+static int64_t tile_count(int64_t N, int64_t T, int bn) { return ((N + kTileM - 1) / kTileM) * ((T + bn - 1) / bn); }
+
 TcPlan tc_plan(int route, int64_t N, int64_t K, int64_t T, int sms) {
   // Token-tile width candidates: the smallest MMA N covering T up to 128
   // tokens; above that 256 or 128.  For each candidate and split factor the
   // cost is waves x per-CTA time; a wave holds as many CTAs (clusters) as can
   // be resident at once (queried; without a device, sms / size).
+  //
+  // Tail plans: when the tiles fill one whole wave and part of a second, the
+  // whole wave can run unsplit and the remaining tiles in a second launch, split
+  // along K so that they fill one wave (6144 x 5120 x 1024 with 256-wide tiles:
+  // 152 tiles, then 40 tiles in clusters of 2; 100.8 us instead of 113.3 us).
   int cand[2] = {0, 0};
   int ncand = 0;
   if (T > 128) {
@@ -675,28 +693,49 @@ TcPlan tc_plan(int route, int64_t N, int64_t K, int64_t T, int sms) {
     ncand = 1;
   }
   const int64_t nk = K / 64;
-  TcPlan best_pl{cand[0], 1};
+  TcPlan best_pl{cand[0], 1, tile_count(N, T, cand[0]), 0};
   double best = -1.0;
   for (int c = 0; c < ncand; ++c) {
     const int bn = cand[c];
     const TileCost& tc = tile_cost(bn);
-    const int64_t tiles = ((N + kTileM - 1) / kTileM) * ((T + bn - 1) / bn);
+    const int64_t tiles = tile_count(N, T, bn);
     const int smax = route == Q4LIN_ROUTE_TC_SPLITK ? (max_splitk_for(bn) < 8 ? max_splitk_for(bn) : 8) : 1;
-    for (int s = 1; s <= smax && s <= nk; ++s) {
+    auto wave_capacity = [&](int s) -> int64_t {
       int64_t per_wave = sms / s;
       if (s > 1) {
         const int q = resident_clusters_for(bn, s);
         if (q > 0 && q < per_wave) per_wave = q;
       }
+      return per_wave;
+    };
+    auto cta_ns = [&](int s) -> double {
+      return (double)((nk + s - 1) / s) * tc.group_ns + tc.fixed_ns + (s > 1 ? kSplitNsPerColumn * bn : 0.0);
+    };
+    for (int s = 1; s <= smax && s <= nk; ++s) {
+      const int64_t per_wave = wave_capacity(s);
       if (per_wave < 1) continue;
       const int64_t waves = (tiles + per_wave - 1) / per_wave;
-      const double per_cta = (double)((nk + s - 1) / s) * tc.group_ns + tc.fixed_ns +
-                             (s > 1 ? kSplitNsPerColumn * bn : 0.0);
-      const double cost = (double)waves * per_cta;
+      const double cost = (double)waves * cta_ns(s);
       if (best < 0 || cost < best - 1e-9) {  // ties keep the earlier (fewer splits, preferred width)
         best = cost;
-        best_pl.bn = bn;
-        best_pl.splitk = s;
+        best_pl = TcPlan{bn, s, tiles, 0};
+      }
+    }
+    // Tail plans are considered after one whole wave only: behind several waves the
+    // single launch's partial last wave already overlaps the stragglers of the one
+    // before.  A tail CTA was measured about 25 % slower per group than the model's
+    // full-occupancy figure (kTailGroupFactor).
+    const int64_t per_wave1 = wave_capacity(1);
+    if (smax > 1 && per_wave1 > 0 && tiles > per_wave1 && tiles < 2 * per_wave1) {
+      const int64_t main_tiles = per_wave1, rest = tiles - main_tiles;
+      const double main_cost = cta_ns(1);
+      for (int st = 2; st <= smax && st <= nk; ++st) {
+        if (rest > wave_capacity(st)) continue;
+        const double cost = main_cost + kTailGroupFactor * cta_ns(st) + kTailLaunchNs;
+        if (cost < best - 1e-9) {
+          best = cost;
+          best_pl = TcPlan{bn, 1, main_tiles, st};
+        }
       }
     }
   }
@@ -709,11 +748,16 @@ TcPlan tc_plan_current_device(int route, int64_t N, int64_t K, int64_t T) {
 
 size_t tc_workspace_bytes(int64_t, int64_t, int64_t) { return 0; }
 
-int tc_launch_count(int64_t, int64_t, int64_t) { return 1; }
+int tc_launch_count(int64_t N, int64_t K, int64_t T) {
+  const TcPlan pl = tc_plan_current_device(Q4LIN_ROUTE_TC_SPLITK, N, K, T);
+  return pl.main_tiles < tile_count(N, T, pl.bn) ? 2 : 1;
+}
 
 bool tc_supported(int64_t N, int64_t K, int64_t T) {
-  // TMA coordinates are 32-bit signed and the grid's y extent is limited.
-  return N < ((int64_t)1 << 31) && K < ((int64_t)1 << 31) && T < ((int64_t)1 << 31) && (T + 15) / 16 < 65535;
+  // TMA coordinates are 32-bit signed, and one launch's tiles (at most, with
+  // 16-token tiles) must fit the grid's x extent.
+  return N < ((int64_t)1 << 31) && K < ((int64_t)1 << 31) && T < ((int64_t)1 << 31) &&
+         tile_count(N, T, 16) < ((int64_t)1 << 31);
 }
 
 int tc_launch(const LinearArgs& a, int route) {
@@ -722,13 +766,19 @@ int tc_launch(const LinearArgs& a, int route) {
     return Q4LIN_ERR_INVALID_ARG;
   }
   const TcPlan pl = tc_plan_current_device(route, a.N, a.K, a.T);
-  switch (pl.bn) {
-    case 256: return launch_tile<256>(a, pl.splitk);
-    case 128: return launch_tile<128>(a, pl.splitk);
-    case 64: return launch_tile<64>(a, pl.splitk);
-    case 32: return launch_tile<32>(a, pl.splitk);
-    default: return launch_tile<16>(a, pl.splitk);
-  }
+  auto launch = [&](int splitk, int64_t base, int64_t n) {
+    switch (pl.bn) {
+      case 256: return launch_tile<256>(a, splitk, base, n);
+      case 128: return launch_tile<128>(a, splitk, base, n);
+      case 64: return launch_tile<64>(a, splitk, base, n);
+      case 32: return launch_tile<32>(a, splitk, base, n);
+      default: return launch_tile<16>(a, splitk, base, n);
+    }
+  };
+  const int64_t tiles = tile_count(a.N, a.T, pl.bn);
+  int rc = launch(pl.splitk, 0, pl.main_tiles);
+  if (rc == Q4LIN_OK && pl.main_tiles < tiles) rc = launch(pl.tail_splitk, pl.main_tiles, tiles - pl.main_tiles);
+  return rc;
 }
 
 int tc_status(int* value, bool clear) {

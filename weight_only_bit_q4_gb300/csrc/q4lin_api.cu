@@ -142,19 +142,19 @@ size_t q4lin_route_workspace_bytes(int route, int64_t N, int64_t K, int64_t T) {
 
 int q4lin_select_route(int64_t N, int64_t K, int64_t T) { return route_for(N, K, T); }
 
-int q4lin_tile_plan(int route, int64_t N, int64_t K, int64_t T, int* tile_n, int* split_k) {
+int q4lin_tile_plan(int route, int64_t N, int64_t K, int64_t T, int* tile_n, int* split_k, int64_t* main_tiles,
+                    int* tail_split_k) {
   if (tile_n == nullptr || split_k == nullptr) return Q4LIN_ERR_INVALID_ARG;
   if (route < Q4LIN_ROUTE_AUTO || route > Q4LIN_ROUTE_TC) return Q4LIN_ERR_INVALID_ARG;
   if (validate_sizes(N, K, T) != Q4LIN_OK) return Q4LIN_ERR_INVALID_ARG;
   if (route == Q4LIN_ROUTE_AUTO) route = route_for(N, K, T);
-  if (route == Q4LIN_ROUTE_GEMV || N == 0 || T == 0 || K == 0 || !q4::tc_supported(N, K, T)) {
-    *tile_n = 0;
-    *split_k = 1;
-    return Q4LIN_OK;
-  }
-  const q4::TcPlan pl = q4::tc_plan_current_device(route, N, K, T);
+  q4::TcPlan pl{0, 1, 0, 0};
+  if (route != Q4LIN_ROUTE_GEMV && N > 0 && T > 0 && K > 0 && q4::tc_supported(N, K, T))
+    pl = q4::tc_plan_current_device(route, N, K, T);
   *tile_n = pl.bn;
   *split_k = pl.splitk;
+  if (main_tiles != nullptr) *main_tiles = pl.main_tiles;
+  if (tail_split_k != nullptr) *tail_split_k = pl.tail_splitk;
   return Q4LIN_OK;
 }
 

@@ -60,6 +60,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q4lin_select_route.argtypes = [i64, i64, i64]
     lib.q4lin_select_route.restype = ctypes.c_int
     lib.q4lin_tile_plan.argtypes = [ctypes.c_int, i64, i64, i64, ctypes.POINTER(ctypes.c_int),
+                                    ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int64),
                                     ctypes.POINTER(ctypes.c_int)]
     lib.q4lin_tile_plan.restype = ctypes.c_int
     lib.q4lin_kernel_launches.argtypes = [i64, i64, i64]
@@ -98,12 +99,19 @@ def select_route(N: int, K: int, T: int) -> int:
 
 
 def tile_plan(N: int, K: int, T: int, route: int = ROUTE_AUTO) -> tuple:
-    """(token-tile width, split-K cluster size) the tensor-core route runs; (0, 1) for the GEMV."""
-    bn, sk = ctypes.c_int(0), ctypes.c_int(0)
-    st = load().q4lin_tile_plan(route, N, K, T, ctypes.byref(bn), ctypes.byref(sk))
+    """(token-tile width, split-K cluster size) of the tensor-core route's main launch; (0, 1) for the GEMV."""
+    p = tile_plan_full(N, K, T, route)
+    return p["n"], p["split_k"]
+
+
+def tile_plan_full(N: int, K: int, T: int, route: int = ROUTE_AUTO) -> dict:
+    """The whole tensor-core plan: tile width, main-launch split, main-launch tiles, tail split (0 = none)."""
+    bn, sk, mt, ts = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int64(0), ctypes.c_int(0)
+    st = load().q4lin_tile_plan(route, N, K, T, ctypes.byref(bn), ctypes.byref(sk), ctypes.byref(mt),
+                                ctypes.byref(ts))
     if st != OK:
         raise Q4LinError(st, "tile plan: ")
-    return int(bn.value), int(sk.value)
+    return {"n": int(bn.value), "split_k": int(sk.value), "main_tiles": int(mt.value), "tail_split_k": int(ts.value)}
 
 
 def kernel_launches(N: int, K: int, T: int) -> int:
