@@ -98,13 +98,29 @@ def unpack_codes(wq: np.ndarray) -> np.ndarray:
 
 
 def dequantize(wq: np.ndarray, scale_bits: np.ndarray) -> np.ndarray:
-    """FP64 weights w[n, k] = (q[n, k] - 8) * s[n, k // 64]."""
+    """FP64 weights w[n, k] = (q[n, k] - 8) * s[n, k // 64] for every k the code plane holds
+    (the last group may be partial: ceil(K / 64) scales for K codes)."""
     q = unpack_codes(wq)
     N, K = q.shape
     s = fp16_bits_to_f64(scale_bits)
-    assert s.shape == (N, K // GROUP), (s.shape, N, K)
+    assert s.shape == (N, (K + GROUP - 1) // GROUP), (s.shape, N, K)
     group_of_k = np.arange(K) // GROUP
     return (q - ZERO_POINT).astype(np.float64) * s[:, group_of_k]
+
+
+def logical_planes(wq: np.ndarray, scale_bits: np.ndarray, K: int):
+    """The part of the stored planes that holds W[:, :K].
+
+    The planes are stored for K_pad = k_pad(K) columns (linear-benchmark.md
+    section 4: groups = N * K_pad / 64); the positions k >= K are padding, not
+    part of W, and whatever bits they hold never enter y.  Planes stored for
+    exactly K columns (K a multiple of 128, or a caller that did not pad) are
+    accepted as they are.
+    """
+    wq = np.asarray(wq)
+    scale_bits = np.asarray(scale_bits)
+    assert K % 2 == 0 and 2 * wq.shape[1] in (K, k_pad(K)), (wq.shape, K)
+    return wq[:, :K // 2], scale_bits[:, :(K + GROUP - 1) // GROUP]
 
 
 def linear(wq: np.ndarray, scale_bits: np.ndarray, x_bits: np.ndarray,
@@ -117,18 +133,20 @@ def linear(wq: np.ndarray, scale_bits: np.ndarray, x_bits: np.ndarray,
     if rows is not None:
         wq = np.asarray(wq)[rows]
         scale_bits = np.asarray(scale_bits)[rows]
-    w = dequantize(wq, scale_bits)               # [N, K]
     x = bf16_bits_to_f64(x_bits)                 # [T, K]
+    wq, scale_bits = logical_planes(wq, scale_bits, x.shape[1])
+    w = dequantize(wq, scale_bits)               # [N, K]
     assert x.shape[1] == w.shape[1]
     return x @ w.T                               # [T, N]
 
 
 def linear_loops(wq, scale_bits, x_bits) -> list:
-    """The same definition as plain Python loops (tiny shapes only)."""
+    """The same definition as plain Python loops (tiny shapes only); the sum runs over the
+    K columns of X, so padded plane positions never enter."""
     wq = np.asarray(wq)
-    N, half = wq.shape
-    K = 2 * half
     x = bf16_bits_to_f64(x_bits)
+    N = wq.shape[0]
+    K = x.shape[1]
     s = fp16_bits_to_f64(scale_bits)
     T = x.shape[0]
     y = [[0.0] * N for _ in range(T)]

@@ -190,6 +190,64 @@ def test_brute_force_tiny_exact(N, K, T):
             assert Fraction(loops[t][n]) == ref[t][n]
 
 
+# ---------------------------------------------------------------- K not a multiple of 128
+def _exact_padded_problem(N, K, T, seed):
+    """Planes stored for K_pad = align_up(K, 128) columns (linear-benchmark.md section 4).
+    The padded codes are random and every wholly padded group gets NaN or Inf scale
+    bits, so anything that lets padding into y shows up."""
+    rng = np.random.default_rng(seed)
+    Kp = (K + 127) // 128 * 128
+    wq = rng.integers(0, 256, (N, Kp // 2), dtype=np.uint8)
+    choices = np.array([0x3C00, 0x4000, 0x3800, 0x4200, 0x3400, 0xBC00], np.uint16)
+    s = choices[rng.integers(0, len(choices), (N, Kp // 64))]
+    g_real = (K + 63) // 64
+    s[:, g_real:] = np.where(rng.integers(0, 2, (N, Kp // 64 - g_real)) == 0, 0x7E00, 0x7C00)
+    xv = rng.integers(-4, 5, (T, K)).astype(np.float32)
+    x = ((xv.view(np.uint32) >> 16)).astype(np.uint16)
+    return wq, s, x
+
+
+def _exact_reference_logical(wq, s, x):
+    """Fractions over k < K, K = the width of X; struct decoders, plain loops."""
+    N = wq.shape[0]
+    T, K = x.shape
+    xv = [[Fraction(struct.unpack("<f", struct.pack("<I", int(b) << 16))[0]) for b in row] for row in x]
+    out = [[Fraction(0)] * N for _ in range(T)]
+    for n in range(N):
+        sv = [Fraction(struct.unpack("<e", struct.pack("<H", int(b)))[0]) for b in s[n, :(K + 63) // 64]]
+        codes = []
+        for j in range(K // 2):
+            byte = int(wq[n, j])
+            codes += [byte % 16, byte // 16]
+        for t in range(T):
+            out[t][n] = sum((codes[k] - 8) * sv[k // 64] * xv[t][k] for k in range(K))
+    return out
+
+
+@pytest.mark.parametrize("N,K,T", [(2, 8, 1), (3, 72, 2), (4, 200, 2), (1, 136, 3), (2, 64, 2)])
+def test_brute_force_padded_k_exact(N, K, T):
+    wq, s, x = _exact_padded_problem(N, K, T, seed=N * 977 + K + T)
+    ref = _exact_reference_logical(wq, s, x)
+    y = oracle.linear(wq, s, x)
+    loops = oracle.linear_loops(wq, s, x)
+    for t in range(T):
+        for n in range(N):
+            assert Fraction(y[t, n]) == ref[t][n]
+            assert Fraction(loops[t][n]) == ref[t][n]
+
+
+def test_padding_bits_do_not_enter():
+    wq, s, x = _exact_padded_problem(5, 200, 3, seed=11)
+    y = oracle.linear(wq, s, x)
+    wq2, s2 = wq.copy(), s.copy()
+    wq2[:, 100:] = 0        # codes of k >= 200
+    s2[:, 4:] = 0           # scales of groups 4.. (k >= 256; group 3 holds k = 192..255)
+    assert np.array_equal(oracle.linear(wq2, s2, x), y)
+    # K a multiple of 128 stores exactly K columns: unchanged behaviour
+    wq3, s3, x3 = _exact_problem(3, 256, 2, seed=5)
+    assert oracle.linear(wq3, s3, x3).shape == (2, 3)
+
+
 # ---------------------------------------------------------------- tolerance
 def test_tolerance_definition():
     y_ref = np.array([[1.0, -2.0, 0.0, 4.0]])

@@ -152,14 +152,17 @@ SWEEP_6144x5120_T = tuple(range(1, 129)) + (384, 385, 512, 640, 641, 1024)
 
 def make_problem(N: int, K: int, T: int, *, w_seed: int = 0, x_seed: int | None = None,
                  scales: str = "halfnormal", outliers: bool = False):
-    """(wq uint8 [N,K/2], scales uint16 [N,K/64], x uint16 [T,K]).
+    """(wq uint8 [N,Kp/2], scales uint16 [N,Kp/64], x uint16 [T,K]), Kp = K rounded up to 128.
 
+    The weight planes are stored for K rounded up to a multiple of 128 (the
+    storage layout of the format); for K a multiple of 128 that is K itself.
     The weight is seeded ``w_seed`` (shared across a T sweep); X is seeded
     ``x_seed``, which defaults to T ("one seed per T").
     """
     if x_seed is None:
         x_seed = T
-    wq = packed_codes(N, K, w_seed)
-    s = group_scales(N, K, w_seed, scales)
+    Kp = (K + 127) // 128 * 128
+    wq = packed_codes(N, Kp, w_seed)
+    s = group_scales(N, Kp, w_seed, scales)
     x = activations(T, K, x_seed, outliers)
     return wq, s, x
