@@ -5,15 +5,19 @@
  * q4-linear.md, header table, and the linear-benchmark contract,
  * linear-benchmark.md, "status and scope" and section 4):
  *
- *   y[t*N + n] = bf16( sum_k w[n,k] * x[t*K + k] ),  accumulated in FP32,
- *   w[n,k]     = (q[n,k] - 8) * s[n, k/64],
- *   q[n,2j]    = wq[n*(K/2) + j] & 0xF,   q[n,2j+1] = wq[n*(K/2) + j] >> 4.
+ *   y[t*N + n] = bf16( sum_{k<K} w[n,k] * x[t*K + k] ),  accumulated in FP32,
+ *   w[n,k]     = (q[n,k] - 8) * s[n*(Kp/64) + k/64],
+ *   q[n,2j]    = wq[n*(Kp/2) + j] & 0xF,   q[n,2j+1] = wq[n*(Kp/2) + j] >> 4,
+ *   Kp         = K rounded up to a multiple of 128 (K_pad).
  *
  * Weight format Q4_G64_FP16 "row-split" (linear-benchmark.md section 4,
- * format table: 32 code bytes + 2 scale bytes per group of 64): two separate
- * planes, codes [N, K/2] uint8 and scales [N, K/64] IEEE fp16, both
- * row-major.  X and Y are bf16, row-major [T, K] and [T, N] -- the same bytes
- * as the column-major X[K,T] / Y[N,T] views the report binds.
+ * format table: 32 code bytes + 2 scale bytes per group of 64; groups =
+ * N * K_pad / 64): two separate planes, codes [N, Kp/2] uint8 and scales
+ * [N, Kp/64] IEEE fp16, both row-major.  The plane positions k >= K are
+ * padding: whatever bits they hold (NaN scale bits included) do not affect y.
+ * X and Y are bf16, row-major [T, K] and [T, N] -- the same bytes as the
+ * column-major X[K,T] / Y[N,T] views the report binds.  K must be a multiple
+ * of 8, so that every X row starts 16-byte aligned.
  *
  * Ownership: the caller owns every buffer.  The library never allocates or
  * frees memory and keeps no state between calls except its error word.
@@ -44,7 +48,7 @@ extern "C" {
 typedef enum {
   Q4LIN_OK = 0,
   Q4LIN_ERR_INVALID_ARG = 1,       /* null pointer with nonzero size, negative size, size overflow */
-  Q4LIN_ERR_UNSUPPORTED_SHAPE = 2, /* K not a multiple of 128 */
+  Q4LIN_ERR_UNSUPPORTED_SHAPE = 2, /* K not a multiple of 8 */
   Q4LIN_ERR_MISALIGNED = 3,        /* a device pointer not 16-byte aligned */
   Q4LIN_ERR_WORKSPACE = 4,         /* workspace NULL while q4lin_workspace_bytes() > 0 */
   Q4LIN_ERR_DEVICE = 5,            /* current device is not compute capability 10.x (sm_100 family) */
@@ -71,12 +75,12 @@ size_t q4lin_workspace_bytes(int64_t N, int64_t K, int64_t T);
 
 /*
  * Y = W . X (see the top of this file).
- *   wq        device, uint8  [N, K/2]  packed codes, 16-byte aligned
- *   scales    device, fp16   [N, K/64] bit patterns, 16-byte aligned
+ *   wq        device, uint8  [N, Kp/2]  packed codes, 16-byte aligned
+ *   scales    device, fp16   [N, Kp/64] bit patterns, 16-byte aligned
  *   x         device, bf16   [T, K]    bit patterns, 16-byte aligned
  *   y         device, bf16   [T, N]    bit patterns, 16-byte aligned (output)
  *   N, T      >= 0; N == 0 or T == 0 is an empty problem: Q4LIN_OK, nothing launched
- *   K         >= 0, multiple of 128 (K == 0 writes y = +0)
+ *   K         >= 0, multiple of 8; Kp = K rounded up to 128 (K == 0 writes y = +0)
  *   workspace device, >= q4lin_workspace_bytes(N, K, T) bytes, 256-byte aligned
  *   stream    cudaStream_t as void*
  * Returns Q4LIN_OK once the work is enqueued.

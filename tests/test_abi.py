@@ -59,8 +59,9 @@ def test_argument_errors_detected_on_host(lib):
     assert _call(-1, 128, 1) == 1
     assert _call(4, -128, 1) == 1
     assert _call(4, 128, -1) == 1
-    assert _call(4, 100, 1) == 2          # K % 128 != 0
-    assert _call(4, 64, 1) == 2
+    assert _call(4, 100, 1) == 2          # K % 8 != 0: X rows would not start 16-byte aligned
+    assert _call(4, 60, 1) == 2
+    assert _call(4, 4, 1) == 2
     assert _call(4, 128, 1, wq=None) == 1
     assert _call(4, 128, 1, s=None) == 1
     assert _call(4, 128, 1, x=None) == 1

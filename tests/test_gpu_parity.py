@@ -121,6 +121,24 @@ def test_decode_gemv_shapes(N, K, T):
         assert_close(run(*to_dev(wq, s, x)), y_ref, f"decode {N}x{K}")
 
 
+@pytest.mark.parametrize("route", ROUTES)
+@pytest.mark.parametrize("N,K", [(5, 8), (130, 64), (300, 72), (257, 200), (1000, 1000), (640, 4304), (129, 8200)])
+def test_k_not_multiple_of_128(route, N, K):
+    """K a multiple of 8 but not of 128: planes stored for K_pad = align_up(K, 128)
+    columns (linear-benchmark.md section 4), padded codes random and every wholly
+    padded group's scale NaN or Inf, which must not reach y."""
+    Kp = (K + 127) // 128 * 128
+    rng = np.random.default_rng(K)
+    for T in [1, 2, 4, 5, 17, 100, 300]:
+        wq, s, x = synth.make_problem(N, K, T, w_seed=N + K, x_seed=T)
+        assert wq.shape[1] == Kp // 2 and s.shape[1] == Kp // 64 and x.shape[1] == K
+        wq[:, K // 2:] = rng.integers(0, 256, (N, Kp // 2 - K // 2), dtype=np.uint8)
+        g = (K + 63) // 64
+        s[:, g:] = np.where(rng.integers(0, 2, (N, Kp // 64 - g)) == 0, 0x7E00, 0x7C00)
+        y_ref = oracle.linear(wq, s, x)
+        assert_close(run(*to_dev(wq, s, x), route), y_ref, f"{q4lin.ROUTE_NAMES[route]} {N}x{K} T={T}")
+
+
 # ------------------------------------------------------------ edge cases and guards
 def test_empty_and_degenerate():
     t = torch()

@@ -21,6 +21,10 @@ struct LinearArgs {
   cudaStream_t stream;
 };
 
+// The weight planes are stored for K rounded up to a multiple of 128
+// (linear-benchmark.md section 4, K_pad); columns k >= K are padding.
+inline int64_t k_pad(int64_t K) { return (K + 127) / 128 * 128; }
+
 // CUDA-core GEMV: each weight is decoded once per block of up to 4 tokens.
 int gemv_launch(const LinearArgs& a);
 size_t gemv_workspace_bytes(int64_t N, int64_t K, int64_t T);

@@ -67,8 +67,8 @@ __device__ int g_tc_status = 0;
 struct TcParams {
   const uint16_t* scales;
   uint16_t* y;
-  int64_t N, K, T;
-  int nk;      // groups (K-steps of 64)
+  int64_t N, Kp, T;   // Kp: the planes' stored width, K rounded up to 128
+  int nk;      // groups (K-steps of 64) holding columns < K
   int splitk;  // CTAs of a cluster sharing one output tile along K (1 = no split)
   uint32_t tile_base;  // first output tile of this launch (tiles are numbered m-major)
   uint32_t tiles_m;    // row tiles, ceil(N / 128)
@@ -377,9 +377,9 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
     bool acc_ok = true;
     const int64_t row = m0 + r_acc;
     const bool row_ok = row < p.N;
-    // Scales are read as pairs of groups (K / 64 is even, so every row starts on a
+    // Scales are read as pairs of groups (a row holds K_pad / 64 scales, an even
     // 4-byte boundary); the next pair is fetched as soon as the current one is used.
-    const uint32_t* srow = reinterpret_cast<const uint32_t*>(p.scales + (row_ok ? row : 0) * (p.K >> 6));
+    const uint32_t* srow = reinterpret_cast<const uint32_t*>(p.scales + (row_ok ? row : 0) * (p.Kp >> 6));
     int pcur = g_begin >> 1;
     uint32_t s_cur = row_ok ? __ldg(srow + pcur) : 0u;
     uint32_t s_nxt = (row_ok && 2 * (pcur + 1) < p.nk) ? __ldg(srow + pcur + 1) : 0u;
@@ -580,14 +580,17 @@ int launch_tile(const LinearArgs& a, int splitk, int64_t tile_base, int64_t n_ti
   }
   if (const int rc = set_kernel_attrs<BN>()) return rc;
   CUtensorMap tm_codes, tm_x;
-  if (!make_map_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.wq, (uint64_t)(a.K / 2), (uint64_t)a.N,
-                   (uint64_t)(a.K / 2), 128, kTileM) ||
+  // code plane rows hold K_pad / 2 bytes; X rows K values, whose positions k >= K read
+  // as zeros (out-of-range tile elements), so a partial last group sees x = 0 beyond K
+  const int64_t Kp = k_pad(a.K);
+  if (!make_map_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.wq, (uint64_t)(Kp / 2), (uint64_t)a.N,
+                   (uint64_t)(Kp / 2), 128, kTileM) ||
       !make_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, (uint64_t)a.K, (uint64_t)a.T, (uint64_t)a.K * 2,
                    64, BN)) {
     set_error_detail("tc: cuTensorMapEncodeTiled failed (or is unavailable)");
     return Q4LIN_ERR_CUDA;
   }
-  const TcParams p{a.scales, a.y, a.N, a.K, a.T, (int)(a.K / 64), splitk, (uint32_t)tile_base,
+  const TcParams p{a.scales, a.y, a.N, Kp, a.T, (int)((a.K + 63) / 64), splitk, (uint32_t)tile_base,
                    (uint32_t)((a.N + kTileM - 1) / kTileM)};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)n_tiles, 1, (unsigned)splitk);
@@ -692,7 +695,7 @@ TcPlan tc_plan(int route, int64_t N, int64_t K, int64_t T, int sms) {
     cand[0] = T > 64 ? 128 : T > 32 ? 64 : T > 16 ? 32 : 16;
     ncand = 1;
   }
-  const int64_t nk = K / 64;
+  const int64_t nk = (K + 63) / 64;   // groups holding columns < K
   TcPlan best_pl{cand[0], 1, tile_count(N, T, cand[0]), 0};
   double best = -1.0;
   for (int c = 0; c < ncand; ++c) {

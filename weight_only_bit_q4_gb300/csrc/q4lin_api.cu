@@ -42,7 +42,9 @@ int validate_sizes(int64_t N, int64_t K, int64_t T) {
   if ((double)N * (double)K > 9.0e17 || (double)T * (double)K > 9.0e17 ||
       (double)N * (double)T > 9.0e17)
     return Q4LIN_ERR_INVALID_ARG;
-  if (K % 128 != 0) return Q4LIN_ERR_UNSUPPORTED_SHAPE;
+  // any K whose X rows stay 16-byte aligned; the weight planes are stored for K
+  // rounded up to 128 (K_pad) and the padded positions are ignored
+  if (K % 8 != 0) return Q4LIN_ERR_UNSUPPORTED_SHAPE;
   return Q4LIN_OK;
 }
 

@@ -150,17 +150,18 @@ def linear_raw(wq_ptr, scales_ptr, x_ptr, y_ptr, N, K, T, ws_ptr=None, stream=No
 def linear(wq, scales, x, y=None, workspace=None, stream=None, route: int = ROUTE_AUTO):
     """Y[T, N] (bf16) = dequant(wq, scales) applied to X[T, K] (bf16) on the GPU.
 
-    wq: uint8 [N, K/2]; scales: fp16 (or int16/uint16 bit patterns) [N, K/64];
-    x: bf16 [T, K]; all CUDA, contiguous.  ``y`` (bf16 [T, N]) and
+    wq: uint8 [N, Kp/2]; scales: fp16 (or int16/uint16 bit patterns) [N, Kp/64],
+    Kp = K rounded up to 128 (the planes' stored width; columns k >= K are
+    padding); x: bf16 [T, K]; all CUDA, contiguous.  ``y`` (bf16 [T, N]) and
     ``workspace`` (uint8, >= workspace_bytes) are allocated here with torch if
     not given.  Runs on ``stream`` (a torch.cuda.Stream) or the current stream.
     """
     import torch
 
-    N, half = wq.shape
-    K = 2 * half
-    T = x.shape[0]
-    if x.shape[1] != K or scales.shape != (N, K // 64):
+    T, K = x.shape
+    N = wq.shape[0]
+    Kp = (K + 127) // 128 * 128
+    if tuple(wq.shape) != (N, Kp // 2) or tuple(scales.shape) != (N, Kp // 64):
         raise ValueError(f"shape mismatch: wq {tuple(wq.shape)} scales {tuple(scales.shape)} x {tuple(x.shape)}")
     for name, t in (("wq", wq), ("scales", scales), ("x", x)):
         if not t.is_cuda or not t.is_contiguous():
