@@ -4,3 +4,4 @@ from .q4_oracle import (  # noqa: F401
     unpack_codes, dequantize, linear, linear_loops, rms, within_tolerance, check,
     REL_TOL, RMS_TOL,
 )
+from . import sibling_formats  # noqa: F401,E402

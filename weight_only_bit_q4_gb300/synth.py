@@ -45,6 +45,8 @@ TAG_CODES = 0x436F646573000001
 TAG_SCALES = 0x5363616C65000002
 TAG_X = 0x4163747300000003
 TAG_OUTLIER = 0x4F75746C69000004
+TAG_HIGH = 0x4869676800000005
+TAG_W8 = 0x5738436F64000006
 
 
 def mix64(z: np.ndarray) -> np.ndarray:
@@ -109,9 +111,9 @@ def packed_codes(N: int, K: int, seed: int = 0) -> np.ndarray:
     return words.astype("<u8").view(np.uint8)[:nbytes].reshape(N, K // 2).copy()
 
 
-def group_scales(N: int, K: int, seed: int = 0, dist: str = "halfnormal") -> np.ndarray:
-    """fp16 bit patterns [N, K/64]."""
-    G = K // 64
+def group_scales(N: int, K: int, seed: int = 0, dist: str = "halfnormal", group: int = 64) -> np.ndarray:
+    """fp16 bit patterns [N, K/group]."""
+    G = K // group
     z = normal(stream_state(seed, TAG_SCALES), N * G).reshape(N, G)
     if dist == "halfnormal":
         s = np.abs(z) * 0.02 + 1e-3
@@ -166,3 +168,30 @@ def make_problem(N: int, K: int, T: int, *, w_seed: int = 0, x_seed: int | None 
     s = group_scales(N, Kp, w_seed, scales)
     x = activations(T, K, x_seed, outliers)
     return wq, s, x
+
+
+def uniform_bytes(rows: int, cols: int, seed: int, tag: int) -> np.ndarray:
+    """uint8 [rows, cols] from the splitmix64 stream of (seed, tag)."""
+    nbytes = rows * cols
+    words = splitmix64(stream_state(seed, tag), (nbytes + 7) // 8)
+    return words.astype("<u8").view(np.uint8)[:nbytes].reshape(rows, cols).copy()
+
+
+# sibling formats: bits per weight in the high plane (0: W8, one int8 code per weight)
+FORMAT_HIGH_BITS = {"q4g64": None, "q5g64": 1, "q6g64": 2, "w8g32": 0}
+
+
+def make_problem_fmt(qtype: str, N: int, K: int, T: int, *, w_seed: int = 0, x_seed: int | None = None):
+    """(planes, scales, x) for a sibling weight format, planes stored for Kp = K rounded
+    up to 128 columns: q5g64 / q6g64 (low [N, Kp/2], high [N, Kp*bits/8]), w8g32
+    (codes [N, Kp]); uniform bytes in every plane, half-normal fp16 scales per group."""
+    if x_seed is None:
+        x_seed = T
+    Kp = (K + 127) // 128 * 128
+    x = activations(T, K, x_seed)
+    if qtype == "w8g32":
+        return (uniform_bytes(N, Kp, w_seed, TAG_W8),), group_scales(N, Kp, w_seed, group=32), x
+    bits = FORMAT_HIGH_BITS[qtype]
+    low = packed_codes(N, Kp, w_seed)
+    high = uniform_bytes(N, Kp * bits // 8, w_seed, TAG_HIGH)
+    return (low, high), group_scales(N, Kp, w_seed), x
