@@ -89,6 +89,35 @@ int q4lin_linear(const uint8_t* wq, const uint16_t* scales, const uint16_t* x, u
                  int64_t N, int64_t K, int64_t T, void* workspace, void* stream);
 
 /*
+ * Sibling weight formats of the format table (linear-benchmark.md section 4):
+ * Q4G64_F16S (the layer's own), Q5G64_F16S (32 low + 8 high + 2 scale bytes
+ * per 64 weights), Q6G64_F16S (32 + 16 + 2) and W8G32_F16S (32 code + 2 scale
+ * bytes per 32 weights).  Readings (the table fixes only the byte counts):
+ *   Q5 / Q6: codes = the Q4 code plane [N, Kp/2] (low 4 bits); high = [N, Kp/8]
+ *     (Q5: bit b of byte i is bit 4 of weight 8i + b) or [N, Kp/4] (Q6: bits
+ *     2b..2b+1 of byte i are bits 4..5 of weight 4i + b); w = (q - 16) * s,
+ *     w = (q - 32) * s; scales [N, Kp/64].
+ *   W8: codes [N, Kp] signed int8, w = code * s, scales [N, Kp/32].
+ */
+typedef enum {
+  Q4LIN_QTYPE_Q4G64 = 0,
+  Q4LIN_QTYPE_Q5G64 = 1,
+  Q4LIN_QTYPE_Q6G64 = 2,
+  Q4LIN_QTYPE_W8G32 = 3
+} q4lin_qtype;
+
+/*
+ * Y = W . X for any of the formats above (arguments as q4lin_linear; `high`
+ * is the Q5 / Q6 high-bit plane, 16-byte aligned, and is ignored otherwise).
+ * Q4G64 is exactly q4lin_linear.  The other formats run on the decode GEMV,
+ * for 1..4 tokens where its shared-memory plan fits; other shapes return
+ * Q4LIN_ERR_UNSUPPORTED_SHAPE.  No workspace (the pointer may be NULL).
+ */
+int q4lin_linear_qtype(int qtype, const uint8_t* codes, const uint8_t* high, const uint16_t* scales,
+                       const uint16_t* x, uint16_t* y, int64_t N, int64_t K, int64_t T, void* workspace,
+                       void* stream);
+
+/*
  * Diagnostic form of q4lin_linear that runs a given route instead of the
  * library's choice (the same arguments; route Q4LIN_ROUTE_AUTO is
  * q4lin_linear itself).  Tests use it to compare every route with the

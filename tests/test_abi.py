@@ -75,6 +75,27 @@ def test_argument_errors_detected_on_host(lib):
     assert _call(4, 128, 1, route=9) == 1  # no such route
 
 
+def _call_qtype(qtype, N, K, T, codes=16, high=16, s=16, x=16, y=16):
+    vp = lambda v: None if v is None else ctypes.c_void_p(v)
+    return int(lib_fn().q4lin_linear_qtype(qtype, vp(codes), vp(high), vp(s), vp(x), vp(y), N, K, T, None, None))
+
+
+def lib_fn():
+    return q4lin.load()
+
+
+def test_qtype_argument_errors_detected_on_host(lib):
+    assert _call_qtype(9, 4, 128, 1) == 1                 # no such format
+    assert _call_qtype(-1, 4, 128, 1) == 1
+    assert _call_qtype(1, 4, 128, 1, high=None) == 1      # Q5 without its high plane
+    assert _call_qtype(2, 4, 128, 1, high=None) == 1      # Q6 without its high plane
+    assert _call_qtype(1, 4, 128, 1, high=24) == 3        # misaligned high plane
+    assert _call_qtype(3, 4, 100, 1) == 2                 # K % 8 != 0
+    assert _call_qtype(3, 4, 128, 1, codes=None) == 1
+    assert _call_qtype(2, 4, 128, 1, s=8) == 3
+    assert _call_qtype(1, 0, 128, 5, codes=None, high=None, s=None, x=None, y=None) == 0   # empty
+
+
 def test_empty_problems_are_noops(lib):
     # N == 0 or T == 0: nothing to compute, nothing launched, even with null pointers.
     assert _call(0, 128, 5, wq=None, s=None, x=None, y=None) == 0

@@ -1,0 +1,76 @@
+"""GPU parity for the sibling weight formats Q5G64, Q6G64 and W8G32 (linear-benchmark.md
+section 4, format table) on the decode GEMV: 1..4 tokens, K a multiple of 128 or padded,
+ragged N, against the FP64 oracle for those formats.  Q4 through the same entry point is
+q4lin_linear itself; shapes outside the GEMV's reach are refused, not approximated."""
+import numpy as np
+import pytest
+
+from oracle import sibling_formats as sf
+from weight_only_bit_q4_gb300 import q4lin, synth
+
+from gpu_util import assert_close, torch, y_bits
+
+pytestmark = pytest.mark.gpu
+
+FMTS = ["q5g64", "q6g64", "w8g32"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from weight_only_bit_q4_gb300 import build
+    build.build()
+    q4lin.load()
+    assert q4lin.clear_device_status() == 0
+    yield
+    assert q4lin.device_status() == 0
+
+
+def _dev(a):
+    t = torch()
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return t.from_numpy(a).cuda()
+
+
+def _run(qtype, planes, s, x):
+    t = torch()
+    y = q4lin.linear_qtype(qtype, tuple(_dev(p) for p in planes), _dev(s), _dev(x).view(t.bfloat16))
+    t.cuda.synchronize()
+    return y_bits(y)
+
+
+@pytest.mark.parametrize("qtype", FMTS)
+@pytest.mark.parametrize("N,K", [(5, 128), (300, 200), (1001, 4096), (257, 5120), (640, 4304), (77, 17408),
+                                 (6144, 5120)])
+def test_formats_match_oracle(qtype, N, K):
+    for T in (1, 2, 3, 4):
+        planes, s, x = synth.make_problem_fmt(qtype, N, K, T, w_seed=N + K, x_seed=K + T)
+        y_ref = sf.linear(qtype, planes, s, x)
+        if T * K * 2 > 100 * 1024:
+            # x of every token must fit in shared memory next to at least two ring slots
+            try:
+                yb = _run(qtype, planes, s, x)
+            except q4lin.Q4LinError as e:
+                assert e.status == 2, e
+                continue
+        else:
+            yb = _run(qtype, planes, s, x)
+        assert_close(yb, y_ref, f"{qtype} {N}x{K} T={T}")
+
+
+def test_q4_through_the_format_entry_is_q4lin_linear():
+    wq, s, x = synth.make_problem(1000, 1152, 3, w_seed=4)
+    t = torch()
+    y_fmt = _run("q4g64", (wq,), s, x)
+    y = q4lin.linear(_dev(wq), _dev(s), _dev(x).view(t.bfloat16))
+    t.cuda.synchronize()
+    assert np.array_equal(y_fmt, y_bits(y))
+
+
+@pytest.mark.parametrize("qtype", FMTS)
+def test_more_than_four_tokens_refused(qtype):
+    planes, s, x = synth.make_problem_fmt(qtype, 64, 256, 5)
+    with pytest.raises(q4lin.Q4LinError) as e:
+        _run(qtype, planes, s, x)
+    assert e.value.status == 2

@@ -176,6 +176,18 @@ __device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
   return v;
 }
 
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// nibbles 0..3 of m (bits 0..15) to the low nibbles of bytes 0..3
+__device__ __forceinline__ uint32_t spread_nibbles_to_bytes(uint32_t m) {
+  m = (m | (m << 8)) & 0x00FF00FFu;
+  return (m | (m << 4)) & 0x0F0F0F0Fu;
+}
+
 __device__ __forceinline__ uint16_t ld_shared_u16(uint32_t addr) {
   uint16_t v;
   asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
@@ -186,25 +198,41 @@ __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
   asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 
+// Weight formats of the streaming GEMV (linear-benchmark.md section 4, format
+// table): Q4G64 (the layer's own), and the sibling formats Q5G64 / Q6G64 (the
+// Q4 code plane plus a plane of 1 or 2 high bits per weight, in k order from
+// each byte's least significant bit; zero points 16 and 32) and W8G32 (signed
+// int8 codes, one scale per 32 weights).
+enum : int { kFmtQ4 = 0, kFmtQ5 = 1, kFmtQ6 = 2, kFmtW8 = 3 };
+__host__ __device__ constexpr int fmt_high_bits(int f) { return f == kFmtQ5 ? 1 : f == kFmtQ6 ? 2 : 0; }
+__host__ __device__ constexpr int fmt_group(int f) { return f == kFmtW8 ? 32 : 64; }
+// bytes of one stored row (Kp columns) of each plane
+__host__ __device__ constexpr int64_t fmt_code_row(int f, int64_t Kp) { return f == kFmtW8 ? Kp : Kp / 2; }
+__host__ __device__ constexpr int64_t fmt_high_row(int f, int64_t Kp) { return Kp * fmt_high_bits(f) / 8; }
+__host__ __device__ constexpr int64_t fmt_scale_row(int f, int64_t Kp) { return Kp / fmt_group(f) * 2; }
+
 struct StreamLayout {
-  uint32_t x_off, part_off, bar_off, code_off, code_stride, sc_off, sc_stride, bytes;
+  uint32_t x_off, part_off, bar_off, code_off, code_stride, high_off, high_stride, sc_off, sc_stride, bytes;
 };
 
 // x (bf16, TT rows of K), partial sums [rows_cap][nj][TT] fp32, the x barrier, nfull
 // "block landed" barriers and `slots` "slot free" barriers, the code slots
-// (128-byte aligned) and the scale slots (16-byte aligned; a block's run of
-// scales plus up to 15 bytes of alignment slack on either side).
+// (128-byte aligned), the high-bit slots (Q5 / Q6 only) and the scale slots
+// (16-byte aligned; a block's run of scales plus up to 15 bytes of alignment
+// slack on either side).
 __host__ __device__ inline StreamLayout stream_layout(int64_t K, int tt, int rb, int64_t rows_cap, int nj, int slots,
-                                                      int nfull) {
+                                                      int nfull, int fmt = kFmtQ4) {
   StreamLayout L;
   const int64_t Kp = (K + 127) & ~(int64_t)127;   // the planes' stored width
   L.x_off = 0;
   L.part_off = (uint32_t)(tt * K * 2);
   L.bar_off = (uint32_t)((L.part_off + rows_cap * nj * tt * 4 + 15) / 16 * 16);
   L.code_off = (L.bar_off + 8 + (uint32_t)(nfull + slots) * 8 + 127) / 128 * 128;
-  L.code_stride = (uint32_t)((rb * (Kp / 2) + 127) / 128 * 128);
-  L.sc_off = L.code_off + (uint32_t)slots * L.code_stride;
-  L.sc_stride = (uint32_t)((rb * (Kp / 32) + 32 + 15) / 16 * 16);
+  L.code_stride = (uint32_t)((rb * fmt_code_row(fmt, Kp) + 127) / 128 * 128);
+  L.high_off = L.code_off + (uint32_t)slots * L.code_stride;
+  L.high_stride = (uint32_t)((rb * fmt_high_row(fmt, Kp) + 15) / 16 * 16);
+  L.sc_off = L.high_off + (uint32_t)slots * L.high_stride;
+  L.sc_stride = (uint32_t)((rb * fmt_scale_row(fmt, Kp) + 32 + 15) / 16 * 16);
   L.bytes = L.sc_off + (uint32_t)slots * L.sc_stride;
   return L;
 }
@@ -216,8 +244,11 @@ __host__ __device__ inline StreamLayout stream_layout(int64_t K, int tt, int rb,
 // stored before the barrier arrival that publishes them).
 __device__ __forceinline__ void stream_issue(const uint8_t* wq, const uint8_t* sc_plane, int64_t plane_bytes,
                                              int64_t row_bytes, int64_t sc_row_bytes, int64_t ra, int nr,
-                                             uint32_t code_dst, uint32_t sc_dst, uint32_t full_bar) {
+                                             uint32_t code_dst, uint32_t sc_dst, uint32_t full_bar,
+                                             const uint8_t* wh = nullptr, int64_t high_row_bytes = 0,
+                                             uint32_t high_dst = 0) {
   const uint32_t cbytes = (uint32_t)(nr * row_bytes);
+  const uint32_t hbytes = (uint32_t)(nr * high_row_bytes);   // Q5 / Q6 high-bit rows
   const int64_t st = ra * sc_row_bytes, en = (ra + nr) * sc_row_bytes;
   const int64_t a = st & ~(int64_t)15;
   const int64_t e_up = (en + 15) & ~(int64_t)15, e_cap = plane_bytes & ~(int64_t)15;
@@ -225,8 +256,9 @@ __device__ __forceinline__ void stream_issue(const uint8_t* wq, const uint8_t* s
   for (int64_t t = (e > st ? e : st); t < en; t += 2)
     st_shared_u16(sc_dst + (uint32_t)(t - a), *reinterpret_cast<const uint16_t*>(sc_plane + t));
   const uint32_t sbytes = (uint32_t)(e - a);
-  mbar_expect_tx(full_bar, cbytes + sbytes);
+  mbar_expect_tx(full_bar, cbytes + hbytes + sbytes);
   bulk_g2s(code_dst, wq + ra * row_bytes, cbytes, full_bar);
+  if (hbytes > 0) bulk_g2s(high_dst, wh + ra * high_row_bytes, hbytes, full_bar);
   if (sbytes > 0) bulk_g2s(sc_dst, sc_plane + a, sbytes, full_bar);
 }
 
@@ -257,16 +289,21 @@ __device__ __forceinline__ float reduce_rows(const float (&acc)[RB], int lane, i
   return a[0];
 }
 
-template <int RB, int TT, bool kPad>
+template <int RB, int TT, bool kPad, int FMT>
 __global__ void __launch_bounds__(kStreamThreads, 1)
 q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict__ scales,
                       const uint16_t* __restrict__ x, uint16_t* __restrict__ y, int64_t N, int64_t K,
-                      int64_t rows_cap, int nj, int nw, int slots, int nfull) {
-  // A lane's chunk: 16 code bytes (32 weights) for one token, 8 code bytes (16
-  // weights) for several, so the x values of every token fit in registers.
-  constexpr int kCW = TT == 1 ? 16 : 8;           // code bytes per lane chunk
-  constexpr int kCV = 2 * kCW;                    // weights per lane chunk
+                      int64_t rows_cap, int nj, int nw, int slots, int nfull, const uint8_t* __restrict__ wh) {
+  // A lane's chunk: 32 weights for one token, 16 for several, so the x values of
+  // every token fit in registers.  Its codes are 16 / 8 bytes (4-bit low plane;
+  // W8: 32 / 16 bytes), its high bits 4 / 2 bytes (Q5) or 8 / 4 bytes (Q6).
+  constexpr int kCV = TT == 1 ? 32 : 16;          // weights per lane chunk
+  constexpr int kCW = FMT == kFmtW8 ? kCV : kCV / 2;   // code bytes per lane chunk
   constexpr int kWords = kCW / 4;                 // 32-bit code words per chunk
+  constexpr int kHB = kCV * fmt_high_bits(FMT) / 8;    // high-bit bytes per lane chunk
+  constexpr int kGroup = fmt_group(FMT);
+  // (128 + q) x summed, minus (128 + zero point) sum x; W8 see the decode below
+  constexpr float kBias = FMT == kFmtQ5 ? 144.f : FMT == kFmtQ6 ? 160.f : FMT == kFmtW8 ? 2304.f : 136.f;
   constexpr int kTP = TT == 1 ? 1 : TT == 2 ? 2 : 4;   // tokens padded to a power of two
   static_assert(RB * kTP <= 32, "one butterfly reduces at most 32 partials");
   extern __shared__ __align__(128) uint8_t smem[];
@@ -278,7 +315,8 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
   // that instantiation keeps the simpler address arithmetic, which measured a few
   // percent faster.
   const int64_t Kp = kPad ? ((K + 127) & ~(int64_t)127) : K;
-  const int64_t row_bytes = Kp / 2, sc_row_bytes = Kp / 32;
+  const int64_t row_bytes = fmt_code_row(FMT, Kp), sc_row_bytes = fmt_scale_row(FMT, Kp);
+  const int64_t high_row_bytes = fmt_high_row(FMT, Kp);
   const int64_t nchunk = kPad ? (K + kCV - 1) / kCV : K / kCV;
   const int64_t plane_bytes = N * sc_row_bytes;
   const uint8_t* sc_plane = reinterpret_cast<const uint8_t*>(scales);
@@ -297,7 +335,7 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
       bulk_prefetch_l2(sc_plane + off, (uint32_t)(a1 - off < 32768 ? a1 - off : 32768));
   }
   pdl_wait_previous();  // before any global-memory read that must see the previous kernel's writes
-  const StreamLayout L = stream_layout(K, TT, RB, rows_cap, nj, slots, nfull);
+  const StreamLayout L = stream_layout(K, TT, RB, rows_cap, nj, slots, nfull, FMT);
   float* part = reinterpret_cast<float*>(smem + L.part_off);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t xbar = sbase + L.bar_off;
@@ -325,7 +363,8 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
     for (int b = 0; b < first; ++b)
       stream_issue(wq, sc_plane, plane_bytes, row_bytes, sc_row_bytes, r0 + (int64_t)b * RB,
                    b == nb - 1 ? (int)last_rows : RB, sbase + L.code_off + (uint32_t)b * L.code_stride,
-                   sbase + L.sc_off + (uint32_t)b * L.sc_stride, full0 + 8u * b);
+                   sbase + L.sc_off + (uint32_t)b * L.sc_stride, full0 + 8u * b, wh, high_row_bytes,
+                   sbase + L.high_off + (uint32_t)b * L.high_stride);
   }
   __syncthreads();
 
@@ -338,7 +377,8 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
       if (lane == 0)
         stream_issue(wq, sc_plane, plane_bytes, row_bytes, sc_row_bytes, r0 + (int64_t)b * RB,
                      b == nb - 1 ? (int)last_rows : RB, sbase + L.code_off + (uint32_t)s * L.code_stride,
-                     sbase + L.sc_off + (uint32_t)s * L.sc_stride, full0 + 8u * (b % nfull));
+                     sbase + L.sc_off + (uint32_t)s * L.sc_stride, full0 + 8u * (b % nfull), wh,
+                     high_row_bytes, sbase + L.high_off + (uint32_t)s * L.high_stride);
       __syncwarp();
     }
     if (b < nb && lane == 0) {  // aborted: let the copies already issued land before the CTA exits
@@ -350,7 +390,7 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
   } else if (warp - 1 < nw) {
     const int w = warp - 1;
     const int items = nb * nj;
-    const uint32_t rowb = (uint32_t)row_bytes, scrb = (uint32_t)sc_row_bytes;
+    const uint32_t rowb = (uint32_t)row_bytes, scrb = (uint32_t)sc_row_bytes, hrowb = (uint32_t)high_row_bytes;
     // alignment slack of block 0's scale run in its slot; block b's is (d0 + b RB scrb) mod 16
     const uint32_t d0 = (uint32_t)((r0 * sc_row_bytes) & 15);
     float2 xv[TT][kCV / 2];
@@ -385,15 +425,16 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
           float2 xs2 = xv[t][0];
 #pragma unroll
           for (int q = 1; q < kCV / 2; ++q) xs2 = fadd2(xs2, xv[t][q]);
-          bias[t] = -136.f * (xs2.x + xs2.y);
+          bias[t] = -kBias * (xs2.x + xs2.y);
         }
         cur_j = j;
       }
       if (!warp_wait(full0 + 8u * fb, fph, abort_flag, &g_gemv_status)) break;
       const int nr = b == nb - 1 ? (int)last_rows : RB;
       const uint32_t crow = sbase + L.code_off + (uint32_t)s * L.code_stride + c * (uint32_t)kCW;
+      const uint32_t hrow = sbase + L.high_off + (uint32_t)s * L.high_stride + c * (uint32_t)kHB;
       const uint32_t srow = sbase + L.sc_off + (uint32_t)s * L.sc_stride +
-                            ((d0 + (uint32_t)b * (uint32_t)RB * scrb) & 15u) + (c * (uint32_t)kCV / 64u) * 2u;
+                            ((d0 + (uint32_t)b * (uint32_t)RB * scrb) & 15u) + (c * (uint32_t)kCV / (uint32_t)kGroup) * 2u;
       float acc[RB * kTP];
 #pragma unroll
       for (int i = 0; i < RB * kTP; ++i) acc[i] = 0.f;
@@ -401,31 +442,87 @@ q4_gemv_stream_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict
       for (int i = 0; i < RB; ++i) {
         if (i < nr && c_ok) {
           uint32_t words[kWords];
-          if constexpr (kWords == 4) {
+          if constexpr (kWords == 8) {
+            const uint4 cw0 = ld_shared_v4(crow + (uint32_t)i * rowb), cw1 = ld_shared_v4(crow + (uint32_t)i * rowb + 16u);
+            words[0] = cw0.x; words[1] = cw0.y; words[2] = cw0.z; words[3] = cw0.w;
+            words[4] = cw1.x; words[5] = cw1.y; words[6] = cw1.z; words[7] = cw1.w;
+          } else if constexpr (kWords == 4) {
             const uint4 cw = ld_shared_v4(crow + (uint32_t)i * rowb);
             words[0] = cw.x; words[1] = cw.y; words[2] = cw.z; words[3] = cw.w;
           } else {
             const uint2 cw = ld_shared_v2(crow + (uint32_t)i * rowb);
             words[0] = cw.x; words[1] = cw.y;
           }
+          // Q5 / Q6: this lane's high bits of row i (in k order from bit 0)
+          uint32_t hb[kHB >= 8 ? 2 : 1] = {};
+          if constexpr (kHB > 0) {
+            const uint32_t ha = hrow + (uint32_t)i * hrowb;
+            if constexpr (kHB == 8) {
+              const uint2 h = ld_shared_v2(ha);
+              hb[0] = h.x;
+              hb[kHB >= 8 ? 1 : 0] = h.y;
+            } else if constexpr (kHB == 4) {
+              hb[0] = ld_shared_u32(ha);
+            } else {
+              hb[0] = ld_shared_u16(ha);
+            }
+          }
           const float sc = fp16_bits_to_float(ld_shared_u16(srow + (uint32_t)i * scrb));
           float2 p2[TT];
+          float2 ph[FMT == kFmtW8 ? TT : 1];   // W8: partials of the high nibbles
 #pragma unroll
           for (int t = 0; t < TT; ++t) p2[t] = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int wi = 0; wi < kWords; ++wi) {
-            const uint32_t lo = words[wi] & 0x0F0F0F0Fu, hi = (words[wi] >> 4) & 0x0F0F0F0Fu;
-            const float2 f0 = make_float2(f128_plus_byte<0>(lo), f128_plus_byte<0>(hi));
-            const float2 f1 = make_float2(f128_plus_byte<1>(lo), f128_plus_byte<1>(hi));
-            const float2 f2 = make_float2(f128_plus_byte<2>(lo), f128_plus_byte<2>(hi));
-            const float2 f3 = make_float2(f128_plus_byte<3>(lo), f128_plus_byte<3>(hi));
+          for (int t = 0; t < (FMT == kFmtW8 ? TT : 1); ++t) ph[t] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int t = 0; t < TT; ++t) {
-              p2[t] = ffma2(f0, xv[t][4 * wi + 0], p2[t]);
-              p2[t] = ffma2(f1, xv[t][4 * wi + 1], p2[t]);
-              p2[t] = ffma2(f2, xv[t][4 * wi + 2], p2[t]);
-              p2[t] = ffma2(f3, xv[t][4 * wi + 3], p2[t]);
+          for (int wi = 0; wi < kWords; ++wi) {
+            if constexpr (FMT == kFmtW8) {
+              // 4 signed codes: code = lo + 16 (hs - 8) with lo, hs in 0..15, so
+              // sum code x = sum (128 + lo) x + 16 sum (128 + hs) x - 2304 sum x
+              const uint32_t lo = words[wi] & 0x0F0F0F0Fu;
+              const uint32_t hs = ((words[wi] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
+              const float2 l01 = make_float2(f128_plus_byte<0>(lo), f128_plus_byte<1>(lo));
+              const float2 l23 = make_float2(f128_plus_byte<2>(lo), f128_plus_byte<3>(lo));
+              const float2 h01 = make_float2(f128_plus_byte<0>(hs), f128_plus_byte<1>(hs));
+              const float2 h23 = make_float2(f128_plus_byte<2>(hs), f128_plus_byte<3>(hs));
+#pragma unroll
+              for (int t = 0; t < TT; ++t) {
+                p2[t] = ffma2(l01, xv[t][2 * wi + 0], p2[t]);
+                p2[t] = ffma2(l23, xv[t][2 * wi + 1], p2[t]);
+                ph[t] = ffma2(h01, xv[t][2 * wi + 0], ph[t]);
+                ph[t] = ffma2(h23, xv[t][2 * wi + 1], ph[t]);
+              }
+            } else {
+              uint32_t lo = words[wi] & 0x0F0F0F0Fu, hi = (words[wi] >> 4) & 0x0F0F0F0Fu;
+              if constexpr (FMT == kFmtQ5) {
+                // the word's 8 high bits: even weights' bits to bit 4 of bytes 0..3 of lo,
+                // odd weights' to hi (one multiply spreads four bits without carries)
+                const uint32_t bits = (hb[0] >> (8 * wi)) & 0xFFu;
+                lo |= ((bits & 0x55u) * 0x00410410u) & 0x10101010u;
+                hi |= ((bits & 0xAAu) * 0x00208208u) & 0x10101010u;
+              } else if constexpr (FMT == kFmtQ6) {
+                // the word's 16 high bits (2 per weight): even weights' fields to bits 4..5
+                // of bytes 0..3 of lo, odd weights' to hi
+                const uint32_t h16 = (hb[wi >> 1] >> (16 * (wi & 1))) & 0xFFFFu;
+                lo |= spread_nibbles_to_bytes(h16 & 0x3333u) << 4;
+                hi |= spread_nibbles_to_bytes((h16 >> 2) & 0x3333u) << 4;
+              }
+              const float2 f0 = make_float2(f128_plus_byte<0>(lo), f128_plus_byte<0>(hi));
+              const float2 f1 = make_float2(f128_plus_byte<1>(lo), f128_plus_byte<1>(hi));
+              const float2 f2 = make_float2(f128_plus_byte<2>(lo), f128_plus_byte<2>(hi));
+              const float2 f3 = make_float2(f128_plus_byte<3>(lo), f128_plus_byte<3>(hi));
+#pragma unroll
+              for (int t = 0; t < TT; ++t) {
+                p2[t] = ffma2(f0, xv[t][4 * wi + 0], p2[t]);
+                p2[t] = ffma2(f1, xv[t][4 * wi + 1], p2[t]);
+                p2[t] = ffma2(f2, xv[t][4 * wi + 2], p2[t]);
+                p2[t] = ffma2(f3, xv[t][4 * wi + 3], p2[t]);
+              }
             }
+          }
+          if constexpr (FMT == kFmtW8) {
+#pragma unroll
+            for (int t = 0; t < TT; ++t) p2[t].x += 16.f * (ph[t].x + ph[t].y);
           }
 #pragma unroll
           for (int t = 0; t < TT; ++t) acc[i * kTP + t] = sc * ((p2[t].x + p2[t].y) + bias[t]);
@@ -478,7 +575,7 @@ int gemv_launch_count(int64_t N, int64_t K, int64_t T) {
 
 struct StreamPlan {
   int64_t grid, rows_cap;
-  int tt, rb, nj, nw, slots, nfull;
+  int tt, rb, nj, nw, slots, nfull, fmt;
   uint32_t bytes;
 };
 
@@ -487,8 +584,9 @@ struct StreamPlan {
 // warp reloads x per row decoded: 6144 x 5120 T = 3 takes 13.4 us with them,
 // 15.7 us with 4-row blocks); the ring gets as many slots as the shared-memory
 // budget holds (at least 2).
-static bool stream_plan(int64_t N, int64_t K, int64_t T, int nsm, StreamPlan* p) {
+static bool stream_plan(int64_t N, int64_t K, int64_t T, int nsm, StreamPlan* p, int fmt = kFmtQ4) {
   if (N < 1 || K < 8 || T < 1 || T > 4) return false;
+  p->fmt = fmt;
   p->tt = (int)T;
   const int64_t chunk_w = T == 1 ? 32 : 16;   // weights per lane chunk
   const int64_t nchunk = (K + chunk_w - 1) / chunk_w;
@@ -498,7 +596,8 @@ static bool stream_plan(int64_t N, int64_t K, int64_t T, int nsm, StreamPlan* p)
   // more than 3 of the 15, then all 15 (a warp reloads x when its group changes)
   const int whole = p->nj <= kStreamConsumers ? (kStreamConsumers / p->nj) * p->nj : 0;
   p->nw = whole >= kStreamConsumers - 3 ? whole : kStreamConsumers;
-  p->rb = 8 * (Kp / 2) <= 32768 ? 8 : 4 * (Kp / 2) <= 40960 ? 4 : 2;
+  const int64_t code_row = fmt_code_row(fmt, Kp);
+  p->rb = 8 * code_row <= 32768 ? 8 : 4 * code_row <= 40960 ? 4 : 2;
   p->grid = (N + 3) / 4;  // at least 4 rows per CTA
   if (p->grid > nsm) p->grid = nsm;
   if (p->grid < 1) p->grid = 1;
@@ -511,15 +610,15 @@ static bool stream_plan(int64_t N, int64_t K, int64_t T, int nsm, StreamPlan* p)
   const int lead = p->nw / p->nj + (p->nw % p->nj != 0 ? 1 : 0);
   const int64_t budget = kStreamSmemBudget;
   if (T * K * 2 > budget) return false;
-  const StreamLayout L0 = stream_layout(K, p->tt, p->rb, p->rows_cap, p->nj, 0, lead);
-  const int64_t per = (int64_t)L0.code_stride + L0.sc_stride + 16;
+  const StreamLayout L0 = stream_layout(K, p->tt, p->rb, p->rows_cap, p->nj, 0, lead, fmt);
+  const int64_t per = (int64_t)L0.code_stride + L0.high_stride + L0.sc_stride + 16;
   if ((int64_t)L0.code_off + 128 > budget) return false;
   int64_t s = (budget - L0.code_off - 128) / per;
   if (s > 32) s = 32;
   if (s < 2) return false;
   p->slots = (int)s;
   p->nfull = p->slots + lead;
-  p->bytes = stream_layout(K, p->tt, p->rb, p->rows_cap, p->nj, p->slots, p->nfull).bytes;
+  p->bytes = stream_layout(K, p->tt, p->rb, p->rows_cap, p->nj, p->slots, p->nfull, fmt).bytes;
   return p->bytes <= budget;
 }
 
@@ -534,13 +633,13 @@ static int device_sms() {
   return n;
 }
 
-template <int RB, int TT, bool kPad>
+template <int RB, int TT, bool kPad, int FMT>
 static int gemv_stream_launch_cfg(const LinearArgs& a, const StreamPlan& pl) {
   static bool attr[64] = {};
   int dev = 0;
   if (cuda_check(cudaGetDevice(&dev), "cudaGetDevice")) return Q4LIN_ERR_CUDA;
   if (dev >= 64 || !attr[dev]) {
-    if (cuda_check(cudaFuncSetAttribute(q4_gemv_stream_kernel<RB, TT, kPad>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cuda_check(cudaFuncSetAttribute(q4_gemv_stream_kernel<RB, TT, kPad, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)kStreamSmemBudget),
                    "gemv: cudaFuncSetAttribute"))
       return Q4LIN_ERR_CUDA;
@@ -557,26 +656,35 @@ static int gemv_stream_launch_cfg(const LinearArgs& a, const StreamPlan& pl) {
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cuda_check(cudaLaunchKernelEx(&cfg, q4_gemv_stream_kernel<RB, TT, kPad>, a.wq, a.scales, a.x, a.y, a.N, a.K,
-                                       pl.rows_cap, pl.nj, pl.nw, pl.slots, pl.nfull),
+  return cuda_check(cudaLaunchKernelEx(&cfg, q4_gemv_stream_kernel<RB, TT, kPad, FMT>, a.wq, a.scales, a.x, a.y, a.N, a.K,
+                                       pl.rows_cap, pl.nj, pl.nw, pl.slots, pl.nfull, a.wh),
                     "gemv: streaming kernel launch");
 }
 
-template <int TT, bool kPad>
+template <int TT, bool kPad, int FMT>
 static int gemv_stream_launch_pad(const LinearArgs& a, const StreamPlan& pl) {
-  if (pl.rb == 8) return gemv_stream_launch_cfg<8, TT, kPad>(a, pl);
-  if (pl.rb == 4) return gemv_stream_launch_cfg<4, TT, kPad>(a, pl);
-  return gemv_stream_launch_cfg<2, TT, kPad>(a, pl);
+  if (pl.rb == 8) return gemv_stream_launch_cfg<8, TT, kPad, FMT>(a, pl);
+  if (pl.rb == 4) return gemv_stream_launch_cfg<4, TT, kPad, FMT>(a, pl);
+  return gemv_stream_launch_cfg<2, TT, kPad, FMT>(a, pl);
 }
 
+// Q4 has an instantiation for K a multiple of 128 and one for padded K; the
+// sibling formats use the padded form, which is correct for every K.
 template <int TT>
 static int gemv_stream_launch_tt(const LinearArgs& a, const StreamPlan& pl) {
-  return a.K % 128 != 0 ? gemv_stream_launch_pad<TT, true>(a, pl) : gemv_stream_launch_pad<TT, false>(a, pl);
+  switch (pl.fmt) {
+    case kFmtQ5: return gemv_stream_launch_pad<TT, true, kFmtQ5>(a, pl);
+    case kFmtQ6: return gemv_stream_launch_pad<TT, true, kFmtQ6>(a, pl);
+    case kFmtW8: return gemv_stream_launch_pad<TT, true, kFmtW8>(a, pl);
+    default:
+      return a.K % 128 != 0 ? gemv_stream_launch_pad<TT, true, kFmtQ4>(a, pl)
+                            : gemv_stream_launch_pad<TT, false, kFmtQ4>(a, pl);
+  }
 }
 
 static int gemv_stream_launch(const LinearArgs& a) {
   StreamPlan pl;
-  if (!stream_plan(a.N, a.K, a.T, device_sms(), &pl)) return Q4LIN_ERR_INVALID_ARG;
+  if (!stream_plan(a.N, a.K, a.T, device_sms(), &pl, a.fmt)) return Q4LIN_ERR_INVALID_ARG;
   switch (pl.tt) {
     case 1: return gemv_stream_launch_tt<1>(a, pl);
     case 2: return gemv_stream_launch_tt<2>(a, pl);
@@ -585,9 +693,17 @@ static int gemv_stream_launch(const LinearArgs& a) {
   }
 }
 
-bool gemv_stream_ok(int64_t N, int64_t K, int64_t T) {
+bool gemv_stream_ok(int64_t N, int64_t K, int64_t T, int fmt) {
   StreamPlan pl;
-  return stream_plan(N, K, T, device_sms(), &pl);   // the plan the launch will make
+  return stream_plan(N, K, T, device_sms(), &pl, fmt);   // the plan the launch will make
+}
+
+int gemv_launch_fmt(const LinearArgs& a) {
+  if (!gemv_stream_ok(a.N, a.K, a.T, a.fmt)) {
+    set_error_detail("gemv: no streaming plan for this format and shape (1..4 tokens only)");
+    return Q4LIN_ERR_UNSUPPORTED_SHAPE;
+  }
+  return gemv_stream_launch(a);
 }
 
 int gemv_launch(const LinearArgs& a) {

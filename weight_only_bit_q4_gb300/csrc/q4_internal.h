@@ -19,6 +19,8 @@ struct LinearArgs {
   int64_t N, K, T;
   void* workspace;
   cudaStream_t stream;
+  int fmt = 0;                   // weight format (0: Q4G64; 1: Q5G64, 2: Q6G64, 3: W8G32)
+  const uint8_t* wh = nullptr;   // Q5G64 / Q6G64: the high-bit plane
 };
 
 // The weight planes are stored for K rounded up to a multiple of 128
@@ -31,7 +33,9 @@ size_t gemv_workspace_bytes(int64_t N, int64_t K, int64_t T);
 int gemv_launch_count(int64_t N, int64_t K, int64_t T);
 // Whether the streaming kernel (1..4 tokens, one launch) has a shared-memory plan for
 // (N, K, T) on the current device.
-bool gemv_stream_ok(int64_t N, int64_t K, int64_t T);
+bool gemv_stream_ok(int64_t N, int64_t K, int64_t T, int fmt = 0);
+// The sibling formats (fmt 1..3) run on the streaming GEMV only.
+int gemv_launch_fmt(const LinearArgs& a);
 
 // tcgen05 tile routes: one CTA per 128-row x BN-token output tile (per K
 // share when split across a cluster), group partials in tensor memory.

@@ -119,6 +119,26 @@ int run_impl(int route, const uint8_t* wq, const uint16_t* scales, const uint16_
   }
 }
 
+// Sibling formats: the same checks as the Q4 layer, plus the high-bit plane for
+// Q5G64 / Q6G64, then the streaming GEMV (1..4 tokens) or UNSUPPORTED_SHAPE.
+int run_qtype_impl(int qtype, const uint8_t* codes, const uint8_t* high, const uint16_t* scales,
+                   const uint16_t* x, uint16_t* y, int64_t N, int64_t K, int64_t T, void* stream) {
+  int st = validate(codes, scales, x, y, N, K, T);
+  if (st != Q4LIN_OK) return st;
+  if (N == 0 || T == 0) return Q4LIN_OK;
+  const bool needs_high = qtype == Q4LIN_QTYPE_Q5G64 || qtype == Q4LIN_QTYPE_Q6G64;
+  if (K > 0 && needs_high && high == nullptr) return Q4LIN_ERR_INVALID_ARG;
+  if (K > 0 && needs_high && !aligned16(high)) return Q4LIN_ERR_MISALIGNED;
+  st = check_device();
+  if (st != Q4LIN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K == 0) return q4::cuda_check(cudaMemsetAsync(y, 0, (size_t)N * (size_t)T * 2, s), "zero fill of y");
+  q4::LinearArgs a{codes, scales, x, y, N, K, T, nullptr, s};
+  a.fmt = qtype;
+  a.wh = needs_high ? high : nullptr;
+  return q4::gemv_launch_fmt(a);
+}
+
 int run(int route, const uint8_t* wq, const uint16_t* scales, const uint16_t* x, uint16_t* y, int64_t N,
         int64_t K, int64_t T, void* workspace, void* stream) {
   q4::set_error_detail("");
@@ -176,6 +196,20 @@ int q4lin_linear(const uint8_t* wq, const uint16_t* scales, const uint16_t* x, u
   return run(Q4LIN_ROUTE_AUTO, wq, scales, x, y, N, K, T, workspace, stream);
 }
 
+int q4lin_linear_qtype(int qtype, const uint8_t* codes, const uint8_t* high, const uint16_t* scales,
+                       const uint16_t* x, uint16_t* y, int64_t N, int64_t K, int64_t T, void* workspace,
+                       void* stream) {
+  if (qtype == Q4LIN_QTYPE_Q4G64) return run(Q4LIN_ROUTE_AUTO, codes, scales, x, y, N, K, T, workspace, stream);
+  if (qtype < Q4LIN_QTYPE_Q5G64 || qtype > Q4LIN_QTYPE_W8G32) {
+    q4::set_error_detail("unknown weight format");
+    return Q4LIN_ERR_INVALID_ARG;
+  }
+  q4::set_error_detail("");
+  const int st = run_qtype_impl(qtype, codes, high, scales, x, y, N, K, T, stream);
+  if (st != Q4LIN_OK && q4::g_detail[0] == 0) q4::set_error_detail(q4lin_status_string(st));
+  return st;
+}
+
 int q4lin_linear_route(int route, const uint8_t* wq, const uint16_t* scales, const uint16_t* x,
                        uint16_t* y, int64_t N, int64_t K, int64_t T, void* workspace, void* stream) {
   return run(route, wq, scales, x, y, N, K, T, workspace, stream);
@@ -185,7 +219,7 @@ const char* q4lin_status_string(int status) {
   switch (status) {
     case Q4LIN_OK: return "ok";
     case Q4LIN_ERR_INVALID_ARG: return "invalid argument (null pointer, negative or overflowing size)";
-    case Q4LIN_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (K must be a multiple of 128)";
+    case Q4LIN_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (K not a multiple of 8, or a format and shape the decode GEMV cannot plan)";
     case Q4LIN_ERR_MISALIGNED: return "misaligned pointer (16-byte buffers, 256-byte workspace)";
     case Q4LIN_ERR_WORKSPACE: return "workspace required but NULL";
     case Q4LIN_ERR_DEVICE: return "unsupported device (needs compute capability 10.x)";

@@ -18,7 +18,9 @@ STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED_SHAPE", 3: "MISALIGNED", 4:
 ROUTE_AUTO, ROUTE_GEMV, ROUTE_TC_SPLITK, ROUTE_TC = 0, 1, 2, 3
 ROUTE_NAMES = {ROUTE_AUTO: "auto", ROUTE_GEMV: "gemv", ROUTE_TC_SPLITK: "tc_splitk", ROUTE_TC: "tc"}
 
-EXPORTS = ("q4lin_workspace_bytes", "q4lin_linear", "q4lin_linear_route",
+QTYPES = {"q4g64": 0, "q5g64": 1, "q6g64": 2, "w8g32": 3}
+
+EXPORTS = ("q4lin_workspace_bytes", "q4lin_linear", "q4lin_linear_route", "q4lin_linear_qtype",
            "q4lin_route_workspace_bytes", "q4lin_select_route", "q4lin_tile_plan", "q4lin_kernel_launches",
            "q4lin_status_string",
            "q4lin_device_status", "q4lin_clear_device_status", "q4lin_last_error_detail",
@@ -56,6 +58,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q4lin_linear.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp]
     lib.q4lin_linear.restype = ctypes.c_int
     lib.q4lin_linear_route.argtypes = [ctypes.c_int, vp, vp, vp, vp, i64, i64, i64, vp, vp]
+    lib.q4lin_linear_qtype.argtypes = [ctypes.c_int, vp, vp, vp, vp, vp, i64, i64, i64, vp, vp]
+    lib.q4lin_linear_qtype.restype = ctypes.c_int
     lib.q4lin_linear_route.restype = ctypes.c_int
     lib.q4lin_select_route.argtypes = [i64, i64, i64]
     lib.q4lin_select_route.restype = ctypes.c_int
@@ -178,6 +182,41 @@ def linear(wq, scales, x, y=None, workspace=None, stream=None, route: int = ROUT
     s = (stream or torch.cuda.current_stream(x.device)).cuda_stream
     st = linear_raw(_ptr(wq), _ptr(scales), _ptr(x), _ptr(y), N, K, T,
                     _ptr(workspace) if need else None, ctypes.c_void_p(s), route)
+    if st != OK:
+        raise Q4LinError(st)
+    return y
+
+
+def linear_qtype(qtype: str, planes, scales, x, y=None, stream=None):
+    """Y[T, N] (bf16) for a sibling weight format ("q4g64", "q5g64", "q6g64", "w8g32").
+
+    planes: (codes,) for q4g64 / w8g32, (low codes, high bits) for q5g64 / q6g64;
+    planes and scales stored for Kp = K rounded up to 128 columns (see q4lin.h);
+    all CUDA, contiguous.  Q5 / Q6 / W8 run for 1..4 tokens.
+    """
+    import torch
+
+    qt = QTYPES[qtype]
+    T, K = x.shape
+    Kp = (K + 127) // 128 * 128
+    codes = planes[0]
+    N = codes.shape[0]
+    code_cols = Kp if qtype == "w8g32" else Kp // 2
+    group = 32 if qtype == "w8g32" else 64
+    bits = {"q5g64": 1, "q6g64": 2}.get(qtype, 0)
+    if tuple(codes.shape) != (N, code_cols) or tuple(scales.shape) != (N, Kp // group):
+        raise ValueError(f"shape mismatch: codes {tuple(codes.shape)} scales {tuple(scales.shape)} x {tuple(x.shape)}")
+    high = planes[1] if bits else None
+    if bits and tuple(high.shape) != (N, Kp * bits // 8):
+        raise ValueError(f"shape mismatch: high {tuple(high.shape)}")
+    for name, t in (("codes", codes), ("scales", scales), ("x", x)) + ((("high", high),) if bits else ()):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if y is None:
+        y = torch.empty((T, N), dtype=torch.bfloat16, device=x.device)
+    s = (stream or torch.cuda.current_stream(x.device)).cuda_stream
+    st = int(load().q4lin_linear_qtype(qt, _ptr(codes), _ptr(high) if bits else None, _ptr(scales), _ptr(x),
+                                       _ptr(y), N, K, T, None, ctypes.c_void_p(s)))
     if st != OK:
         raise Q4LinError(st)
     return y
