@@ -2,7 +2,7 @@
 """Benchmark of the Q4_G64_FP16 linear layer on one GB300 (or N replicas).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--t T] [--profile]
+                    [--workload NAME] [--t T] [--qtype FMT] [--profile]
 
 Timing (the linear-benchmark contract, section 6, and the Q4 measurement
 report's header table): every sample is one complete public call captured in
@@ -14,7 +14,9 @@ no host synchronisation.  The primary figure is the median; min and p95 are
 reported too.  Metrics follow the contract's sections 4-5 (weight_only_bit_q4_gb300.metrics).
 
 A step is one call of the layer on one batch of the workload's synthetic
-input.  Default workload: the decode GEMV, N=6144 K=5120 T=1.
+input.  Default workload: the decode GEMV, N=6144 K=5120 T=1.  --qtype times
+a sibling weight format (Q5G64, Q6G64, W8G32; 1..4 tokens) on the same
+geometry through q4lin_linear_qtype; its bytes are that format's.
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
 (the layer does not exchange data between GPUs); value = the units all ranks
 processed / the slowest rank's time.
@@ -69,6 +71,8 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     p.add_argument("--t", type=int, default=None, help="T for the sweep workloads")
+    p.add_argument("--qtype", default="q4g64", choices=sorted(metrics.GROUP_BYTES),
+                   help="weight format (the sibling formats run for 1..4 tokens)")
     p.add_argument("--profile", action="store_true",
                    help="one call between cudaProfilerStart/Stop after warm-up and flush (for ncu --profile-from-start off)")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -89,7 +93,21 @@ def workload(args):
     if xs is None:
         xs = T
     name = args.workload if WORKLOADS[args.workload][2] is not None else f"{args.workload}_t{T}"
-    return dict(name=name, N=N, K=K, T=T, dist=dist, outliers=outl, w_seed=ws, x_seed=xs)
+    qtype = getattr(args, "qtype", "q4g64")
+    if qtype != "q4g64":
+        if T > 4:
+            raise SystemExit(f"{qtype} runs for 1..4 tokens")
+        name = qtype + name[2:]            # q4_6144x5120_t1 -> q5g64_6144x5120_t1
+    return dict(name=name, N=N, K=K, T=T, dist=dist, outliers=outl, w_seed=ws, x_seed=xs, qtype=qtype)
+
+
+def format_problem(wl, rows=None):
+    """(planes, scales, x) of a sibling-format workload (its first ``rows`` rows)."""
+    planes, sc, x = synth.make_problem_fmt(wl["qtype"], wl["N"], wl["K"], wl["T"],
+                                           w_seed=wl["w_seed"], x_seed=wl["x_seed"])
+    if rows is not None:
+        planes, sc = tuple(p[:rows] for p in planes), sc[:rows]
+    return planes, sc, x
 
 
 def small_t(wl):
@@ -242,16 +260,20 @@ def measure_ours(args, wl, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     N, K, T = wl["N"], wl["K"], wl["T"]
-    wq = synth.packed_codes(N, K, wl["w_seed"])
-    sc = synth.group_scales(N, K, wl["w_seed"], wl["dist"])
-    x = synth.activations(T, K, wl["x_seed"], wl["outliers"])
-    per_copy = metrics.model_bytes(N, K, T)
+    qtype = wl["qtype"]
+    if qtype == "q4g64":
+        planes = (synth.packed_codes(N, K, wl["w_seed"]),)
+        sc = synth.group_scales(N, K, wl["w_seed"], wl["dist"])
+        x = synth.activations(T, K, wl["x_seed"], wl["outliers"])
+    else:
+        planes, sc, x = format_problem(wl)
+    per_copy = metrics.model_bytes(N, K, T, qtype)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size or (128 << 20)
     R = int(max(2, min(64, -(-int(2.5 * l2) // per_copy))))
-    wq_d = torch.from_numpy(wq).to(dev)
+    pl_d = tuple(torch.from_numpy(p).to(dev) for p in planes)
     sc_d = torch.from_numpy(sc.view(np.int16)).to(dev)
     x_d = torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
-    wqs = [wq_d] + [wq_d.clone() for _ in range(R - 1)]
+    pls = [pl_d] + [tuple(p.clone() for p in pl_d) for _ in range(R - 1)]
     scs = [sc_d] + [sc_d.clone() for _ in range(R - 1)]
     xs = [x_d] + [x_d.clone() for _ in range(R - 1)]
     ys = [torch.empty((T, N), dtype=torch.bfloat16, device=dev) for _ in range(R)]
@@ -261,8 +283,14 @@ def measure_ours(args, wl, rank, world, local):
     launches = q4lin.kernel_launches(N, K, T)
     stream = torch.cuda.Stream(dev)
 
+    if qtype != "q4g64":
+        route, launches = q4lin.ROUTE_GEMV, 1            # the sibling formats run on the streaming GEMV alone
+
     def call(i):
-        q4lin.linear(wqs[i], scs[i], xs[i], y=ys[i], workspace=ws_d if ws_n else None, stream=stream)
+        if qtype == "q4g64":
+            q4lin.linear(pls[i][0], scs[i], xs[i], y=ys[i], workspace=ws_d if ws_n else None, stream=stream)
+        else:
+            q4lin.linear_qtype(qtype, pls[i], scs[i], xs[i], y=ys[i], stream=stream)
 
     with torch.cuda.stream(stream):
         for i in range(R):
@@ -372,6 +400,8 @@ def oracle_rows_for_budget(wl, seconds_per_step):
     N, K, T = wl["N"], wl["K"], wl["T"]
     # decode + FP64 matmul, measured on this class of host at roughly 2e8 weight*token/s per call
     per_row = K * (1.0 + T / 8.0) / 2.0e8
+    if wl["qtype"] != "q4g64":
+        per_row *= 3.5          # two planes (or int8 codes at twice the count) to decode
     return int(max(1, min(N, seconds_per_step / max(per_row, 1e-12))))
 
 
@@ -380,14 +410,23 @@ def time_oracle(wl, rows, reps_budget_s, max_reps, exact=False):
     import oracle
 
     N, K, T = wl["N"], wl["K"], wl["T"]
-    wq = synth.packed_codes(rows, K, wl["w_seed"])   # the first `rows` rows of the same weight stream
-    sc = synth.group_scales(N, K, wl["w_seed"], wl["dist"])[:rows]
-    x = synth.activations(T, K, wl["x_seed"], wl["outliers"])
+    if wl["qtype"] == "q4g64":
+        wq = synth.packed_codes(rows, K, wl["w_seed"])   # the first `rows` rows of the same weight stream
+        sc = synth.group_scales(N, K, wl["w_seed"], wl["dist"])[:rows]
+        x = synth.activations(T, K, wl["x_seed"], wl["outliers"])
+
+        def run():
+            return oracle.linear(wq, sc, x)
+    else:
+        planes, sc, x = format_problem(wl, rows)
+
+        def run():
+            return oracle.sibling_formats.linear(wl["qtype"], planes, sc, x)
     times = []
     t_end = time.monotonic() + reps_budget_s
     while len(times) < max_reps and (exact or len(times) < 3 or time.monotonic() < t_end):
         t0 = time.perf_counter()
-        y = oracle.linear(wq, sc, x)
+        y = run()
         times.append(time.perf_counter() - t0)
         assert y.shape == (T, rows) and np.isfinite(y).all()
     return times
@@ -395,7 +434,7 @@ def time_oracle(wl, rows, reps_budget_s, max_reps, exact=False):
 
 def oracle_units(wl, rows):
     K, T = wl["K"], wl["T"]
-    b = metrics.model_bytes(rows, K, T)
+    b = metrics.model_bytes(rows, K, T, wl["qtype"])
     f = metrics.useful_flops(rows, K, T)
     return b, f
 
@@ -436,7 +475,7 @@ def reference_arm(args, wl, rank, world):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": unit,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(med * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl["name"], "N": wl["N"], "K": wl["K"], "T": wl["T"]},
+        "config": {"workload": wl["name"], "N": wl["N"], "K": wl["K"], "T": wl["T"], "qtype": wl["qtype"]},
         "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": blas_threads(), "kind": "oracle",
                          "sample": f"each step: FP64 oracle on rows 0..{rows - 1} of the weight, all {wl['T']} tokens"},
         "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -452,7 +491,7 @@ def main(argv=None):
     wl = workload(args)
     if args.steps is None:
         # about a second of GPU time at the expected rate, so the clock sampler sees the timed region
-        us_guess = max(2.0, metrics.model_bytes(wl["N"], wl["K"], wl["T"]) / 5e3 / 1e3,
+        us_guess = max(2.0, metrics.model_bytes(wl["N"], wl["K"], wl["T"], wl["qtype"]) / 5e3 / 1e3,
                        metrics.useful_flops(wl["N"], wl["K"], wl["T"]) / 1.0e15 * 1e6)
         args.steps = int(min(200000, max(1000, 1.0e6 / us_guess)))
     if args.impl == "reference":
@@ -471,7 +510,7 @@ def main(argv=None):
     med_rep = statistics.median(res["per_call_us"])         # median over graph replays
     mean_max, med_max = reduce_max([mean_us, med_rep], world, dev)
     N, K, T = wl["N"], wl["K"], wl["T"]
-    mb, fl = metrics.model_bytes(N, K, T), metrics.useful_flops(N, K, T)
+    mb, fl = metrics.model_bytes(N, K, T, wl["qtype"]), metrics.useful_flops(N, K, T)
     small = small_t(wl)
     unit = "GB/s" if small else "TFLOP/s"
 
@@ -512,7 +551,7 @@ def main(argv=None):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32" if res["route"] == "gemv" else "bf16xbf16->f32",
         "data": "synthetic",
-        "config": {"workload": wl["name"], "N": N, "K": K, "T": T, "route": res["route"],
+        "config": {"workload": wl["name"], "N": N, "K": K, "T": T, "qtype": wl["qtype"], "route": res["route"],
                    "tile": res["tile"],
                    "timing": f"steady state: CUDA graph of {res['copies']} back-to-back calls replayed, events per replay",
                    "l2": f"inputs larger than L2: {res['copies']} rotating copies of weights, X and Y "

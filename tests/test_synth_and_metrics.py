@@ -78,3 +78,25 @@ def test_metric_functions_reproduce_printed_table(golden):
 def test_percentile():
     v = sorted(range(1, 101))
     assert metrics.percentile(v, 50) == 50 and metrics.percentile(v, 95) == 95
+
+
+def test_sibling_format_bytes_per_group():
+    # format table: Q5G64 42 B and Q6G64 50 B per 64 weights, W8G32 34 B per 32 (6144 x 5120 has 80 / 160 groups per row)
+    assert metrics.weight_bytes("q4g64", 6144, 5120) == metrics.q4_weight_bytes(6144, 5120) == 6144 * 80 * 34
+    assert metrics.weight_bytes("q5g64", 6144, 5120) == 6144 * 80 * 42
+    assert metrics.weight_bytes("q6g64", 6144, 5120) == 6144 * 80 * 50
+    assert metrics.weight_bytes("w8g32", 6144, 5120) == 6144 * 160 * 34
+    assert metrics.weight_bytes("q6g64", 4304, 1152) == 4304 * 1152 // 64 * 50
+    assert metrics.model_bytes(6144, 5120, 2, "w8g32") == 6144 * 160 * 34 + 4 * 5120 + 4 * 6144
+
+
+def test_bench_format_workloads():
+    import bench
+    wl = bench.workload(bench.parse_args(["--qtype", "q5g64"]))
+    assert (wl["name"], wl["N"], wl["K"], wl["T"], wl["qtype"]) == ("q5g64_6144x5120_t1", 6144, 5120, 1, "q5g64")
+    wl = bench.workload(bench.parse_args(["--qtype", "w8g32", "--workload", "q4_34816x5120", "--t", "4"]))
+    assert wl["name"] == "w8g32_34816x5120_t4"
+    with pytest.raises(SystemExit):
+        bench.workload(bench.parse_args(["--qtype", "q6g64", "--workload", "q4_6144x5120", "--t", "8"]))
+    planes, s, x = bench.format_problem(dict(wl, N=40, K=256, T=2), rows=7)
+    assert planes[0].shape == (7, 256) and s.shape == (7, 8) and x.shape == (2, 256)

@@ -10,6 +10,9 @@ measurement report (q4-linear.md, metric definitions):
     useful FLOPs  = 2*N*K*T  (decode, padding and split-K work not counted)
     TFLOP/s       = useful FLOPs / seconds / 1e12
     memory floor  = model_bytes / bandwidth
+
+The sibling formats of the same table count their own bytes per group:
+Q5G64 42 and Q6G64 50 per 64 weights, W8G32 34 per 32 weights.
 """
 from __future__ import annotations
 
@@ -22,8 +25,17 @@ def q4_weight_bytes(N: int, K: int) -> int:
     return N * align_up(K, 128) // 64 * (32 + 2)
 
 
-def model_bytes(N: int, K: int, T: int) -> int:
-    return q4_weight_bytes(N, K) + 2 * K * T + 2 * N * T
+# qtype -> (weights per group, bytes per group, scale included)
+GROUP_BYTES = {"q4g64": (64, 34), "q5g64": (64, 42), "q6g64": (64, 50), "w8g32": (32, 34)}
+
+
+def weight_bytes(qtype: str, N: int, K: int) -> int:
+    group, per_group = GROUP_BYTES[qtype]
+    return N * align_up(K, 128) // group * per_group
+
+
+def model_bytes(N: int, K: int, T: int, qtype: str = "q4g64") -> int:
+    return weight_bytes(qtype, N, K) + 2 * K * T + 2 * N * T
 
 
 def useful_flops(N: int, K: int, T: int) -> int:
