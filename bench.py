@@ -2,7 +2,7 @@
 """Benchmark of the Q4_G64_FP16 linear layer on one GB300 (or N replicas).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--t T] [--qtype FMT] [--profile]
+                    [--workload NAME] [--t T] [--qtype FMT] [--route R] [--profile]
 
 Timing (the linear-benchmark contract, section 6, and the Q4 measurement
 report's header table): every sample is one complete public call captured in
@@ -73,6 +73,8 @@ def parse_args(argv=None):
     p.add_argument("--t", type=int, default=None, help="T for the sweep workloads")
     p.add_argument("--qtype", default="q4g64", choices=sorted(metrics.GROUP_BYTES),
                    help="weight format (the sibling formats run for 1..4 tokens)")
+    p.add_argument("--route", default="auto", choices=["auto", "tc_fp16"],
+                   help="auto: the library's choice; tc_fp16: the opt-in tile route on fp16-rounded weights")
     p.add_argument("--profile", action="store_true",
                    help="one call between cudaProfilerStart/Stop after warm-up and flush (for ncu --profile-from-start off)")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -98,6 +100,11 @@ def workload(args):
         if T > 4:
             raise SystemExit(f"{qtype} runs for 1..4 tokens")
         name = qtype + name[2:]            # q4_6144x5120_t1 -> q5g64_6144x5120_t1
+    route = getattr(args, "route", "auto")
+    if route != "auto":
+        if qtype != "q4g64":
+            raise SystemExit(f"--route {route} runs the Q4 format only")
+        name += "_" + route
     return dict(name=name, N=N, K=K, T=T, dist=dist, outliers=outl, w_seed=ws, x_seed=xs, qtype=qtype)
 
 
@@ -277,10 +284,14 @@ def measure_ours(args, wl, rank, world, local):
     scs = [sc_d] + [sc_d.clone() for _ in range(R - 1)]
     xs = [x_d] + [x_d.clone() for _ in range(R - 1)]
     ys = [torch.empty((T, N), dtype=torch.bfloat16, device=dev) for _ in range(R)]
-    ws_n = q4lin.workspace_bytes(N, K, T)
+    route_arg = q4lin.ROUTE_TC_FP16 if args.route == "tc_fp16" else q4lin.ROUTE_AUTO
+    ws_n = q4lin.workspace_bytes(N, K, T, route_arg)
     ws_d = torch.empty(max(ws_n, 256), dtype=torch.uint8, device=dev)
-    route = q4lin.select_route(N, K, T)
+    route = q4lin.select_route(N, K, T) if route_arg == q4lin.ROUTE_AUTO else route_arg
     launches = q4lin.kernel_launches(N, K, T)
+    if route_arg != q4lin.ROUTE_AUTO:   # operand pass + main launch (+ tail launch)
+        pl = q4lin.tile_plan_full(N, K, T, route_arg)
+        launches = 1 + (2 if pl["main_tiles"] < -(-N // 128) * -(-T // pl["n"]) else 1)
     stream = torch.cuda.Stream(dev)
 
     if qtype != "q4g64":
@@ -288,7 +299,8 @@ def measure_ours(args, wl, rank, world, local):
 
     def call(i):
         if qtype == "q4g64":
-            q4lin.linear(pls[i][0], scs[i], xs[i], y=ys[i], workspace=ws_d if ws_n else None, stream=stream)
+            q4lin.linear(pls[i][0], scs[i], xs[i], y=ys[i], workspace=ws_d if ws_n else None, stream=stream,
+                         route=route_arg)
         else:
             q4lin.linear_qtype(qtype, pls[i], scs[i], xs[i], y=ys[i], stream=stream)
 
@@ -390,7 +402,7 @@ def measure_ours(args, wl, rank, world, local):
 
     return dict(per_call_us=per_call_us, total_ms=total_ms, calls=calls, copies=R, cold_us=cold_us,
                 clocks=clocks, route=q4lin.ROUTE_NAMES.get(route, str(route)), launches=launches, e2e=e2e,
-                tile=q4lin.tile_plan_full(N, K, T),
+                tile=q4lin.tile_plan_full(N, K, T, route_arg),
                 ws_bytes=ws_n)
 
 
@@ -549,7 +561,7 @@ def main(argv=None):
         "metric": METRIC, "value": round(value, 3), "unit": unit,
         "n_gpus": world, "steps": res["calls"], "warmup": args.warmup, "ms_per_step": round(mean_max * 1e-3, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32" if res["route"] == "gemv" else "bf16xbf16->f32",
+        "dtype": {"gemv": "f32", "tc_fp16": "fp16xfp16->f32"}.get(res["route"], "bf16xbf16->f32"),
         "data": "synthetic",
         "config": {"workload": wl["name"], "N": N, "K": K, "T": T, "qtype": wl["qtype"], "route": res["route"],
                    "tile": res["tile"],

@@ -60,9 +60,29 @@ typedef enum {
 typedef enum {
   Q4LIN_ROUTE_AUTO = 0,     /* let the library choose (what q4lin_linear does) */
   Q4LIN_ROUTE_GEMV = 1,     /* CUDA-core GEMV, weights decoded once per token block of <= 4 */
-  Q4LIN_ROUTE_TC_SPLITK = 2,/* tcgen05 tile, K split across a thread-block cluster (small T) */
-  Q4LIN_ROUTE_TC = 3        /* tcgen05 tile, whole K per CTA, TMEM accumulator (large T) */
+  Q4LIN_ROUTE_TC_SPLITK = 2,/* tcgen05 tile, K split across a thread-block cluster where the
+                               planner finds it pays (what q4lin_linear uses from 5 tokens) */
+  Q4LIN_ROUTE_TC = 3,       /* tcgen05 tile, whole K per CTA */
+  Q4LIN_ROUTE_TC_FP16 = 4   /* opt-in: tcgen05 tile on fp16-rounded weights (see below) */
 } q4lin_route;
+
+/*
+ * Operand precision of the tile routes.  Q4LIN_ROUTE_TC and Q4LIN_ROUTE_TC_SPLITK
+ * keep every product (q - 8) * x exact (bf16 operands) and apply the group scale
+ * to FP32 per-group partial sums; they need no workspace.  The decode GEMV also
+ * applies the scale in FP32.
+ *
+ * Q4LIN_ROUTE_TC_FP16 is never chosen by q4lin_linear.  It folds the scale into the
+ * weight: each w = (q - 8) * s is rounded once to fp16 (taken at a power of two per
+ * weight row so it cannot overflow), X is converted to fp16 exactly (taken at a
+ * power of two per token), one FP32 tensor-memory accumulator sums the whole K
+ * share, and the powers of two are undone on the FP32 result.  The weight rounding
+ * (relative error at most 2^-11 per weight) puts rare outputs near y = 0 above the layer's
+ * 1e-3 * rms(y) accuracy floor; its guaranteed bound is looser:
+ * |y - y_ref| <= 8e-3 |y_ref| + 4e-3 rms(y_ref).  It needs workspace
+ * (2*T*K + 4*T + 4*N bytes, each part rounded up to 256; q4lin_route_workspace_bytes)
+ * and launches an operand pass before the tile kernel.
+ */
 
 /*
  * Bytes of device workspace q4lin_linear needs for (N, K, T); 0 means none
@@ -109,9 +129,10 @@ typedef enum {
 /*
  * Y = W . X for any of the formats above (arguments as q4lin_linear; `high`
  * is the Q5 / Q6 high-bit plane, 16-byte aligned, and is ignored otherwise).
- * Q4G64 is exactly q4lin_linear.  The other formats run on the decode GEMV,
- * for 1..4 tokens where its shared-memory plan fits; other shapes return
- * Q4LIN_ERR_UNSUPPORTED_SHAPE.  No workspace (the pointer may be NULL).
+ * Q4G64 is exactly q4lin_linear (workspace as q4lin_workspace_bytes).  The
+ * other formats run on the decode GEMV, for 1..4 tokens where its shared-memory
+ * plan fits; other shapes return Q4LIN_ERR_UNSUPPORTED_SHAPE.  They take no
+ * workspace (the pointer may be NULL).
  */
 int q4lin_linear_qtype(int qtype, const uint8_t* codes, const uint8_t* high, const uint16_t* scales,
                        const uint16_t* x, uint16_t* y, int64_t N, int64_t K, int64_t T, void* workspace,

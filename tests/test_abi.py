@@ -112,6 +112,29 @@ def test_workspace_query_and_route_selection(lib):
     assert q4lin.workspace_bytes(4, 100, 1) == 0
     assert q4lin.workspace_bytes(0, 128, 1) == 0
     assert q4lin.select_route(6144, 5120, 1) == q4lin.ROUTE_GEMV
+    assert q4lin.workspace_bytes(6144, 5120, 1) == 0
+
+
+def test_fp16_tile_route_workspace_checked_on_host(lib):
+    # the opt-in fp16 route refuses a NULL or misaligned workspace before any CUDA call
+    assert _call(64, 256, 8, route=q4lin.ROUTE_TC_FP16) == 4
+    assert _call(64, 256, 8, ws=16 + 128, route=q4lin.ROUTE_TC_FP16) == 3
+    assert _call(64, 256, 8, route=5) == 1
+
+
+def test_fp16_tile_route_workspace(lib):
+    # the opt-in fp16 route: fp16 X [T, K], then a per-token and a per-row int, each
+    # part rounded up to 256 bytes; the default routes take none
+    def r256(b):
+        return -(-b // 256) * 256
+    for N, K, T in [(6144, 5120, 1024), (1000, 1152, 37), (77, 72, 5)]:
+        want = r256(2 * T * K) + r256(4 * T) + r256(4 * N)
+        assert q4lin.workspace_bytes(N, K, T, q4lin.ROUTE_TC_FP16) == want
+        for r in (q4lin.ROUTE_AUTO, q4lin.ROUTE_TC, q4lin.ROUTE_TC_SPLITK, q4lin.ROUTE_GEMV):
+            assert q4lin.workspace_bytes(N, K, T, r) == 0
+    # it plans like the split route (clusters along K allowed)
+    assert q4lin.tile_plan(1024, 65536, 16, q4lin.ROUTE_TC_FP16)[1] > 1
+    assert q4lin.tile_plan(1024, 65536, 16, q4lin.ROUTE_TC)[1] == 1
 
 
 def test_valid_call_without_gpu_reports_error_not_crash(lib):

@@ -48,8 +48,10 @@ struct TcPlan {
 TcPlan tc_plan(int route, int64_t N, int64_t K, int64_t T, int sms);
 TcPlan tc_plan_current_device(int route, int64_t N, int64_t K, int64_t T);
 int tc_launch(const LinearArgs& a, int route);
-size_t tc_workspace_bytes(int64_t N, int64_t K, int64_t T);
-int tc_launch_count(int64_t N, int64_t K, int64_t T);
+// The folded tile routes (Q4LIN_ROUTE_TC, Q4LIN_ROUTE_TC_SPLITK) need workspace for
+// their fp16 operands and launch a prep kernel first; the exact route needs none.
+size_t tc_workspace_bytes(int route, int64_t N, int64_t K, int64_t T);
+int tc_launch_count(int route, int64_t N, int64_t K, int64_t T);
 bool tc_supported(int64_t N, int64_t K, int64_t T);
 
 // Reads (and optionally clears) the device error word of one translation unit.

@@ -285,6 +285,37 @@ __device__ __forceinline__ uint4 decode_word_bf16(uint32_t w) {
   return make_uint4(h[0], h[1], h[2], h[3]);
 }
 
+// fp16 pair arithmetic, round to nearest even, subnormals kept.
+__device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// As decode_word_bf16, with the group scale folded in: the 8 weights of one code
+// word as fp16 pairs (q - 8) * s2, each rounded once to fp16.  1024 + q is exact in
+// fp16 (0x6400 | q), minus 1032 (0x6408) gives q - 8 exactly; s2 holds the scale
+// twice.
+__device__ __forceinline__ uint4 decode_word_f16s(uint32_t w, uint32_t s2) {
+  const uint32_t w4 = w >> 4;
+  uint32_t h[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t t = __byte_perm(w, w4, (uint32_t)(j | ((4 + j) << 8)));
+    h[j] = f16x2_mul(f16x2_sub((t & 0x000F000Fu) | 0x64006400u, 0x64086408u), s2);
+  }
+  return make_uint4(h[0], h[1], h[2], h[3]);
+}
+
+// 2^k as a float for -126 <= k <= 127.
+__device__ __forceinline__ float exp2i(int k) { return __int_as_float((127 + k) << 23); }
+
 }  // namespace q4
 
 namespace q4 {

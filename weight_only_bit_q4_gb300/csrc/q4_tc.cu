@@ -67,6 +67,8 @@ __device__ int g_tc_status = 0;
 struct TcParams {
   const uint16_t* scales;
   uint16_t* y;
+  const int* xe;  // folded form: per token, X was stored as fp16 x * 2^-xe[t]
+  const int* rf;  // folded form: per weight row, the scales enter as s * 2^-rf[n]
   int64_t N, Kp, T;   // Kp: the planes' stored width, K rounded up to 128
   int nk;      // groups (K-steps of 64) holding columns < K
   int splitk;  // CTAs of a cluster sharing one output tile along K (1 = no split)
@@ -80,6 +82,7 @@ constexpr uint32_t kWBytes = kTileM * 128;  // one code stage
 constexpr uint32_t kABytes = kTileM * 128;  // one shared-memory A stage: 128 rows x 64 bf16
 constexpr int kRing = 8;                    // depth of the per-group MMA-done / issue rings
 constexpr uint32_t kIssueBar0 = 1;          // named barriers kIssueBar0 .. kIssueBar0 + kRing - 1
+constexpr uint32_t kAccBar = kIssueBar0 + kRing;  // folded form: the accumulate warps' start barrier
 
 // Per token-tile width: X stages, A stages, accumulator buffers, accumulate
 // warpgroups, code stages and where A lives.  Tensor memory holds NB * BN
@@ -97,17 +100,19 @@ template <> struct TcCfg<16> { static constexpr int SX = 8, SA = 8, NB = 8, NACC
 //   wg1 / wg2: decode teams of the even / odd groups, one thread per tile row
 //   wg3..: FP32 accumulation of the scaled group partials and the epilogue;
 //        warp w reads TMEM lane quadrant w % 4 and column chunk (w - 12) / 4
-template <int BN>
+template <int BN, bool kFold>
 struct TcSmem {
   using C = TcCfg<BN>;
-  static constexpr int SX = C::SX, SA = C::SA, NB = C::NB, NACC = C::NACC, SW = C::SW;
+  // the folded form keeps one accumulator for the whole K share
+  static constexpr int SX = C::SX, SA = C::SA, NB = kFold ? 1 : C::NB, NACC = C::NACC, SW = C::SW;
   static constexpr bool kATmem = C::kATmem;
   static_assert(SA % 2 == 0 && SX % 2 == 0, "the A and X ring depths must be even (one decode team per slot)");
   static_assert(kRing % 2 == 0 && kRing >= SX && kRing >= SA && kRing >= NB,
                 "the barrier rings must cover every buffer ring (no waiter two phases behind)");
   static_assert(NB * BN + (kATmem ? SA * 32 : 0) <= 512, "tensor memory budget");
   static constexpr int threads = 128 * (3 + NACC);
-  static constexpr uint32_t issue_threads = 128 + 128 * NACC + 32;  // decode team + accumulate + issuer
+  // decode team + issuer, and (exact form) the accumulate warps handing back a buffer
+  static constexpr uint32_t issue_threads = 128 + (kFold ? 0 : 128 * NACC) + 32;
   static constexpr uint32_t kB = BN * 128;  // one group of X: BN rows x 64 bf16
   static constexpr uint32_t x_off = 0;
   static constexpr uint32_t a_off = x_off + SX * kB;  // shared-memory A stages (A not in tensor memory)
@@ -140,11 +145,11 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* v) {
   else tmem_ld4(taddr, *reinterpret_cast<uint32_t(*)[4]>(v));
 }
 
-template <int BN>
-__global__ void __launch_bounds__(TcSmem<BN>::threads, 1)
+template <int BN, bool kFold>
+__global__ void __launch_bounds__(TcSmem<BN, kFold>::threads, 1)
 q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_x,
              const TcParams p) {
-  using L = TcSmem<BN>;
+  using L = TcSmem<BN, kFold>;
   using R = TcRegs<L::kATmem>;
   constexpr int SX = L::SX, SA = L::SA, NB = L::NB, NACC = L::NACC, SW = L::SW;
   constexpr int kAccWarps = 4 * NACC;
@@ -250,7 +255,8 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
           mbar_drain(c_full(ws % SW), (ws / SW) & 1);
     } else if (warp == 3) {
       // ----------------------------------------------------------- MMA issuer (no shared-memory access)
-      constexpr uint32_t idesc = idesc_kind_f16(kTileM, BN, 1);  // bf16 x bf16 -> f32
+      // exact form bf16 x bf16 -> f32; folded form fp16 x fp16 -> f32
+      constexpr uint32_t idesc = idesc_kind_f16(kTileM, BN, kFold ? 0u : 1u);
       // descriptors as 32-bit halves: the start address (low half) advances in 16-byte
       // units by the stage offset and by 2 per 32-byte K step
       const uint64_t bd = sw128_desc(sbase + L::x_off), ad = sw128_desc(sbase + L::a_off);
@@ -263,14 +269,18 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
           const int s = i % SX, sa = i % SA, b = i % NB;
           const uint32_t b_lo = b_lo0 + ((uint32_t)(s * L::kB) >> 4);
           const uint32_t d = tmem_base + (uint32_t)(b * BN);
+          // exact form: each group starts its own buffer; folded form: one sum over the share
+          const bool first = kFold ? i == 0 : true;
           if constexpr (L::kATmem) {
             const uint32_t a = tmem_base + L::a_col + (uint32_t)(sa * 32);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) mma_f16_ts32(d, a + 8 * kk, b_lo + 2 * kk, b_hi, idesc, kk != 0);
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16_ts32(d, a + 8 * kk, b_lo + 2 * kk, b_hi, idesc, !(first && kk == 0));
           } else {
             const uint32_t a_lo = a_lo0 + ((uint32_t)(sa * kABytes) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) mma_f16_ss(d, a_lo + 2 * kk, a_hi, b_lo + 2 * kk, b_hi, idesc, kk != 0);
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16_ss(d, a_lo + 2 * kk, a_hi, b_lo + 2 * kk, b_hi, idesc, !(first && kk == 0));
           }
           mma_commit(mma_done(i));
         }
@@ -303,9 +313,24 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
     const int q = warp & 3;
     const int r = q * 32 + lane;  // tile row = tensor-memory lane
     const uint32_t a_lane = tmem_base + ((uint32_t)(q * 32) << 16) + L::a_col;
+    // folded form: this row's scales, and the power of two they are taken at (rows past N:
+    // scale 0, and their codes read as zeros)
+    const int64_t drow = m0 + r;
+    const bool drow_ok = drow < p.N;
+    const uint16_t* dsrow = p.scales + (drow_ok ? drow : 0) * (p.Kp >> 6) + g_begin;
+    float smul = 0.f;
+    if constexpr (kFold) smul = drow_ok ? exp2i(-__ldg(p.rf + drow)) : 0.f;
     bool ok = true;
     for (int ws = 0; ws < nws; ++ws) {
       const int slot = ws % SW;
+      uint32_t sbits[2] = {0u, 0u};
+      if constexpr (kFold) {  // issued before the wait, used after it
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int i = ws * kGroupsPerW + team + 2 * h;
+          if (drow_ok && i < ng) sbits[h] = __ldg(dsrow + i);
+        }
+      }
       ok = ok && warp_wait(c_full(slot), (ws / SW) & 1, abort_flag, &g_tc_status);
       const uint32_t csrc = sbase + L::c_off + slot * kWBytes + r * 128;
       uint4 cw[4];
@@ -330,11 +355,17 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
           tc_fence_after();
           const uint32_t words[8] = {cw[2 * h].x,     cw[2 * h].y,     cw[2 * h].z,     cw[2 * h].w,
                                      cw[2 * h + 1].x, cw[2 * h + 1].y, cw[2 * h + 1].z, cw[2 * h + 1].w};
+          uint32_t s2 = 0u;  // folded form: fp16(s * 2^-rf) twice
+          if constexpr (kFold) {
+            const uint32_t hb =
+                __half_as_ushort(__float2half_rn(fp16_bits_to_float((uint16_t)sbits[h]) * smul));
+            s2 = hb | (hb << 16);
+          }
           if constexpr (L::kATmem) {
             uint32_t v[32];  // column j = code byte j = (k = 2j, k = 2j + 1)
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              const uint4 d4 = decode_word_bf16(words[j]);
+              const uint4 d4 = kFold ? decode_word_f16s(words[j], s2) : decode_word_bf16(words[j]);
               v[4 * j + 0] = d4.x;
               v[4 * j + 1] = d4.y;
               v[4 * j + 2] = d4.z;
@@ -346,7 +377,8 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
             // row r of the 128-byte-swizzled K-major A stage: 16-byte chunk j holds k = 8j .. 8j + 7
             const uint32_t adst = sbase + L::a_off + sa * kABytes + r * 128;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) st_shared_v4(adst + ((j ^ (r & 7)) << 4), decode_word_bf16(words[j]));
+            for (int j = 0; j < 8; ++j)
+              st_shared_v4(adst + ((j ^ (r & 7)) << 4), kFold ? decode_word_f16s(words[j], s2) : decode_word_bf16(words[j]));
             fence_proxy_async();  // generic-proxy stores -> the tensor core's (async-proxy) reads
           }
         }
@@ -377,75 +409,103 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
     bool acc_ok = true;
     const int64_t row = m0 + r_acc;
     const bool row_ok = row < p.N;
-    // Scales are read as pairs of groups (a row holds K_pad / 64 scales, an even
-    // 4-byte boundary); the next pair is fetched as soon as the current one is used.
-    const uint32_t* srow = reinterpret_cast<const uint32_t*>(p.scales + (row_ok ? row : 0) * (p.Kp >> 6));
-    int pcur = g_begin >> 1;
-    uint32_t s_cur = row_ok ? __ldg(srow + pcur) : 0u;
-    uint32_t s_nxt = (row_ok && 2 * (pcur + 1) < p.nk) ? __ldg(srow + pcur + 1) : 0u;
     const uint32_t tlane = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(cq * kCols);
-    // the first NB groups find their accumulator buffers free
-    for (int i = 0; i < NB && i < ng; ++i) named_bar_arrive(issue_bar(i), L::issue_threads);
-    for (int i = 0; i < ng; ++i) {
-      const int b = i % NB, ga = g_begin + i;
-      if ((ga >> 1) != pcur) {
-        ++pcur;
-        s_cur = s_nxt;
-        s_nxt = (row_ok && 2 * (pcur + 1) < p.nk) ? __ldg(srow + pcur + 1) : 0u;
-      }
-      const float sf = fp16_bits_to_float((uint16_t)((ga & 1) ? (s_cur >> 16) : (s_cur & 0xFFFFu)));
-      const float2 s2 = make_float2(sf, sf);
-      acc_ok = acc_ok && warp_wait(mma_done(i), ring_par(i), abort_flag, &g_tc_status);
-      bool released = false;
-      if (acc_ok) {
+    if constexpr (kFold) {
+      // The sum over the whole K share is complete once the issuer's final commit has
+      // landed: one warp polls for it, the others sleep on a named barrier.  Then one
+      // readback, undoing the powers of two the operands were taken at.
+      if (warp == 12) acc_ok = warp_wait(fin_bar, 0, abort_flag, &g_tc_status);
+      named_bar_sync(kAccBar, 128 * NACC);
+      acc_ok = acc_ok && !*abort_flag;
+      const int rfr = row_ok ? __ldg(p.rf + row) : 0;
+      if (acc_ok && ng > 0) {
         tc_fence_after();
-        const uint32_t dcol = tlane + (uint32_t)(b * BN);
 #pragma unroll
         for (int c = 0; c < kCols; c += 16) {
-          constexpr int kRest = kCols % 16;
-          if (c + 16 <= kCols) {
-            uint32_t v[16];
-            tmem_ld_cols<16>(dcol + c, v);
-            tmem_ld_wait();
-            if (kEarlyRelease && c + 16 == kCols) {
-              // the whole partial is in registers: hand buffer b back to the MMA
-              // before the last chunk's FMAs
-              tc_fence_before();
-              __syncwarp();
-              if (i + NB < ng) named_bar_arrive(issue_bar(i + NB), L::issue_threads);
-              released = true;
-            }
+          uint32_t v[16];
+          tmem_ld_cols<16>(tlane + c, v);
+          tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 16; j += 2)
-              acc[(c + j) / 2] = ffma2(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), s2, acc[(c + j) / 2]);
-          } else {
-            // remainder of 4, 8 or 12 columns
-            if constexpr (kRest >= 8) {
-              uint32_t v[8];
-              tmem_ld_cols<8>(dcol + c, v);
-              tmem_ld_wait();
-#pragma unroll
-              for (int j = 0; j < 8; j += 2)
-                acc[(c + j) / 2] = ffma2(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), s2, acc[(c + j) / 2]);
-            }
-            if constexpr (kRest % 8 == 4) {
-              constexpr int c4 = (kRest >= 8) ? 8 : 0;
-              uint32_t v[4];
-              tmem_ld_cols<4>(dcol + c + c4, v);
-              tmem_ld_wait();
-#pragma unroll
-              for (int j = 0; j < 4; j += 2)
-                acc[(c + c4 + j) / 2] =
-                    ffma2(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), s2, acc[(c + c4 + j) / 2]);
-            }
+          for (int j = 0; j < 16; j += 2) {
+            const int64_t t = t0 + cq * kCols + c + j;
+            const int e0 = t < p.T ? __ldg(p.xe + t) : 0;
+            const int e1 = t + 1 < p.T ? __ldg(p.xe + t + 1) : 0;
+            acc[(c + j) / 2] = make_float2(__uint_as_float(v[j]) * exp2i(rfr + e0),
+                                           __uint_as_float(v[j + 1]) * exp2i(rfr + e1));
           }
         }
       }
-      if (!released) {
-        tc_fence_before();
-        __syncwarp();
-        if (i + NB < ng) named_bar_arrive(issue_bar(i + NB), L::issue_threads);  // buffer b is free for group i + NB
+    } else {
+      // Scales are read as pairs of groups (a row holds K_pad / 64 scales, an even
+      // 4-byte boundary); the next pair is fetched as soon as the current one is used.
+      const uint32_t* srow = reinterpret_cast<const uint32_t*>(p.scales + (row_ok ? row : 0) * (p.Kp >> 6));
+      int pcur = g_begin >> 1;
+      uint32_t s_cur = row_ok ? __ldg(srow + pcur) : 0u;
+      uint32_t s_nxt = (row_ok && 2 * (pcur + 1) < p.nk) ? __ldg(srow + pcur + 1) : 0u;
+      // the first NB groups find their accumulator buffers free
+      for (int i = 0; i < NB && i < ng; ++i) named_bar_arrive(issue_bar(i), L::issue_threads);
+      for (int i = 0; i < ng; ++i) {
+        const int b = i % NB, ga = g_begin + i;
+        if ((ga >> 1) != pcur) {
+          ++pcur;
+          s_cur = s_nxt;
+          s_nxt = (row_ok && 2 * (pcur + 1) < p.nk) ? __ldg(srow + pcur + 1) : 0u;
+        }
+        const float sf = fp16_bits_to_float((uint16_t)((ga & 1) ? (s_cur >> 16) : (s_cur & 0xFFFFu)));
+        const float2 s2 = make_float2(sf, sf);
+        acc_ok = acc_ok && warp_wait(mma_done(i), ring_par(i), abort_flag, &g_tc_status);
+        bool released = false;
+        if (acc_ok) {
+          tc_fence_after();
+          const uint32_t dcol = tlane + (uint32_t)(b * BN);
+  #pragma unroll
+          for (int c = 0; c < kCols; c += 16) {
+            constexpr int kRest = kCols % 16;
+            if (c + 16 <= kCols) {
+              uint32_t v[16];
+              tmem_ld_cols<16>(dcol + c, v);
+              tmem_ld_wait();
+              if (kEarlyRelease && c + 16 == kCols) {
+                // the whole partial is in registers: hand buffer b back to the MMA
+                // before the last chunk's FMAs
+                tc_fence_before();
+                __syncwarp();
+                if (i + NB < ng) named_bar_arrive(issue_bar(i + NB), L::issue_threads);
+                released = true;
+              }
+  #pragma unroll
+              for (int j = 0; j < 16; j += 2)
+                acc[(c + j) / 2] = ffma2(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), s2, acc[(c + j) / 2]);
+            } else {
+              // remainder of 4, 8 or 12 columns
+              if constexpr (kRest >= 8) {
+                uint32_t v[8];
+                tmem_ld_cols<8>(dcol + c, v);
+                tmem_ld_wait();
+  #pragma unroll
+                for (int j = 0; j < 8; j += 2)
+                  acc[(c + j) / 2] = ffma2(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), s2, acc[(c + j) / 2]);
+              }
+              if constexpr (kRest % 8 == 4) {
+                constexpr int c4 = (kRest >= 8) ? 8 : 0;
+                uint32_t v[4];
+                tmem_ld_cols<4>(dcol + c + c4, v);
+                tmem_ld_wait();
+  #pragma unroll
+                for (int j = 0; j < 4; j += 2)
+                  acc[(c + c4 + j) / 2] =
+                      ffma2(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), s2, acc[(c + c4 + j) / 2]);
+              }
+            }
+          }
+        }
+        if (!released) {
+          tc_fence_before();
+          __syncwarp();
+          if (i + NB < ng) named_bar_arrive(issue_bar(i + NB), L::issue_threads);  // buffer b is free for group i + NB
+        }
       }
+
     }
 
     // ----------------------------------------------------------- split-K reduction across the cluster
@@ -490,6 +550,77 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
   }
 }
 
+// ----------------------------------------------------------------- folded-form operands
+// One pass before the tile kernel, in two kinds of CTA:
+//   * CTA t < T: token t.  Its largest |x| (compared as bf16 magnitude bits) fixes a
+//     power of two 2^xe[t] that puts that maximum in [2^14, 2^15); x * 2^-xe[t] is then
+//     exact in fp16 for every element down to 2^-38 of the maximum (smaller ones round
+//     as fp16 subnormals), and is stored as the fp16 token row xh[t, :].
+//   * the other CTAs: 8 weight rows each, one warp per row.  The row's largest scale
+//     magnitude (groups holding columns < K) fixes 2^rf[n] that puts it in
+//     [2^11, 2^12), so every decoded weight (q - 8) * s * 2^-rf stays below 2^15 in
+//     magnitude (no fp16 overflow) and small scales keep their precision.
+// Rows and tokens holding Inf or NaN keep a shift of 0 so those values propagate.
+constexpr int kPrepRowsPerCta = 8;
+
+__global__ void __launch_bounds__(256) q4_tc_prep_kernel(const uint16_t* __restrict__ x,
+                                                         const uint16_t* __restrict__ scales, uint16_t* __restrict__ xh,
+                                                         int* __restrict__ xe, int* __restrict__ rf, int64_t T, int64_t K,
+                                                         int64_t N, int64_t sc_pitch, int nk) {
+  pdl_launch_dependents();
+  pdl_wait_previous();  // x and the scales may come from the previous kernel; xh may still be read by it
+  __shared__ uint32_t red[8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if ((int64_t)blockIdx.x < T) {
+    const int64_t t = blockIdx.x;
+    const uint4* src = reinterpret_cast<const uint4*>(x + t * K);
+    uint4* dst = reinterpret_cast<uint4*>(xh + t * K);
+    const int64_t nc = K / 8;  // K is a multiple of 8
+    uint32_t m2 = 0;           // two 16-bit maxima of |x| bits
+    for (int64_t c = threadIdx.x; c < nc; c += 256) {
+      const uint4 v = __ldg(src + c);
+      m2 = __vmaxu2(m2, v.x & 0x7FFF7FFFu);
+      m2 = __vmaxu2(m2, v.y & 0x7FFF7FFFu);
+      m2 = __vmaxu2(m2, v.z & 0x7FFF7FFFu);
+      m2 = __vmaxu2(m2, v.w & 0x7FFF7FFFu);
+    }
+    uint32_t m = __reduce_max_sync(0xffffffffu, max(m2 & 0xFFFFu, m2 >> 16));
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < 8; ++w) m = max(m, red[w]);
+    const int E = (int)(m >> 7);  // bf16 biased exponent of the largest |x|
+    const int e = (m == 0 || E == 255) ? 0 : min(max(E - 141, -100), 100);
+    const float sc = exp2i(-e);
+    for (int64_t c = threadIdx.x; c < nc; c += 256) {
+      const uint4 v = __ldg(src + c);
+      const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+      uint32_t out[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(out[j]) : "f"(bf16hi(in[j]) * sc), "f"(bf16lo(in[j]) * sc));
+      dst[c] = make_uint4(out[0], out[1], out[2], out[3]);
+    }
+    if (threadIdx.x == 0) xe[t] = e;
+  } else {
+    const int64_t n = ((int64_t)blockIdx.x - T) * kPrepRowsPerCta + warp;
+    if (n < N) {
+      const uint16_t* srow = scales + n * sc_pitch;
+      uint32_t m = 0;
+      for (int g = lane; g < nk; g += 32) m = max(m, (uint32_t)(__ldg(srow + g) & 0x7FFFu));
+      m = __reduce_max_sync(0xffffffffu, m);
+      const int E = (int)(m >> 10);  // fp16 biased exponent of the largest |s|
+      if (lane == 0) rf[n] = (m == 0 || E == 31) ? 0 : E - 26;
+    }
+  }
+}
+
+// Folded-form workspace: xh [T, K] fp16, xe [T] int, rf [N] int, each 256-byte aligned.
+size_t r256(size_t b) { return (b + 255) / 256 * 256; }
+size_t fold_ws_xe(int64_t, int64_t K, int64_t T) { return r256((size_t)T * (size_t)K * 2); }
+size_t fold_ws_rf(int64_t N, int64_t K, int64_t T) { return fold_ws_xe(N, K, T) + r256((size_t)T * 4); }
+size_t fold_ws_bytes(int64_t N, int64_t K, int64_t T) { return fold_ws_rf(N, K, T) + r256((size_t)N * 4); }
+
 // ----------------------------------------------------------------- host side
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -522,17 +653,17 @@ bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint6
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN>
+template <int BN, bool kFold>
 int set_kernel_attrs() {
-  using L = TcSmem<BN>;
+  using L = TcSmem<BN, kFold>;
   static bool attr_set[64] = {};
   int dev = 0;
   if (cuda_check(cudaGetDevice(&dev), "cudaGetDevice")) return Q4LIN_ERR_CUDA;
   if (dev < 64 && attr_set[dev]) return Q4LIN_OK;
-  if (cuda_check(cudaFuncSetAttribute(q4_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc),
+  if (cuda_check(cudaFuncSetAttribute(q4_tc_kernel<BN, kFold>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc),
                  "tc: cudaFuncSetAttribute(max dynamic shared memory)"))
     return Q4LIN_ERR_CUDA;
-  if (cuda_check(cudaFuncSetAttribute(q4_tc_kernel<BN>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+  if (cuda_check(cudaFuncSetAttribute(q4_tc_kernel<BN, kFold>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
                  "tc: cudaFuncSetAttribute(cluster size)"))
     return Q4LIN_ERR_CUDA;
   if (dev < 64) attr_set[dev] = true;
@@ -542,14 +673,14 @@ int set_kernel_attrs() {
 // How many clusters of `size` CTAs of this kernel can be resident at once (0 on
 // error).  Clusters are placed within one GPC, so this is below sms / size when
 // the GPCs' SM counts are not multiples of the cluster size.
-template <int BN>
+template <int BN, bool kFold>
 int resident_clusters(int size) {
-  using L = TcSmem<BN>;
+  using L = TcSmem<BN, kFold>;
   static int cache[64][9] = {};
   int dev = 0;
   if (size < 1 || size > 8 || cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (dev < 64 && cache[dev][size]) return cache[dev][size];
-  if (set_kernel_attrs<BN>() != Q4LIN_OK) return 0;
+  if (set_kernel_attrs<BN, kFold>() != Q4LIN_OK) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1, 1, (unsigned)size);
   cfg.blockDim = dim3(L::threads, 1, 1);
@@ -562,7 +693,7 @@ int resident_clusters(int size) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, q4_tc_kernel<BN>, &cfg) != cudaSuccess || n < 0) {
+  if (cudaOccupancyMaxActiveClusters(&n, q4_tc_kernel<BN, kFold>, &cfg) != cudaSuccess || n < 0) {
     cudaGetLastError();
     n = 0;
   }
@@ -570,27 +701,32 @@ int resident_clusters(int size) {
   return n;
 }
 
-template <int BN>
+template <int BN, bool kFold>
 int launch_tile(const LinearArgs& a, int splitk, int64_t tile_base, int64_t n_tiles) {
-  using L = TcSmem<BN>;
+  using L = TcSmem<BN, kFold>;
   static_assert(L::alloc <= 232448, "shared memory budget");
   if (splitk < 1 || splitk > 8 || splitk > L::max_splitk) {
     set_error_detail("tc: split-K factor out of range for this tile");
     return Q4LIN_ERR_INVALID_ARG;
   }
-  if (const int rc = set_kernel_attrs<BN>()) return rc;
+  if (const int rc = set_kernel_attrs<BN, kFold>()) return rc;
   CUtensorMap tm_codes, tm_x;
   // code plane rows hold K_pad / 2 bytes; X rows K values, whose positions k >= K read
-  // as zeros (out-of-range tile elements), so a partial last group sees x = 0 beyond K
+  // as zeros (out-of-range tile elements), so a partial last group sees x = 0 beyond K.
+  // The folded form reads the fp16 token rows the prep kernel left in the workspace.
   const int64_t Kp = k_pad(a.K);
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  const void* xsrc = kFold ? static_cast<const void*>(ws) : static_cast<const void*>(a.x);
   if (!make_map_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.wq, (uint64_t)(Kp / 2), (uint64_t)a.N,
                    (uint64_t)(Kp / 2), 128, kTileM) ||
-      !make_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, (uint64_t)a.K, (uint64_t)a.T, (uint64_t)a.K * 2,
-                   64, BN)) {
+      !make_map_2d(&tm_x, kFold ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xsrc,
+                   (uint64_t)a.K, (uint64_t)a.T, (uint64_t)a.K * 2, 64, BN)) {
     set_error_detail("tc: cuTensorMapEncodeTiled failed (or is unavailable)");
     return Q4LIN_ERR_CUDA;
   }
-  const TcParams p{a.scales, a.y, a.N, Kp, a.T, (int)((a.K + 63) / 64), splitk, (uint32_t)tile_base,
+  const int* xe = kFold ? reinterpret_cast<const int*>(ws + fold_ws_xe(a.N, a.K, a.T)) : nullptr;
+  const int* rf = kFold ? reinterpret_cast<const int*>(ws + fold_ws_rf(a.N, a.K, a.T)) : nullptr;
+  const TcParams p{a.scales, a.y, xe, rf, a.N, Kp, a.T, (int)((a.K + 63) / 64), splitk, (uint32_t)tile_base,
                    (uint32_t)((a.N + kTileM - 1) / kTileM)};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)n_tiles, 1, (unsigned)splitk);
@@ -613,26 +749,46 @@ int launch_tile(const LinearArgs& a, int splitk, int64_t tile_base, int64_t n_ti
   ++na;
   cfg.attrs = attr;
   cfg.numAttrs = (unsigned)na;
-  return cuda_check(cudaLaunchKernelEx(&cfg, q4_tc_kernel<BN>, tm_codes, tm_x, p), "tc: kernel launch");
+  return cuda_check(cudaLaunchKernelEx(&cfg, q4_tc_kernel<BN, kFold>, tm_codes, tm_x, p), "tc: kernel launch");
 }
 
-int max_splitk_for(int bn) {
+// The folded form's operand pass (programmatic dependent launch like the tile kernel).
+int launch_prep(const LinearArgs& a) {
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  const int64_t blocks = a.T + (a.N + kPrepRowsPerCta - 1) / kPrepRowsPerCta;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_check(cudaLaunchKernelEx(&cfg, q4_tc_prep_kernel, a.x, a.scales, reinterpret_cast<uint16_t*>(ws),
+                                       reinterpret_cast<int*>(ws + fold_ws_xe(a.N, a.K, a.T)),
+                                       reinterpret_cast<int*>(ws + fold_ws_rf(a.N, a.K, a.T)), a.T, a.K, a.N,
+                                       k_pad(a.K) / 64, (int)((a.K + 63) / 64)),
+                    "tc: prep kernel launch");
+}
+
+int max_splitk_for(int bn) {  // the same shared-memory layout in both forms
   switch (bn) {
-    case 256: return TcSmem<256>::max_splitk;
-    case 128: return TcSmem<128>::max_splitk;
-    case 64: return TcSmem<64>::max_splitk;
-    case 32: return TcSmem<32>::max_splitk;
-    default: return TcSmem<16>::max_splitk;
+    case 256: return TcSmem<256, true>::max_splitk;
+    case 128: return TcSmem<128, true>::max_splitk;
+    case 64: return TcSmem<64, true>::max_splitk;
+    case 32: return TcSmem<32, true>::max_splitk;
+    default: return TcSmem<16, true>::max_splitk;
   }
 }
 
-int resident_clusters_for(int bn, int size) {
+int resident_clusters_for(int bn, int size) {  // same block size and shared memory in both forms
   switch (bn) {
-    case 256: return resident_clusters<256>(size);
-    case 128: return resident_clusters<128>(size);
-    case 64: return resident_clusters<64>(size);
-    case 32: return resident_clusters<32>(size);
-    default: return resident_clusters<16>(size);
+    case 256: return resident_clusters<256, true>(size);
+    case 128: return resident_clusters<128, true>(size);
+    case 64: return resident_clusters<64, true>(size);
+    case 32: return resident_clusters<32, true>(size);
+    default: return resident_clusters<16, true>(size);
   }
 }
 
@@ -659,15 +815,22 @@ struct TileCost {
   double group_ns;
   double fixed_ns;
 };
-constexpr TileCost kTileCost[] = {
+// exact form (per-group accumulators read back and scaled in FP32)
+constexpr TileCost kTileCostExact[] = {
     {16, 310.0, 4300.0}, {32, 330.0, 4400.0}, {64, 335.0, 6500.0}, {128, 440.0, 5300.0}, {256, 615.0, 7800.0}};
+// folded form (one accumulator per K share)
+constexpr TileCost kTileCostFold[] = {
+    {16, 150.0, 4300.0}, {32, 160.0, 4400.0}, {64, 180.0, 5500.0}, {128, 220.0, 5300.0}, {256, 330.0, 7000.0}};
 constexpr double kSplitNsPerColumn = 22.0;
 
-const TileCost& tile_cost(int bn) {
-  for (const TileCost& c : kTileCost)
-    if (c.bn == bn) return c;
-  return kTileCost[0];
+const TileCost& tile_cost(int bn, bool fold) {
+  const TileCost* t = fold ? kTileCostFold : kTileCostExact;
+  for (int i = 0; i < 5; ++i)
+    if (t[i].bn == bn) return t[i];
+  return t[0];
 }
+
+bool route_folds(int route) { return route == Q4LIN_ROUTE_TC_FP16; }
 
 // The second launch of a tail plan: launch latency not hidden behind a previous kernel.
 constexpr double kTailLaunchNs = 1500.0;
@@ -700,9 +863,9 @@ TcPlan tc_plan(int route, int64_t N, int64_t K, int64_t T, int sms) {
   double best = -1.0;
   for (int c = 0; c < ncand; ++c) {
     const int bn = cand[c];
-    const TileCost& tc = tile_cost(bn);
+    const TileCost& tc = tile_cost(bn, route_folds(route));
     const int64_t tiles = tile_count(N, T, bn);
-    const int smax = route == Q4LIN_ROUTE_TC_SPLITK ? (max_splitk_for(bn) < 8 ? max_splitk_for(bn) : 8) : 1;
+    const int smax = route == Q4LIN_ROUTE_TC ? 1 : (max_splitk_for(bn) < 8 ? max_splitk_for(bn) : 8);
     auto wave_capacity = [&](int s) -> int64_t {
       int64_t per_wave = sms / s;
       if (s > 1) {
@@ -749,18 +912,21 @@ TcPlan tc_plan_current_device(int route, int64_t N, int64_t K, int64_t T) {
   return tc_plan(route, N, K, T, sm_count());
 }
 
-size_t tc_workspace_bytes(int64_t, int64_t, int64_t) { return 0; }
+size_t tc_workspace_bytes(int route, int64_t N, int64_t K, int64_t T) {
+  return route_folds(route) ? fold_ws_bytes(N, K, T) : 0;
+}
 
-int tc_launch_count(int64_t N, int64_t K, int64_t T) {
-  const TcPlan pl = tc_plan_current_device(Q4LIN_ROUTE_TC_SPLITK, N, K, T);
-  return pl.main_tiles < tile_count(N, T, pl.bn) ? 2 : 1;
+int tc_launch_count(int route, int64_t N, int64_t K, int64_t T) {
+  const TcPlan pl = tc_plan_current_device(route, N, K, T);
+  return (pl.main_tiles < tile_count(N, T, pl.bn) ? 2 : 1) + (route_folds(route) ? 1 : 0);
 }
 
 bool tc_supported(int64_t N, int64_t K, int64_t T) {
-  // TMA coordinates are 32-bit signed, and one launch's tiles (at most, with
-  // 16-token tiles) must fit the grid's x extent.
+  // TMA coordinates are 32-bit signed, one launch's tiles (at most, with 16-token
+  // tiles) must fit the grid's x extent, and so must the prep kernel's T + N / 8 CTAs.
   return N < ((int64_t)1 << 31) && K < ((int64_t)1 << 31) && T < ((int64_t)1 << 31) &&
-         tile_count(N, T, 16) < ((int64_t)1 << 31);
+         tile_count(N, T, 16) < ((int64_t)1 << 31) &&
+         T + (N + kPrepRowsPerCta - 1) / kPrepRowsPerCta < ((int64_t)1 << 31);
 }
 
 int tc_launch(const LinearArgs& a, int route) {
@@ -769,17 +935,28 @@ int tc_launch(const LinearArgs& a, int route) {
     return Q4LIN_ERR_INVALID_ARG;
   }
   const TcPlan pl = tc_plan_current_device(route, a.N, a.K, a.T);
+  const bool fold = route_folds(route);
   auto launch = [&](int splitk, int64_t base, int64_t n) {
+    if (fold) {
+      switch (pl.bn) {
+        case 256: return launch_tile<256, true>(a, splitk, base, n);
+        case 128: return launch_tile<128, true>(a, splitk, base, n);
+        case 64: return launch_tile<64, true>(a, splitk, base, n);
+        case 32: return launch_tile<32, true>(a, splitk, base, n);
+        default: return launch_tile<16, true>(a, splitk, base, n);
+      }
+    }
     switch (pl.bn) {
-      case 256: return launch_tile<256>(a, splitk, base, n);
-      case 128: return launch_tile<128>(a, splitk, base, n);
-      case 64: return launch_tile<64>(a, splitk, base, n);
-      case 32: return launch_tile<32>(a, splitk, base, n);
-      default: return launch_tile<16>(a, splitk, base, n);
+      case 256: return launch_tile<256, false>(a, splitk, base, n);
+      case 128: return launch_tile<128, false>(a, splitk, base, n);
+      case 64: return launch_tile<64, false>(a, splitk, base, n);
+      case 32: return launch_tile<32, false>(a, splitk, base, n);
+      default: return launch_tile<16, false>(a, splitk, base, n);
     }
   };
   const int64_t tiles = tile_count(a.N, a.T, pl.bn);
-  int rc = launch(pl.splitk, 0, pl.main_tiles);
+  int rc = fold ? launch_prep(a) : Q4LIN_OK;
+  if (rc == Q4LIN_OK) rc = launch(pl.splitk, 0, pl.main_tiles);
   if (rc == Q4LIN_OK && pl.main_tiles < tiles) rc = launch(pl.tail_splitk, pl.main_tiles, tiles - pl.main_tiles);
   return rc;
 }

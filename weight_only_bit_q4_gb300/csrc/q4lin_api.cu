@@ -91,7 +91,8 @@ size_t route_ws(int route, int64_t N, int64_t K, int64_t T) {
   switch (route) {
     case Q4LIN_ROUTE_GEMV: return round256(q4::gemv_workspace_bytes(N, K, T));
     case Q4LIN_ROUTE_TC:
-    case Q4LIN_ROUTE_TC_SPLITK: return round256(q4::tc_workspace_bytes(N, K, T));
+    case Q4LIN_ROUTE_TC_SPLITK:
+    case Q4LIN_ROUTE_TC_FP16: return round256(q4::tc_workspace_bytes(route, N, K, T));
     default: return 0;
   }
 }
@@ -102,7 +103,7 @@ int run_impl(int route, const uint8_t* wq, const uint16_t* scales, const uint16_
   if (st != Q4LIN_OK) return st;
   if (N == 0 || T == 0) return Q4LIN_OK;
   if (route == Q4LIN_ROUTE_AUTO) route = route_for(N, K, T);
-  if (route < Q4LIN_ROUTE_GEMV || route > Q4LIN_ROUTE_TC) return Q4LIN_ERR_INVALID_ARG;
+  if (route < Q4LIN_ROUTE_GEMV || route > Q4LIN_ROUTE_TC_FP16) return Q4LIN_ERR_INVALID_ARG;
   const size_t ws = route_ws(route, N, K, T);
   if (ws > 0 && workspace == nullptr) return Q4LIN_ERR_WORKSPACE;
   if (ws > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return Q4LIN_ERR_MISALIGNED;
@@ -114,7 +115,8 @@ int run_impl(int route, const uint8_t* wq, const uint16_t* scales, const uint16_
   switch (route) {
     case Q4LIN_ROUTE_GEMV: return q4::gemv_launch(a);
     case Q4LIN_ROUTE_TC:
-    case Q4LIN_ROUTE_TC_SPLITK: return q4::tc_launch(a, route);
+    case Q4LIN_ROUTE_TC_SPLITK:
+    case Q4LIN_ROUTE_TC_FP16: return q4::tc_launch(a, route);
     default: return Q4LIN_ERR_INVALID_ARG;
   }
 }
@@ -167,7 +169,7 @@ int q4lin_select_route(int64_t N, int64_t K, int64_t T) { return route_for(N, K,
 int q4lin_tile_plan(int route, int64_t N, int64_t K, int64_t T, int* tile_n, int* split_k, int64_t* main_tiles,
                     int* tail_split_k) {
   if (tile_n == nullptr || split_k == nullptr) return Q4LIN_ERR_INVALID_ARG;
-  if (route < Q4LIN_ROUTE_AUTO || route > Q4LIN_ROUTE_TC) return Q4LIN_ERR_INVALID_ARG;
+  if (route < Q4LIN_ROUTE_AUTO || route > Q4LIN_ROUTE_TC_FP16) return Q4LIN_ERR_INVALID_ARG;
   if (validate_sizes(N, K, T) != Q4LIN_OK) return Q4LIN_ERR_INVALID_ARG;
   if (route == Q4LIN_ROUTE_AUTO) route = route_for(N, K, T);
   q4::TcPlan pl{0, 1, 0, 0};
@@ -183,10 +185,12 @@ int q4lin_tile_plan(int route, int64_t N, int64_t K, int64_t T, int* tile_n, int
 int q4lin_kernel_launches(int64_t N, int64_t K, int64_t T) {
   if (validate_sizes(N, K, T) != Q4LIN_OK || N == 0 || T == 0) return 0;
   if (K == 0) return 1;  // the zero fill
-  switch (route_for(N, K, T)) {
+  const int route = route_for(N, K, T);
+  switch (route) {
     case Q4LIN_ROUTE_GEMV: return q4::gemv_launch_count(N, K, T);
     case Q4LIN_ROUTE_TC:
-    case Q4LIN_ROUTE_TC_SPLITK: return q4::tc_launch_count(N, K, T);
+    case Q4LIN_ROUTE_TC_SPLITK:
+    case Q4LIN_ROUTE_TC_FP16: return q4::tc_launch_count(route, N, K, T);
     default: return 0;
   }
 }

@@ -15,8 +15,9 @@ LIB_PATH = os.path.join(_PKG, "libq4lin.so")
 OK = 0
 STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED_SHAPE", 3: "MISALIGNED", 4: "WORKSPACE",
           5: "DEVICE", 6: "CUDA", 7: "TIMEOUT"}
-ROUTE_AUTO, ROUTE_GEMV, ROUTE_TC_SPLITK, ROUTE_TC = 0, 1, 2, 3
-ROUTE_NAMES = {ROUTE_AUTO: "auto", ROUTE_GEMV: "gemv", ROUTE_TC_SPLITK: "tc_splitk", ROUTE_TC: "tc"}
+ROUTE_AUTO, ROUTE_GEMV, ROUTE_TC_SPLITK, ROUTE_TC, ROUTE_TC_FP16 = 0, 1, 2, 3, 4
+ROUTE_NAMES = {ROUTE_AUTO: "auto", ROUTE_GEMV: "gemv", ROUTE_TC_SPLITK: "tc_splitk", ROUTE_TC: "tc",
+               ROUTE_TC_FP16: "tc_fp16"}
 
 QTYPES = {"q4g64": 0, "q5g64": 1, "q6g64": 2, "w8g32": 3}
 
@@ -122,7 +123,7 @@ def kernel_launches(N: int, K: int, T: int) -> int:
     return int(load().q4lin_kernel_launches(N, K, T))
 
 
-_IMPLEMENTED = (ROUTE_GEMV, ROUTE_TC_SPLITK, ROUTE_TC)
+_IMPLEMENTED = (ROUTE_GEMV, ROUTE_TC_SPLITK, ROUTE_TC, ROUTE_TC_FP16)
 
 
 def implemented_routes():
@@ -214,9 +215,11 @@ def linear_qtype(qtype: str, planes, scales, x, y=None, stream=None):
             raise ValueError(f"{name} must be a contiguous CUDA tensor")
     if y is None:
         y = torch.empty((T, N), dtype=torch.bfloat16, device=x.device)
+    need = workspace_bytes(N, K, T) if qtype == "q4g64" else 0   # Q4 is q4lin_linear
+    ws = torch.empty(need, dtype=torch.uint8, device=x.device) if need else None
     s = (stream or torch.cuda.current_stream(x.device)).cuda_stream
     st = int(load().q4lin_linear_qtype(qt, _ptr(codes), _ptr(high) if bits else None, _ptr(scales), _ptr(x),
-                                       _ptr(y), N, K, T, None, ctypes.c_void_p(s)))
+                                       _ptr(y), N, K, T, _ptr(ws), ctypes.c_void_p(s)))
     if st != OK:
         raise Q4LinError(st)
     return y
