@@ -25,9 +25,17 @@
 //
 // Every product (q - 8) * x is exact in FP32 and the group scale multiplies
 // an FP32 partial sum, so the only rounding is FP32 accumulation and the final
-// bf16 store.  (Folding the scale into a 16-bit weight instead rounds
-// (q - 8) * s to 11 bits -- about 2e-4 of rms(y) -- which brushes the layer's
-// 1e-3 rms accuracy floor on large outputs; bf16 folding misses it outright.)
+// bf16 store.
+//
+// The same kernel has a folded form (template flag kFold, the opt-in route
+// Q4LIN_ROUTE_TC_FP16): a prep kernel writes X as fp16 (per token at a power of
+// two, exact) and a power of two per weight row; the decode teams write
+// fp16((q - 8) * s * 2^-rf) as the A operand, the MMAs accumulate the whole K
+// share into one tensor-memory buffer, and the accumulate warps read it back once,
+// undoing the powers of two.  Rounding each weight to 11 bits costs about 2e-4 of
+// rms(y) per output, which brushes the layer's 1e-3 rms accuracy floor (measured:
+// one element in 3.5 million at 1.03x the bound), so the folded form is never the
+// library's choice; bf16 folding would miss the floor outright.
 //
 // Synchronisation, shaped by what the hardware charges for it:
 //   * while the tensor core streams its shared-memory operands an mbarrier
