@@ -147,6 +147,28 @@ int q4lin_linear_qtype(int qtype, const uint8_t* codes, const uint8_t* high, con
  */
 int q4lin_linear_route(int route, const uint8_t* wq, const uint16_t* scales, const uint16_t* x,
                        uint16_t* y, int64_t N, int64_t K, int64_t T, void* workspace, void* stream);
+
+/*
+ * The fp16 tile route (Q4LIN_ROUTE_TC_FP16, the same kernels and bound) for callers
+ * that cannot allocate device memory: no workspace argument, and the call allocates
+ * nothing.  The pages describe no such entry point; it exists for code that must
+ * not call cudaMalloc around the layer (work issued inside a capture that may not
+ * allocate, an allocator that owns the device, a host without an allocator).
+ *   Scratch: a fixed 16 MiB device array inside the library, which every process
+ *     that loads the library holds on each GPU it uses until it exits.  Shapes whose
+ *     2*T*K + 4*T + 4*N bytes (each part rounded up to 256) exceed it return
+ *     Q4LIN_ERR_UNSUPPORTED_SHAPE (N = 6144, K = 5120 fits up to T = 1635).
+ *   Set-up: the first call on a device looks up the array's device address (one
+ *     cudaGetSymbolAddress, no allocation); make that first call before any stream
+ *     capture on that device.
+ *   Sharing: every call uses the same array, so calls that overlap on the GPU (in
+ *     different streams, or from different host threads) race on it; order them.
+ *     Each call rewrites all the scratch it reads, so nothing needs clearing.
+ * Arguments, alignment, ownership of inputs and outputs and the other error codes
+ * are those of q4lin_linear.
+ */
+int q4lin_linear_fp16_static(const uint8_t* wq, const uint16_t* scales, const uint16_t* x, uint16_t* y,
+                             int64_t N, int64_t K, int64_t T, void* stream);
 size_t q4lin_route_workspace_bytes(int route, int64_t N, int64_t K, int64_t T);
 
 /* The route q4lin_linear picks for (N, K, T) on the current device (host-only logic). */

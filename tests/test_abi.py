@@ -122,6 +122,16 @@ def test_fp16_tile_route_workspace_checked_on_host(lib):
     assert _call(64, 256, 8, route=5) == 1
 
 
+def test_static_scratch_entry_host_checks(lib):
+    vp = ctypes.c_void_p
+    f = lib.q4lin_linear_fp16_static
+    assert f(vp(16), vp(16), vp(16), vp(16), 256, 5120, 2048, None) == 2   # beyond its 16 MiB array
+    assert "16 MiB" in q4lin.last_error_detail()
+    assert f(vp(16), vp(16), vp(16), vp(16), 256, 100, 8, None) == 2       # K % 8 != 0
+    assert f(None, None, None, None, 0, 5120, 8, None) == 0                # empty
+    assert f(vp(16), vp(16), vp(16), vp(8), 64, 256, 8, None) == 3         # misaligned y
+
+
 def test_fp16_tile_route_workspace(lib):
     # the opt-in fp16 route: fp16 X [T, K], then a per-token and a per-row int, each
     # part rounded up to 256 bytes; the default routes take none

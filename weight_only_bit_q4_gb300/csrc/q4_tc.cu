@@ -969,6 +969,56 @@ int tc_launch(const LinearArgs& a, int route) {
   return rc;
 }
 
+// ----------------------------------------------------------------- allocation-free fp16 route
+// Some callers cannot allocate device memory per call: code that runs where
+// cudaMalloc is off limits (inside a stream capture that must not allocate, or
+// under an allocator that owns the whole device and hands out no scratch), or a
+// host that links this library without any allocator at all.  For them the fp16
+// tile route keeps its operand scratch in this fixed array instead of a caller
+// workspace.  Every process that loads the library holds the array on every GPU it
+// uses until it exits; all calls share it, and each call's prep kernel rewrites
+// every byte the tile kernel reads, so nothing needs clearing between calls.
+constexpr size_t kStaticScratchBytes = (size_t)16 << 20;
+static __device__ __align__(256) uint8_t g_fp16_scratch[kStaticScratchBytes];
+
+size_t tc_fp16_static_capacity() { return kStaticScratchBytes; }
+
+bool tc_fp16_static_fits(int64_t N, int64_t K, int64_t T) {
+  return tc_supported(N, K, T) && fold_ws_bytes(N, K, T) <= kStaticScratchBytes;
+}
+
+int tc_fp16_static_launch(const LinearArgs& args) {
+  if (!tc_fp16_static_fits(args.N, args.K, args.T)) {
+    set_error_detail("fp16 route without allocation: 2*T*K + 4*T + 4*N bytes (each rounded up to 256) "
+                     "exceed its 16 MiB static scratch");
+    return Q4LIN_ERR_UNSUPPORTED_SHAPE;
+  }
+  // The array's device address, looked up once per device with that device
+  // current (in host code its name is only a stand-in, not a device address).
+  static void* addr[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (const int rc = cuda_check(cudaGetDevice(&dev), "cudaGetDevice")) return rc;
+  if (dev < 0 || dev >= 64) {
+    set_error_detail("fp16 route without allocation: device ordinal beyond 63");
+    return Q4LIN_ERR_DEVICE;
+  }
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+      void* p = nullptr;
+      if (const int rc = cuda_check(cudaGetSymbolAddress(&p, g_fp16_scratch), "cudaGetSymbolAddress(scratch)"))
+        return rc;
+      addr[dev] = p;
+    }
+    scratch = addr[dev];
+  }
+  LinearArgs a = args;
+  a.workspace = scratch;
+  return tc_launch(a, Q4LIN_ROUTE_TC_FP16);
+}
+
 int tc_status(int* value, bool clear) {
   if (cudaMemcpyFromSymbol(value, g_tc_status, sizeof(int)) != cudaSuccess) return Q4LIN_ERR_CUDA;
   if (clear) {

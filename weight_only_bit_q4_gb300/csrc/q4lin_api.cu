@@ -200,6 +200,29 @@ int q4lin_linear(const uint8_t* wq, const uint16_t* scales, const uint16_t* x, u
   return run(Q4LIN_ROUTE_AUTO, wq, scales, x, y, N, K, T, workspace, stream);
 }
 
+int q4lin_linear_fp16_static(const uint8_t* wq, const uint16_t* scales, const uint16_t* x, uint16_t* y,
+                             int64_t N, int64_t K, int64_t T, void* stream) {
+  q4::set_error_detail("");
+  int st = validate(wq, scales, x, y, N, K, T);
+  if (st == Q4LIN_OK && N > 0 && T > 0 && K > 0 && !q4::tc_fp16_static_fits(N, K, T)) {
+    q4::set_error_detail("fp16 route without allocation: 2*T*K + 4*T + 4*N bytes (each rounded up to 256) "
+                         "exceed its 16 MiB static scratch");
+    return Q4LIN_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (st == Q4LIN_OK && N > 0 && T > 0) st = check_device();
+  if (st == Q4LIN_OK && N > 0 && T > 0) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) {
+      st = q4::cuda_check(cudaMemsetAsync(y, 0, (size_t)N * (size_t)T * 2, s), "zero fill of y");
+    } else {
+      const q4::LinearArgs a{wq, scales, x, y, N, K, T, nullptr, s};
+      st = q4::tc_fp16_static_launch(a);
+    }
+  }
+  if (st != Q4LIN_OK && q4::g_detail[0] == 0) q4::set_error_detail(q4lin_status_string(st));
+  return st;
+}
+
 int q4lin_linear_qtype(int qtype, const uint8_t* codes, const uint8_t* high, const uint16_t* scales,
                        const uint16_t* x, uint16_t* y, int64_t N, int64_t K, int64_t T, void* workspace,
                        void* stream) {

@@ -22,6 +22,7 @@ ROUTE_NAMES = {ROUTE_AUTO: "auto", ROUTE_GEMV: "gemv", ROUTE_TC_SPLITK: "tc_spli
 QTYPES = {"q4g64": 0, "q5g64": 1, "q6g64": 2, "w8g32": 3}
 
 EXPORTS = ("q4lin_workspace_bytes", "q4lin_linear", "q4lin_linear_route", "q4lin_linear_qtype",
+           "q4lin_linear_fp16_static",
            "q4lin_route_workspace_bytes", "q4lin_select_route", "q4lin_tile_plan", "q4lin_kernel_launches",
            "q4lin_status_string",
            "q4lin_device_status", "q4lin_clear_device_status", "q4lin_last_error_detail",
@@ -61,6 +62,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q4lin_linear_route.argtypes = [ctypes.c_int, vp, vp, vp, vp, i64, i64, i64, vp, vp]
     lib.q4lin_linear_qtype.argtypes = [ctypes.c_int, vp, vp, vp, vp, vp, i64, i64, i64, vp, vp]
     lib.q4lin_linear_qtype.restype = ctypes.c_int
+    lib.q4lin_linear_fp16_static.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
+    lib.q4lin_linear_fp16_static.restype = ctypes.c_int
     lib.q4lin_linear_route.restype = ctypes.c_int
     lib.q4lin_select_route.argtypes = [i64, i64, i64]
     lib.q4lin_select_route.restype = ctypes.c_int
