@@ -15,8 +15,8 @@ reported too.  Metrics follow the contract's sections 4-5 (weight_only_bit_q4_gb
 
 A step is one call of the layer on one batch of the workload's synthetic
 input.  Default workload: the decode GEMV, N=6144 K=5120 T=1.  --qtype times
-a sibling weight format (Q5G64, Q6G64, W8G32; 1..4 tokens) on the same
-geometry through q4lin_linear_qtype; its bytes are that format's.
+a sibling weight format (Q5G64, Q6G64, W8G32) on the same geometry through
+q4lin_linear_qtype (W8G32 for 1..4 tokens); its bytes are that format's.
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
 (the layer does not exchange data between GPUs); value = the units all ranks
 processed / the slowest rank's time.
@@ -97,7 +97,7 @@ def workload(args):
     name = args.workload if WORKLOADS[args.workload][2] is not None else f"{args.workload}_t{T}"
     qtype = getattr(args, "qtype", "q4g64")
     if qtype != "q4g64":
-        if T > 4:
+        if T > 4 and qtype == "w8g32":
             raise SystemExit(f"{qtype} runs for 1..4 tokens")
         name = qtype + name[2:]            # q4_6144x5120_t1 -> q5g64_6144x5120_t1
     route = getattr(args, "route", "auto")
@@ -294,8 +294,11 @@ def measure_ours(args, wl, rank, world, local):
         launches = 1 + (2 if pl["main_tiles"] < -(-N // 128) * -(-T // pl["n"]) else 1)
     stream = torch.cuda.Stream(dev)
 
-    if qtype != "q4g64":
-        route, launches = q4lin.ROUTE_GEMV, 1            # the sibling formats run on the streaming GEMV alone
+    if qtype != "q4g64":   # the streaming GEMV (1..4 tokens), else Q5 / Q6 on the exact tile route
+        if q4lin.select_route(N, K, T) == q4lin.ROUTE_GEMV and T <= 4:
+            route, launches = q4lin.ROUTE_GEMV, 1
+        else:
+            route, launches = q4lin.ROUTE_TC_SPLITK, q4lin.kernel_launches(N, K, T)
 
     def call(i):
         if qtype == "q4g64":

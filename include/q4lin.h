@@ -130,8 +130,10 @@ typedef enum {
  * Y = W . X for any of the formats above (arguments as q4lin_linear; `high`
  * is the Q5 / Q6 high-bit plane, 16-byte aligned, and is ignored otherwise).
  * Q4G64 is exactly q4lin_linear (workspace as q4lin_workspace_bytes).  The
- * other formats run on the decode GEMV, for 1..4 tokens where its shared-memory
- * plan fits; other shapes return Q4LIN_ERR_UNSUPPORTED_SHAPE.  They take no
+ * other formats run on the decode GEMV for 1..4 tokens where its shared-memory
+ * plan fits.  Other shapes of Q5G64 and Q6G64 run on the exact tile route
+ * (token tiles up to 128 wide; the high-bit plane is staged beside the codes), and
+ * other shapes of W8G32 return Q4LIN_ERR_UNSUPPORTED_SHAPE.  They take no
  * workspace (the pointer may be NULL).
  */
 int q4lin_linear_qtype(int qtype, const uint8_t* codes, const uint8_t* high, const uint16_t* scales,

@@ -1,7 +1,9 @@
 """GPU parity for the sibling weight formats Q5G64, Q6G64 and W8G32 (linear-benchmark.md
-section 4, format table) on the decode GEMV: 1..4 tokens, K a multiple of 128 or padded,
-ragged N, against the FP64 oracle for those formats.  Q4 through the same entry point is
-q4lin_linear itself; shapes outside the GEMV's reach are refused, not approximated."""
+section 4, format table) against the FP64 oracle for those formats: the decode GEMV for
+1..4 tokens (K a multiple of 128 or padded, ragged N), and for Q5G64 / Q6G64 the exact
+tile route beyond that (token tiles up to 128 wide, K split across clusters where the
+planner chooses it).  Q4 through the same entry point is q4lin_linear itself; W8G32
+shapes outside the GEMV's reach are refused, not approximated."""
 import numpy as np
 import pytest
 
@@ -68,9 +70,24 @@ def test_q4_through_the_format_entry_is_q4lin_linear():
     assert np.array_equal(y_fmt, y_bits(y))
 
 
-@pytest.mark.parametrize("qtype", FMTS)
-def test_more_than_four_tokens_refused(qtype):
-    planes, s, x = synth.make_problem_fmt(qtype, 64, 256, 5)
+def test_w8_more_than_four_tokens_refused():
+    planes, s, x = synth.make_problem_fmt("w8g32", 64, 256, 5)
     with pytest.raises(q4lin.Q4LinError) as e:
-        _run(qtype, planes, s, x)
+        _run("w8g32", planes, s, x)
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("qtype", ["q5g64", "q6g64"])
+@pytest.mark.parametrize("N,K,T", [(64, 256, 5), (300, 200, 37), (1001, 4096, 130), (640, 4304, 300),
+                                   (77, 17408, 8), (6144, 5120, 128), (257, 1152, 517), (5, 128, 1000)])
+def test_q5_q6_tile_route_matches_oracle(qtype, N, K, T):
+    planes, s, x = synth.make_problem_fmt(qtype, N, K, T, w_seed=N + 3, x_seed=K + T)
+    assert_close(_run(qtype, planes, s, x), sf.linear(qtype, planes, s, x), f"{qtype} {N}x{K} T={T}")
+
+
+@pytest.mark.parametrize("qtype", ["q5g64", "q6g64"])
+def test_q5_q6_gemv_without_plan_goes_to_tiles(qtype):
+    # four tokens whose x does not fit the streaming GEMV's shared memory: the tile route
+    N, K, T = 128, 17408, 4
+    planes, s, x = synth.make_problem_fmt(qtype, N, K, T, w_seed=9, x_seed=10)
+    assert_close(_run(qtype, planes, s, x), sf.linear(qtype, planes, s, x), f"{qtype} {N}x{K} T={T}")

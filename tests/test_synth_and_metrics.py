@@ -97,6 +97,6 @@ def test_bench_format_workloads():
     wl = bench.workload(bench.parse_args(["--qtype", "w8g32", "--workload", "q4_34816x5120", "--t", "4"]))
     assert wl["name"] == "w8g32_34816x5120_t4"
     with pytest.raises(SystemExit):
-        bench.workload(bench.parse_args(["--qtype", "q6g64", "--workload", "q4_6144x5120", "--t", "8"]))
+        bench.workload(bench.parse_args(["--qtype", "w8g32", "--workload", "q4_6144x5120", "--t", "8"]))
     planes, s, x = bench.format_problem(dict(wl, N=40, K=256, T=2), rows=7)
     assert planes[0].shape == (7, 256) and s.shape == (7, 8) and x.shape == (2, 256)

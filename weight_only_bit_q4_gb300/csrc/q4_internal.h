@@ -45,8 +45,9 @@ struct TcPlan {
   int64_t main_tiles;  // output tiles of the main launch (all of them without a tail launch)
   int tail_splitk;     // cluster size along K of the tail launch over the other tiles (0 = none)
 };
-TcPlan tc_plan(int route, int64_t N, int64_t K, int64_t T, int sms);
-TcPlan tc_plan_current_device(int route, int64_t N, int64_t K, int64_t T);
+// fmt: 0 Q4G64, 1 Q5G64, 2 Q6G64 (the latter two on token tiles up to 128 wide)
+TcPlan tc_plan(int route, int64_t N, int64_t K, int64_t T, int sms, int fmt = 0);
+TcPlan tc_plan_current_device(int route, int64_t N, int64_t K, int64_t T, int fmt = 0);
 int tc_launch(const LinearArgs& a, int route);
 // The folded tile routes (Q4LIN_ROUTE_TC, Q4LIN_ROUTE_TC_SPLITK) need workspace for
 // their fp16 operands and launch a prep kernel first; the exact route needs none.

@@ -285,6 +285,42 @@ __device__ __forceinline__ uint4 decode_word_bf16(uint32_t w) {
   return make_uint4(h[0], h[1], h[2], h[3]);
 }
 
+// Q5G64 / Q6G64 form of decode_word_bf16: the 8 weights of one code word with their
+// high bits, as exact bf16 pairs q - zero (|q - zero| <= 32, exact in bf16).  `h`
+// holds the word's high bits in weight order: Q5 one bit per weight (bit b of the
+// low byte is weight b's bit 4), Q6 two (bits 2b..2b+1 are weight b's bits 4..5).
+// Each pair's high bits are moved to bit 4 (low half) and bit 20 (high half) of
+// the nibble pair, then 128 + q is taken as a bf16 and 128 + zero subtracted
+// (0x4310 = 144 for Q5, 0x4320 = 160 for Q6).
+template <int kHB>
+__device__ __forceinline__ uint4 decode_word_bf16_hi(uint32_t w, uint32_t h) {
+  const uint32_t w4 = w >> 4;
+  uint32_t r[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t t = __byte_perm(w, w4, (uint32_t)(j | ((4 + j) << 8)));
+    uint32_t m;
+    if constexpr (kHB == 1) {
+      const uint32_t b = h >> (2 * j);
+      m = ((b & 1u) << 4) | ((b & 2u) << 19);
+    } else {
+      const uint32_t b = h >> (4 * j);
+      m = ((b & 3u) << 4) | ((b & 0xCu) << 18);
+    }
+    const uint32_t v = (t & 0x000F000Fu) | m | 0x43004300u;
+    uint32_t d;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(v), "r"(kHB == 1 ? 0x43104310u : 0x43204320u));
+    r[j] = d;
+  }
+  return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+__device__ __forceinline__ uint2 ld_shared_u64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
 // fp16 pair arithmetic, round to nearest even, subnormals kept.
 __device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
   uint32_t r;

@@ -108,9 +108,13 @@ template <> struct TcCfg<16> { static constexpr int SX = 8, SA = 8, NB = 8, NACC
 //   wg1 / wg2: decode teams of the even / odd groups, one thread per tile row
 //   wg3..: FP32 accumulation of the scaled group partials and the epilogue;
 //        warp w reads TMEM lane quadrant w % 4 and column chunk (w - 12) / 4
-template <int BN, bool kFold>
+// FMT: 0 = Q4G64; 1 = Q5G64 and 2 = Q6G64 add a high-bit plane of 1 or 2 bits per
+// weight, staged beside the codes (exact form only, token tiles up to 128 wide).
+template <int BN, bool kFold, int FMT = 0>
 struct TcSmem {
   using C = TcCfg<BN>;
+  static constexpr int kHB = FMT;  // high bits per weight
+  static_assert(FMT == 0 || (!kFold && BN <= 128), "sibling formats: exact form, BN <= 128");
   // The folded form keeps one accumulator for the whole K share, which leaves tensor
   // memory room for A at BN = 256 too; the shared memory freed there holds six X
   // stages instead of four (measured 8-12 % faster at T = 1024).
@@ -128,7 +132,9 @@ struct TcSmem {
   static constexpr uint32_t x_off = 0;
   static constexpr uint32_t a_off = x_off + SX * kB;  // shared-memory A stages (A not in tensor memory)
   static constexpr uint32_t c_off = a_off + (kATmem ? 0 : SA * kABytes);
-  static constexpr uint32_t bar_off = c_off + SW * kWBytes;
+  static constexpr uint32_t kHBytes = kTileM * kGroupsPerW * 8 * kHB;  // one high-bit stage
+  static constexpr uint32_t h_off = c_off + SW * kWBytes;
+  static constexpr uint32_t bar_off = h_off + SW * kHBytes;
   // x_full[SX], c_full[SW], c_empty[SW], mma_done[kRing], done, fin
   static constexpr uint32_t n_bars = SX + 2 * SW + kRing + 2;
   static constexpr uint32_t misc_off = bar_off + n_bars * 8;
@@ -156,11 +162,12 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* v) {
   else tmem_ld4(taddr, *reinterpret_cast<uint32_t(*)[4]>(v));
 }
 
-template <int BN, bool kFold>
-__global__ void __launch_bounds__(TcSmem<BN, kFold>::threads, 1)
+template <int BN, bool kFold, int FMT>
+__global__ void __launch_bounds__(TcSmem<BN, kFold, FMT>::threads, 1)
 q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_x,
-             const TcParams p) {
-  using L = TcSmem<BN, kFold>;
+             const __grid_constant__ CUtensorMap tm_high, const TcParams p) {
+  using L = TcSmem<BN, kFold, FMT>;
+  constexpr int kHB = L::kHB;
   using R = TcRegs<L::kATmem>;
   constexpr int SX = L::SX, SA = L::SA, NB = L::NB, NACC = L::NACC, SW = L::SW;
   constexpr int kAccWarps = 4 * NACC;
@@ -205,8 +212,15 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
   int g_begin = 0, g_end = p.nk;
   if (splitk > 1) {
     crank = cluster_ctarank();
-    g_begin = (int)(((int64_t)p.nk * crank) / splitk);
-    g_end = (int)(((int64_t)p.nk * (crank + 1)) / splitk);
+    // Q5's high plane holds 8 bytes per group: shares start on even groups so every
+    // TMA x coordinate into it is a multiple of 16 bytes
+    auto split_at = [&](uint32_t rk) {
+      if (rk >= (uint32_t)splitk) return p.nk;
+      const int g = (int)(((int64_t)p.nk * rk) / splitk);
+      return kHB == 1 ? (g & ~1) : g;
+    };
+    g_begin = split_at(crank);
+    g_end = split_at(crank + 1);
   }
   const int ng = g_end - g_begin;
   const int nws = (ng + kGroupsPerW - 1) / kGroupsPerW;
@@ -224,6 +238,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
     fence_mbar_init();
     prefetch_tmap(&tm_codes);
     prefetch_tmap(&tm_x);
+    if constexpr (kHB > 0) prefetch_tmap(&tm_high);
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), L::tmem_cols);
   tc_fence_before();
@@ -256,9 +271,12 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
       for (int ws = 0; ws < nws; ++ws) {
         const int slot = ws % SW;
         if (!(ok = mbar_wait(c_empty(slot), ((ws / SW) & 1) ^ 1, abort_flag, &g_tc_status))) break;
-        mbar_expect_tx(c_full(slot), kWBytes);
+        mbar_expect_tx(c_full(slot), kWBytes + L::kHBytes);
         tma_load_2d(sbase + L::c_off + slot * kWBytes, &tm_codes, c_full(slot), (g_begin + ws * kGroupsPerW) * 32,
                     (int32_t)m0);
+        if constexpr (kHB > 0)  // the stage's high bits: 8 * kHB bytes per group and row
+          tma_load_2d(sbase + L::h_off + slot * L::kHBytes, &tm_high, c_full(slot),
+                      (g_begin + ws * kGroupsPerW) * 8 * kHB, (int32_t)m0);
         last = ws;
       }
       if (!ok)
@@ -351,6 +369,23 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
         cw[2 * h] = ok ? ld_shared_v4(csrc + ((c0 ^ (r & 7)) << 4)) : make_uint4(0, 0, 0, 0);
         cw[2 * h + 1] = ok ? ld_shared_v4(csrc + (((c0 + 1) ^ (r & 7)) << 4)) : make_uint4(0, 0, 0, 0);
       }
+      // Q5 / Q6: the two groups' high bits (8 * kHB bytes per group in a row of the
+      // unswizzled high-bit stage)
+      uint4 hw[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+      if constexpr (kHB > 0) {
+        const uint32_t hsrc = sbase + L::h_off + slot * L::kHBytes + r * (32 * kHB);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t ga = hsrc + (uint32_t)((team + 2 * h) * 8 * kHB);
+          if (!ok) continue;
+          if constexpr (kHB == 1) {
+            const uint2 v = ld_shared_u64(ga);
+            hw[h] = make_uint4(v.x, v.y, 0, 0);
+          } else {
+            hw[h] = ld_shared_v4(ga);
+          }
+        }
+      }
       // The code slot is free once both teams have their chunks in registers (a TMA
       // refill must not race the reads above).
       __syncwarp();
@@ -366,6 +401,16 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
           tc_fence_after();
           const uint32_t words[8] = {cw[2 * h].x,     cw[2 * h].y,     cw[2 * h].z,     cw[2 * h].w,
                                      cw[2 * h + 1].x, cw[2 * h + 1].y, cw[2 * h + 1].z, cw[2 * h + 1].w};
+          // high bits of code word j of this group, in weight order
+          const uint32_t hv[4] = {hw[h].x, hw[h].y, hw[h].z, hw[h].w};
+          auto high_of = [&](int j) -> uint32_t {
+            return kHB == 1 ? (hv[j >> 2] >> (8 * (j & 3))) & 0xFFu : (hv[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
+          };
+          auto decode = [&](int j, uint32_t sc2) -> uint4 {
+            if constexpr (kFold) return decode_word_f16s(words[j], sc2);
+            else if constexpr (kHB > 0) return decode_word_bf16_hi<kHB>(words[j], high_of(j));
+            else return decode_word_bf16(words[j]);
+          };
           uint32_t s2 = 0u;  // folded form: fp16(s * 2^-rf) twice
           if constexpr (kFold) {
             const uint32_t hb =
@@ -376,7 +421,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
             uint32_t v[32];  // column j = code byte j = (k = 2j, k = 2j + 1)
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              const uint4 d4 = kFold ? decode_word_f16s(words[j], s2) : decode_word_bf16(words[j]);
+              const uint4 d4 = decode(j, s2);
               v[4 * j + 0] = d4.x;
               v[4 * j + 1] = d4.y;
               v[4 * j + 2] = d4.z;
@@ -389,7 +434,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
             const uint32_t adst = sbase + L::a_off + sa * kABytes + r * 128;
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              st_shared_v4(adst + ((j ^ (r & 7)) << 4), kFold ? decode_word_f16s(words[j], s2) : decode_word_bf16(words[j]));
+              st_shared_v4(adst + ((j ^ (r & 7)) << 4), decode(j, s2));
             fence_proxy_async();  // generic-proxy stores -> the tensor core's (async-proxy) reads
           }
         }
@@ -652,7 +697,8 @@ EncodeTiledFn encode_fn() {
 }
 
 bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
-                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                 CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {inner, outer};
@@ -660,21 +706,21 @@ bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint6
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
   return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, bool kFold>
+template <int BN, bool kFold, int FMT = 0>
 int set_kernel_attrs() {
-  using L = TcSmem<BN, kFold>;
+  using L = TcSmem<BN, kFold, FMT>;
   static bool attr_set[64] = {};
   int dev = 0;
   if (cuda_check(cudaGetDevice(&dev), "cudaGetDevice")) return Q4LIN_ERR_CUDA;
   if (dev < 64 && attr_set[dev]) return Q4LIN_OK;
-  if (cuda_check(cudaFuncSetAttribute(q4_tc_kernel<BN, kFold>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc),
+  if (cuda_check(cudaFuncSetAttribute(q4_tc_kernel<BN, kFold, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc),
                  "tc: cudaFuncSetAttribute(max dynamic shared memory)"))
     return Q4LIN_ERR_CUDA;
-  if (cuda_check(cudaFuncSetAttribute(q4_tc_kernel<BN, kFold>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+  if (cuda_check(cudaFuncSetAttribute(q4_tc_kernel<BN, kFold, FMT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
                  "tc: cudaFuncSetAttribute(cluster size)"))
     return Q4LIN_ERR_CUDA;
   if (dev < 64) attr_set[dev] = true;
@@ -704,7 +750,7 @@ int resident_clusters(int size) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, q4_tc_kernel<BN, kFold>, &cfg) != cudaSuccess || n < 0) {
+  if (cudaOccupancyMaxActiveClusters(&n, q4_tc_kernel<BN, kFold, 0>, &cfg) != cudaSuccess || n < 0) {
     cudaGetLastError();
     n = 0;
   }
@@ -712,16 +758,16 @@ int resident_clusters(int size) {
   return n;
 }
 
-template <int BN, bool kFold>
+template <int BN, bool kFold, int FMT = 0>
 int launch_tile(const LinearArgs& a, int splitk, int64_t tile_base, int64_t n_tiles) {
-  using L = TcSmem<BN, kFold>;
+  using L = TcSmem<BN, kFold, FMT>;
   static_assert(L::alloc <= 232448, "shared memory budget");
   if (splitk < 1 || splitk > 8 || splitk > L::max_splitk) {
     set_error_detail("tc: split-K factor out of range for this tile");
     return Q4LIN_ERR_INVALID_ARG;
   }
-  if (const int rc = set_kernel_attrs<BN, kFold>()) return rc;
-  CUtensorMap tm_codes, tm_x;
+  if (const int rc = set_kernel_attrs<BN, kFold, FMT>()) return rc;
+  CUtensorMap tm_codes, tm_x, tm_high;
   // code plane rows hold K_pad / 2 bytes; X rows K values, whose positions k >= K read
   // as zeros (out-of-range tile elements), so a partial last group sees x = 0 beyond K.
   // The folded form reads the fp16 token rows the prep kernel left in the workspace.
@@ -734,6 +780,17 @@ int launch_tile(const LinearArgs& a, int splitk, int64_t tile_base, int64_t n_ti
                    (uint64_t)a.K, (uint64_t)a.T, (uint64_t)a.K * 2, 64, BN)) {
     set_error_detail("tc: cuTensorMapEncodeTiled failed (or is unavailable)");
     return Q4LIN_ERR_CUDA;
+  }
+  // Q5 / Q6 high-bit plane: rows of K_pad * kHB / 8 bytes, boxes of 4 groups x 128 rows, unswizzled
+  if constexpr (L::kHB > 0) {
+    const uint64_t hrow = (uint64_t)(Kp * L::kHB / 8);
+    if (!make_map_2d(&tm_high, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.wh, hrow, (uint64_t)a.N, hrow,
+                     (uint32_t)(kGroupsPerW * 8 * L::kHB), kTileM, CU_TENSOR_MAP_SWIZZLE_NONE)) {
+      set_error_detail("tc: cuTensorMapEncodeTiled failed for the high-bit plane");
+      return Q4LIN_ERR_CUDA;
+    }
+  } else {
+    tm_high = tm_codes;  // unused
   }
   const int* xe = kFold ? reinterpret_cast<const int*>(ws + fold_ws_xe(a.N, a.K, a.T)) : nullptr;
   const int* rf = kFold ? reinterpret_cast<const int*>(ws + fold_ws_rf(a.N, a.K, a.T)) : nullptr;
@@ -760,7 +817,8 @@ int launch_tile(const LinearArgs& a, int splitk, int64_t tile_base, int64_t n_ti
   ++na;
   cfg.attrs = attr;
   cfg.numAttrs = (unsigned)na;
-  return cuda_check(cudaLaunchKernelEx(&cfg, q4_tc_kernel<BN, kFold>, tm_codes, tm_x, p), "tc: kernel launch");
+  return cuda_check(cudaLaunchKernelEx(&cfg, q4_tc_kernel<BN, kFold, FMT>, tm_codes, tm_x, tm_high, p),
+                    "tc: kernel launch");
 }
 
 // The folded form's operand pass (programmatic dependent launch like the tile kernel).
@@ -850,7 +908,7 @@ constexpr double kTailGroupFactor = 1.3;
 
 static int64_t tile_count(int64_t N, int64_t T, int bn) { return ((N + kTileM - 1) / kTileM) * ((T + bn - 1) / bn); }
 
-TcPlan tc_plan(int route, int64_t N, int64_t K, int64_t T, int sms) {
+TcPlan tc_plan(int route, int64_t N, int64_t K, int64_t T, int sms, int fmt) {
   // Token-tile width candidates: the smallest MMA N covering T up to 128
   // tokens; above that 256 or 128.  For each candidate and split factor the
   // cost is waves x per-CTA time; a wave holds as many CTAs (clusters) as can
@@ -862,7 +920,10 @@ TcPlan tc_plan(int route, int64_t N, int64_t K, int64_t T, int sms) {
   // 152 tiles, then 40 tiles in clusters of 2; 100.8 us instead of 113.3 us).
   int cand[2] = {0, 0};
   int ncand = 0;
-  if (T > 128) {
+  if (T > 128 && fmt != 0) {  // Q5 / Q6: the high-bit stages leave no room for 256-wide tiles
+    cand[0] = 128;
+    ncand = 1;
+  } else if (T > 128) {
     cand[0] = 256;
     cand[1] = 128;
     ncand = 2;
@@ -920,8 +981,8 @@ TcPlan tc_plan(int route, int64_t N, int64_t K, int64_t T, int sms) {
   return best_pl;
 }
 
-TcPlan tc_plan_current_device(int route, int64_t N, int64_t K, int64_t T) {
-  return tc_plan(route, N, K, T, sm_count());
+TcPlan tc_plan_current_device(int route, int64_t N, int64_t K, int64_t T, int fmt) {
+  return tc_plan(route, N, K, T, sm_count(), fmt);
 }
 
 size_t tc_workspace_bytes(int route, int64_t N, int64_t K, int64_t T) {
@@ -946,9 +1007,23 @@ int tc_launch(const LinearArgs& a, int route) {
     set_error_detail("tc: shape beyond the tensor-core route's limits");
     return Q4LIN_ERR_INVALID_ARG;
   }
-  const TcPlan pl = tc_plan_current_device(route, a.N, a.K, a.T);
+  if (a.fmt != 0 && (route_folds(route) || (a.fmt != 1 && a.fmt != 2))) {
+    set_error_detail("tc: sibling formats run on the exact tile routes, Q5G64 and Q6G64 only");
+    return Q4LIN_ERR_UNSUPPORTED_SHAPE;
+  }
+  const TcPlan pl = tc_plan_current_device(route, a.N, a.K, a.T, a.fmt);
   const bool fold = route_folds(route);
   auto launch = [&](int splitk, int64_t base, int64_t n) {
+    if (a.fmt != 0) {
+      const bool q5 = a.fmt == 1;
+      switch (pl.bn) {
+        case 128: return q5 ? launch_tile<128, false, 1>(a, splitk, base, n) : launch_tile<128, false, 2>(a, splitk, base, n);
+        case 64: return q5 ? launch_tile<64, false, 1>(a, splitk, base, n) : launch_tile<64, false, 2>(a, splitk, base, n);
+        case 32: return q5 ? launch_tile<32, false, 1>(a, splitk, base, n) : launch_tile<32, false, 2>(a, splitk, base, n);
+        case 16: return q5 ? launch_tile<16, false, 1>(a, splitk, base, n) : launch_tile<16, false, 2>(a, splitk, base, n);
+        default: set_error_detail("tc: no tile width for this format"); return (int)Q4LIN_ERR_UNSUPPORTED_SHAPE;
+      }
+    }
     if (fold) {
       switch (pl.bn) {
         case 256: return launch_tile<256, true>(a, splitk, base, n);

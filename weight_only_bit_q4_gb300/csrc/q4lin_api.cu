@@ -138,7 +138,11 @@ int run_qtype_impl(int qtype, const uint8_t* codes, const uint8_t* high, const u
   q4::LinearArgs a{codes, scales, x, y, N, K, T, nullptr, s};
   a.fmt = qtype;
   a.wh = needs_high ? high : nullptr;
-  return q4::gemv_launch_fmt(a);
+  // The streaming GEMV where it has a plan (1..4 tokens); otherwise Q5 / Q6 run on the
+  // exact tile route (token tiles up to 128 wide), and W8 is refused.
+  if (q4::gemv_stream_ok(N, K, T, qtype) || !needs_high || !q4::tc_supported(N, K, T))
+    return q4::gemv_launch_fmt(a);
+  return q4::tc_launch(a, Q4LIN_ROUTE_TC_SPLITK);
 }
 
 int run(int route, const uint8_t* wq, const uint16_t* scales, const uint16_t* x, uint16_t* y, int64_t N,
