@@ -220,13 +220,14 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- traffic record
-def kernel_source_digest():
+def kernel_source_digest(source: str = "q4_gemv.cu"):
+    """Digest of one kernel's translation unit: its .cu file and the device-code headers
+    (.cuh).  The .h headers hold host declarations only and are left out."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "weight_only_bit_q4_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + b"\0" + fh.read())
+    for f in [source] + sorted(f for f in os.listdir(csrc) if f.endswith(".cuh")):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
 
 
@@ -237,7 +238,7 @@ def recorded_traffic(wl_name):
         with open(path) as f:
             d = json.load(f)
         e = d.get(wl_name)
-        if e and e.get("src_digest") == kernel_source_digest():
+        if e and e.get("src_digest") == kernel_source_digest(e.get("source", "q4_gemv.cu")):
             return float(e["dram_bytes_per_launch"]), e.get("kernel")
     except (OSError, ValueError, KeyError):
         pass
@@ -295,10 +296,9 @@ def measure_ours(args, wl, rank, world, local):
     stream = torch.cuda.Stream(dev)
 
     if qtype != "q4g64":   # the streaming GEMV (1..4 tokens), else Q5 / Q6 on the exact tile route
-        if q4lin.select_route(N, K, T) == q4lin.ROUTE_GEMV and T <= 4:
-            route, launches = q4lin.ROUTE_GEMV, 1
-        else:
-            route, launches = q4lin.ROUTE_TC_SPLITK, q4lin.kernel_launches(N, K, T)
+        launches = q4lin.kernel_launches(N, K, T, qtype)
+        route = q4lin.ROUTE_GEMV if (T <= 4 and q4lin.select_route(N, K, T) == q4lin.ROUTE_GEMV) \
+            else q4lin.ROUTE_TC_SPLITK
 
     def call(i):
         if qtype == "q4g64":

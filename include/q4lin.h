@@ -141,6 +141,12 @@ int q4lin_linear_qtype(int qtype, const uint8_t* codes, const uint8_t* high, con
                        void* stream);
 
 /*
+ * Kernels one q4lin_linear_qtype call of this format and shape launches (0 for a
+ * shape it refuses or an unknown format); Q4G64 is q4lin_kernel_launches.
+ */
+int q4lin_qtype_kernel_launches(int qtype, int64_t N, int64_t K, int64_t T);
+
+/*
  * Diagnostic form of q4lin_linear that runs a given route instead of the
  * library's choice (the same arguments; route Q4LIN_ROUTE_AUTO is
  * q4lin_linear itself).  Tests use it to compare every route with the

@@ -84,6 +84,18 @@ def lib_fn():
     return q4lin.load()
 
 
+def test_qtype_launch_counts_on_host(lib):
+    # q4g64 is q4lin_kernel_launches; unknown formats and refused shapes launch nothing
+    assert q4lin.kernel_launches(6144, 5120, 1024, "q4g64") == q4lin.kernel_launches(6144, 5120, 1024)
+    assert lib.q4lin_qtype_kernel_launches(9, 64, 256, 8) == 0
+    assert q4lin.kernel_launches(64, 100, 8, "q5g64") == 0            # K % 8 != 0
+    assert q4lin.kernel_launches(0, 256, 8, "q6g64") == 0             # empty
+    assert q4lin.kernel_launches(64, 0, 8, "q6g64") == 1              # the zero fill
+    assert q4lin.kernel_launches(6144, 5120, 1024, "w8g32") == 0      # W8 beyond the GEMV: refused
+    for q in ("q5g64", "q6g64"):                                      # the tile route (one wave or a tail)
+        assert q4lin.kernel_launches(6144, 5120, 1024, q) in (1, 2)
+
+
 def test_qtype_argument_errors_detected_on_host(lib):
     assert _call_qtype(9, 4, 128, 1) == 1                 # no such format
     assert _call_qtype(-1, 4, 128, 1) == 1

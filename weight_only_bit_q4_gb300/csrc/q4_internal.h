@@ -52,7 +52,7 @@ int tc_launch(const LinearArgs& a, int route);
 // The folded tile routes (Q4LIN_ROUTE_TC, Q4LIN_ROUTE_TC_SPLITK) need workspace for
 // their fp16 operands and launch a prep kernel first; the exact route needs none.
 size_t tc_workspace_bytes(int route, int64_t N, int64_t K, int64_t T);
-int tc_launch_count(int route, int64_t N, int64_t K, int64_t T);
+int tc_launch_count(int route, int64_t N, int64_t K, int64_t T, int fmt = 0);
 // The fp16 tile route with its operand scratch in a fixed device array instead of
 // a caller workspace (q4lin_linear_fp16_static): whether (N, K, T) fits, and the call.
 bool tc_fp16_static_fits(int64_t N, int64_t K, int64_t T);

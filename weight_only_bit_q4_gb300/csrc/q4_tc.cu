@@ -989,8 +989,8 @@ size_t tc_workspace_bytes(int route, int64_t N, int64_t K, int64_t T) {
   return route_folds(route) ? fold_ws_bytes(N, K, T) : 0;
 }
 
-int tc_launch_count(int route, int64_t N, int64_t K, int64_t T) {
-  const TcPlan pl = tc_plan_current_device(route, N, K, T);
+int tc_launch_count(int route, int64_t N, int64_t K, int64_t T, int fmt) {
+  const TcPlan pl = tc_plan_current_device(route, N, K, T, fmt);
   return (pl.main_tiles < tile_count(N, T, pl.bn) ? 2 : 1) + (route_folds(route) ? 1 : 0);
 }
 

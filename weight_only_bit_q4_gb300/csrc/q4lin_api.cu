@@ -199,6 +199,16 @@ int q4lin_kernel_launches(int64_t N, int64_t K, int64_t T) {
   }
 }
 
+int q4lin_qtype_kernel_launches(int qtype, int64_t N, int64_t K, int64_t T) {
+  if (qtype == Q4LIN_QTYPE_Q4G64) return q4lin_kernel_launches(N, K, T);
+  if (qtype < Q4LIN_QTYPE_Q5G64 || qtype > Q4LIN_QTYPE_W8G32) return 0;
+  if (validate_sizes(N, K, T) != Q4LIN_OK || N == 0 || T == 0) return 0;
+  if (K == 0) return 1;  // the zero fill
+  if (q4::gemv_stream_ok(N, K, T, qtype)) return 1;
+  if (qtype == Q4LIN_QTYPE_W8G32 || !q4::tc_supported(N, K, T)) return 0;  // refused
+  return q4::tc_launch_count(Q4LIN_ROUTE_TC_SPLITK, N, K, T, qtype);
+}
+
 int q4lin_linear(const uint8_t* wq, const uint16_t* scales, const uint16_t* x, uint16_t* y,
                  int64_t N, int64_t K, int64_t T, void* workspace, void* stream) {
   return run(Q4LIN_ROUTE_AUTO, wq, scales, x, y, N, K, T, workspace, stream);

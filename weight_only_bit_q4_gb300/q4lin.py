@@ -22,7 +22,7 @@ ROUTE_NAMES = {ROUTE_AUTO: "auto", ROUTE_GEMV: "gemv", ROUTE_TC_SPLITK: "tc_spli
 QTYPES = {"q4g64": 0, "q5g64": 1, "q6g64": 2, "w8g32": 3}
 
 EXPORTS = ("q4lin_workspace_bytes", "q4lin_linear", "q4lin_linear_route", "q4lin_linear_qtype",
-           "q4lin_linear_fp16_static",
+           "q4lin_linear_fp16_static", "q4lin_qtype_kernel_launches",
            "q4lin_route_workspace_bytes", "q4lin_select_route", "q4lin_tile_plan", "q4lin_kernel_launches",
            "q4lin_status_string",
            "q4lin_device_status", "q4lin_clear_device_status", "q4lin_last_error_detail",
@@ -73,6 +73,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q4lin_tile_plan.restype = ctypes.c_int
     lib.q4lin_kernel_launches.argtypes = [i64, i64, i64]
     lib.q4lin_kernel_launches.restype = ctypes.c_int
+    lib.q4lin_qtype_kernel_launches.argtypes = [ctypes.c_int, i64, i64, i64]
+    lib.q4lin_qtype_kernel_launches.restype = ctypes.c_int
     lib.q4lin_status_string.argtypes = [ctypes.c_int]
     lib.q4lin_status_string.restype = ctypes.c_char_p
     lib.q4lin_device_status.argtypes = []
@@ -122,8 +124,11 @@ def tile_plan_full(N: int, K: int, T: int, route: int = ROUTE_AUTO) -> dict:
     return {"n": int(bn.value), "split_k": int(sk.value), "main_tiles": int(mt.value), "tail_split_k": int(ts.value)}
 
 
-def kernel_launches(N: int, K: int, T: int) -> int:
-    return int(load().q4lin_kernel_launches(N, K, T))
+def kernel_launches(N: int, K: int, T: int, qtype: str = "q4g64") -> int:
+    """Kernels one call launches (q4lin_linear, or q4lin_linear_qtype for another format)."""
+    if qtype == "q4g64":
+        return int(load().q4lin_kernel_launches(N, K, T))
+    return int(load().q4lin_qtype_kernel_launches(QTYPES[qtype], N, K, T))
 
 
 _IMPLEMENTED = (ROUTE_GEMV, ROUTE_TC_SPLITK, ROUTE_TC, ROUTE_TC_FP16)
