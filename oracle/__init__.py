@@ -5,3 +5,4 @@ from .q4_oracle import (  # noqa: F401
     REL_TOL, RMS_TOL,
 )
 from . import sibling_formats  # noqa: F401,E402
+from . import fused_ops  # noqa: F401,E402
