@@ -141,6 +141,18 @@ int q4lin_linear_qtype(int qtype, const uint8_t* codes, const uint8_t* high, con
                        void* stream);
 
 /*
+ * LinearAdd (a fused operation the linear-benchmark page names and leaves to its
+ * own benchmark; the reading here): y = W . x + r, the bf16 residual r [T, N]
+ * (row-major like y, 16-byte aligned) added to the FP32 sum before y's one bf16
+ * rounding.  r may be y itself (in-place residual add); otherwise r and y must not
+ * overlap.  Runs the exact tile route for every T (a fused GEMV form for 1..4
+ * tokens is not built); no workspace.  Other arguments and errors as q4lin_linear;
+ * r NULL gives Q4LIN_ERR_INVALID_ARG.  K = 0 gives y = r.
+ */
+int q4lin_linear_add(const uint8_t* wq, const uint16_t* scales, const uint16_t* x, const uint16_t* r, uint16_t* y,
+                     int64_t N, int64_t K, int64_t T, void* stream);
+
+/*
  * Kernels one q4lin_linear_qtype call of this format and shape launches (0 for a
  * shape it refuses or an unknown format); Q4G64 is q4lin_kernel_launches.
  */

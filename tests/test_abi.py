@@ -84,6 +84,15 @@ def lib_fn():
     return q4lin.load()
 
 
+def test_linear_add_host_checks(lib):
+    vp = ctypes.c_void_p
+    f = lib.q4lin_linear_add
+    assert f(vp(16), vp(16), vp(16), None, vp(16), 64, 256, 8, None) == 1      # no residual
+    assert f(vp(16), vp(16), vp(16), vp(24), vp(16), 64, 256, 8, None) == 3    # misaligned residual
+    assert f(vp(16), vp(16), vp(16), vp(16), vp(16), 64, 100, 8, None) == 2    # K % 8 != 0
+    assert f(None, None, None, None, None, 0, 256, 8, None) == 0               # empty
+
+
 def test_qtype_launch_counts_on_host(lib):
     # q4g64 is q4lin_kernel_launches; unknown formats and refused shapes launch nothing
     assert q4lin.kernel_launches(6144, 5120, 1024, "q4g64") == q4lin.kernel_launches(6144, 5120, 1024)

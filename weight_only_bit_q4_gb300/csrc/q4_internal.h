@@ -21,6 +21,7 @@ struct LinearArgs {
   cudaStream_t stream;
   int fmt = 0;                   // weight format (0: Q4G64; 1: Q5G64, 2: Q6G64, 3: W8G32)
   const uint8_t* wh = nullptr;   // Q5G64 / Q6G64: the high-bit plane
+  const uint16_t* r = nullptr;   // LinearAdd: bf16 residual [T, N] (tile route)
 };
 
 // The weight planes are stored for K rounded up to a multiple of 128

@@ -77,6 +77,7 @@ struct TcParams {
   uint16_t* y;
   const int* xe;  // folded form: per token, X was stored as fp16 x * 2^-xe[t]
   const int* rf;  // folded form: per weight row, the scales enter as s * 2^-rf[n]
+  const uint16_t* r;  // LinearAdd: bf16 residual [T, N] added before the bf16 store (may be y itself)
   int64_t N, Kp, T;   // Kp: the planes' stored width, K rounded up to 128
   int nk;      // groups (K-steps of 64) holding columns < K
   int splitk;  // CTAs of a cluster sharing one output tile along K (1 = no split)
@@ -591,13 +592,17 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
       }
     }
 
-    // ----------------------------------------------------------- epilogue: Y[t, row] = bf16(acc)
+    // ----------------------------------------------------------- epilogue: Y[t, row] = bf16(acc [+ R[t, row]])
     if (crank == 0 && acc_ok && !*abort_flag && row_ok) {
 #pragma unroll
       for (int j = 0; j < kCols; ++j) {
         const int64_t t = t0 + cq * kCols + j;
-        const float v = (j & 1) ? acc[j / 2].y : acc[j / 2].x;
-        if (t < p.T) p.y[t * p.N + row] = float_to_bf16_bits(v);
+        float v = (j & 1) ? acc[j / 2].y : acc[j / 2].x;
+        if (t < p.T) {
+          // LinearAdd: the residual joins the FP32 sum; read before the store, so R may be Y
+          if (p.r != nullptr) v += __uint_as_float((uint32_t)p.r[t * p.N + row] << 16);
+          p.y[t * p.N + row] = float_to_bf16_bits(v);
+        }
       }
     }
     tc_fence_before();
@@ -794,7 +799,7 @@ int launch_tile(const LinearArgs& a, int splitk, int64_t tile_base, int64_t n_ti
   }
   const int* xe = kFold ? reinterpret_cast<const int*>(ws + fold_ws_xe(a.N, a.K, a.T)) : nullptr;
   const int* rf = kFold ? reinterpret_cast<const int*>(ws + fold_ws_rf(a.N, a.K, a.T)) : nullptr;
-  const TcParams p{a.scales, a.y, xe, rf, a.N, Kp, a.T, (int)((a.K + 63) / 64), splitk, (uint32_t)tile_base,
+  const TcParams p{a.scales, a.y, xe, rf, a.r, a.N, Kp, a.T, (int)((a.K + 63) / 64), splitk, (uint32_t)tile_base,
                    (uint32_t)((a.N + kTileM - 1) / kTileM)};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)n_tiles, 1, (unsigned)splitk);

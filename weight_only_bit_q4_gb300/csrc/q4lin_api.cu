@@ -199,6 +199,32 @@ int q4lin_kernel_launches(int64_t N, int64_t K, int64_t T) {
   }
 }
 
+int q4lin_linear_add(const uint8_t* wq, const uint16_t* scales, const uint16_t* x, const uint16_t* r, uint16_t* y,
+                     int64_t N, int64_t K, int64_t T, void* stream) {
+  q4::set_error_detail("");
+  int st = validate(wq, scales, x, y, N, K, T);
+  if (st == Q4LIN_OK && N > 0 && T > 0) {
+    if (r == nullptr) st = Q4LIN_ERR_INVALID_ARG;
+    else if (!aligned16(r)) st = Q4LIN_ERR_MISALIGNED;
+    else if (K > 0 && !q4::tc_supported(N, K, T)) st = Q4LIN_ERR_INVALID_ARG;
+  }
+  if (st == Q4LIN_OK && N > 0 && T > 0) st = check_device();
+  if (st == Q4LIN_OK && N > 0 && T > 0) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) {  // the empty sum: Y = R
+      if (r != y)
+        st = q4::cuda_check(cudaMemcpyAsync(y, r, (size_t)N * (size_t)T * 2, cudaMemcpyDeviceToDevice, s),
+                            "copy of the residual");
+    } else {
+      q4::LinearArgs a{wq, scales, x, y, N, K, T, nullptr, s};
+      a.r = r;
+      st = q4::tc_launch(a, Q4LIN_ROUTE_TC_SPLITK);
+    }
+  }
+  if (st != Q4LIN_OK && q4::g_detail[0] == 0) q4::set_error_detail(q4lin_status_string(st));
+  return st;
+}
+
 int q4lin_qtype_kernel_launches(int qtype, int64_t N, int64_t K, int64_t T) {
   if (qtype == Q4LIN_QTYPE_Q4G64) return q4lin_kernel_launches(N, K, T);
   if (qtype < Q4LIN_QTYPE_Q5G64 || qtype > Q4LIN_QTYPE_W8G32) return 0;

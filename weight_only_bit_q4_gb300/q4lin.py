@@ -22,7 +22,7 @@ ROUTE_NAMES = {ROUTE_AUTO: "auto", ROUTE_GEMV: "gemv", ROUTE_TC_SPLITK: "tc_spli
 QTYPES = {"q4g64": 0, "q5g64": 1, "q6g64": 2, "w8g32": 3}
 
 EXPORTS = ("q4lin_workspace_bytes", "q4lin_linear", "q4lin_linear_route", "q4lin_linear_qtype",
-           "q4lin_linear_fp16_static", "q4lin_qtype_kernel_launches",
+           "q4lin_linear_fp16_static", "q4lin_qtype_kernel_launches", "q4lin_linear_add",
            "q4lin_route_workspace_bytes", "q4lin_select_route", "q4lin_tile_plan", "q4lin_kernel_launches",
            "q4lin_status_string",
            "q4lin_device_status", "q4lin_clear_device_status", "q4lin_last_error_detail",
@@ -73,6 +73,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q4lin_tile_plan.restype = ctypes.c_int
     lib.q4lin_kernel_launches.argtypes = [i64, i64, i64]
     lib.q4lin_kernel_launches.restype = ctypes.c_int
+    lib.q4lin_linear_add.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, vp]
+    lib.q4lin_linear_add.restype = ctypes.c_int
     lib.q4lin_qtype_kernel_launches.argtypes = [ctypes.c_int, i64, i64, i64]
     lib.q4lin_qtype_kernel_launches.restype = ctypes.c_int
     lib.q4lin_status_string.argtypes = [ctypes.c_int]
@@ -191,6 +193,28 @@ def linear(wq, scales, x, y=None, workspace=None, stream=None, route: int = ROUT
     s = (stream or torch.cuda.current_stream(x.device)).cuda_stream
     st = linear_raw(_ptr(wq), _ptr(scales), _ptr(x), _ptr(y), N, K, T,
                     _ptr(workspace) if need else None, ctypes.c_void_p(s), route)
+    if st != OK:
+        raise Q4LinError(st)
+    return y
+
+
+def linear_add(wq, scales, x, r, y=None, stream=None):
+    """LinearAdd: Y = W . X + R (bf16 [T, N]); ``y`` may be ``r`` itself for an in-place add."""
+    import torch
+
+    T, K = x.shape
+    N = wq.shape[0]
+    Kp = (K + 127) // 128 * 128
+    if tuple(wq.shape) != (N, Kp // 2) or tuple(scales.shape) != (N, Kp // 64) or tuple(r.shape) != (T, N):
+        raise ValueError(f"shape mismatch: wq {tuple(wq.shape)} scales {tuple(scales.shape)} x {tuple(x.shape)} "
+                         f"r {tuple(r.shape)}")
+    for name, t in (("wq", wq), ("scales", scales), ("x", x), ("r", r)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if y is None:
+        y = torch.empty((T, N), dtype=torch.bfloat16, device=x.device)
+    s = (stream or torch.cuda.current_stream(x.device)).cuda_stream
+    st = int(load().q4lin_linear_add(_ptr(wq), _ptr(scales), _ptr(x), _ptr(r), _ptr(y), N, K, T, ctypes.c_void_p(s)))
     if st != OK:
         raise Q4LinError(st)
     return y
