@@ -37,6 +37,13 @@
 // one element in 3.5 million at 1.03x the bound), so the folded form is never the
 // library's choice; bf16 folding would miss the floor outright.
 //
+// Two more template parameters reuse the same pipeline.  FMT = 1 / 2 (Q5G64 /
+// Q6G64, exact form, token tiles up to 128 wide) adds a second TMA stream per code
+// stage for the high-bit plane; the decode teams move each weight's high bits to
+// bit 4 of its nibble before taking the exact bf16 q - 16 / q - 32.  The epilogue
+// optionally adds a bf16 residual R[t, n] to the FP32 sum before the store
+// (LinearAdd).
+//
 // Synchronisation, shaped by what the hardware charges for it:
 //   * while the tensor core streams its shared-memory operands an mbarrier
 //     wait costs a few hundred cycles even when the phase has long completed,
