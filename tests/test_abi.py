@@ -42,6 +42,20 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(declared_functions()) <= exported
 
 
+def test_c_client_compiles_links_and_runs(lib, tmp_path):
+    # the boundary from C, without Python in between: header alone, library linked
+    src = os.path.join(ROOT, "tests", "c_abi", "abi_host_checks.c")
+    exe = str(tmp_path / "abi_host_checks")
+    libdir = os.path.dirname(q4lin.LIB_PATH)
+    cmd = ["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), src, "-o", exe,
+           "-L" + libdir, "-lq4lin", "-Wl,-rpath," + libdir]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    run = subprocess.run([exe], capture_output=True, text=True)
+    assert run.returncode == 0, run.stdout + run.stderr
+    assert "FAIL" not in run.stdout
+
+
 def test_status_strings(lib):
     for code in range(8):
         assert q4lin.status_string(code) and q4lin.status_string(code) != "unknown status"
