@@ -20,10 +20,11 @@
  * of 8, so that every X row starts 16-byte aligned.
  *
  * Ownership: the caller owns every buffer.  The library never allocates or
- * frees memory and keeps no state between calls except its error word.
- * Inputs (wq, scales, x) are only read.  Exactly the N*T elements of y are
- * written.  The workspace belongs to the call for its stream-ordered
- * duration.
+ * frees memory.  It keeps no state between calls except its error word and the
+ * fixed scratch array of q4lin_linear_fp16_static (declared with it below).
+ * Inputs (wq, scales, x, and LinearAdd's residual r unless it is y) are only
+ * read.  Exactly the N*T elements of y are written.  The workspace belongs to
+ * the call for its stream-ordered duration.
  *
  * Execution: every compute entry point is asynchronous on `stream` (a
  * cudaStream_t passed as void*; NULL = the legacy default stream), performs
