@@ -1,0 +1,57 @@
+"""The benchmark's JSON line, checked on the CPU with the GPU measurement stubbed:
+every key the line must carry, the types, and the figures derived from the
+timings (whole-job rate, roofline fraction, end-to-end rate, launch count)."""
+import json
+
+import pytest
+
+import bench
+from weight_only_bit_q4_gb300 import metrics
+
+
+def _fake_measure(args, wl, rank, world, local):
+    return dict(per_call_us=[8.0] * 10, total_ms=0.08, calls=10, copies=8,
+                cold_us=[12.0] * 200, route="gemv", launches=1,
+                clocks={"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 5},
+                e2e=dict(us=[32.0] * 100, h2d=2 * wl["K"] * wl["T"], d2h=2 * wl["N"] * wl["T"]),
+                tile={"n": 0, "split_k": 1, "main_tiles": 0, "tail_split_k": 0}, ws_bytes=0)
+
+
+@pytest.fixture
+def line(monkeypatch, capsys):
+    monkeypatch.setattr(bench, "measure_ours", _fake_measure)
+    monkeypatch.setattr(bench, "cpu_baseline", lambda wl: {"value": 0.05, "unit": "GB/s", "cores": 8,
+                                                           "kind": "oracle", "sample": "rows 0..9"})
+    assert bench.main(["--steps", "10", "--warmup", "3"]) == 0
+    out = [l for l in capsys.readouterr().out.splitlines() if l.startswith("{")]
+    assert len(out) == 1
+    return json.loads(out[0])
+
+
+def test_line_carries_every_key(line):
+    for k, typ in [("metric", str), ("value", float), ("unit", str), ("n_gpus", int), ("steps", int),
+                   ("warmup", int), ("ms_per_step", float), ("higher_is_better", bool), ("scaling", str),
+                   ("dtype", str), ("data", str), ("config", dict), ("roofline", dict), ("e2e", dict),
+                   ("gpu_launches", int), ("clocks", dict), ("cpu_baseline", dict)]:
+        assert isinstance(line[k], typ), k
+    assert "vs_baseline" in line and line["vs_baseline"] is None
+    assert line["config"]["workload"] == "q4_6144x5120_t1"
+    for k in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
+        assert k in line["roofline"], k
+    for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"):
+        assert k in line["e2e"], k
+    for k in ("value", "unit", "cores", "kind", "sample"):
+        assert k in line["cpu_baseline"], k
+    assert line["warmup"] >= 3 and line["scaling"] == "weak" and line["data"] == "synthetic"
+
+
+def test_derived_figures(line):
+    mb = metrics.model_bytes(6144, 5120, 1)
+    # 10 calls in 0.08 ms: 8 us per call
+    assert line["ms_per_step"] == pytest.approx(0.008)
+    assert line["value"] == pytest.approx(mb / 8e-6 / 1e9, rel=1e-3)
+    assert line["unit"] == "GB/s" and line["roofline"]["bound"] == "hbm"
+    assert line["roofline"]["frac"] == pytest.approx(line["roofline"]["achieved"] / line["roofline"]["peak"], rel=1e-3)
+    assert line["e2e"]["value"] == pytest.approx(mb / 32e-6 / 1e9, rel=1e-3)
+    assert line["e2e"]["h2d_bytes_per_step"] == 2 * 5120 and line["e2e"]["d2h_bytes_per_step"] == 2 * 6144
+    assert line["gpu_launches"] == 10
