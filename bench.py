@@ -2,7 +2,7 @@
 """Benchmark of the Q4_G64_FP16 linear layer on one GB300 (or N replicas).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--t T] [--qtype FMT] [--route R] [--profile]
+                    [--workload NAME] [--t T] [--qtype FMT] [--route R] [--op OP] [--profile]
 
 Timing (the linear-benchmark contract, section 6, and the Q4 measurement
 report's header table): every sample is one complete public call captured in
@@ -73,6 +73,8 @@ def parse_args(argv=None):
     p.add_argument("--t", type=int, default=None, help="T for the sweep workloads")
     p.add_argument("--qtype", default="q4g64", choices=sorted(metrics.GROUP_BYTES),
                    help="weight format (the sibling formats run for 1..4 tokens)")
+    p.add_argument("--op", default="linear", choices=["linear", "add"],
+                   help="linear: Y = W.X; add: LinearAdd, Y = W.X + R (the tile route for every T)")
     p.add_argument("--route", default="auto", choices=["auto", "tc_fp16"],
                    help="auto: the library's choice; tc_fp16: the opt-in tile route on fp16-rounded weights")
     p.add_argument("--profile", action="store_true",
@@ -105,7 +107,18 @@ def workload(args):
         if qtype != "q4g64":
             raise SystemExit(f"--route {route} runs the Q4 format only")
         name += "_" + route
-    return dict(name=name, N=N, K=K, T=T, dist=dist, outliers=outl, w_seed=ws, x_seed=xs, qtype=qtype)
+    op = getattr(args, "op", "linear")
+    if op == "add":
+        if qtype != "q4g64" or route != "auto":
+            raise SystemExit("--op add runs the Q4 format on its own route")
+        name += "_add"
+    return dict(name=name, N=N, K=K, T=T, dist=dist, outliers=outl, w_seed=ws, x_seed=xs, qtype=qtype, op=op)
+
+
+def op_bytes(wl):
+    """Logical bytes of one call: the layer's model bytes, plus the residual read by LinearAdd."""
+    N, K, T = wl["N"], wl["K"], wl["T"]
+    return metrics.model_bytes(N, K, T, wl["qtype"]) + (2 * N * T if wl.get("op") == "add" else 0)
 
 
 def format_problem(wl, rows=None):
@@ -275,7 +288,9 @@ def measure_ours(args, wl, rank, world, local):
         x = synth.activations(T, K, wl["x_seed"], wl["outliers"])
     else:
         planes, sc, x = format_problem(wl)
-    per_copy = metrics.model_bytes(N, K, T, qtype)
+    per_copy = op_bytes(wl)
+    add = wl.get("op") == "add"
+    r = synth.activations(T, N, wl["x_seed"] + 7919) if add else None   # LinearAdd's bf16 residual [T, N]
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size or (128 << 20)
     R = int(max(2, min(64, -(-int(2.5 * l2) // per_copy))))
     pl_d = tuple(torch.from_numpy(p).to(dev) for p in planes)
@@ -285,6 +300,7 @@ def measure_ours(args, wl, rank, world, local):
     scs = [sc_d] + [sc_d.clone() for _ in range(R - 1)]
     xs = [x_d] + [x_d.clone() for _ in range(R - 1)]
     ys = [torch.empty((T, N), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    rs = [torch.from_numpy(r.view(np.int16)).to(dev).view(torch.bfloat16) for _ in range(R)] if add else None
     route_arg = q4lin.ROUTE_TC_FP16 if args.route == "tc_fp16" else q4lin.ROUTE_AUTO
     ws_n = q4lin.workspace_bytes(N, K, T, route_arg)
     ws_d = torch.empty(max(ws_n, 256), dtype=torch.uint8, device=dev)
@@ -300,8 +316,15 @@ def measure_ours(args, wl, rank, world, local):
         route = q4lin.ROUTE_GEMV if (T <= 4 and q4lin.select_route(N, K, T) == q4lin.ROUTE_GEMV) \
             else q4lin.ROUTE_TC_SPLITK
 
+    if add:   # the exact tile route for every T: one launch, or two with a tail launch
+        pl = q4lin.tile_plan_full(N, K, T, q4lin.ROUTE_TC_SPLITK)
+        route = q4lin.ROUTE_TC_SPLITK
+        launches = 2 if pl["main_tiles"] < -(-N // 128) * -(-T // pl["n"]) else 1
+
     def call(i):
-        if qtype == "q4g64":
+        if add:
+            q4lin.linear_add(pls[i][0], scs[i], xs[i], rs[i], y=ys[i], stream=stream)
+        elif qtype == "q4g64":
             q4lin.linear(pls[i][0], scs[i], xs[i], y=ys[i], workspace=ws_d if ws_n else None, stream=stream,
                          route=route_arg)
         else:
@@ -389,6 +412,7 @@ def measure_ours(args, wl, rank, world, local):
         if not args.no_e2e:
             x_h = [torch.from_numpy(x.view(np.int16)).pin_memory() for _ in range(2)]
             y_h = [torch.empty((T, N), dtype=torch.int16).pin_memory() for _ in range(2)]
+            r_h = [torch.from_numpy(r.view(np.int16)).pin_memory() for _ in range(2)] if add else None
             n_e2e = min(max(args.steps // 10, 100), 2000)
             ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_e2e)]
             for i in range(20 + n_e2e):
@@ -396,16 +420,19 @@ def measure_ours(args, wl, rank, world, local):
                 if i >= 20:
                     ee[i - 20][0].record(stream)
                 xs[c].view(torch.int16).copy_(x_h[i & 1], non_blocking=True)
+                if add:
+                    rs[c].view(torch.int16).copy_(r_h[i & 1], non_blocking=True)
                 call(c)
                 y_h[i & 1].copy_(ys[c].view(torch.int16), non_blocking=True)
                 if i >= 20:
                     ee[i - 20][1].record(stream)
             torch.cuda.synchronize(dev)
-            e2e = dict(us=sorted(a.elapsed_time(b) * 1e3 for a, b in ee), h2d=2 * K * T, d2h=2 * N * T)
+            e2e = dict(us=sorted(a.elapsed_time(b) * 1e3 for a, b in ee), h2d=2 * K * T + (2 * N * T if add else 0),
+                       d2h=2 * N * T)
 
     return dict(per_call_us=per_call_us, total_ms=total_ms, calls=calls, copies=R, cold_us=cold_us,
                 clocks=clocks, route=q4lin.ROUTE_NAMES.get(route, str(route)), launches=launches, e2e=e2e,
-                tile=q4lin.tile_plan_full(N, K, T, route_arg),
+                tile=q4lin.tile_plan_full(N, K, T, q4lin.ROUTE_TC_SPLITK if add else route_arg),
                 ws_bytes=ws_n)
 
 
@@ -430,8 +457,14 @@ def time_oracle(wl, rows, reps_budget_s, max_reps, exact=False):
         sc = synth.group_scales(N, K, wl["w_seed"], wl["dist"])[:rows]
         x = synth.activations(T, K, wl["x_seed"], wl["outliers"])
 
-        def run():
-            return oracle.linear(wq, sc, x)
+        if wl.get("op") == "add":
+            r = synth.activations(T, N, wl["x_seed"] + 7919)[:, :rows]
+
+            def run():
+                return oracle.fused_ops.linear_add(wq, sc, x, r)
+        else:
+            def run():
+                return oracle.linear(wq, sc, x)
     else:
         planes, sc, x = format_problem(wl, rows)
 
@@ -449,7 +482,7 @@ def time_oracle(wl, rows, reps_budget_s, max_reps, exact=False):
 
 def oracle_units(wl, rows):
     K, T = wl["K"], wl["T"]
-    b = metrics.model_bytes(rows, K, T, wl["qtype"])
+    b = metrics.model_bytes(rows, K, T, wl["qtype"]) + (2 * rows * T if wl.get("op") == "add" else 0)
     f = metrics.useful_flops(rows, K, T)
     return b, f
 
@@ -525,7 +558,7 @@ def main(argv=None):
     med_rep = statistics.median(res["per_call_us"])         # median over graph replays
     mean_max, med_max = reduce_max([mean_us, med_rep], world, dev)
     N, K, T = wl["N"], wl["K"], wl["T"]
-    mb, fl = metrics.model_bytes(N, K, T, wl["qtype"]), metrics.useful_flops(N, K, T)
+    mb, fl = op_bytes(wl), metrics.useful_flops(N, K, T)
     small = small_t(wl)
     unit = "GB/s" if small else "TFLOP/s"
 

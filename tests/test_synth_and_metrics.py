@@ -100,3 +100,15 @@ def test_bench_format_workloads():
         bench.workload(bench.parse_args(["--qtype", "w8g32", "--workload", "q4_6144x5120", "--t", "8"]))
     planes, s, x = bench.format_problem(dict(wl, N=40, K=256, T=2), rows=7)
     assert planes[0].shape == (7, 256) and s.shape == (7, 8) and x.shape == (2, 256)
+
+
+def test_bench_linear_add_workload():
+    import bench
+    wl = bench.workload(bench.parse_args(["--op", "add", "--workload", "q4_6144x5120", "--t", "1024"]))
+    assert wl["name"] == "q4_6144x5120_t1024_add" and wl["op"] == "add"
+    # the residual is read once: 2 N T bytes on top of the layer's model bytes
+    assert bench.op_bytes(wl) == metrics.model_bytes(6144, 5120, 1024) + 2 * 6144 * 1024
+    with pytest.raises(SystemExit):
+        bench.workload(bench.parse_args(["--op", "add", "--qtype", "q5g64"]))
+    with pytest.raises(SystemExit):
+        bench.workload(bench.parse_args(["--op", "add", "--route", "tc_fp16"]))
