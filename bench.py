@@ -546,14 +546,20 @@ def main(argv=None):
         return reference_arm(args, wl, rank, world)
 
     import torch
+    # NCCL on the GPUs; gloo with CPU tensors where there is no GPU (the multi-rank
+    # host path, exercised by the CPU tests with the measurement stubbed)
+    on_gpu = torch.cuda.is_available()
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if on_gpu:
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group("gloo")
     res = measure_ours(args, wl, rank, world, local)
     if res is None:
         return 0
-    dev = torch.device("cuda", local)
+    dev = torch.device("cuda", local) if on_gpu else None
     mean_us = res["total_ms"] * 1e3 / res["calls"]          # steady state, all calls of the timed region
     med_rep = statistics.median(res["per_call_us"])         # median over graph replays
     mean_max, med_max = reduce_max([mean_us, med_rep], world, dev)
