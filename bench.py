@@ -1,25 +1,29 @@
 #!/usr/bin/env python3
 """Benchmark of the Q4_G64_FP16 linear layer on one GB300 (or N replicas).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--samples S] [--impl ours|reference]
                     [--workload NAME] [--t T] [--qtype FMT] [--route R] [--op OP] [--profile]
 
-Timing (the linear-benchmark contract, section 6, and the Q4 measurement
-report's header table): every sample is one complete public call captured in
-a CUDA graph; before each sample a 256 MiB buffer is written and then read
-back (the write evicts L2, the read leaves it clean so no dirty lines are
-written back inside the sample); CUDA events on the launching stream bracket
-only the graph launch; the flush and the graph are queued back to back with
-no host synchronisation.  The primary figure is the median; min and p95 are
-reported too.  Metrics follow the contract's sections 4-5 (weight_only_bit_q4_gb300.metrics).
+A step is one call of the layer on one batch of the workload's synthetic input.
+With no --workload the run times three records of the 6144 x 5120 layer: the
+decode GEMV at T = 1 (the headline), T = 8 (the small-T route) and T = 1024 (the
+large-T tile route); otherwise one record of the named workload.
 
-A step is one call of the layer on one batch of the workload's synthetic
-input.  Default workload: the decode GEMV, N=6144 K=5120 T=1.  --qtype times
-a sibling weight format (Q5G64, Q6G64, W8G32) on the same geometry through
-q4lin_linear_qtype (W8G32 for 1..4 tokens); its bytes are that format's.
-Under torchrun (N > 1) every rank runs an independent replica on its own GPU
-(the layer does not exchange data between GPUs); value = the units all ranks
-processed / the slowest rank's time.
+Timing of a record: W untimed warm-up calls, then S samples (at least 50).  A
+sample is exactly K back-to-back calls captured in one CUDA graph (call i on
+rotating copy i mod R of the weights, X and Y, R copies larger than 2.5 x L2 in
+total, so every call streams from HBM), queued right after a 256 MiB L2 flush
+(the buffer is written, then read back so no dirty line is written back inside
+the sample), with CUDA events on the launching stream around the graph launch.
+ms_per_step = median sample / K; value = the metric at that time; min and p95
+are reported too.  The linear-benchmark contract's own method (section 6: one
+call per sample behind the flush, median) is reported as cold_call.  Metrics
+follow the contract's sections 4-5 (weight_only_bit_q4_gb300.metrics).
+
+--qtype times a sibling weight format (Q5G64, Q6G64, W8G32) on the same geometry
+through q4lin_linear_qtype; its bytes are that format's.  Under torchrun (N > 1)
+every rank runs an independent replica on its own GPU (the layer does not exchange
+data between GPUs); value = the units all ranks processed / the slowest rank's time.
 """
 from __future__ import annotations
 
@@ -62,14 +66,21 @@ WORKLOADS = {
 DEFAULT_WORKLOAD = "q4_6144x5120_t1"
 
 
+# the records of the default run: the decode GEMV headline, then the small-T and the
+# large-T routes on the same 6144 x 5120 weight
+DEFAULT_RECORDS = (("q4_6144x5120_t1", None), ("q4_6144x5120", 8), ("q4_6144x5120", 1024))
+MIN_SAMPLES = 50
+
+
 def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=None,
-                   help="timed calls (default: enough for about a second of GPU time)")
-    p.add_argument("--warmup", type=int, default=100)
+    p.add_argument("--steps", type=int, default=20, help="calls per timed sample (K)")
+    p.add_argument("--warmup", type=int, default=10, help="untimed warm-up calls per record (W >= 3)")
+    p.add_argument("--samples", type=int, default=MIN_SAMPLES, help=f"timed samples per record (>= {MIN_SAMPLES})")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    p.add_argument("--workload", default=None, choices=sorted(WORKLOADS),
+                   help=f"time this workload alone (default: the three records of {DEFAULT_WORKLOAD} at T = 1, 8, 1024)")
     p.add_argument("--t", type=int, default=None, help="T for the sweep workloads")
     p.add_argument("--qtype", default="q4g64", choices=sorted(metrics.GROUP_BYTES),
                    help="weight format (the sibling formats run for 1..4 tokens)")
@@ -81,38 +92,51 @@ def parse_args(argv=None):
                    help="one call between cudaProfilerStart/Stop after warm-up and flush (for ncu --profile-from-start off)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-probe", action="store_true", help="skip the HBM read probe")
     a = p.parse_args(argv)
     a.warmup = max(a.warmup, 3)
-    if a.steps is not None:
-        a.steps = max(a.steps, 1)
+    a.steps = max(a.steps, 1)
+    a.samples = max(a.samples, MIN_SAMPLES)
     return a
 
 
-def workload(args):
-    N, K, T, dist, outl, ws, xs = WORKLOADS[args.workload]
+def record_specs(args):
+    """(workload name, T) of every record this run times; the first is the headline."""
+    single = (args.workload is not None or args.qtype != "q4g64" or args.route != "auto" or args.op != "linear"
+              or args.t is not None)
+    if single:
+        return [(args.workload or DEFAULT_WORKLOAD, args.t)]
+    return list(DEFAULT_RECORDS)
+
+
+def workload(args, name=None, t=None):
+    name = name if name is not None else (args.workload or DEFAULT_WORKLOAD)
+    t = t if t is not None else args.t
+    N, K, T, dist, outl, ws, xs = WORKLOADS[name]
     if T is None:
-        T = args.t if args.t is not None else 1
-    elif args.t is not None and args.t != T:
-        raise SystemExit(f"workload {args.workload} has fixed T={T}")
+        T = t if t is not None else 1
+    elif t is not None and t != T:
+        raise SystemExit(f"workload {name} has fixed T={T}")
     if xs is None:
         xs = T
-    name = args.workload if WORKLOADS[args.workload][2] is not None else f"{args.workload}_t{T}"
+    wname = name if WORKLOADS[name][2] is not None else f"{name}_t{T}"
     qtype = getattr(args, "qtype", "q4g64")
     if qtype != "q4g64":
         if T > 4 and qtype == "w8g32":
             raise SystemExit(f"{qtype} runs for 1..4 tokens")
-        name = qtype + name[2:]            # q4_6144x5120_t1 -> q5g64_6144x5120_t1
+        wname = qtype + wname[2:]            # q4_6144x5120_t1 -> q5g64_6144x5120_t1
     route = getattr(args, "route", "auto")
     if route != "auto":
         if qtype != "q4g64":
             raise SystemExit(f"--route {route} runs the Q4 format only")
-        name += "_" + route
+        wname += "_" + route
     op = getattr(args, "op", "linear")
     if op == "add":
         if qtype != "q4g64" or route != "auto":
             raise SystemExit("--op add runs the Q4 format on its own route")
-        name += "_add"
-    return dict(name=name, N=N, K=K, T=T, dist=dist, outliers=outl, w_seed=ws, x_seed=xs, qtype=qtype, op=op)
+        wname += "_add"
+    return dict(name=wname, N=N, K=K, T=T, dist=dist, outliers=outl, w_seed=ws, x_seed=xs, qtype=qtype, op=op,
+                route=route)
 
 
 def op_bytes(wl):
@@ -167,17 +191,17 @@ def reduce_max(values, world, device=None):
 
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 100 ms in the background."""
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms in the background;
+    summary() reports the samples inside one window of time.monotonic()."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
-        self.t_start = self.t_stop = None
 
     def start(self):
         try:
@@ -195,24 +219,21 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append((time.monotonic(), line.strip()))
 
-    def mark_start(self):
-        self.t_start = time.monotonic()
-
-    def mark_stop(self):
-        self.t_stop = time.monotonic()
-
     def stop(self):
         if self.proc is None:
-            return None
+            return
         time.sleep(0.15)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        rows = [l for (t, l) in self.lines if self.t_start is not None and self.t_start <= t <= (self.t_stop or t) + 0.1]
-        if not rows:
-            rows = [l for (_, l) in self.lines[-3:]]
+
+    def summary(self, t0, t1):
+        rows = [l for (t, l) in self.lines if t0 <= t <= t1 + 0.1]
+        if not rows:   # a window shorter than the sampling period: the samples around it
+            near = sorted(self.lines, key=lambda e: abs(e[0] - 0.5 * (t0 + t1)))[:2]
+            rows = [l for (_, l) in near]
         sm, mx, reasons = [], [], set()
         for r in rows:
             f = [x.strip() for x in r.split(",")]
@@ -259,18 +280,17 @@ def recorded_traffic(wl_name):
 
 
 # ----------------------------------------------------------------------------- our arm
-def measure_ours(args, wl, rank, world, local):
-    """Times the layer on this rank's GPU.
+def measure_ours(args, wl, rank, world, local, sampler=None, with_e2e=True):
+    """Times one record of the layer on this rank's GPU.
 
-    Steady state (the primary figure): R copies of the weight planes and of X
-    (and R outputs) whose total exceeds 2.5x the L2 size, so every call streams
-    its operands from HBM; one CUDA graph holds R consecutive calls (call i on
-    copy i) and the timed region replays it back to back, with CUDA events on
-    the launching stream around every replay.  ms_per_step = total / calls.
+    R copies of the weight planes, X and Y (R * logical bytes >= 2.5 x L2) rotate
+    call by call.  One CUDA graph holds K = args.steps back-to-back calls (call i on
+    copy i mod R); a sample is a 256 MiB write+read L2 flush, then the graph launch
+    bracketed by CUDA events on the launching stream; S = args.samples samples, all
+    queued without host synchronisation.  Reported per sample: its time / K.
 
-    Cold single call (the linear-benchmark contract's method, reported beside
-    it): before each sample a 256 MiB buffer is written then read back, then
-    events bracket one graph launch of one call; median / min / p95.
+    Cold single call (the linear-benchmark contract's method, reported beside it):
+    the flush, then events around one graph launch of one call; median / min / p95.
     """
     import numpy as np
     import torch
@@ -301,7 +321,7 @@ def measure_ours(args, wl, rank, world, local):
     xs = [x_d] + [x_d.clone() for _ in range(R - 1)]
     ys = [torch.empty((T, N), dtype=torch.bfloat16, device=dev) for _ in range(R)]
     rs = [torch.from_numpy(r.view(np.int16)).to(dev).view(torch.bfloat16) for _ in range(R)] if add else None
-    route_arg = q4lin.ROUTE_TC_FP16 if args.route == "tc_fp16" else q4lin.ROUTE_AUTO
+    route_arg = q4lin.ROUTE_TC_FP16 if wl.get("route") == "tc_fp16" else q4lin.ROUTE_AUTO
     ws_n = q4lin.workspace_bytes(N, K, T, route_arg)
     ws_d = torch.empty(max(ws_n, 256), dtype=torch.uint8, device=dev)
     route = q4lin.select_route(N, K, T) if route_arg == q4lin.ROUTE_AUTO else route_arg
@@ -322,6 +342,7 @@ def measure_ours(args, wl, rank, world, local):
         launches = 2 if pl["main_tiles"] < -(-N // 128) * -(-T // pl["n"]) else 1
 
     def call(i):
+        i %= R
         if add:
             q4lin.linear_add(pls[i][0], scs[i], xs[i], rs[i], y=ys[i], stream=stream)
         elif qtype == "q4g64":
@@ -330,13 +351,21 @@ def measure_ours(args, wl, rank, world, local):
         else:
             q4lin.linear_qtype(qtype, pls[i], scs[i], xs[i], y=ys[i], stream=stream)
 
+    K_steps, S = args.steps, args.samples
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    sink = torch.empty((), dtype=torch.int32, device=dev)
+
+    def flush_l2(i):
+        flush.fill_(i & 0x7FFF)                 # write 256 MiB: evicts L2
+        torch.sum(flush, dim=0, out=sink)       # read it back: no dirty lines left to write back
+
     with torch.cuda.stream(stream):
         for i in range(R):
             call(i)
         torch.cuda.synchronize(dev)
-        g_all = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_all, stream=stream):
-            for i in range(R):
+        g_k = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_k, stream=stream):
+            for i in range(K_steps):
                 call(i)
         g_one = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_one, stream=stream):
@@ -344,12 +373,9 @@ def measure_ours(args, wl, rank, world, local):
         torch.cuda.synchronize(dev)
 
         if args.profile:
-            flush = torch.empty((256 << 20) // 4, dtype=torch.int32, device=dev)
-            sink = torch.empty((), dtype=torch.int32, device=dev)
             for _ in range(args.warmup):
                 g_one.replay()
-            flush.fill_(1)
-            torch.sum(flush, dim=0, out=sink)
+            flush_l2(0)
             torch.cuda.synchronize(dev)
             torch.cuda.profiler.start()
             call(0)
@@ -357,47 +383,45 @@ def measure_ours(args, wl, rank, world, local):
             torch.cuda.profiler.stop()
             return None
 
-        # ---- steady state
-        reps = max(1, -(-args.steps // R))
-        calls = reps * R
-        for _ in range(max(1, -(-args.warmup // R))):
-            g_all.replay()
+        # ---- warm-up: W untimed calls, then one untimed sample, whose length sets the
+        # sample count so the timed region lasts about 0.4 s (the clock sampler reads every
+        # 100 ms): at least args.samples samples
+        for _ in range(args.warmup):
+            g_one.replay()
+        wa, wb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush_l2(1)
+        wa.record(stream)
+        g_k.replay()
+        wb.record(stream)
         torch.cuda.synchronize(dev)
-        cvd = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
-        sampler = ClockSampler(cvd[local].strip() if local < len(cvd) else str(local))
-        sampler.start()
-        t_wait = time.monotonic() + 0.6
-        while time.monotonic() < t_wait:   # keep the GPU busy while the sampler starts
-            g_all.replay()
-            torch.cuda.synchronize(dev)
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-        torch.cuda.synchronize(dev)
-        sampler.mark_start()
-        ev[0].record(stream)
-        for r in range(reps):
-            g_all.replay()
-            ev[r + 1].record(stream)
-        torch.cuda.synchronize(dev)
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-        sampler.mark_stop()
-        clocks = sampler.stop()
-        rep_ms = [ev[r].elapsed_time(ev[r + 1]) for r in range(reps)]
-        total_ms = ev[0].elapsed_time(ev[reps])
-        per_call_us = sorted(m * 1e3 / R for m in rep_ms)
+        sample_ms = max(wa.elapsed_time(wb), 1e-3) + 0.08     # + the flush
+        S = int(min(5000, max(S, -(-400.0 // sample_ms))))
 
-        # ---- cold single call behind a 256 MiB write+read flush (linear-benchmark contract, section 6)
-        flush = torch.empty((256 << 20) // 4, dtype=torch.int32, device=dev)
-        sink = torch.empty((), dtype=torch.int32, device=dev)
+        # ---- timed: S samples of exactly K calls, each behind an L2 flush
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(S)]
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        t0 = time.monotonic()
+        for i in range(S):
+            flush_l2(i)
+            ev[i][0].record(stream)
+            g_k.replay()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        t1 = time.monotonic()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        clocks = sampler.summary(t0, t1) if sampler is not None else None
+        sample_us = sorted(a.elapsed_time(b) * 1e3 / K_steps for a, b in ev)
+
+        # ---- cold single call behind the flush (linear-benchmark contract, section 6)
         n_cold = 200
         ce = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_cold)]
         for i in range(5 + n_cold):
-            flush.fill_(i & 0x7FFF)
-            torch.sum(flush, dim=0, out=sink)
+            flush_l2(i)
             if i >= 5:
                 ce[i - 5][0].record(stream)
             g_one.replay()
@@ -405,15 +429,14 @@ def measure_ours(args, wl, rank, world, local):
                 ce[i - 5][1].record(stream)
         torch.cuda.synchronize(dev)
         cold_us = sorted(a.elapsed_time(b) * 1e3 for a, b in ce)
-        del flush
 
         # ---- end to end through the public call: pinned host X -> device, call, device Y -> pinned host
         e2e = None
-        if not args.no_e2e:
+        if with_e2e:
             x_h = [torch.from_numpy(x.view(np.int16)).pin_memory() for _ in range(2)]
             y_h = [torch.empty((T, N), dtype=torch.int16).pin_memory() for _ in range(2)]
             r_h = [torch.from_numpy(r.view(np.int16)).pin_memory() for _ in range(2)] if add else None
-            n_e2e = min(max(args.steps // 10, 100), 2000)
+            n_e2e = 200
             ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_e2e)]
             for i in range(20 + n_e2e):
                 c = i % R
@@ -429,11 +452,59 @@ def measure_ours(args, wl, rank, world, local):
             torch.cuda.synchronize(dev)
             e2e = dict(us=sorted(a.elapsed_time(b) * 1e3 for a, b in ee), h2d=2 * K * T + (2 * N * T if add else 0),
                        d2h=2 * N * T)
+    del flush
+    return dict(sample_us=sample_us, steps=K_steps, samples=S, copies=R, cold_us=cold_us, clocks=clocks,
+                route=q4lin.ROUTE_NAMES.get(route, str(route)), launches=launches, e2e=e2e,
+                tile=q4lin.tile_plan_full(N, K, T, q4lin.ROUTE_TC_SPLITK if add else route_arg), ws_bytes=ws_n)
 
-    return dict(per_call_us=per_call_us, total_ms=total_ms, calls=calls, copies=R, cold_us=cold_us,
-                clocks=clocks, route=q4lin.ROUTE_NAMES.get(route, str(route)), launches=launches, e2e=e2e,
-                tile=q4lin.tile_plan_full(N, K, T, q4lin.ROUTE_TC_SPLITK if add else route_arg),
-                ws_bytes=ws_n)
+
+def measure_read_probe(local, logical_bytes):
+    """The HBM read probe (q4lin_hbm_read_probe): back-to-back passes over 4 GiB, and
+    back-to-back passes over rotating slices of ``logical_bytes`` (the headline call's
+    bytes; the slices together exceed L2), timed with CUDA events."""
+    import torch
+    from weight_only_bit_q4_gb300 import q4lin
+
+    dev = torch.device("cuda", local)
+    big_n = 4 << 30
+    big = torch.empty(big_n, dtype=torch.uint8, device=dev)
+    big.fill_(1)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    sink = torch.empty(8 * sms, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    out = {}
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            q4lin.hbm_read_probe(big, sink, stream=stream)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(10)]
+        for a, b in ev:
+            a.record(stream)
+            q4lin.hbm_read_probe(big, sink, stream=stream)
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+        out["gbs_4gib"] = round(big_n / (ms * 1e-3) / 1e9, 1)
+        # slices of the headline's size, 48 of them (~800 MB), each launch on the next slice
+        nb = (logical_bytes + 15) // 16 * 16
+        nslice = 48
+        views = [big[i * nb:(i + 1) * nb] for i in range(nslice)]
+        for v in views:
+            q4lin.hbm_read_probe(v, sink, stream=stream)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for rep in range(4):
+            for v in views:
+                q4lin.hbm_read_probe(v, sink, stream=stream)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        us = a.elapsed_time(b) * 1e3 / (4 * nslice)
+        out["bytes_per_launch"] = nb
+        out["us_per_launch"] = round(us, 3)
+        out["gbs_per_launch"] = round(nb / (us * 1e-6) / 1e9, 1)
+    del big
+    out["method"] = ("q4lin_hbm_read_probe: 16-byte non-allocating loads, 4 CTAs of 512 threads per SM; "
+                     "4 GiB: median of 10 launches; per launch: back-to-back launches over 48 rotating slices")
+    return out
 
 
 # ----------------------------------------------------------------------------- oracle (CPU) arms
@@ -488,11 +559,52 @@ def oracle_units(wl, rows):
 
 
 def blas_threads():
+    """(threads, how it was found) of the BLAS numpy calls: the thread count the loaded
+    OpenBLAS reports, else the environment's setting, else the host's core count."""
+    import ctypes
+
+    import numpy as np
+    np.dot(np.ones((64, 64)), np.ones((64, 64)))   # make sure the BLAS library is loaded
+    try:
+        with open("/proc/self/maps") as f:
+            libs = sorted({l.split()[-1] for l in f if "blas" in l.lower() and l.split()[-1].startswith("/")})
+    except OSError:
+        libs = []
+    for path in libs:
+        try:
+            lib = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for sym in ("scipy_openblas_get_num_threads64_", "openblas_get_num_threads64_",
+                    "scipy_openblas_get_num_threads", "openblas_get_num_threads"):
+            fn = getattr(lib, sym, None)
+            if fn is not None:
+                fn.restype = ctypes.c_int
+                return int(fn()), f"{os.path.basename(path)}: {sym}()"
     for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
         v = os.environ.get(var)
         if v and v.isdigit():
-            return int(v)
-    return os.cpu_count() or 1
+            return int(v), var
+    return os.cpu_count() or 1, "os.cpu_count() (BLAS thread count not readable)"
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
 
 
 def cpu_baseline(wl):
@@ -501,8 +613,10 @@ def cpu_baseline(wl):
     med = statistics.median(times)
     b, f = oracle_units(wl, rows)
     value = b / med / 1e9 if small_t(wl) else f / med / 1e12
+    threads, how = blas_threads()
     return {"value": round(value, 4), "unit": "GB/s" if small_t(wl) else "TFLOP/s",
-            "cores": blas_threads(), "kind": "oracle",
+            "cores": threads, "threads_source": how, "cpu_model": cpu_model(), "host_cores": os.cpu_count(),
+            "kind": "oracle",
             "sample": f"FP64 oracle (numpy decode + BLAS matmul) on rows 0..{rows - 1} of the {wl['name']} weight "
                       f"with all {wl['T']} tokens; median of {len(times)} runs; logical units of that sub-problem"}
 
@@ -524,7 +638,8 @@ def reference_arm(args, wl, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(med * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": wl["name"], "N": wl["N"], "K": wl["K"], "T": wl["T"], "qtype": wl["qtype"]},
-        "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": blas_threads(), "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": blas_threads()[0],
+                         "cpu_model": cpu_model(), "kind": "oracle",
                          "sample": f"each step: FP64 oracle on rows 0..{rows - 1} of the weight, all {wl['T']} tokens"},
         "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -533,37 +648,13 @@ def reference_arm(args, wl, rank, world):
 
 
 # ----------------------------------------------------------------------------- main
-def main(argv=None):
-    args = parse_args(argv)
-    rank, world, local = dist_env()
-    wl = workload(args)
-    if args.steps is None:
-        # about a second of GPU time at the expected rate, so the clock sampler sees the timed region
-        us_guess = max(2.0, metrics.model_bytes(wl["N"], wl["K"], wl["T"], wl["qtype"]) / 5e3 / 1e3,
-                       metrics.useful_flops(wl["N"], wl["K"], wl["T"]) / 1.0e15 * 1e6)
-        args.steps = int(min(200000, max(1000, 1.0e6 / us_guess)))
-    if args.impl == "reference":
-        return reference_arm(args, wl, rank, world)
-
-    import torch
-    # NCCL on the GPUs; gloo with CPU tensors where there is no GPU (the multi-rank
-    # host path, exercised by the CPU tests with the measurement stubbed)
-    on_gpu = torch.cuda.is_available()
-    if world > 1:
-        import torch.distributed as dist
-        if on_gpu:
-            torch.cuda.set_device(local)
-            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-        else:
-            dist.init_process_group("gloo")
-    res = measure_ours(args, wl, rank, world, local)
-    if res is None:
-        return 0
-    dev = torch.device("cuda", local) if on_gpu else None
-    mean_us = res["total_ms"] * 1e3 / res["calls"]          # steady state, all calls of the timed region
-    med_rep = statistics.median(res["per_call_us"])         # median over graph replays
-    mean_max, med_max = reduce_max([mean_us, med_rep], world, dev)
+def record_summary(wl, res, peaks, world, dev):
+    """The figures of one timed record (rates are whole-job: all ranks' units over the
+    slowest rank's median sample)."""
     N, K, T = wl["N"], wl["K"], wl["T"]
+    su = res["sample_us"]
+    med, lo, p95 = statistics.median(su), su[0], metrics.percentile(su, 95)
+    med_max, lo_max, p95_max = reduce_max([med, lo, p95], world, dev)
     mb, fl = op_bytes(wl), metrics.useful_flops(N, K, T)
     small = small_t(wl)
     unit = "GB/s" if small else "TFLOP/s"
@@ -571,11 +662,9 @@ def main(argv=None):
     def rate(us):
         return mb / (us * 1e-6) / 1e9 if small else fl / (us * 1e-6) / 1e12
 
-    value = rate(mean_max) * world
-    peaks = load_peaks()
     # roofline of the dominant kernel: algorithmic bytes (FLOPs) per launch / its mean launch duration
     nl = max(1, res["launches"])
-    per_launch_us = mean_max / nl
+    per_launch_us = med_max / nl
     if small:
         roof = {"bound": "hbm", "achieved": round(mb / nl / (per_launch_us * 1e-6) / 1e9, 2),
                 "peak": peaks["hbm_gbs"], "unit": "GB/s"}
@@ -588,44 +677,108 @@ def main(argv=None):
     roof["traffic"] = traffic
     if tkernel:
         roof["traffic_kernel"] = tkernel
-
     cold = res["cold_us"]
     cold_med = statistics.median(cold)
-    e2e = None
-    if res["e2e"]:
-        e = res["e2e"]
-        emed = reduce_max([statistics.median(e["us"])], world, dev)[0]
-        e2e = {"value": round(rate(emed) * world, 3), "unit": unit, "us": round(emed, 3),
-               "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]}
-    if rank != 0:
-        return 0
-    line = {
-        "metric": METRIC, "value": round(value, 3), "unit": unit,
-        "n_gpus": world, "steps": res["calls"], "warmup": args.warmup, "ms_per_step": round(mean_max * 1e-3, 6),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": {"gemv": "f32", "tc_fp16": "fp16xfp16->f32"}.get(res["route"], "bf16xbf16->f32"),
-        "data": "synthetic",
-        "config": {"workload": wl["name"], "N": N, "K": K, "T": T, "qtype": wl["qtype"], "route": res["route"],
-                   "tile": res["tile"],
-                   "timing": f"steady state: CUDA graph of {res['copies']} back-to-back calls replayed, events per replay",
-                   "l2": f"inputs larger than L2: {res['copies']} rotating copies of weights, X and Y "
-                         f"({res['copies'] * mb / 1e6:.0f} MB)",
-                   "parallelism": "replicas" if world > 1 else "single"},
-        "us": {"mean": round(mean_us, 3), "median_replay": round(med_rep, 3),
-               "min_replay": round(res["per_call_us"][0], 3)},
-        "logical_gbs": round(mb / (mean_us * 1e-6) / 1e9, 2),
-        "tflops": round(fl / (mean_us * 1e-6) / 1e12, 3),
+    return {
+        "workload": wl["name"], "N": N, "K": K, "T": T, "qtype": wl["qtype"], "route": res["route"],
+        "tile": res["tile"], "launches_per_step": res["launches"],
+        "steps": res["steps"], "samples": res["samples"],
+        "value": round(rate(med_max) * world, 3), "unit": unit, "ms_per_step": round(med_max * 1e-3, 6),
+        "us": {"median": round(med_max, 3), "min": round(lo_max, 3), "p95": round(p95_max, 3)},
+        "logical_gbs": round(mb / (med_max * 1e-6) / 1e9, 2), "tflops": round(fl / (med_max * 1e-6) / 1e12, 3),
+        "roofline": roof,
         "cold_call": {"method": "256 MiB write+read L2 flush, events around one graph launch of one call",
                       "median_us": round(cold_med, 3), "min_us": round(cold[0], 3),
                       "p95_us": round(metrics.percentile(cold, 95), 3), "samples": len(cold),
                       "value": round(rate(cold_med), 3), "unit": unit},
-        "roofline": roof,
-        "e2e": e2e,
-        "gpu_launches": res["launches"] * res["calls"],
         "clocks": res["clocks"],
+        "gpu_launches": res["launches"] * res["steps"] * res["samples"],
+        "l2": f"{res['copies']} rotating copies of weights, X and Y ({res['copies'] * mb / 1e6:.0f} MB) "
+              f"and a 256 MiB write+read flush before every sample",
     }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    specs = record_specs(args)
+    wls = [workload(args, n, t) for (n, t) in specs]
+    if args.impl == "reference":
+        return reference_arm(args, wls[0], rank, world)
+
+    import torch
+    # NCCL on the GPUs; gloo with CPU tensors where there is no GPU (the multi-rank
+    # host path, exercised by the CPU tests with the measurement stubbed)
+    on_gpu = torch.cuda.is_available()
+    if world > 1:
+        import torch.distributed as dist
+        if on_gpu:
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group("gloo")
+    dev = torch.device("cuda", local) if on_gpu else None
+    cvd = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    sampler = ClockSampler(cvd[local].strip() if local < len(cvd) else str(local)) if on_gpu else None
+    if sampler is not None:
+        sampler.start()
+        time.sleep(0.5)   # let the sampler's first readings arrive
+    peaks = load_peaks()
+    recs = []
+    try:
+        for i, wl in enumerate(wls):
+            res = measure_ours(args, wl, rank, world, local, sampler=sampler,
+                               with_e2e=(i == 0 and not args.no_e2e))
+            if res is None:
+                return 0
+            recs.append((wl, res))
+        probe = None
+        if on_gpu and not args.no_probe and args.workload is None and world == 1:
+            probe = measure_read_probe(local, op_bytes(wls[0]))
+    finally:
+        if sampler is not None:
+            sampler.stop()
+    summaries = [record_summary(wl, res, peaks, world, dev) for wl, res in recs]
+    wl0, res0 = recs[0]
+    head = summaries[0]
+    e2e = None
+    if res0["e2e"]:
+        e = res0["e2e"]
+        emed = reduce_max([statistics.median(e["us"])], world, dev)[0]
+        mb0, fl0 = op_bytes(wl0), metrics.useful_flops(wl0["N"], wl0["K"], wl0["T"])
+        ev = mb0 / (emed * 1e-6) / 1e9 if small_t(wl0) else fl0 / (emed * 1e-6) / 1e12
+        e2e = {"value": round(ev * world, 3), "unit": head["unit"], "us": round(emed, 3),
+               "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
+               "method": "per step: pinned host X -> device, the public call, device Y -> pinned host; "
+                         "events around the three; median of 200"}
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": head["value"], "unit": head["unit"],
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "samples": head["samples"],
+        "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": {"gemv": "f32", "tc_fp16": "fp16xfp16->f32"}.get(head["route"], "bf16xbf16->f32"),
+        "data": "synthetic",
+        "config": {"workload": wl0["name"], "N": wl0["N"], "K": wl0["K"], "T": wl0["T"], "qtype": wl0["qtype"],
+                   "route": head["route"], "tile": head["tile"],
+                   "timing": f"median of {head['samples']} samples; a sample is one CUDA graph of {args.steps} "
+                             f"back-to-back calls behind an L2 flush, events on the launching stream",
+                   "l2": head["l2"],
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "us": head["us"], "logical_gbs": head["logical_gbs"], "tflops": head["tflops"],
+        "cold_call": head["cold_call"],
+        "roofline": head["roofline"],
+        "e2e": e2e,
+        "gpu_launches": head["gpu_launches"],
+        "clocks": head["clocks"],
+        "records": summaries[1:],
+    }
+    if probe is not None:
+        probe["frac_4gib_of_copy"] = round(probe["gbs_4gib"] / peaks["hbm_gbs"], 4)
+        line["hbm_read_probe"] = probe
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl)
+        line["cpu_baseline"] = cpu_baseline(wl0)
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

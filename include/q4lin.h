@@ -52,7 +52,7 @@ typedef enum {
   Q4LIN_ERR_UNSUPPORTED_SHAPE = 2, /* K not a multiple of 8 */
   Q4LIN_ERR_MISALIGNED = 3,        /* a device pointer not 16-byte aligned */
   Q4LIN_ERR_WORKSPACE = 4,         /* workspace NULL while q4lin_workspace_bytes() > 0 */
-  Q4LIN_ERR_DEVICE = 5,            /* current device is not compute capability 10.x (sm_100 family) */
+  Q4LIN_ERR_DEVICE = 5,            /* current device is not compute capability 10.3 (the build targets sm_103a) */
   Q4LIN_ERR_CUDA = 6,              /* a CUDA runtime/driver call or a launch failed */
   Q4LIN_ERR_TIMEOUT = 7            /* a device-side bounded wait expired (see q4lin_device_status) */
 } q4lin_status;
@@ -179,7 +179,8 @@ int q4lin_linear_route(int route, const uint8_t* wq, const uint16_t* scales, con
  *     that loads the library holds on each GPU it uses until it exits.  Shapes whose
  *     2*T*K + 4*T + 4*N bytes (each part rounded up to 256) exceed it return
  *     Q4LIN_ERR_UNSUPPORTED_SHAPE (N = 6144, K = 5120 fits up to T = 1635).
- *   Set-up: the first call on a device looks up the array's device address (one
+ *   Set-up: the first call in each CUDA context (per device, and again after a
+ *     cudaDeviceReset) looks up the array's device address (one
  *     cudaGetSymbolAddress, no allocation); make that first call before any stream
  *     capture on that device.
  *   Sharing: every call uses the same array, so calls that overlap on the GPU (in
@@ -234,6 +235,32 @@ int q4lin_clear_device_status(void);
  * and the CUDA error text, if any); "" if the last call succeeded.  Owned by the library, valid
  * until the next q4lin call on the same thread. */
 const char* q4lin_last_error_detail(void);
+
+/*
+ * Diagnostics (no counterpart in the layer's operation).
+ *
+ * HBM read probe: the pure-read ceiling the linear-benchmark contract (section 4,
+ * theoretical traffic) prefers to a copy for a weight-streaming GEMV.  Reads
+ * `bytes` bytes at `src` (device, 16-byte aligned; bytes a multiple of 16) with
+ * 16-byte non-allocating loads in a grid-stride loop of `blocks` CTAs of 512
+ * threads (blocks <= 0: four per SM), and writes one XOR word per CTA to `sink`
+ * (device, >= blocks words) so the loads cannot be removed.  Asynchronous on
+ * `stream`; the caller times it.  Returns Q4LIN_OK once enqueued,
+ * Q4LIN_ERR_INVALID_ARG / Q4LIN_ERR_MISALIGNED for bad arguments.
+ */
+int q4lin_hbm_read_probe(const void* src, size_t bytes, uint32_t* sink, int blocks, void* stream);
+
+/*
+ * Wait-expiry check: one warp runs the kernels' bounded mbarrier wait, with the
+ * bound `limit` polls (1 .. 2^20; each poll suspends for at most about a
+ * microsecond), on a phase that nothing ever completes.  The wait must expire:
+ * the kernel records Q4LIN_ERR_TIMEOUT in the device error word that
+ * q4lin_device_status() reports, raises its CTA's abort flag and returns.  `out`
+ * (device, one int) receives 1 if the wait succeeded (it cannot) plus 2 if the
+ * abort flag was raised.  Asynchronous on `stream`.  It faults and hangs nothing;
+ * it exists so that tests can check the timeout path on a live GPU.
+ */
+int q4lin_diag_wait_expiry(uint32_t limit, int* out, void* stream);
 
 /* Library version, "major.minor.patch". */
 const char* q4lin_version(void);

@@ -223,3 +223,17 @@ def test_tile_plan_query(lib):
         else:
             assert p["tail_split_k"] == 0 and q4lin.kernel_launches(N, K, T) == 1
     assert q4lin.tile_plan_full(6144, 5120, 1) == {"n": 0, "split_k": 1, "main_tiles": 0, "tail_split_k": 0}
+
+
+def test_diagnostics_host_checks(lib):
+    import ctypes
+    vp = ctypes.c_void_p
+    # null source or sink, size not a multiple of 16: refused before any CUDA call
+    assert lib.q4lin_hbm_read_probe(None, 1024, vp(256), 0, None) == 1
+    assert lib.q4lin_hbm_read_probe(vp(256), 1024, None, 0, None) == 1
+    assert lib.q4lin_hbm_read_probe(vp(256), 1000, vp(256), 0, None) == 1
+    assert lib.q4lin_hbm_read_probe(vp(264), 1024, vp(256), 0, None) == 3
+    # wait-expiry bound outside 1 .. 2^20, or no output word
+    assert lib.q4lin_diag_wait_expiry(0, vp(256), None) == 1
+    assert lib.q4lin_diag_wait_expiry((1 << 20) + 1, vp(256), None) == 1
+    assert lib.q4lin_diag_wait_expiry(100, None, None) == 1

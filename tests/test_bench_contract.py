@@ -9,11 +9,12 @@ import bench
 from weight_only_bit_q4_gb300 import metrics
 
 
-def _fake_measure(args, wl, rank, world, local):
-    return dict(per_call_us=[8.0] * 10, total_ms=0.08, calls=10, copies=8,
-                cold_us=[12.0] * 200, route="gemv", launches=1,
+def _fake_measure(args, wl, rank, world, local, sampler=None, with_e2e=True):
+    us = 8.0 if wl["T"] == 1 else (20.0 if wl["T"] == 8 else 100.0)
+    return dict(sample_us=[us] * 60, steps=args.steps, samples=60, copies=8,
+                cold_us=[12.0] * 200, route="gemv" if wl["T"] == 1 else "tc_splitk", launches=1,
                 clocks={"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 5},
-                e2e=dict(us=[32.0] * 100, h2d=2 * wl["K"] * wl["T"], d2h=2 * wl["N"] * wl["T"]),
+                e2e=dict(us=[32.0] * 100, h2d=2 * wl["K"] * wl["T"], d2h=2 * wl["N"] * wl["T"]) if with_e2e else None,
                 tile={"n": 0, "split_k": 1, "main_tiles": 0, "tail_split_k": 0}, ws_bytes=0)
 
 
@@ -47,11 +48,27 @@ def test_line_carries_every_key(line):
 
 def test_derived_figures(line):
     mb = metrics.model_bytes(6144, 5120, 1)
-    # 10 calls in 0.08 ms: 8 us per call
+    # median sample: 8 us per call
     assert line["ms_per_step"] == pytest.approx(0.008)
+    assert line["steps"] == 10 and line["samples"] >= 50
     assert line["value"] == pytest.approx(mb / 8e-6 / 1e9, rel=1e-3)
     assert line["unit"] == "GB/s" and line["roofline"]["bound"] == "hbm"
     assert line["roofline"]["frac"] == pytest.approx(line["roofline"]["achieved"] / line["roofline"]["peak"], rel=1e-3)
     assert line["e2e"]["value"] == pytest.approx(mb / 32e-6 / 1e9, rel=1e-3)
     assert line["e2e"]["h2d_bytes_per_step"] == 2 * 5120 and line["e2e"]["d2h_bytes_per_step"] == 2 * 6144
-    assert line["gpu_launches"] == 10
+    assert line["gpu_launches"] == 10 * 60
+
+
+def test_secondary_records(line):
+    # the small-T (T = 8) and large-T (T = 1024) records of the same weight, each with its own figures
+    recs = line["records"]
+    assert [r["workload"] for r in recs] == ["q4_6144x5120_t8", "q4_6144x5120_t1024"]
+    r8, r1024 = recs
+    assert r8["unit"] == "GB/s" and r8["roofline"]["bound"] == "hbm"
+    assert r8["value"] == pytest.approx(metrics.model_bytes(6144, 5120, 8) / 20e-6 / 1e9, rel=1e-3)
+    assert r1024["unit"] == "TFLOP/s" and r1024["roofline"]["bound"] == "tensor"
+    assert r1024["value"] == pytest.approx(metrics.useful_flops(6144, 5120, 1024) / 100e-6 / 1e12, rel=1e-3)
+    for r in recs:
+        for k in ("us", "roofline", "cold_call", "clocks", "steps", "samples", "route", "tile"):
+            assert k in r, k
+        assert r["steps"] == 10

@@ -28,9 +28,9 @@ def _rank_main(rank, world, port, outdir, impl):
                       MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     import bench
 
-    def fake_measure(args, wl, rk, wd, local):
+    def fake_measure(args, wl, rk, wd, local, sampler=None, with_e2e=True):
         us = 8.0 + 2.0 * rk
-        return dict(per_call_us=[us] * 10, total_ms=us * 10 / 1e3, calls=10, copies=8, cold_us=[12.0] * 200,
+        return dict(sample_us=[us] * 60, steps=args.steps, samples=60, copies=8, cold_us=[12.0] * 200,
                     route="gemv", launches=1, clocks={"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [],
                                                       "samples": 5},
                     e2e=None, tile={"n": 0, "split_k": 1, "main_tiles": 0, "tail_split_k": 0}, ws_bytes=0)
@@ -38,7 +38,7 @@ def _rank_main(rank, world, port, outdir, impl):
     bench.measure_ours = fake_measure
     buf = io.StringIO()
     with contextlib.redirect_stdout(buf):
-        argv = ["--gpus", str(world), "--steps", "10", "--warmup", "3", "--no-e2e"]
+        argv = ["--gpus", str(world), "--steps", "10", "--warmup", "3", "--no-e2e", "--workload", "q4_6144x5120_t1"]
         if impl == "reference":
             argv += ["--impl", "reference", "--steps", "1", "--workload", "q4_512x1024_t8"]
         rc = bench.main(argv)

@@ -63,5 +63,10 @@ bool tc_supported(int64_t N, int64_t K, int64_t T);
 // Reads (and optionally clears) the device error word of one translation unit.
 int gemv_status(int* value, bool clear);
 int tc_status(int* value, bool clear);
+int probe_status(int* value, bool clear);
+
+// Diagnostics: HBM read probe and the bounded-wait expiry check.
+int hbm_read_probe(const void* src, size_t bytes, uint32_t* sink, int blocks, cudaStream_t stream);
+int wait_expiry(uint32_t limit, int* out, cudaStream_t stream);
 
 }  // namespace q4

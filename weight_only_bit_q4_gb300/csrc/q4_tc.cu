@@ -708,6 +708,21 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current_fn() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(f);
+  });
+  return fn;
+}
+
 bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
                  CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
@@ -1084,26 +1099,42 @@ int tc_fp16_static_launch(const LinearArgs& args) {
                      "exceed its 16 MiB static scratch");
     return Q4LIN_ERR_UNSUPPORTED_SHAPE;
   }
-  // The array's device address, looked up once per device with that device
-  // current (in host code its name is only a stand-in, not a device address).
-  static void* addr[64] = {};
+  // The array's device address, looked up once per CUDA context with that context
+  // current (in host code its name is only a stand-in, not a device address).  The
+  // cache is keyed by the context, not the device ordinal: after cudaDeviceReset, or
+  // under another context on the same device, the address is looked up again.
+  static CUcontext ctx_of[64] = {};
+  static void* addr_of[64] = {};
+  static int n_ctx = 0;
   static std::mutex mu;
-  int dev = 0;
-  if (const int rc = cuda_check(cudaGetDevice(&dev), "cudaGetDevice")) return rc;
-  if (dev < 0 || dev >= 64) {
-    set_error_detail("fp16 route without allocation: device ordinal beyond 63");
-    return Q4LIN_ERR_DEVICE;
+  CUcontext ctx = nullptr;
+  if (CtxGetCurrentFn get = ctx_get_current_fn()) {
+    if (get(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+  }
+  if (ctx == nullptr) {
+    // make the runtime's primary context current, then ask again
+    if (const int rc = cuda_check(cudaFree(nullptr), "cudaFree(nullptr) (context set-up)")) return rc;
+    CtxGetCurrentFn get = ctx_get_current_fn();
+    if (get == nullptr || get(&ctx) != CUDA_SUCCESS || ctx == nullptr) {
+      set_error_detail("fp16 route without allocation: no current CUDA context");
+      return Q4LIN_ERR_CUDA;
+    }
   }
   void* scratch = nullptr;
   {
     std::lock_guard<std::mutex> lock(mu);
-    if (addr[dev] == nullptr) {
+    for (int i = 0; i < n_ctx; ++i)
+      if (ctx_of[i] == ctx) scratch = addr_of[i];
+    if (scratch == nullptr) {
       void* p = nullptr;
       if (const int rc = cuda_check(cudaGetSymbolAddress(&p, g_fp16_scratch), "cudaGetSymbolAddress(scratch)"))
         return rc;
-      addr[dev] = p;
+      // a context seen before whose slot is reused (table full): overwrite round robin
+      const int slot = n_ctx < 64 ? n_ctx++ : (int)(reinterpret_cast<uintptr_t>(ctx) % 64);
+      ctx_of[slot] = ctx;
+      addr_of[slot] = p;
+      scratch = p;
     }
-    scratch = addr[dev];
   }
   LinearArgs a = args;
   a.workspace = scratch;

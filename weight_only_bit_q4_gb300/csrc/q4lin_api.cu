@@ -62,16 +62,28 @@ int validate(const uint8_t* wq, const uint16_t* scales, const uint16_t* x, uint1
   return Q4LIN_OK;
 }
 
+// The library is built for sm_103a only (compute capability 10.3); any other device
+// would fail every launch with "no kernel image", so it is refused up front.
 int check_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return Q4LIN_ERR_CUDA;
   static int cached[128];   // 0 unknown, 1 ok, 2 not supported
-  if (dev >= 0 && dev < 128 && cached[dev] != 0) return cached[dev] == 1 ? Q4LIN_OK : Q4LIN_ERR_DEVICE;
-  int major = 0;
-  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+  if (dev >= 0 && dev < 128 && cached[dev] != 0) {
+    if (cached[dev] == 2) q4::set_error_detail("device is not compute capability 10.3 (the library is built for sm_103a)");
+    return cached[dev] == 1 ? Q4LIN_OK : Q4LIN_ERR_DEVICE;
+  }
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
     return Q4LIN_ERR_CUDA;
-  const int ok = (major == 10) ? 1 : 2;
+  const int ok = (major == 10 && minor == 3) ? 1 : 2;
   if (dev >= 0 && dev < 128) cached[dev] = ok;
+  if (ok != 1) {
+    char msg[160];
+    std::snprintf(msg, sizeof(msg), "device is compute capability %d.%d; the library is built for sm_103a (10.3)",
+                  major, minor);
+    q4::set_error_detail(msg);
+  }
   return ok == 1 ? Q4LIN_OK : Q4LIN_ERR_DEVICE;
 }
 
@@ -289,7 +301,7 @@ const char* q4lin_status_string(int status) {
     case Q4LIN_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (K not a multiple of 8, or a format and shape the decode GEMV cannot plan)";
     case Q4LIN_ERR_MISALIGNED: return "misaligned pointer (16-byte buffers, 256-byte workspace)";
     case Q4LIN_ERR_WORKSPACE: return "workspace required but NULL";
-    case Q4LIN_ERR_DEVICE: return "unsupported device (needs compute capability 10.x)";
+    case Q4LIN_ERR_DEVICE: return "unsupported device (needs compute capability 10.3, sm_103a)";
     case Q4LIN_ERR_CUDA: return "CUDA error";
     case Q4LIN_ERR_TIMEOUT: return "device-side bounded wait expired";
     default: return "unknown status";
@@ -301,6 +313,8 @@ static int read_status(bool clear) {
   if (q4::gemv_status(&v, clear) != Q4LIN_OK) return Q4LIN_ERR_CUDA;
   if (v) worst = v;
   if (q4::tc_status(&v, clear) != Q4LIN_OK) return Q4LIN_ERR_CUDA;
+  if (v) worst = v;
+  if (q4::probe_status(&v, clear) != Q4LIN_OK) return Q4LIN_ERR_CUDA;
   if (v) worst = v;
   return worst;
 }
@@ -315,7 +329,27 @@ int q4lin_clear_device_status(void) {
   return read_status(true) == Q4LIN_ERR_CUDA ? Q4LIN_ERR_CUDA : Q4LIN_OK;
 }
 
-const char* q4lin_version(void) { return "0.1.0"; }
+int q4lin_hbm_read_probe(const void* src, size_t bytes, uint32_t* sink, int blocks, void* stream) {
+  q4::set_error_detail("");
+  if (src == nullptr || sink == nullptr || bytes == 0 || bytes % 16 != 0) return Q4LIN_ERR_INVALID_ARG;
+  if (!aligned16(src) || (reinterpret_cast<uintptr_t>(sink) & 3u) != 0) return Q4LIN_ERR_MISALIGNED;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return Q4LIN_ERR_CUDA;
+  if (blocks <= 0) blocks = 4 * sms;
+  return q4::hbm_read_probe(src, bytes, sink, blocks, static_cast<cudaStream_t>(stream));
+}
+
+int q4lin_diag_wait_expiry(uint32_t limit, int* out, void* stream) {
+  q4::set_error_detail("");
+  if (out == nullptr || limit == 0 || limit > (1u << 20)) return Q4LIN_ERR_INVALID_ARG;
+  const int st = check_device();
+  if (st != Q4LIN_OK) return st;
+  return q4::wait_expiry(limit, out, static_cast<cudaStream_t>(stream));
+}
+
+const char* q4lin_version(void) { return "0.2.0"; }
 
 const char* q4lin_last_error_detail(void) { return q4::g_detail; }
 

@@ -26,7 +26,7 @@ EXPORTS = ("q4lin_workspace_bytes", "q4lin_linear", "q4lin_linear_route", "q4lin
            "q4lin_route_workspace_bytes", "q4lin_select_route", "q4lin_tile_plan", "q4lin_kernel_launches",
            "q4lin_status_string",
            "q4lin_device_status", "q4lin_clear_device_status", "q4lin_last_error_detail",
-           "q4lin_version")
+           "q4lin_hbm_read_probe", "q4lin_diag_wait_expiry", "q4lin_version")
 
 _lib = None
 
@@ -85,6 +85,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q4lin_clear_device_status.restype = ctypes.c_int
     lib.q4lin_last_error_detail.argtypes = []
     lib.q4lin_last_error_detail.restype = ctypes.c_char_p
+    lib.q4lin_hbm_read_probe.argtypes = [vp, sz, vp, ctypes.c_int, vp]
+    lib.q4lin_hbm_read_probe.restype = ctypes.c_int
+    lib.q4lin_diag_wait_expiry.argtypes = [ctypes.c_uint32, vp, vp]
+    lib.q4lin_diag_wait_expiry.restype = ctypes.c_int
     lib.q4lin_version.argtypes = []
     lib.q4lin_version.restype = ctypes.c_char_p
     if path is None:
@@ -255,3 +259,26 @@ def linear_qtype(qtype: str, planes, scales, x, y=None, stream=None):
     if st != OK:
         raise Q4LinError(st)
     return y
+
+
+def hbm_read_probe(buf, sink, blocks: int = 0, stream=None) -> None:
+    """Enqueue one pass of the HBM read probe over ``buf`` (a CUDA tensor, 16-byte
+    aligned, size a multiple of 16 bytes); ``sink`` is an int32 CUDA tensor with at
+    least ``blocks`` (default four per SM) elements."""
+    import torch
+
+    s = (stream or torch.cuda.current_stream(buf.device)).cuda_stream
+    st = int(load().q4lin_hbm_read_probe(_ptr(buf), buf.numel() * buf.element_size(), _ptr(sink), int(blocks),
+                                         ctypes.c_void_p(s)))
+    if st != OK:
+        raise Q4LinError(st, "hbm read probe: ")
+
+
+def diag_wait_expiry(limit: int, out, stream=None) -> None:
+    """Enqueue the wait-expiry check (see q4lin.h); ``out`` is an int32 CUDA tensor."""
+    import torch
+
+    s = (stream or torch.cuda.current_stream(out.device)).cuda_stream
+    st = int(load().q4lin_diag_wait_expiry(int(limit), _ptr(out), ctypes.c_void_p(s)))
+    if st != OK:
+        raise Q4LinError(st, "wait expiry check: ")
