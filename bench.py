@@ -84,10 +84,13 @@ def parse_args(argv=None):
     p.add_argument("--t", type=int, default=None, help="T for the sweep workloads")
     p.add_argument("--qtype", default="q4g64", choices=sorted(metrics.GROUP_BYTES),
                    help="weight format (the sibling formats run for 1..4 tokens)")
-    p.add_argument("--op", default="linear", choices=["linear", "add"],
-                   help="linear: Y = W.X; add: LinearAdd, Y = W.X + R (the tile route for every T)")
-    p.add_argument("--route", default="auto", choices=["auto", "tc_fp16"],
-                   help="auto: the library's choice; tc_fp16: the opt-in tile route on fp16-rounded weights")
+    p.add_argument("--op", default="linear", choices=["linear", "add", "swiglu", "pair"],
+                   help="linear: Y = W.X; add: LinearAdd, Y = W.X + R; swiglu: LinearSwiGLU on the workload's "
+                        "weight as a gate/up pair (F = N / 2); pair: LinearPair, two weights of the workload's "
+                        "shape on one X (the fused forms run the exact tile route for every T)")
+    p.add_argument("--route", default="auto", choices=["auto", "tc_fp16", "gemv", "stream_mma", "tc_splitk"],
+                   help="auto: the library's choice; tc_fp16: the opt-in tile route on fp16-rounded weights; "
+                        "the others force that route (q4lin_linear_route)")
     p.add_argument("--profile", action="store_true",
                    help="one call between cudaProfilerStart/Stop after warm-up and flush (for ncu --profile-from-start off)")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -122,8 +125,6 @@ def workload(args, name=None, t=None):
     wname = name if WORKLOADS[name][2] is not None else f"{name}_t{T}"
     qtype = getattr(args, "qtype", "q4g64")
     if qtype != "q4g64":
-        if T > 4 and qtype == "w8g32":
-            raise SystemExit(f"{qtype} runs for 1..4 tokens")
         wname = qtype + wname[2:]            # q4_6144x5120_t1 -> q5g64_6144x5120_t1
     route = getattr(args, "route", "auto")
     if route != "auto":
@@ -131,18 +132,33 @@ def workload(args, name=None, t=None):
             raise SystemExit(f"--route {route} runs the Q4 format only")
         wname += "_" + route
     op = getattr(args, "op", "linear")
-    if op == "add":
+    if op != "linear":
         if qtype != "q4g64" or route != "auto":
-            raise SystemExit("--op add runs the Q4 format on its own route")
-        wname += "_add"
+            raise SystemExit(f"--op {op} runs the Q4 format on its own route")
+        if op == "swiglu" and N % 2:
+            raise SystemExit("--op swiglu needs an even number of weight rows")
+        wname += "_" + op
     return dict(name=wname, N=N, K=K, T=T, dist=dist, outliers=outl, w_seed=ws, x_seed=xs, qtype=qtype, op=op,
                 route=route)
 
 
 def op_bytes(wl):
-    """Logical bytes of one call: the layer's model bytes, plus the residual read by LinearAdd."""
+    """Logical bytes of one call: the layer's model bytes; LinearAdd reads the residual too,
+    LinearSwiGLU writes F = N / 2 outputs per token, LinearPair reads two weights and writes
+    two outputs."""
     N, K, T = wl["N"], wl["K"], wl["T"]
-    return metrics.model_bytes(N, K, T, wl["qtype"]) + (2 * N * T if wl.get("op") == "add" else 0)
+    op = wl.get("op")
+    if op == "swiglu":
+        return metrics.model_bytes(N, K, T, wl["qtype"]) - 2 * N * T + 2 * (N // 2) * T
+    if op == "pair":
+        return 2 * metrics.model_bytes(N, K, T, wl["qtype"]) - 2 * K * T
+    return metrics.model_bytes(N, K, T, wl["qtype"]) + (2 * N * T if op == "add" else 0)
+
+
+def op_flops(wl):
+    """Useful FLOPs of one call (LinearPair: both weights)."""
+    f = metrics.useful_flops(wl["N"], wl["K"], wl["T"])
+    return 2 * f if wl.get("op") == "pair" else f
 
 
 def format_problem(wl, rows=None):
@@ -309,7 +325,8 @@ def measure_ours(args, wl, rank, world, local, sampler=None, with_e2e=True):
     else:
         planes, sc, x = format_problem(wl)
     per_copy = op_bytes(wl)
-    add = wl.get("op") == "add"
+    op = wl.get("op", "linear")
+    add = op == "add"
     r = synth.activations(T, N, wl["x_seed"] + 7919) if add else None   # LinearAdd's bf16 residual [T, N]
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size or (128 << 20)
     R = int(max(2, min(64, -(-int(2.5 * l2) // per_copy))))
@@ -319,32 +336,52 @@ def measure_ours(args, wl, rank, world, local, sampler=None, with_e2e=True):
     pls = [pl_d] + [tuple(p.clone() for p in pl_d) for _ in range(R - 1)]
     scs = [sc_d] + [sc_d.clone() for _ in range(R - 1)]
     xs = [x_d] + [x_d.clone() for _ in range(R - 1)]
-    ys = [torch.empty((T, N), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    n_out = N // 2 if op == "swiglu" else N
+    ys = [torch.empty((T, n_out), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    if op == "pair":   # the second weight (seed + 1) and its outputs
+        pl_b = torch.from_numpy(synth.packed_codes(N, K, wl["w_seed"] + 1)).to(dev)
+        sc_b = torch.from_numpy(synth.group_scales(N, K, wl["w_seed"] + 1, wl["dist"]).view(np.int16)).to(dev)
+        pls_b = [pl_b] + [pl_b.clone() for _ in range(R - 1)]
+        scs_b = [sc_b] + [sc_b.clone() for _ in range(R - 1)]
+        ys_b = [torch.empty((T, N), dtype=torch.bfloat16, device=dev) for _ in range(R)]
     rs = [torch.from_numpy(r.view(np.int16)).to(dev).view(torch.bfloat16) for _ in range(R)] if add else None
-    route_arg = q4lin.ROUTE_TC_FP16 if wl.get("route") == "tc_fp16" else q4lin.ROUTE_AUTO
+    route_arg = {"tc_fp16": q4lin.ROUTE_TC_FP16, "gemv": q4lin.ROUTE_GEMV, "stream_mma": q4lin.ROUTE_STREAM_MMA,
+                 "tc_splitk": q4lin.ROUTE_TC_SPLITK}.get(wl.get("route"), q4lin.ROUTE_AUTO)
     ws_n = q4lin.workspace_bytes(N, K, T, route_arg)
     ws_d = torch.empty(max(ws_n, 256), dtype=torch.uint8, device=dev)
     route = q4lin.select_route(N, K, T) if route_arg == q4lin.ROUTE_AUTO else route_arg
     launches = q4lin.kernel_launches(N, K, T)
-    if route_arg != q4lin.ROUTE_AUTO:   # operand pass + main launch (+ tail launch)
+    if route_arg == q4lin.ROUTE_TC_FP16:   # operand pass + main launch (+ tail launch)
         pl = q4lin.tile_plan_full(N, K, T, route_arg)
         launches = 1 + (2 if pl["main_tiles"] < -(-N // 128) * -(-T // pl["n"]) else 1)
+    elif route_arg == q4lin.ROUTE_STREAM_MMA:   # operand pass + streaming kernel, per 32 tokens
+        launches = 2 * -(-T // 32)
+    elif route_arg == q4lin.ROUTE_TC_SPLITK:
+        pl = q4lin.tile_plan_full(N, K, T, route_arg)
+        launches = 2 if pl["main_tiles"] < -(-N // 128) * -(-T // pl["n"]) else 1
+    elif route_arg == q4lin.ROUTE_GEMV:
+        launches = 1 if T <= 4 else -(-T // 4)
     stream = torch.cuda.Stream(dev)
 
-    if qtype != "q4g64":   # the streaming GEMV (1..4 tokens), else Q5 / Q6 on the exact tile route
+    if qtype != "q4g64":   # the streaming GEMV (1..4 tokens), else Q5 / Q6 tiles, W8 warp-MMA
         launches = q4lin.kernel_launches(N, K, T, qtype)
-        route = q4lin.ROUTE_GEMV if (T <= 4 and q4lin.select_route(N, K, T) == q4lin.ROUTE_GEMV) \
-            else q4lin.ROUTE_TC_SPLITK
+        route = q4lin.ROUTE_GEMV if launches == 1 else (
+            q4lin.ROUTE_STREAM_MMA if qtype == "w8g32" else q4lin.ROUTE_TC_SPLITK)
 
-    if add:   # the exact tile route for every T: one launch, or two with a tail launch
-        pl = q4lin.tile_plan_full(N, K, T, q4lin.ROUTE_TC_SPLITK)
+    if op != "linear":   # the exact tile route for every T: one launch, or two with a tail launch
+        n_plan = 128 * 2 * -(-N // 128) if op == "pair" else N
+        pl = q4lin.tile_plan_full(n_plan, K, T, q4lin.ROUTE_TC_SPLITK)
         route = q4lin.ROUTE_TC_SPLITK
-        launches = 2 if pl["main_tiles"] < -(-N // 128) * -(-T // pl["n"]) else 1
+        launches = 2 if pl["main_tiles"] < -(-n_plan // 128) * -(-T // pl["n"]) else 1
 
     def call(i):
         i %= R
         if add:
             q4lin.linear_add(pls[i][0], scs[i], xs[i], rs[i], y=ys[i], stream=stream)
+        elif op == "swiglu":
+            q4lin.linear_swiglu(pls[i][0], scs[i], xs[i], y=ys[i], stream=stream)
+        elif op == "pair":
+            q4lin.linear_pair(pls[i][0], scs[i], pls_b[i], scs_b[i], xs[i], y_a=ys[i], y_b=ys_b[i], stream=stream)
         elif qtype == "q4g64":
             q4lin.linear(pls[i][0], scs[i], xs[i], y=ys[i], workspace=ws_d if ws_n else None, stream=stream,
                          route=route_arg)
@@ -434,7 +471,7 @@ def measure_ours(args, wl, rank, world, local, sampler=None, with_e2e=True):
         e2e = None
         if with_e2e:
             x_h = [torch.from_numpy(x.view(np.int16)).pin_memory() for _ in range(2)]
-            y_h = [torch.empty((T, N), dtype=torch.int16).pin_memory() for _ in range(2)]
+            y_h = [torch.empty((T, n_out), dtype=torch.int16).pin_memory() for _ in range(2)]
             r_h = [torch.from_numpy(r.view(np.int16)).pin_memory() for _ in range(2)] if add else None
             n_e2e = 200
             ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_e2e)]
@@ -451,11 +488,11 @@ def measure_ours(args, wl, rank, world, local, sampler=None, with_e2e=True):
                     ee[i - 20][1].record(stream)
             torch.cuda.synchronize(dev)
             e2e = dict(us=sorted(a.elapsed_time(b) * 1e3 for a, b in ee), h2d=2 * K * T + (2 * N * T if add else 0),
-                       d2h=2 * N * T)
+                       d2h=2 * n_out * T)
     del flush
     return dict(sample_us=sample_us, steps=K_steps, samples=S, copies=R, cold_us=cold_us, clocks=clocks,
                 route=q4lin.ROUTE_NAMES.get(route, str(route)), launches=launches, e2e=e2e,
-                tile=q4lin.tile_plan_full(N, K, T, q4lin.ROUTE_TC_SPLITK if add else route_arg), ws_bytes=ws_n)
+                tile=(pl if op != "linear" else q4lin.tile_plan_full(N, K, T, route_arg)), ws_bytes=ws_n)
 
 
 def measure_read_probe(local, logical_bytes):
@@ -523,21 +560,47 @@ def time_oracle(wl, rows, reps_budget_s, max_reps, exact=False):
     import oracle
 
     N, K, T = wl["N"], wl["K"], wl["T"]
+    op = wl.get("op", "linear")
     if wl["qtype"] == "q4g64":
-        wq = synth.packed_codes(rows, K, wl["w_seed"])   # the first `rows` rows of the same weight stream
-        sc = synth.group_scales(N, K, wl["w_seed"], wl["dist"])[:rows]
         x = synth.activations(T, K, wl["x_seed"], wl["outliers"])
-
-        if wl.get("op") == "add":
-            r = synth.activations(T, N, wl["x_seed"] + 7919)[:, :rows]
+        if op == "swiglu":
+            # the first rows // 2 gate rows and their up rows (rows F .. F + rows // 2 of the weight)
+            h = max(1, rows // 2)
+            F = N // 2
+            full_wq = synth.packed_codes(N, K, wl["w_seed"])
+            full_sc = synth.group_scales(N, K, wl["w_seed"], wl["dist"])
+            wq = np.concatenate([full_wq[:h], full_wq[F:F + h]])
+            sc = np.concatenate([full_sc[:h], full_sc[F:F + h]])
 
             def run():
-                return oracle.fused_ops.linear_add(wq, sc, x, r)
+                return oracle.fused_ops.linear_swiglu(wq, sc, x)
+            out_cols = h
+        elif op == "pair":
+            h = max(1, rows // 2)
+            wa = synth.packed_codes(h, K, wl["w_seed"])
+            sa = synth.group_scales(N, K, wl["w_seed"], wl["dist"])[:h]
+            wb = synth.packed_codes(h, K, wl["w_seed"] + 1)
+            sb = synth.group_scales(N, K, wl["w_seed"] + 1, wl["dist"])[:h]
+
+            def run():
+                ya, yb = oracle.fused_ops.linear_pair(wa, sa, wb, sb, x)
+                return np.concatenate([ya, yb], axis=1)
+            out_cols = 2 * h
         else:
-            def run():
-                return oracle.linear(wq, sc, x)
+            wq = synth.packed_codes(rows, K, wl["w_seed"])   # the first `rows` rows of the same weight stream
+            sc = synth.group_scales(N, K, wl["w_seed"], wl["dist"])[:rows]
+            out_cols = rows
+            if op == "add":
+                r = synth.activations(T, N, wl["x_seed"] + 7919)[:, :rows]
+
+                def run():
+                    return oracle.fused_ops.linear_add(wq, sc, x, r)
+            else:
+                def run():
+                    return oracle.linear(wq, sc, x)
     else:
         planes, sc, x = format_problem(wl, rows)
+        out_cols = rows
 
         def run():
             return oracle.sibling_formats.linear(wl["qtype"], planes, sc, x)
@@ -547,15 +610,21 @@ def time_oracle(wl, rows, reps_budget_s, max_reps, exact=False):
         t0 = time.perf_counter()
         y = run()
         times.append(time.perf_counter() - t0)
-        assert y.shape == (T, rows) and np.isfinite(y).all()
+        assert y.shape == (T, out_cols) and np.isfinite(y).all()
     return times
 
 
 def oracle_units(wl, rows):
+    """Logical bytes and useful FLOPs of the oracle's sub-problem (rows weight rows; the fused
+    forms: rows // 2 gate + up rows, or rows // 2 rows of each of the two weights)."""
     K, T = wl["K"], wl["T"]
-    b = metrics.model_bytes(rows, K, T, wl["qtype"]) + (2 * rows * T if wl.get("op") == "add" else 0)
-    f = metrics.useful_flops(rows, K, T)
-    return b, f
+    op = wl.get("op", "linear")
+    if op in ("swiglu", "pair"):
+        h = max(1, rows // 2)
+        sub = dict(wl, N=2 * h if op == "swiglu" else h)
+        return op_bytes(sub), op_flops(sub)
+    b = metrics.model_bytes(rows, K, T, wl["qtype"]) + (2 * rows * T if op == "add" else 0)
+    return b, metrics.useful_flops(rows, K, T)
 
 
 def blas_threads():
@@ -655,7 +724,7 @@ def record_summary(wl, res, peaks, world, dev):
     su = res["sample_us"]
     med, lo, p95 = statistics.median(su), su[0], metrics.percentile(su, 95)
     med_max, lo_max, p95_max = reduce_max([med, lo, p95], world, dev)
-    mb, fl = op_bytes(wl), metrics.useful_flops(N, K, T)
+    mb, fl = op_bytes(wl), op_flops(wl)
     small = small_t(wl)
     unit = "GB/s" if small else "TFLOP/s"
 
@@ -745,7 +814,7 @@ def main(argv=None):
     if res0["e2e"]:
         e = res0["e2e"]
         emed = reduce_max([statistics.median(e["us"])], world, dev)[0]
-        mb0, fl0 = op_bytes(wl0), metrics.useful_flops(wl0["N"], wl0["K"], wl0["T"])
+        mb0, fl0 = op_bytes(wl0), op_flops(wl0)
         ev = mb0 / (emed * 1e-6) / 1e9 if small_t(wl0) else fl0 / (emed * 1e-6) / 1e12
         e2e = {"value": round(ev * world, 3), "unit": head["unit"], "us": round(emed, 3),
                "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
@@ -758,7 +827,8 @@ def main(argv=None):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "samples": head["samples"],
         "ms_per_step": head["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": {"gemv": "f32", "tc_fp16": "fp16xfp16->f32"}.get(head["route"], "bf16xbf16->f32"),
+        "dtype": {"gemv": "f32", "tc_fp16": "fp16xfp16->f32",
+                  "stream_mma": "fp16xfp16->f32 (exact operands)"}.get(head["route"], "bf16xbf16->f32"),
         "data": "synthetic",
         "config": {"workload": wl0["name"], "N": wl0["N"], "K": wl0["K"], "T": wl0["T"], "qtype": wl0["qtype"],
                    "route": head["route"], "tile": head["tile"],

@@ -64,7 +64,10 @@ typedef enum {
   Q4LIN_ROUTE_TC_SPLITK = 2,/* tcgen05 tile, K split across a thread-block cluster where the
                                planner finds it pays (what q4lin_linear uses from 5 tokens) */
   Q4LIN_ROUTE_TC = 3,       /* tcgen05 tile, whole K per CTA */
-  Q4LIN_ROUTE_TC_FP16 = 4   /* opt-in: tcgen05 tile on fp16-rounded weights (see below) */
+  Q4LIN_ROUTE_TC_FP16 = 4,  /* opt-in: tcgen05 tile on fp16-rounded weights (see below) */
+  Q4LIN_ROUTE_STREAM_MMA = 5/* streaming warp-MMA: weights streamed once by TMA, decoded in
+                               registers to exact fp16 operands, reduced by mma.sync; X
+                               converted by an operand pass (workspace); passes of 32 tokens */
 } q4lin_route;
 
 /*
@@ -134,12 +137,18 @@ typedef enum {
  * other formats run on the decode GEMV for 1..4 tokens where its shared-memory
  * plan fits.  Other shapes of Q5G64 and Q6G64 run on the exact tile route
  * (token tiles up to 128 wide; the high-bit plane is staged beside the codes), and
- * other shapes of W8G32 return Q4LIN_ERR_UNSUPPORTED_SHAPE.  They take no
- * workspace (the pointer may be NULL).
+ * other shapes of W8G32 on the streaming warp-MMA route (passes of 32 tokens), whose
+ * operand pass needs workspace: q4lin_qtype_workspace_bytes (256-byte aligned, NULL
+ * allowed where that is 0).  W8G32 shapes no route can plan return
+ * Q4LIN_ERR_UNSUPPORTED_SHAPE.
  */
 int q4lin_linear_qtype(int qtype, const uint8_t* codes, const uint8_t* high, const uint16_t* scales,
                        const uint16_t* x, uint16_t* y, int64_t N, int64_t K, int64_t T, void* workspace,
                        void* stream);
+
+/* Workspace bytes q4lin_linear_qtype needs for this format and shape (0: none; a
+ * multiple of 256; 0 for invalid sizes or an unknown format). */
+size_t q4lin_qtype_workspace_bytes(int qtype, int64_t N, int64_t K, int64_t T);
 
 /*
  * LinearAdd (a fused operation the linear-benchmark page names and leaves to its
@@ -152,6 +161,36 @@ int q4lin_linear_qtype(int qtype, const uint8_t* codes, const uint8_t* high, con
  */
 int q4lin_linear_add(const uint8_t* wq, const uint16_t* scales, const uint16_t* x, const uint16_t* r, uint16_t* y,
                      int64_t N, int64_t K, int64_t T, void* stream);
+
+/*
+ * LinearSwiGLU (a fused operation the linear-benchmark page names and leaves to its
+ * own benchmark; the reading here): one packed weight of 2F rows -- rows [0, F) the
+ * gate projection, rows [F, 2F) the up projection (the MLP gate/up parent of the
+ * page's model suites, 34816 = 2 x 17408 rows) -- applied to x, and
+ *   y[t*F + f] = bf16( silu(g) * u ),  g = (W x)[t, f],  u = (W x)[t, F + f],
+ *   silu(z) = z / (1 + e^-z), all in FP32 before the one bf16 rounding.
+ *   wq        device, uint8 [2F, Kp/2]; scales device, fp16 [2F, Kp/64]
+ *   x         device, bf16 [T, K];     y device, bf16 [T, F] (output)
+ * Runs the exact tile route for every T: a tile stacks 64 gate rows over the matching
+ * 64 up rows, and the product is formed in the epilogue.  No workspace.  Alignment,
+ * sizes and errors as q4lin_linear (with N = 2F).  K = 0 gives y = +0.
+ */
+int q4lin_linear_swiglu(const uint8_t* wq, const uint16_t* scales, const uint16_t* x, uint16_t* y, int64_t F,
+                        int64_t K, int64_t T, void* stream);
+
+/*
+ * LinearPair (a fused operation the linear-benchmark page names; the reading here):
+ * two packed weights applied to the same x in one call, y_a = W_a x and y_b = W_b x.
+ *   wq_a / scales_a  [N_a, Kp/2] / [N_a, Kp/64];  wq_b / scales_b  [N_b, Kp/2] / [N_b, Kp/64]
+ *   x  bf16 [T, K];  y_a  bf16 [T, N_a];  y_b  bf16 [T, N_b] (outputs, must not overlap)
+ * Runs the exact tile route for every T in one launch (plus a tail launch where the
+ * planner splits the last wave): the row tiles of W_a are followed by those of W_b,
+ * and both read the same X tiles.  No workspace.  Alignment and errors as q4lin_linear;
+ * N_a or N_b may be 0 (that output is not touched).  K = 0 gives zeros.
+ */
+int q4lin_linear_pair(const uint8_t* wq_a, const uint16_t* scales_a, const uint8_t* wq_b, const uint16_t* scales_b,
+                      const uint16_t* x, uint16_t* y_a, uint16_t* y_b, int64_t N_a, int64_t N_b, int64_t K, int64_t T,
+                      void* stream);
 
 /*
  * Kernels one q4lin_linear_qtype call of this format and shape launches (0 for a

@@ -114,7 +114,11 @@ def test_qtype_launch_counts_on_host(lib):
     assert q4lin.kernel_launches(64, 100, 8, "q5g64") == 0            # K % 8 != 0
     assert q4lin.kernel_launches(0, 256, 8, "q6g64") == 0             # empty
     assert q4lin.kernel_launches(64, 0, 8, "q6g64") == 1              # the zero fill
-    assert q4lin.kernel_launches(6144, 5120, 1024, "w8g32") == 0      # W8 beyond the GEMV: refused
+    # W8 beyond the GEMV: the warp-MMA route, an operand pass and a kernel per 32 tokens
+    assert q4lin.kernel_launches(6144, 5120, 1024, "w8g32") == 64
+    assert lib.q4lin_qtype_workspace_bytes(3, 6144, 5120, 1024) > 0
+    assert lib.q4lin_qtype_workspace_bytes(3, 6144, 5120, 1) == 0   # the decode GEMV
+    assert lib.q4lin_qtype_workspace_bytes(1, 6144, 5120, 1024) == 0  # Q5: the exact tile route
     for q in ("q5g64", "q6g64"):                                      # the tile route (one wave or a tail)
         assert q4lin.kernel_launches(6144, 5120, 1024, q) in (1, 2)
 
@@ -142,7 +146,12 @@ def test_workspace_query_and_route_selection(lib):
     for N, K, T in [(6144, 5120, 1), (6144, 5120, 16), (6144, 5120, 1024), (512, 1024, 8)]:
         ws = q4lin.workspace_bytes(N, K, T)
         assert ws % 256 == 0
-        assert q4lin.select_route(N, K, T) in (1, 2, 3)
+        assert q4lin.select_route(N, K, T) in (1, 2, 3, 5)
+    # 2..24 tokens: the streaming warp-MMA route, whose operand pass needs workspace
+    for T in (2, 8, 16, 24):
+        assert q4lin.select_route(6144, 5120, T) == q4lin.ROUTE_STREAM_MMA
+        assert q4lin.workspace_bytes(6144, 5120, T) > 0
+    assert q4lin.select_route(6144, 5120, 25) == q4lin.ROUTE_TC_SPLITK
     assert q4lin.workspace_bytes(-1, 128, 1) == 0
     assert q4lin.workspace_bytes(4, 100, 1) == 0
     assert q4lin.workspace_bytes(0, 128, 1) == 0
@@ -154,7 +163,8 @@ def test_fp16_tile_route_workspace_checked_on_host(lib):
     # the opt-in fp16 route refuses a NULL or misaligned workspace before any CUDA call
     assert _call(64, 256, 8, route=q4lin.ROUTE_TC_FP16) == 4
     assert _call(64, 256, 8, ws=16 + 128, route=q4lin.ROUTE_TC_FP16) == 3
-    assert _call(64, 256, 8, route=5) == 1
+    assert _call(64, 256, 8, route=q4lin.ROUTE_STREAM_MMA) == 4   # its operand pass needs workspace
+    assert _call(64, 256, 8, route=6) == 1
 
 
 def test_static_scratch_entry_host_checks(lib):
@@ -175,7 +185,7 @@ def test_fp16_tile_route_workspace(lib):
     for N, K, T in [(6144, 5120, 1024), (1000, 1152, 37), (77, 72, 5)]:
         want = r256(2 * T * K) + r256(4 * T) + r256(4 * N)
         assert q4lin.workspace_bytes(N, K, T, q4lin.ROUTE_TC_FP16) == want
-        for r in (q4lin.ROUTE_AUTO, q4lin.ROUTE_TC, q4lin.ROUTE_TC_SPLITK, q4lin.ROUTE_GEMV):
+        for r in (q4lin.ROUTE_TC, q4lin.ROUTE_TC_SPLITK, q4lin.ROUTE_GEMV):
             assert q4lin.workspace_bytes(N, K, T, r) == 0
     # it plans like the split route (clusters along K allowed)
     assert q4lin.tile_plan(1024, 65536, 16, q4lin.ROUTE_TC_FP16)[1] > 1
@@ -197,13 +207,14 @@ def test_tile_plan_query(lib):
     assert q4lin.tile_plan(6144, 5120, 64, q4lin.ROUTE_GEMV) == (0, 1)
     assert q4lin.tile_plan(6144, 5120, 0) == (0, 1)                      # empty problem
     for T, widths in ((8, {16}), (24, {32}), (48, {64}), (100, {128}), (1024, {128, 256})):
-        bn, sk = q4lin.tile_plan(6144, 5120, T)
+        bn, sk = q4lin.tile_plan(6144, 5120, T, q4lin.ROUTE_TC_SPLITK)
         assert bn in widths and 1 <= sk <= 8, (T, bn, sk)
         bn, sk = q4lin.tile_plan(6144, 5120, T, q4lin.ROUTE_TC)
         assert bn in widths and sk == 1, (T, bn, sk)
     # a deep K with few row tiles is split; a long N that fills the GPU is not
-    assert q4lin.tile_plan(1024, 65536, 16)[1] > 1
-    assert q4lin.tile_plan(65536, 1024, 16)[1] == 1
+    assert q4lin.tile_plan(1024, 65536, 16, q4lin.ROUTE_TC_SPLITK)[1] > 1
+    assert q4lin.tile_plan(65536, 1024, 16, q4lin.ROUTE_TC_SPLITK)[1] == 1
+    assert q4lin.tile_plan(6144, 5120, 8) == (0, 1)   # the streaming warp-MMA route: no tiles
     with pytest.raises(q4lin.Q4LinError):
         q4lin.tile_plan(6144, 100, 8)
     with pytest.raises(q4lin.Q4LinError):
@@ -213,7 +224,7 @@ def test_tile_plan_query(lib):
     sk = ctypes.c_int(0)
     assert lib.q4lin_tile_plan(0, 6144, 5120, 8, ctypes.byref(bn), ctypes.byref(sk), None, None) == 0
     # a tail launch covers exactly the tiles the main launch leaves, split along K
-    for N, K, T in ((6144, 5120, 1024), (5120, 17408, 1024), (34816, 5120, 1024), (6144, 5120, 8)):
+    for N, K, T in ((6144, 5120, 1024), (5120, 17408, 1024), (34816, 5120, 1024), (6144, 5120, 100)):
         p = q4lin.tile_plan_full(N, K, T)
         tiles = -(-N // 128) * -(-T // p["n"])
         assert 0 < p["main_tiles"] <= tiles
@@ -237,3 +248,19 @@ def test_diagnostics_host_checks(lib):
     assert lib.q4lin_diag_wait_expiry(0, vp(256), None) == 1
     assert lib.q4lin_diag_wait_expiry((1 << 20) + 1, vp(256), None) == 1
     assert lib.q4lin_diag_wait_expiry(100, None, None) == 1
+
+
+def test_fused_entry_points_host_checks(lib):
+    vp = ctypes.c_void_p
+    sw, pr = lib.q4lin_linear_swiglu, lib.q4lin_linear_pair
+    a, b = vp(256), vp(512)
+    # null weight, misaligned output, K not a multiple of 8, negative F: refused before any CUDA call
+    assert sw(None, a, a, b, 64, 256, 4, None) == 1
+    assert sw(a, a, a, vp(8), 64, 256, 4, None) == 3
+    assert sw(a, a, a, b, 64, 100, 4, None) == 2
+    assert sw(a, a, a, b, -1, 256, 4, None) == 1
+    assert sw(None, None, None, None, 0, 256, 4, None) == 0     # empty
+    assert pr(a, a, None, a, a, b, b, 64, 64, 256, 4, None) == 1
+    assert pr(a, a, a, a, a, b, vp(8), 64, 64, 256, 4, None) == 3
+    assert pr(a, a, a, a, a, b, b, 64, 64, 100, 4, None) == 2
+    assert pr(None, None, None, None, None, None, None, 0, 0, 256, 4, None) == 0

@@ -70,11 +70,25 @@ def test_q4_through_the_format_entry_is_q4lin_linear():
     assert np.array_equal(y_fmt, y_bits(y))
 
 
-def test_w8_more_than_four_tokens_refused():
+@pytest.mark.parametrize("N,K,T", [(64, 256, 5), (300, 200, 37), (1001, 4096, 130), (640, 4304, 33),
+                                   (77, 17408, 8), (6144, 5120, 24), (257, 1152, 517), (5, 128, 1000),
+                                   (6144, 5120, 1024)])
+def test_w8_beyond_four_tokens_matches_oracle(N, K, T):
+    """W8G32 beyond the decode GEMV: the streaming warp-MMA route (signed codes offset by
+    128 as exact fp16 subnormals, two MMAs per 32-wide group, passes of 32 tokens)."""
+    planes, s, x = synth.make_problem_fmt("w8g32", N, K, T, w_seed=N + 5, x_seed=K + T)
+    assert q4lin.kernel_launches(N, K, T, "w8g32") == 2 * -(-T // 32)
+    assert_close(_run("w8g32", planes, s, x), sf.linear("w8g32", planes, s, x), f"w8g32 {N}x{K} T={T}")
+
+
+def test_w8_beyond_four_tokens_needs_workspace():
+    t = torch()
     planes, s, x = synth.make_problem_fmt("w8g32", 64, 256, 5)
-    with pytest.raises(q4lin.Q4LinError) as e:
-        _run("w8g32", planes, s, x)
-    assert e.value.status == 2
+    y = t.empty((5, 64), dtype=t.bfloat16, device="cuda")
+    d = [_dev(p) for p in planes] + [_dev(s), _dev(x)]
+    st = q4lin.load().q4lin_linear_qtype(3, q4lin._ptr(d[0]), None, q4lin._ptr(d[1]), q4lin._ptr(d[2]),
+                                         q4lin._ptr(y), 64, 256, 5, None, None)
+    assert st == 4  # Q4LIN_ERR_WORKSPACE
 
 
 @pytest.mark.parametrize("qtype", ["q5g64", "q6g64"])

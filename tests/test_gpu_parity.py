@@ -14,7 +14,7 @@ from gpu_util import assert_close, reference, to_dev, torch, weights, x_to_dev, 
 
 pytestmark = pytest.mark.gpu
 
-ROUTES = [q4lin.ROUTE_GEMV, q4lin.ROUTE_TC_SPLITK, q4lin.ROUTE_TC]
+ROUTES = [q4lin.ROUTE_GEMV, q4lin.ROUTE_TC_SPLITK, q4lin.ROUTE_TC, q4lin.ROUTE_STREAM_MMA]
 
 
 def implemented(route):

@@ -96,8 +96,8 @@ def test_bench_format_workloads():
     assert (wl["name"], wl["N"], wl["K"], wl["T"], wl["qtype"]) == ("q5g64_6144x5120_t1", 6144, 5120, 1, "q5g64")
     wl = bench.workload(bench.parse_args(["--qtype", "w8g32", "--workload", "q4_34816x5120", "--t", "4"]))
     assert wl["name"] == "w8g32_34816x5120_t4"
-    with pytest.raises(SystemExit):
-        bench.workload(bench.parse_args(["--qtype", "w8g32", "--workload", "q4_6144x5120", "--t", "8"]))
+    wl8 = bench.workload(bench.parse_args(["--qtype", "w8g32", "--workload", "q4_6144x5120", "--t", "8"]))
+    assert wl8["name"] == "w8g32_6144x5120_t8"     # beyond four tokens: the warp-MMA route
     planes, s, x = bench.format_problem(dict(wl, N=40, K=256, T=2), rows=7)
     assert planes[0].shape == (7, 256) and s.shape == (7, 8) and x.shape == (2, 256)
 

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace q4 {
@@ -22,6 +23,13 @@ struct LinearArgs {
   int fmt = 0;                   // weight format (0: Q4G64; 1: Q5G64, 2: Q6G64, 3: W8G32)
   const uint8_t* wh = nullptr;   // Q5G64 / Q6G64: the high-bit plane
   const uint16_t* r = nullptr;   // LinearAdd: bf16 residual [T, N] (tile route)
+  // fused forms on the exact tile route: 1 = LinearSwiGLU (wq / scales hold 2N rows, gate then
+  // up; y is [T, N]), 2 = LinearPair (a second weight wq_b / scales_b of n_b rows into y_b)
+  int mode = 0;
+  const uint8_t* wq_b = nullptr;
+  const uint16_t* scales_b = nullptr;
+  uint16_t* y_b = nullptr;
+  int64_t n_b = 0;
 };
 
 // The weight planes are stored for K rounded up to a multiple of 128
@@ -59,6 +67,22 @@ int tc_launch_count(int route, int64_t N, int64_t K, int64_t T, int fmt = 0);
 bool tc_fp16_static_fits(int64_t N, int64_t K, int64_t T);
 int tc_fp16_static_launch(const LinearArgs& a);
 bool tc_supported(int64_t N, int64_t K, int64_t T);
+
+// A 2-D tensor map (inner extent, outer extent, row pitch in bytes, box); false if the
+// driver's encoder is unavailable or refuses the arguments.
+bool encode_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
+
+// Streaming warp-MMA route (a few tokens; any T in passes of 32): an operand pass
+// writes X as fp16 MMA fragments into the workspace, then one persistent kernel
+// streams the weights.  Whether it has a shared-memory plan for (N, K, T), its
+// workspace, its launch count and the call.
+// fmt: 0 Q4G64, 3 W8G32
+bool mma_supported(int64_t N, int64_t K, int64_t T, int fmt = 0);
+size_t mma_workspace_bytes(int64_t N, int64_t K, int64_t T, int fmt = 0);
+int mma_launch_count(int64_t N, int64_t K, int64_t T);
+int mma_launch(const LinearArgs& a);
+int mma_status(int* value, bool clear);
 
 // Reads (and optionally clears) the device error word of one translation unit.
 int gemv_status(int* value, bool clear);

@@ -1,0 +1,709 @@
+// Streaming warp-MMA route of the Q4_G64_FP16 linear layer, for a few tokens.
+//
+// Below a few dozen tokens the layer is a stream of packed weights: every weight
+// is read once from HBM and used T times.  The tile route's per-group pipeline
+// (decode team -> tensor memory -> single MMA issuer -> tensor-memory readback)
+// costs several instructions per weight there and leaves most of HBM idle, and
+// CUDA-core FMAs cost T / 2 instructions per weight.  This route keeps the whole
+// inner loop in registers: one AND per weight pair turns the packed nibbles
+// straight into fp16 operands, and the warp-level tensor-core MMA
+// (mma.sync m16n8k16, fp16 x fp16 -> fp32) does the multiply and the reduction
+// along K, so a weight costs about one instruction whatever the token count.
+//
+// Exactness.  A nibble pair masked out of a code word, w & 0x000F000F, is read as
+// two fp16 bit patterns q and q': fp16 subnormals worth q * 2^-24 exactly.  The
+// odd nibbles, w & 0x00F000F0, are 16 q * 2^-24, also exact (at most 240 < 2^10),
+// and meet x / 16 on the other side.  X is converted to fp16 once per call by a
+// prep kernel, taken per token at the power of two 2^-e that puts its largest
+// |x| in [2^14, 2^15) (bf16 -> fp16 is then exact down to 2^-38 of that largest
+// value).  Every product q * x is exact in FP32, so the MMA of one 64-wide group
+// gives D = 2^-24 sum q x, and
+//     sum_k (q - 8) x  =  2^24 D - 8 sum_k x,
+// where the prep kernel has summed -8 sum_k x per group and token.  The group
+// scale multiplies that FP32 partial; the powers of two are undone on the FP32
+// result before the one bf16 rounding.  No product is rounded.
+//
+// Operand layout.  In one m16n8k16 MMA a thread (g = lane / 4, c = lane % 4) holds
+// A elements of rows g and g + 8 at K slots 2c, 2c + 1, 2c + 8, 2c + 9, and B
+// elements of token g at the same K slots.  The K order inside an MMA is free as
+// long as A and B agree, so thread c takes the 8 code bytes [8c, 8c + 8) of a
+// 64-wide group (k = 16c .. 16c + 15) from its two rows and uses the masked
+// nibble pairs as they come: (k, k + 4) pairs of one 32-bit code word.  The prep
+// kernel writes X in exactly that order ("B fragments"), so a thread loads its
+// B operands with two 16-byte shared-memory loads per group and token tile.
+// Rows: mma row g is band row 16 m + 2g and row g + 8 is 16 m + 2g + 1, which makes
+// the 8-byte code loads of a warp conflict-free in the 128-byte-swizzled stage.
+//
+// Work split.  One persistent CTA per SM owns a contiguous range of rows
+// (balanced to one row), cut into bands of at most 240 rows.  For each band the
+// producer warp streams K in chunks: KS code sub-boxes of 256 K values x band
+// rows (TMA, 128-byte swizzle), the chunk's B fragments and zero-point terms
+// (bulk copies from the prep kernel's buffer), into a ring of stages; the band's
+// scale run (contiguous rows of the scale plane) goes into one of two buffers.
+// Consumer warp (m, s) handles m-tile m (16 rows) of sub-box s of every chunk and
+// keeps its FP32 partial sums in registers across the band; at the end of the
+// band the KS partials of each row are summed in a fixed order through shared
+// memory (deterministic) and the band's outputs are rounded to bf16 and stored.
+//
+// Every mbarrier wait is bounded (kSpinLimit): on expiry the kernel records
+// Q4LIN_ERR_TIMEOUT, every role skips its remaining work but still passes the
+// band barriers, and the producer drains the copies it issued before exiting.
+#include "q4_internal.h"
+#include "q4_sm100.cuh"
+
+namespace q4 {
+
+namespace {
+
+__device__ int g_mma_status = 0;
+
+constexpr int kMmaWarps = 16;  // warp 0: producer; warps 1..15: consumers
+constexpr int kMmaThreads = 32 * kMmaWarps;
+constexpr int kMaxConsumers = kMmaWarps - 1;
+constexpr int kMaxBand = 240;  // rows per band: TMA box height <= 256, 15 m-tiles
+constexpr uint32_t kMmaSmem = 232448;  // dynamic shared memory per CTA (incl. 1024-byte alignment slack)
+constexpr int kRedBar = 1;             // named barrier of the consumer warps
+
+struct MmaParams {
+  const uint8_t* wq;       // packed codes [N, Kp/2]
+  const uint16_t* scales;  // fp16 bits [N, Kp/64]
+  const uint8_t* xf;       // B fragments [galloc][NT][2][lanes][16 bytes]
+  const float* zs;         // zero-point terms -8 sum x [galloc][NT][4][2]
+  const int* xe;           // per token of the pass: X was taken as x * 2^-xe[t]
+  uint16_t* y;             // bf16 [T, N]
+  const uint16_t* r;       // LinearAdd: bf16 residual [T, N], added before the bf16 store (may be y)
+  int64_t N, Kp, T;
+  int t0;       // first token of this pass
+  int tp;       // tokens of this pass (<= 8 NT)
+  int nk;       // groups holding columns < K
+  int br;       // band rows (TMA box height, a multiple of 8)
+  int ks;       // code sub-boxes per chunk
+  int mt;       // m-tiles per band
+  int nchunks;  // chunks per band
+  int stages;
+  int lanes;    // B-fragment lanes stored per (group, token tile)
+  uint32_t stage_bytes, xf_off, zs_off;  // stage size; B fragments and zero points inside a stage
+  uint32_t scl_off, scl_bytes;           // the two band scale buffers
+  uint32_t red_off, bar_off;
+};
+
+// Shared-memory layout of one launch.
+struct MmaLayout {
+  uint32_t code_bytes, xf_bytes, zs_bytes, stage_bytes, scl_bytes, red_bytes;
+  uint32_t scl_off, red_off, bar_off, total;
+};
+
+// fbytes: B-fragment bytes per lane per group and token tile (Q4: 32, four MMAs; W8: 16, two)
+__host__ __device__ inline MmaLayout mma_layout(int nt, int br, int ks, int mt, int stages, int lanes, int64_t Kp,
+                                                int fbytes = 32, int64_t srb = 0) {
+  MmaLayout L;
+  L.code_bytes = (uint32_t)(ks * br * 128);  // ks sub-boxes of br rows x 128 bytes (128-byte swizzle)
+  L.xf_bytes = (uint32_t)(4 * ks * nt * lanes * fbytes);
+  L.zs_bytes = (uint32_t)(4 * ks * nt * 32);
+  L.stage_bytes = (L.code_bytes + L.xf_bytes + L.zs_bytes + 1023) / 1024 * 1024;
+  // a band's scale run: br rows of Kp / 64 scales, plus up to 15 bytes of alignment slack
+  // on either side
+  if (srb == 0) srb = Kp / 32;  // bytes of a scale row (Q4: Kp / 64 scales)
+  L.scl_bytes = (uint32_t)((br * srb + 32 + 15) / 16 * 16);
+  L.red_bytes = (uint32_t)(ks * mt * 16 * 8 * nt * 4);
+  L.scl_off = (uint32_t)stages * L.stage_bytes;
+  L.red_off = L.scl_off + 2 * L.scl_bytes;
+  L.bar_off = (L.red_off + L.red_bytes + 15) / 16 * 16;
+  L.total = L.bar_off + (uint32_t)(2 * stages + 4) * 8 + 16;
+  return L;
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ uint2 lds_u64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ float2 lds_f2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint16_t lds_u16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void sts_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+// D = A . B + C, m16n8k16, fp16 operands, fp32 accumulate.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The 16 weights k = 16c .. 16c + 15 of one row of a group (code words w0, w1) as the
+// eight A operand registers of the group's four MMAs: p[2i] holds (q, q') of the
+// even-position nibbles as fp16 subnormal patterns (q * 2^-24), p[2i + 1] the
+// odd-position ones at 16 q * 2^-24.  K order: p[0] = (0, 4), p[1] = (1, 5),
+// p[2] = (2, 6), p[3] = (3, 7), p[4..7] the same for k + 8.
+__device__ __forceinline__ void decode_q4_pairs(uint32_t w0, uint32_t w1, uint32_t (&p)[8]) {
+  const uint32_t v0 = w0 >> 8, v1 = w1 >> 8;
+  p[0] = w0 & 0x000F000Fu;
+  p[1] = w0 & 0x00F000F0u;
+  p[2] = v0 & 0x000F000Fu;
+  p[3] = v0 & 0x00F000F0u;
+  p[4] = w1 & 0x000F000Fu;
+  p[5] = w1 & 0x00F000F0u;
+  p[6] = v1 & 0x000F000Fu;
+  p[7] = v1 & 0x00F000F0u;
+}
+
+// FMT: 0 Q4G64 (64-wide groups, four MMAs per group), 3 W8G32 (32-wide groups of signed
+// bytes, two MMAs per group; the scale plane has Kp / 32 scales per row).
+// W8G32: the 8 signed codes k = 8c .. 8c + 7 of one row of a 32-wide group (words w0, w1) as
+// the four A registers of the group's two MMAs: each code offset to u = code + 128 (the sign
+// bit flipped) and read as the fp16 subnormal u * 2^-24 (u <= 255).  K order: p[0] = (0, 2),
+// p[1] = (1, 3), p[2] = (4, 6), p[3] = (5, 7).
+__device__ __forceinline__ void decode_w8_pairs(uint32_t w0, uint32_t w1, uint32_t (&p)[8]) {
+  const uint32_t u0 = w0 ^ 0x80808080u, u1 = w1 ^ 0x80808080u;
+  p[0] = u0 & 0x00FF00FFu;
+  p[1] = (u0 >> 8) & 0x00FF00FFu;
+  p[2] = u1 & 0x00FF00FFu;
+  p[3] = (u1 >> 8) & 0x00FF00FFu;
+  p[4] = p[5] = p[6] = p[7] = 0u;
+}
+
+template <int NT, int FMT>
+__global__ void __launch_bounds__(kMmaThreads, 1)
+q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const MmaParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  pdl_launch_dependents();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t r0 = (int64_t)blockIdx.x * p.N / gridDim.x;
+  const int64_t r1 = (int64_t)(blockIdx.x + 1) * p.N / gridDim.x;
+  const int BR = p.br, KS = p.ks, NS = p.stages, NCH = p.nchunks;
+  const int WC = KS * p.mt;
+  const int nbands = (int)((r1 - r0 + BR - 1) / BR);
+  constexpr bool kW8 = FMT == 3;
+  constexpr int FB = kW8 ? 16 : 32;                   // B-fragment bytes per lane per group and token tile
+  const int64_t srb = kW8 ? p.Kp / 16 : p.Kp / 32;    // bytes of one row of the scale plane
+  const uint32_t bars = sbase + p.bar_off;
+  auto full = [&](int s) { return bars + 8u * (uint32_t)s; };
+  auto empty = [&](int s) { return bars + 8u * (uint32_t)(NS + s); };
+  const uint32_t sfull0 = bars + 8u * (uint32_t)(2 * NS), sempty0 = sfull0 + 16u;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + p.bar_off + (2 * NS + 4) * 8);
+  auto stage = [&](int s) { return sbase + (uint32_t)s * p.stage_bytes; };
+  auto scl_buf = [&](int b) { return sbase + p.scl_off + (uint32_t)(b & 1) * p.scl_bytes; };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), (uint32_t)WC);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(sfull0 + 8u * b, 1);
+      mbar_init(sempty0 + 8u * b, (uint32_t)WC);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tm_codes);
+  }
+  __syncthreads();
+  // Launch order (programmatic dependent launch): the prep kernel waits for its own
+  // predecessor before it lets this kernel launch, so every kernel before this call has
+  // completed when this one starts, and the weight planes can be streamed at once.
+  // Only what the prep kernel writes (B fragments, zero points, exponents) waits for
+  // griddepcontrol.wait: the producer before its first fragment copy, the consumers
+  // before the first epilogue.
+
+  const uint32_t xf_chunk = (uint32_t)(4 * KS * NT * p.lanes * FB);  // B-fragment bytes per chunk
+  const uint32_t zs_chunk = (uint32_t)(4 * KS * NT * 32);
+  if (warp == 0) {
+    // ------------------------------------------------------------- producer (lane 0 issues)
+    if (lane == 0) {
+      const uint8_t* sc_plane = reinterpret_cast<const uint8_t*>(p.scales);
+      const int64_t plane_bytes = p.N * srb;
+      bool ok = true, waited = false;
+      int it = 0, last_it = -1, last_band = -1, frag_next = 0;
+      auto issue_frags = [&](int q) {  // the B fragments and zero points of iteration q
+        const int gq = (q % NCH) * 4 * KS;
+        const uint32_t sq = stage(q % NS);
+        bulk_g2s(sq + p.xf_off, p.xf + (size_t)gq * NT * p.lanes * FB, xf_chunk, full(q % NS));
+        bulk_g2s(sq + p.zs_off, reinterpret_cast<const uint8_t*>(p.zs) + (size_t)gq * NT * 32, zs_chunk,
+                 full(q % NS));
+      };
+      for (int b = 0; ok && b < nbands; ++b) {
+        const int64_t R0 = r0 + (int64_t)b * BR;
+        const int64_t Re = (R0 + BR < r1) ? R0 + BR : r1;
+        if (b >= 2 && !(ok = mbar_wait(sempty0 + 8u * (b & 1), (uint32_t)(((b - 2) >> 1) & 1), abort_flag,
+                                       &g_mma_status)))
+          break;
+        {
+          // the band's scale run [st, en) of the plane: its 16-byte granules by one bulk copy,
+          // the at most 7 scales past the plane's last full granule by plain loads
+          const int64_t st = R0 * srb, en = Re * srb;
+          const int64_t a = st & ~(int64_t)15;
+          const int64_t e_up = (en + 15) & ~(int64_t)15, e_cap = plane_bytes & ~(int64_t)15;
+          const int64_t e = e_up < e_cap ? e_up : e_cap;
+          const uint32_t dst = scl_buf(b);
+          for (int64_t t = (e > st ? e : st); t < en; t += 2)
+            sts_u16(dst + (uint32_t)(t - a), *reinterpret_cast<const uint16_t*>(sc_plane + t));
+          const uint32_t bytes = e > a ? (uint32_t)(e - a) : 0u;
+          mbar_expect_tx(sfull0 + 8u * (b & 1), bytes);
+          if (bytes > 0) bulk_g2s(dst, sc_plane + a, bytes, sfull0 + 8u * (b & 1));
+          last_band = b;
+        }
+        for (int j = 0; j < NCH; ++j, ++it) {
+          const int s = it % NS;
+          if (it >= NS && !(ok = mbar_wait(empty(s), (uint32_t)(((it / NS) - 1) & 1), abort_flag, &g_mma_status)))
+            break;
+          // sub-boxes holding a group < nk (the consumers skip the others)
+          const int g0 = j * 4 * KS;
+          int nsub = (p.nk - g0 + 3) / 4;
+          nsub = nsub < KS ? nsub : KS;
+          const uint32_t sb = stage(s);
+          mbar_expect_tx(full(s), (uint32_t)(nsub * BR * 128) + xf_chunk + zs_chunk);
+          for (int k = 0; k < nsub; ++k)
+            tma_load_2d(sb + (uint32_t)(k * BR * 128), &tm_codes, full(s), (j * KS + k) * 128, (int32_t)R0);
+          // band 0's first stages carry their code sub-boxes before the wait; every later
+          // wait of the producer (a free stage, a free scale buffer) comes after it
+          if (waited || it == (NS < NCH ? NS : NCH) - 1) {
+            if (!waited) {
+              pdl_wait_previous();
+              waited = true;
+            }
+            for (int q = frag_next; q <= it; ++q) issue_frags(q);
+            frag_next = it + 1;
+          }
+          last_it = it;
+        }
+      }
+      if (!ok) {  // aborted: let every copy already issued land before shared memory is released
+        if (!waited) pdl_wait_previous();
+        for (int q = frag_next; q <= last_it; ++q) issue_frags(q);  // complete the stages missing fragments
+        for (int i = (last_it - NS + 1 > 0 ? last_it - NS + 1 : 0); i <= last_it; ++i)
+          mbar_drain(full(i % NS), (uint32_t)((i / NS) & 1));
+        for (int q = (last_band - 1 > 0 ? last_band - 1 : 0); q <= last_band; ++q)
+          mbar_drain(sfull0 + 8u * (q & 1), (uint32_t)((q >> 1) & 1));
+      }
+    }
+    __syncwarp();
+    return;
+  }
+  if (warp - 1 >= WC) return;
+
+  // ------------------------------------------------------------- consumers
+  const int wc = warp - 1;
+  const int m = wc / KS, sub = wc % KS;
+  const int g = lane >> 2, c = lane & 3;
+  const int ra = 16 * m + 2 * g, rb = ra + 1;  // band rows of mma rows g and g + 8
+  const bool bload = lane < p.lanes;           // this lane's B fragment is stored (the others are zero)
+  const float k2p24 = 16777216.f;  // 2^24
+  int it = 0;
+  bool ok = true;
+  for (int b = 0; b < nbands; ++b) {
+    const int64_t R0 = r0 + (int64_t)b * BR;
+    const int rows = (int)(((R0 + BR < r1) ? R0 + BR : r1) - R0);
+    const bool va = ra < rows, vb = rb < rows;
+    ok = ok && warp_wait(sfull0 + 8u * (b & 1), (uint32_t)((b >> 1) & 1), abort_flag, &g_mma_status);
+    const uint32_t sc0 = scl_buf(b) + (uint32_t)((R0 * srb) & 15);
+    const uint32_t sca = sc0 + (uint32_t)(ra * srb), scb = sc0 + (uint32_t)(rb * srb);
+    float acc[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    for (int j = 0; j < NCH; ++j, ++it) {
+      const int s = it % NS;
+      ok = ok && warp_wait(full(s), (uint32_t)((it / NS) & 1), abort_flag, &g_mma_status);
+      const int gb = j * 4 * KS + 4 * sub;  // first group of this warp's sub-box
+      if (ok && gb < p.nk) {
+        const uint32_t code = stage(s) + (uint32_t)(sub * BR * 128);
+        const uint32_t rowa = code + (uint32_t)(ra * 128), rowb = code + (uint32_t)(rb * 128);
+        const uint32_t xf = stage(s) + p.xf_off + (uint32_t)(4 * sub * NT * p.lanes * FB) + (uint32_t)lane * 16u;
+        const uint32_t zs = stage(s) + p.zs_off + (uint32_t)(4 * sub * NT * 32) + (uint32_t)c * 8u;
+#pragma unroll
+        for (int gl = 0; gl < 4; ++gl) {
+          const int G = gb + gl;
+          if (G >= p.nk) break;
+          // 8 code bytes [8c, 8c + 8) of the group in each row: 16-byte chunk (2 gl + c / 2) of the
+          // 128-byte row, swizzled by the row; rows past the band (zero-filled or the next CTA's)
+          // decode to finite subnormals whose results are never stored
+          const uint32_t ch = (uint32_t)(2 * gl + (c >> 1)), cofs = (uint32_t)((c & 1) << 3);
+          const uint2 wa = lds_u64(rowa + (((ch ^ (uint32_t)(ra & 7)) << 4) | cofs));
+          const uint2 wb = lds_u64(rowb + (((ch ^ (uint32_t)(rb & 7)) << 4) | cofs));
+          uint32_t pa[8], pb[8];
+          if constexpr (kW8) {
+            decode_w8_pairs(wa.x, wa.y, pa);
+            decode_w8_pairs(wb.x, wb.y, pb);
+          } else {
+            decode_q4_pairs(wa.x, wa.y, pa);
+            decode_q4_pairs(wb.x, wb.y, pb);
+          }
+          const float sa = va ? fp16_bits_to_float(lds_u16(sca + 2u * (uint32_t)G)) : 0.f;
+          const float sbv = vb ? fp16_bits_to_float(lds_u16(scb + 2u * (uint32_t)G)) : 0.f;
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            const uint32_t fa = xf + (uint32_t)((gl * NT + n) * p.lanes * FB);
+            const uint4 b0 = bload ? ld_shared_v4(fa) : make_uint4(0u, 0u, 0u, 0u);
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_16816(d, pa[0], pb[0], pa[1], pb[1], b0.x, b0.y);
+            mma_16816(d, pa[2], pb[2], pa[3], pb[3], b0.z, b0.w);
+            if constexpr (!kW8) {
+              const uint4 b1 = bload ? ld_shared_v4(fa + (uint32_t)(p.lanes * 16)) : make_uint4(0u, 0u, 0u, 0u);
+              mma_16816(d, pa[4], pb[4], pa[5], pb[5], b1.x, b1.y);
+              mma_16816(d, pa[6], pb[6], pa[7], pb[7], b1.z, b1.w);
+            }
+            const float2 z = lds_f2(zs + (uint32_t)((gl * NT + n) * 32));
+            const float2 e01 = ffma2(make_float2(d[0], d[1]), make_float2(k2p24, k2p24), z);
+            const float2 e23 = ffma2(make_float2(d[2], d[3]), make_float2(k2p24, k2p24), z);
+            const float2 a01 = ffma2(make_float2(sa, sa), e01, make_float2(acc[n][0], acc[n][1]));
+            const float2 a23 = ffma2(make_float2(sbv, sbv), e23, make_float2(acc[n][2], acc[n][3]));
+            acc[n][0] = a01.x;
+            acc[n][1] = a01.y;
+            acc[n][2] = a23.x;
+            acc[n][3] = a23.y;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty(s));
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sempty0 + 8u * (b & 1));  // the band's scales are no longer read
+
+    // ---- band end: partial sums of the KS sub-boxes, summed in a fixed order
+    const int TP = 8 * NT, MR = 16 * p.mt;
+    float* red = reinterpret_cast<float*>(smem + p.red_off);
+    if (ok) {
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        const int t = 8 * n + 2 * c;
+        red[((size_t)sub * MR + ra) * TP + t] = acc[n][0];
+        red[((size_t)sub * MR + ra) * TP + t + 1] = acc[n][1];
+        red[((size_t)sub * MR + rb) * TP + t] = acc[n][2];
+        red[((size_t)sub * MR + rb) * TP + t + 1] = acc[n][3];
+      }
+    }
+    named_bar_sync(kRedBar, (uint32_t)(WC * 32));
+    if (b == 0) pdl_wait_previous();  // the exponents are the prep kernel's; every earlier kernel is done
+    if (ok && !*abort_flag) {
+      for (int e = wc * 32 + lane; e < rows * p.tp; e += WC * 32) {
+        const int t = e / rows, rw = e - (e / rows) * rows;
+        float v = 0.f;
+        for (int q = 0; q < KS; ++q) v += red[((size_t)q * MR + rw) * TP + t];
+        v *= exp2i(__ldg(p.xe + t));
+        const int64_t gi = (int64_t)(p.t0 + t) * p.N + R0 + rw;
+        if (p.r != nullptr) v += __uint_as_float((uint32_t)p.r[gi] << 16);
+        p.y[gi] = float_to_bf16_bits(v);
+      }
+    }
+    named_bar_sync(kRedBar, (uint32_t)(WC * 32));  // the partial-sum buffer is free again
+  }
+}
+
+// ----------------------------------------------------------------- operand pass
+// One CTA per token slot of the pass (8 NT of them; slots past the pass's tokens
+// write zeros): the token's largest |x| (compared as bf16 magnitude bits) fixes the
+// power of two 2^-e[t] that puts it in [2^14, 2^15); then every (group, c) pair --
+// the 16 values k = 64 G + 16 c .. + 15 -- becomes the eight fp16x2 B registers of
+// lane 4 (t mod 8) + c in the order the decode produces A, and the group's
+// -8 sum x is reduced over its four c.  Tokens holding Inf or NaN keep e = 0.
+// W8G32 (FMT 3): a group is 32 wide, a (group, c) pair holds the 8 values k = 32 G + 8 c
+// .. + 7 as four fp16x2 registers (no 1/16 halves), and the zero-point term is -128 sum x.
+constexpr int kPrepThreads = 256;
+
+template <int NT, int FMT>
+__global__ void __launch_bounds__(kPrepThreads)
+q4_mma_prep_kernel(const uint16_t* __restrict__ x, uint8_t* __restrict__ xf, float* __restrict__ zs,
+                   int* __restrict__ xe, int64_t K, int tp, int galloc, int lanes) {
+  // Wait for the previous kernel (it may write x, or still read these buffers), and only
+  // then let the streaming kernel launch: it reads the weight planes as soon as it starts.
+  pdl_wait_previous();
+  pdl_launch_dependents();
+  __shared__ uint32_t red[kPrepThreads / 32];
+  const int t = blockIdx.x;  // token slot of the pass
+  const bool live = t < tp;
+  const uint16_t* xr = x + (int64_t)(live ? t : 0) * K;
+  // largest |x| of the token
+  uint32_t m2 = 0;
+  if (live)
+    for (int64_t i = threadIdx.x; i < K / 8; i += kPrepThreads) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr) + i);
+      m2 = __vmaxu2(m2, v.x & 0x7FFF7FFFu);
+      m2 = __vmaxu2(m2, v.y & 0x7FFF7FFFu);
+      m2 = __vmaxu2(m2, v.z & 0x7FFF7FFFu);
+      m2 = __vmaxu2(m2, v.w & 0x7FFF7FFFu);
+    }
+  uint32_t mx = __reduce_max_sync(0xffffffffu, max(m2 & 0xFFFFu, m2 >> 16));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < kPrepThreads / 32; ++w) mx = max(mx, red[w]);
+  const int E = (int)(mx >> 7);  // bf16 biased exponent of the largest |x|
+  const int e = (mx == 0 || E == 255) ? 0 : min(max(E - 141, -100), 100);
+  const float s1 = exp2i(-e), s16 = exp2i(-e - 4);
+  const int n = t / 8, tl = t % 8;
+  const bool stored = (tl * 4) < lanes;  // this token's B lanes exist in the buffer
+  constexpr bool kW8 = FMT == 3;
+  constexpr int kVals = kW8 ? 8 : 16;    // values of one (group, c) pair
+  // every thread runs the same number of iterations (the group sums below shuffle across
+  // the four threads of a group, with the whole warp taking part)
+  for (int base = 0; base < galloc * 4; base += kPrepThreads) {
+    const int idx = base + (int)threadIdx.x;
+    const bool act = idx < galloc * 4;
+    const int G = idx >> 2, c = idx & 3;
+    const int64_t k0 = (int64_t)G * (4 * kVals) + kVals * c;
+    float v[16];
+#pragma unroll
+    for (int h = 0; h < kVals / 8; ++h) {
+      // K is a multiple of 8: each run of 8 columns is either wholly inside or wholly past K
+      const bool in = act && live && k0 + 8 * h < K;
+      const uint4 q = in ? __ldg(reinterpret_cast<const uint4*>(xr + k0 + 8 * h)) : make_uint4(0u, 0u, 0u, 0u);
+      v[8 * h + 0] = bf16lo(q.x); v[8 * h + 1] = bf16hi(q.x);
+      v[8 * h + 2] = bf16lo(q.y); v[8 * h + 3] = bf16hi(q.y);
+      v[8 * h + 4] = bf16lo(q.z); v[8 * h + 5] = bf16hi(q.z);
+      v[8 * h + 6] = bf16lo(q.w); v[8 * h + 7] = bf16hi(q.w);
+    }
+    // x-hat = fp16(x 2^-e) (exact in fp16's normal range); the zero-point term sums the
+    // same fp16 values
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < kVals; ++i) sum += __half2float(__float2half_rn(v[i] * s1));
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    auto pk = [&](int i0, int i1, float sc) -> uint32_t {
+      return (uint32_t)__half_as_ushort(__float2half_rn(v[i0] * sc)) |
+             ((uint32_t)__half_as_ushort(__float2half_rn(v[i1] * sc)) << 16);
+    };
+    if (act && stored) {
+      const int L = tl * 4 + c;
+      if constexpr (kW8) {
+        // registers per MMA kk: (x[k0 + 4kk], x[+2]) then (x[+1], x[+3])
+        uint4* dst = reinterpret_cast<uint4*>(xf + (size_t)(G * NT + n) * lanes * 16);
+        dst[L] = make_uint4(pk(0, 2, s1), pk(1, 3, s1), pk(4, 6, s1), pk(5, 7, s1));
+      } else {
+        // registers per MMA kk: (x[k0 + 2kk'], x[+4]) then (x[+1] / 16, x[+5] / 16), kk' = 0, 1, 4, 5
+        const uint4 h0 = make_uint4(pk(0, 4, s1), pk(1, 5, s16), pk(2, 6, s1), pk(3, 7, s16));
+        const uint4 h1 = make_uint4(pk(8, 12, s1), pk(9, 13, s16), pk(10, 14, s1), pk(11, 15, s16));
+        uint4* dst = reinterpret_cast<uint4*>(xf + ((size_t)(G * NT + n) * 2) * lanes * 16);
+        dst[L] = h0;
+        dst[lanes + L] = h1;
+      }
+    }
+    if (act && c == 0) zs[((size_t)(G * NT + n) * 4 + tl / 2) * 2 + (tl & 1)] = (kW8 ? -128.f : -8.f) * sum;
+  }
+  if (threadIdx.x == 0) xe[t] = e;
+}
+
+// ----------------------------------------------------------------- host side
+struct MmaPlan {
+  int fmt, nt, grid, br, ks, mt, nchunks, stages, lanes, galloc, nk, fbytes;
+  int64_t code_row, srb;  // bytes of one row of the code plane and of the scale plane
+  MmaLayout L;
+};
+
+// Token tiles per pass: T <= 8, 16, 24 or 32; a call with more tokens runs passes of 32.
+int mma_nt(int64_t T) { return T >= 32 ? 4 : (int)((T + 7) / 8); }
+
+// fmt 0: Q4G64; fmt 3: W8G32 (the other formats have no plan here)
+bool mma_plan_for(int64_t N, int64_t K, int64_t T, int sms, MmaPlan* pl, int fmt = 0) {
+  if (N < 1 || K < 8 || T < 1 || (fmt != 0 && fmt != 3)) return false;
+  if (N >= ((int64_t)1 << 31) || K >= ((int64_t)1 << 31)) return false;
+  const bool w8 = fmt == 3;
+  const int64_t Kp = (K + 127) / 128 * 128;
+  pl->fmt = fmt;
+  pl->nk = (int)(w8 ? (K + 31) / 32 : (K + 63) / 64);
+  pl->fbytes = w8 ? 16 : 32;
+  pl->code_row = w8 ? Kp : Kp / 2;
+  pl->srb = w8 ? Kp / 16 : Kp / 32;
+  const int nk = pl->nk;
+  pl->nt = mma_nt(T);
+  const int tpass = (int)(T < 8 * pl->nt ? T : 8 * pl->nt);
+  pl->lanes = (pl->nt == 1 && tpass < 8) ? 4 * tpass : 32;
+  int64_t grid = (N + 7) / 8;  // at least 8 rows per CTA
+  if (grid > sms) grid = sms;
+  pl->grid = (int)grid;
+  const int64_t rows_max = (N + grid - 1) / grid;
+  // band height: at most 240 rows, and low enough that a band's scale run fits a 32 KB
+  // buffer (two of them alternate between bands)
+  int64_t cap = 32768 / pl->srb;
+  cap = cap > kMaxBand ? kMaxBand : cap / 8 * 8;
+  if (cap < 8) return false;
+  const int64_t nbands = (rows_max + cap - 1) / cap;
+  int br = (int)((rows_max + nbands - 1) / nbands);
+  br = (br + 7) / 8 * 8;
+  pl->br = br;
+  pl->mt = (br + 15) / 16;
+  if (pl->mt > kMaxConsumers) return false;
+  // sub-boxes per chunk: as many as the consumer warps allow, fewer if the stages do not fit
+  for (int ks = kMaxConsumers / pl->mt; ks >= 1; --ks) {
+    const int chunk_groups = 4 * ks;
+    const int nchunks = (nk + chunk_groups - 1) / chunk_groups;
+    int stages = 8;
+    for (; stages >= 2; --stages) {
+      const MmaLayout L = mma_layout(pl->nt, br, ks, pl->mt, stages, pl->lanes, Kp, pl->fbytes, pl->srb);
+      if (L.total + 1024 <= kMmaSmem) break;
+    }
+    if (stages < 2) continue;
+    pl->ks = ks;
+    pl->nchunks = nchunks;
+    pl->stages = stages;
+    pl->galloc = nchunks * chunk_groups;
+    pl->L = mma_layout(pl->nt, br, ks, pl->mt, stages, pl->lanes, Kp, pl->fbytes, pl->srb);
+    return true;
+  }
+  return false;
+}
+
+int mma_sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev < 64 && cached[dev]) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (dev < 64) cached[dev] = n;
+  return n;
+}
+
+// Workspace of one pass: B fragments, zero-point terms, exponents (each 256-byte aligned).
+size_t mma_ws_xf(const MmaPlan& pl) { return ((size_t)pl.galloc * pl.nt * pl.lanes * pl.fbytes + 255) / 256 * 256; }
+size_t mma_ws_zs(const MmaPlan& pl) { return ((size_t)pl.galloc * pl.nt * 32 + 255) / 256 * 256; }
+size_t mma_ws_total(const MmaPlan& pl) { return mma_ws_xf(pl) + mma_ws_zs(pl) + 256; }
+
+template <int NT, int FMT>
+int mma_launch_pass(const LinearArgs& a, const MmaPlan& pl, const CUtensorMap& tm, int64_t t0, int tp) {
+  static bool attr[64] = {};
+  int dev = 0;
+  if (cuda_check(cudaGetDevice(&dev), "cudaGetDevice")) return Q4LIN_ERR_CUDA;
+  if (dev >= 64 || !attr[dev]) {
+    if (cuda_check(cudaFuncSetAttribute(q4_mma_kernel<NT, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)kMmaSmem),
+                   "mma: cudaFuncSetAttribute"))
+      return Q4LIN_ERR_CUDA;
+    if (dev < 64) attr[dev] = true;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  uint8_t* xf = ws;
+  float* zs = reinterpret_cast<float*>(ws + mma_ws_xf(pl));
+  int* xe = reinterpret_cast<int*>(ws + mma_ws_xf(pl) + mma_ws_zs(pl));
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(8 * NT), 1, 1);
+    cfg.blockDim = dim3(kPrepThreads, 1, 1);
+    cfg.stream = a.stream;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (cuda_check(cudaLaunchKernelEx(&cfg, q4_mma_prep_kernel<NT, FMT>, a.x + t0 * a.K, xf, zs, xe, a.K, tp,
+                                      pl.galloc, pl.lanes),
+                   "mma: prep kernel launch"))
+      return Q4LIN_ERR_CUDA;
+  }
+  MmaParams p{};
+  p.wq = a.wq;
+  p.scales = a.scales;
+  p.xf = xf;
+  p.zs = zs;
+  p.xe = xe;
+  p.y = a.y;
+  p.r = a.r;
+  p.N = a.N;
+  p.Kp = k_pad(a.K);
+  p.T = a.T;
+  p.t0 = (int)t0;
+  p.tp = tp;
+  p.nk = pl.nk;
+  p.br = pl.br;
+  p.ks = pl.ks;
+  p.mt = pl.mt;
+  p.nchunks = pl.nchunks;
+  p.stages = pl.stages;
+  p.lanes = pl.lanes;
+  p.stage_bytes = pl.L.stage_bytes;
+  p.xf_off = pl.L.code_bytes;
+  p.zs_off = pl.L.code_bytes + pl.L.xf_bytes;
+  p.scl_off = pl.L.scl_off;
+  p.scl_bytes = pl.L.scl_bytes;
+  p.red_off = pl.L.red_off;
+  p.bar_off = pl.L.bar_off;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)pl.grid, 1, 1);
+  cfg.blockDim = dim3(kMmaThreads, 1, 1);
+  cfg.dynamicSmemBytes = kMmaSmem;
+  cfg.stream = a.stream;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cuda_check(cudaLaunchKernelEx(&cfg, q4_mma_kernel<NT, FMT>, tm, p), "mma: kernel launch");
+}
+
+template <int FMT>
+int mma_launch_fmt(const LinearArgs& a, const MmaPlan& pl, const CUtensorMap& tm) {
+  // passes of at most 32 tokens (8 NT each), sharing the workspace in stream order
+  for (int64_t t0 = 0; t0 < a.T; t0 += 8 * pl.nt) {
+    const int tp = (int)((a.T - t0) < 8 * pl.nt ? (a.T - t0) : 8 * pl.nt);
+    int rc;
+    switch (pl.nt) {
+      case 1: rc = mma_launch_pass<1, FMT>(a, pl, tm, t0, tp); break;
+      case 2: rc = mma_launch_pass<2, FMT>(a, pl, tm, t0, tp); break;
+      case 3: rc = mma_launch_pass<3, FMT>(a, pl, tm, t0, tp); break;
+      default: rc = mma_launch_pass<4, FMT>(a, pl, tm, t0, tp); break;
+    }
+    if (rc != Q4LIN_OK) return rc;
+  }
+  return Q4LIN_OK;
+}
+
+}  // namespace
+
+bool mma_supported(int64_t N, int64_t K, int64_t T, int fmt) {
+  MmaPlan pl;
+  return mma_plan_for(N, K, T, mma_sm_count(), &pl, fmt);
+}
+
+size_t mma_workspace_bytes(int64_t N, int64_t K, int64_t T, int fmt) {
+  MmaPlan pl;
+  if (!mma_plan_for(N, K, T, mma_sm_count(), &pl, fmt)) return 0;
+  return mma_ws_total(pl);
+}
+
+int mma_launch_count(int64_t, int64_t, int64_t T) { return 2 * (int)((T + 31) / 32); }
+
+int mma_launch(const LinearArgs& a) {
+  MmaPlan pl;
+  if (!mma_plan_for(a.N, a.K, a.T, mma_sm_count(), &pl, a.fmt)) {
+    set_error_detail("mma: no shared-memory plan for this format and shape");
+    return Q4LIN_ERR_UNSUPPORTED_SHAPE;
+  }
+  CUtensorMap tm;
+  if (!encode_map_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.wq, (uint64_t)pl.code_row, (uint64_t)a.N,
+                     (uint64_t)pl.code_row, 128, (uint32_t)pl.br, CU_TENSOR_MAP_SWIZZLE_128B)) {
+    set_error_detail("mma: cuTensorMapEncodeTiled failed (or is unavailable)");
+    return Q4LIN_ERR_CUDA;
+  }
+  return pl.fmt == 3 ? mma_launch_fmt<3>(a, pl, tm) : mma_launch_fmt<0>(a, pl, tm);
+}
+
+int mma_status(int* value, bool clear) {
+  if (cudaMemcpyFromSymbol(value, g_mma_status, sizeof(int)) != cudaSuccess) return Q4LIN_ERR_CUDA;
+  if (clear) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_mma_status, &zero, sizeof(int)) != cudaSuccess) return Q4LIN_ERR_CUDA;
+  }
+  return Q4LIN_OK;
+}
+
+}  // namespace q4

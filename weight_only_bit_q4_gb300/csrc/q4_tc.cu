@@ -90,7 +90,21 @@ struct TcParams {
   int splitk;  // CTAs of a cluster sharing one output tile along K (1 = no split)
   uint32_t tile_base;  // first output tile of this launch (tiles are numbered m-major)
   uint32_t tiles_m;    // row tiles, ceil(N / 128)
+  // Fused forms of the exact tile route (FMT = 0):
+  //   mode 1, LinearSwiGLU: the weight has 2F rows (gate rows [0, F), up rows [F, 2F)) and a
+  //     tile stacks gate rows [f0, f0 + 64) over up rows [F + f0, F + f0 + 64); y is [T, F],
+  //     y = silu(gate) * up.  N holds F, tiles_m = ceil(F / 64).
+  //   mode 2, LinearPair: row tiles [0, tiles_a) are W_a's (codes tm_codes, scales, y, N),
+  //     the rest W_b's (codes in the high-plane map slot, scales_b, y_b, n_b).
+  int mode;
+  uint32_t tiles_a;
+  const uint16_t* scales_b;
+  uint16_t* y_b;
+  int64_t n_b;
 };
+
+// Named barrier of the accumulate warps for the SwiGLU exchange (after the issue ring and kAccBar).
+constexpr uint32_t kSwiBar = 10;
 
 constexpr int kTileM = 128;
 constexpr int kGroupsPerW = 4;              // code stage: 128 rows x 128 bytes = 4 groups
@@ -211,8 +225,13 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
   // CTAs share a token tile and its X stays in L2.  32-bit arithmetic (the host
   // keeps tile numbers below 2^31): a 64-bit division would be a subroutine call.
   const uint32_t tile = p.tile_base + blockIdx.x;
-  const int64_t m0 = (int64_t)(tile % p.tiles_m) * kTileM;
+  const uint32_t mt = tile % p.tiles_m;
   const int64_t t0 = (int64_t)(tile / p.tiles_m) * BN;
+  // the weight this tile reads: first row (the gate rows' first row for SwiGLU), row count,
+  // and for LinearPair which of the two weights
+  const bool wsel_b = p.mode == 2 && mt >= p.tiles_a;
+  const int64_t m0 = p.mode == 1 ? (int64_t)mt * 64 : (int64_t)(wsel_b ? mt - p.tiles_a : mt) * kTileM;
+  const int64_t n_rows = wsel_b ? p.n_b : p.N;   // rows of this tile's output (SwiGLU: F)
 
   // This CTA's share of the K groups (the whole K without a split).
   const int splitk = p.splitk;
@@ -246,7 +265,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
     fence_mbar_init();
     prefetch_tmap(&tm_codes);
     prefetch_tmap(&tm_x);
-    if constexpr (kHB > 0) prefetch_tmap(&tm_high);
+    if (kHB > 0 || p.mode == 2) prefetch_tmap(&tm_high);
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), L::tmem_cols);
   tc_fence_before();
@@ -280,8 +299,15 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
         const int slot = ws % SW;
         if (!(ok = mbar_wait(c_empty(slot), ((ws / SW) & 1) ^ 1, abort_flag, &g_tc_status))) break;
         mbar_expect_tx(c_full(slot), kWBytes + L::kHBytes);
-        tma_load_2d(sbase + L::c_off + slot * kWBytes, &tm_codes, c_full(slot), (g_begin + ws * kGroupsPerW) * 32,
-                    (int32_t)m0);
+        if (p.mode == 1) {  // SwiGLU: gate rows into tile rows 0..63, up rows into 64..127 (64-row boxes)
+          tma_load_2d(sbase + L::c_off + slot * kWBytes, &tm_codes, c_full(slot), (g_begin + ws * kGroupsPerW) * 32,
+                      (int32_t)m0);
+          tma_load_2d(sbase + L::c_off + slot * kWBytes + kWBytes / 2, &tm_codes, c_full(slot),
+                      (g_begin + ws * kGroupsPerW) * 32, (int32_t)(p.N + m0));
+        } else {
+          tma_load_2d(sbase + L::c_off + slot * kWBytes, wsel_b ? &tm_high : &tm_codes, c_full(slot),
+                      (g_begin + ws * kGroupsPerW) * 32, (int32_t)m0);
+        }
         if constexpr (kHB > 0)  // the stage's high bits: 8 * kHB bytes per group and row
           tma_load_2d(sbase + L::h_off + slot * L::kHBytes, &tm_high, c_full(slot),
                       (g_begin + ws * kGroupsPerW) * 8 * kHB, (int32_t)m0);
@@ -471,8 +497,10 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
 #pragma unroll
     for (int i = 0; i < kCols / 2; ++i) acc[i] = make_float2(0.f, 0.f);
     bool acc_ok = true;
-    const int64_t row = m0 + r_acc;
-    const bool row_ok = row < p.N;
+    // weight row of this tile row (SwiGLU: gate rows then up rows), and whether it is a real row
+    const int64_t row = p.mode == 1 ? (r_acc < 64 ? m0 + r_acc : p.N + m0 + (r_acc - 64)) : m0 + r_acc;
+    const bool row_ok = p.mode == 1 ? (m0 + (r_acc & 63) < p.N) : row < n_rows;
+    const uint16_t* scl = wsel_b ? p.scales_b : p.scales;
     const uint32_t tlane = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(cq * kCols);
     if constexpr (kFold) {
       // The sum over the whole K share is complete once the issuer's final commit has
@@ -502,7 +530,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
     } else {
       // Scales are read as pairs of groups (a row holds K_pad / 64 scales, an even
       // 4-byte boundary); the next pair is fetched as soon as the current one is used.
-      const uint32_t* srow = reinterpret_cast<const uint32_t*>(p.scales + (row_ok ? row : 0) * (p.Kp >> 6));
+      const uint32_t* srow = reinterpret_cast<const uint32_t*>(scl + (row_ok ? row : 0) * (p.Kp >> 6));
       int pcur = g_begin >> 1;
       uint32_t s_cur = row_ok ? __ldg(srow + pcur) : 0u;
       uint32_t s_nxt = (row_ok && 2 * (pcur + 1) < p.nk) ? __ldg(srow + pcur + 1) : 0u;
@@ -600,15 +628,37 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
     }
 
     // ----------------------------------------------------------- epilogue: Y[t, row] = bf16(acc [+ R[t, row]])
-    if (crank == 0 && acc_ok && !*abort_flag && row_ok) {
+    if (p.mode == 1) {
+      // SwiGLU: the up rows (tile rows 64..127) hand their FP32 sums to the gate rows through
+      // shared memory (the pipeline buffers are free: every MMA and copy has completed); the
+      // gate rows store y[t, f] = bf16(silu(g) * u), silu(g) = g / (1 + e^-g) in FP32
+      float* xch = reinterpret_cast<float*>(smem);   // [64 rows][BN tokens]
+      named_bar_sync(kSwiBar, 128 * NACC);            // the split-K partials in these buffers are consumed
+      if (crank == 0 && r_acc >= 64) {
+#pragma unroll
+        for (int j = 0; j < kCols; ++j)
+          xch[(r_acc - 64) * BN + cq * kCols + j] = (j & 1) ? acc[j / 2].y : acc[j / 2].x;
+      }
+      named_bar_sync(kSwiBar, 128 * NACC);
+      if (crank == 0 && acc_ok && !*abort_flag && row_ok && r_acc < 64) {
+#pragma unroll
+        for (int j = 0; j < kCols; ++j) {
+          const int64_t t = t0 + cq * kCols + j;
+          const float gt = (j & 1) ? acc[j / 2].y : acc[j / 2].x;
+          const float up = xch[r_acc * BN + cq * kCols + j];
+          if (t < p.T) p.y[t * p.N + m0 + r_acc] = float_to_bf16_bits(gt / (1.f + expf(-gt)) * up);
+        }
+      }
+    } else if (crank == 0 && acc_ok && !*abort_flag && row_ok) {
+      uint16_t* yo = wsel_b ? p.y_b : p.y;
 #pragma unroll
       for (int j = 0; j < kCols; ++j) {
         const int64_t t = t0 + cq * kCols + j;
         float v = (j & 1) ? acc[j / 2].y : acc[j / 2].x;
         if (t < p.T) {
           // LinearAdd: the residual joins the FP32 sum; read before the store, so R may be Y
-          if (p.r != nullptr) v += __uint_as_float((uint32_t)p.r[t * p.N + row] << 16);
-          p.y[t * p.N + row] = float_to_bf16_bits(v);
+          if (p.r != nullptr) v += __uint_as_float((uint32_t)p.r[t * n_rows + row] << 16);
+          yo[t * n_rows + row] = float_to_bf16_bits(v);
         }
       }
     }
@@ -723,9 +773,10 @@ CtxGetCurrentFn ctx_get_current_fn() {
   return fn;
 }
 
-bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
-                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
-                 CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+}  // namespace
+
+bool encode_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {inner, outer};
@@ -735,6 +786,14 @@ bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint6
   return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
+
+bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                 CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+  return encode_map_2d(m, dt, base, inner, outer, row_bytes, box_inner, box_outer, swizzle);
 }
 
 template <int BN, bool kFold, int FMT = 0>
@@ -801,8 +860,10 @@ int launch_tile(const LinearArgs& a, int splitk, int64_t tile_base, int64_t n_ti
   const int64_t Kp = k_pad(a.K);
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   const void* xsrc = kFold ? static_cast<const void*>(ws) : static_cast<const void*>(a.x);
-  if (!make_map_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.wq, (uint64_t)(Kp / 2), (uint64_t)a.N,
-                   (uint64_t)(Kp / 2), 128, kTileM) ||
+  // SwiGLU: the code plane holds 2N rows and a tile loads 64 gate rows and 64 up rows
+  const uint64_t code_rows = a.mode == 1 ? (uint64_t)(2 * a.N) : (uint64_t)a.N;
+  if (!make_map_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.wq, (uint64_t)(Kp / 2), code_rows,
+                   (uint64_t)(Kp / 2), 128, a.mode == 1 ? kTileM / 2 : kTileM) ||
       !make_map_2d(&tm_x, kFold ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xsrc,
                    (uint64_t)a.K, (uint64_t)a.T, (uint64_t)a.K * 2, 64, BN)) {
     set_error_detail("tc: cuTensorMapEncodeTiled failed (or is unavailable)");
@@ -816,13 +877,23 @@ int launch_tile(const LinearArgs& a, int splitk, int64_t tile_base, int64_t n_ti
       set_error_detail("tc: cuTensorMapEncodeTiled failed for the high-bit plane");
       return Q4LIN_ERR_CUDA;
     }
+  } else if (a.mode == 2) {  // LinearPair: the second weight's code plane in this slot
+    if (!make_map_2d(&tm_high, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.wq_b, (uint64_t)(Kp / 2), (uint64_t)a.n_b,
+                     (uint64_t)(Kp / 2), 128, kTileM)) {
+      set_error_detail("tc: cuTensorMapEncodeTiled failed for the second weight");
+      return Q4LIN_ERR_CUDA;
+    }
   } else {
     tm_high = tm_codes;  // unused
   }
   const int* xe = kFold ? reinterpret_cast<const int*>(ws + fold_ws_xe(a.N, a.K, a.T)) : nullptr;
   const int* rf = kFold ? reinterpret_cast<const int*>(ws + fold_ws_rf(a.N, a.K, a.T)) : nullptr;
+  const uint32_t tiles_a = (uint32_t)((a.N + kTileM - 1) / kTileM);
+  const uint32_t tiles_m = a.mode == 1 ? (uint32_t)((a.N + kTileM / 2 - 1) / (kTileM / 2))
+                         : a.mode == 2 ? tiles_a + (uint32_t)((a.n_b + kTileM - 1) / kTileM)
+                                       : tiles_a;
   const TcParams p{a.scales, a.y, xe, rf, a.r, a.N, Kp, a.T, (int)((a.K + 63) / 64), splitk, (uint32_t)tile_base,
-                   (uint32_t)((a.N + kTileM - 1) / kTileM)};
+                   tiles_m, a.mode, tiles_a, a.scales_b, a.y_b, a.n_b};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)n_tiles, 1, (unsigned)splitk);
   cfg.blockDim = dim3(L::threads, 1, 1);
@@ -1038,7 +1109,15 @@ int tc_launch(const LinearArgs& a, int route) {
     set_error_detail("tc: sibling formats run on the exact tile routes, Q5G64 and Q6G64 only");
     return Q4LIN_ERR_UNSUPPORTED_SHAPE;
   }
-  const TcPlan pl = tc_plan_current_device(route, a.N, a.K, a.T, a.fmt);
+  // rows the tile space covers: SwiGLU 2N (64 + 64 per tile), Pair both weights' row tiles
+  const int64_t n_plan = a.mode == 1 ? 2 * a.N
+                       : a.mode == 2 ? kTileM * ((a.N + kTileM - 1) / kTileM + (a.n_b + kTileM - 1) / kTileM)
+                                     : a.N;
+  if (a.mode != 0 && (a.fmt != 0 || route_folds(route))) {
+    set_error_detail("tc: the fused forms run on the exact Q4 tile route");
+    return Q4LIN_ERR_INVALID_ARG;
+  }
+  const TcPlan pl = tc_plan_current_device(route, n_plan, a.K, a.T, a.fmt);
   const bool fold = route_folds(route);
   auto launch = [&](int splitk, int64_t base, int64_t n) {
     if (a.fmt != 0) {
@@ -1068,7 +1147,7 @@ int tc_launch(const LinearArgs& a, int route) {
       default: return launch_tile<16, false>(a, splitk, base, n);
     }
   };
-  const int64_t tiles = tile_count(a.N, a.T, pl.bn);
+  const int64_t tiles = tile_count(n_plan, a.T, pl.bn);
   int rc = fold ? launch_prep(a) : Q4LIN_OK;
   if (rc == Q4LIN_OK) rc = launch(pl.splitk, 0, pl.main_tiles);
   if (rc == Q4LIN_OK && pl.main_tiles < tiles) rc = launch(pl.tail_splitk, pl.main_tiles, tiles - pl.main_tiles);

@@ -87,13 +87,20 @@ int check_device() {
   return ok == 1 ? Q4LIN_OK : Q4LIN_ERR_DEVICE;
 }
 
+// Tokens at or below which the streaming warp-MMA route is chosen (where it has a plan):
+// measured on 6144 x 5120 against the tile route, 12.5 against 18.1 us at T = 8, 16.5 us
+// at T = 24, level at T = 32.
+constexpr int64_t kMmaMaxT = 24;
+
 int route_for(int64_t N, int64_t K, int64_t T) {
-  // One token: the streaming GEMV.  Two to four: the streaming GEMV where its shared
-  // memory holds their x (measured faster than the tile route there, e.g. 6144 x 5120
-  // T = 4: 16 us against 19 us); otherwise the tile route, whose planner splits K only
-  // where that fills the GPU better.
+  // One token: the streaming CUDA-core GEMV.  Two to kMmaMaxT tokens: the streaming
+  // warp-MMA route (every weight read once and decoded once for all the tokens);
+  // above, the tcgen05 tile route, whose planner splits K only where that fills the
+  // GPU better.  Shapes a route has no plan for fall through to the next one.
+  if (T == 1 && q4::gemv_stream_ok(N, K, T)) return Q4LIN_ROUTE_GEMV;
+  if (T <= kMmaMaxT && q4::mma_supported(N, K, T)) return Q4LIN_ROUTE_STREAM_MMA;
   if (!q4::tc_supported(N, K, T)) return Q4LIN_ROUTE_GEMV;
-  if (T == 1 || (T <= 4 && q4::gemv_stream_ok(N, K, T))) return Q4LIN_ROUTE_GEMV;
+  if (T <= 4 && q4::gemv_stream_ok(N, K, T)) return Q4LIN_ROUTE_GEMV;
   return Q4LIN_ROUTE_TC_SPLITK;
 }
 
@@ -105,6 +112,7 @@ size_t route_ws(int route, int64_t N, int64_t K, int64_t T) {
     case Q4LIN_ROUTE_TC:
     case Q4LIN_ROUTE_TC_SPLITK:
     case Q4LIN_ROUTE_TC_FP16: return round256(q4::tc_workspace_bytes(route, N, K, T));
+    case Q4LIN_ROUTE_STREAM_MMA: return round256(q4::mma_workspace_bytes(N, K, T));
     default: return 0;
   }
 }
@@ -115,7 +123,11 @@ int run_impl(int route, const uint8_t* wq, const uint16_t* scales, const uint16_
   if (st != Q4LIN_OK) return st;
   if (N == 0 || T == 0) return Q4LIN_OK;
   if (route == Q4LIN_ROUTE_AUTO) route = route_for(N, K, T);
-  if (route < Q4LIN_ROUTE_GEMV || route > Q4LIN_ROUTE_TC_FP16) return Q4LIN_ERR_INVALID_ARG;
+  if (route < Q4LIN_ROUTE_GEMV || route > Q4LIN_ROUTE_STREAM_MMA) return Q4LIN_ERR_INVALID_ARG;
+  if (route == Q4LIN_ROUTE_STREAM_MMA && K > 0 && !q4::mma_supported(N, K, T)) {
+    q4::set_error_detail("streaming warp-MMA route: no shared-memory plan for this shape");
+    return Q4LIN_ERR_UNSUPPORTED_SHAPE;
+  }
   const size_t ws = route_ws(route, N, K, T);
   if (ws > 0 && workspace == nullptr) return Q4LIN_ERR_WORKSPACE;
   if (ws > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return Q4LIN_ERR_MISALIGNED;
@@ -129,6 +141,7 @@ int run_impl(int route, const uint8_t* wq, const uint16_t* scales, const uint16_
     case Q4LIN_ROUTE_TC:
     case Q4LIN_ROUTE_TC_SPLITK:
     case Q4LIN_ROUTE_TC_FP16: return q4::tc_launch(a, route);
+    case Q4LIN_ROUTE_STREAM_MMA: return q4::mma_launch(a);
     default: return Q4LIN_ERR_INVALID_ARG;
   }
 }
@@ -136,7 +149,7 @@ int run_impl(int route, const uint8_t* wq, const uint16_t* scales, const uint16_
 // Sibling formats: the same checks as the Q4 layer, plus the high-bit plane for
 // Q5G64 / Q6G64, then the streaming GEMV (1..4 tokens) or UNSUPPORTED_SHAPE.
 int run_qtype_impl(int qtype, const uint8_t* codes, const uint8_t* high, const uint16_t* scales,
-                   const uint16_t* x, uint16_t* y, int64_t N, int64_t K, int64_t T, void* stream) {
+                   const uint16_t* x, uint16_t* y, int64_t N, int64_t K, int64_t T, void* workspace, void* stream) {
   int st = validate(codes, scales, x, y, N, K, T);
   if (st != Q4LIN_OK) return st;
   if (N == 0 || T == 0) return Q4LIN_OK;
@@ -151,9 +164,17 @@ int run_qtype_impl(int qtype, const uint8_t* codes, const uint8_t* high, const u
   a.fmt = qtype;
   a.wh = needs_high ? high : nullptr;
   // The streaming GEMV where it has a plan (1..4 tokens); otherwise Q5 / Q6 run on the
-  // exact tile route (token tiles up to 128 wide), and W8 is refused.
-  if (q4::gemv_stream_ok(N, K, T, qtype) || !needs_high || !q4::tc_supported(N, K, T))
-    return q4::gemv_launch_fmt(a);
+  // exact tile route (token tiles up to 128 wide), and W8 on the streaming warp-MMA route
+  // (passes of 32 tokens; its operand pass needs workspace).
+  if (q4::gemv_stream_ok(N, K, T, qtype)) return q4::gemv_launch_fmt(a);
+  if (qtype == Q4LIN_QTYPE_W8G32 && q4::mma_supported(N, K, T, 3)) {
+    const size_t ws = round256(q4::mma_workspace_bytes(N, K, T, 3));
+    if (ws > 0 && workspace == nullptr) return Q4LIN_ERR_WORKSPACE;
+    if (ws > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return Q4LIN_ERR_MISALIGNED;
+    a.workspace = workspace;
+    return q4::mma_launch(a);
+  }
+  if (!needs_high || !q4::tc_supported(N, K, T)) return q4::gemv_launch_fmt(a);
   return q4::tc_launch(a, Q4LIN_ROUTE_TC_SPLITK);
 }
 
@@ -185,11 +206,12 @@ int q4lin_select_route(int64_t N, int64_t K, int64_t T) { return route_for(N, K,
 int q4lin_tile_plan(int route, int64_t N, int64_t K, int64_t T, int* tile_n, int* split_k, int64_t* main_tiles,
                     int* tail_split_k) {
   if (tile_n == nullptr || split_k == nullptr) return Q4LIN_ERR_INVALID_ARG;
-  if (route < Q4LIN_ROUTE_AUTO || route > Q4LIN_ROUTE_TC_FP16) return Q4LIN_ERR_INVALID_ARG;
+  if (route < Q4LIN_ROUTE_AUTO || route > Q4LIN_ROUTE_STREAM_MMA) return Q4LIN_ERR_INVALID_ARG;
   if (validate_sizes(N, K, T) != Q4LIN_OK) return Q4LIN_ERR_INVALID_ARG;
   if (route == Q4LIN_ROUTE_AUTO) route = route_for(N, K, T);
   q4::TcPlan pl{0, 1, 0, 0};
-  if (route != Q4LIN_ROUTE_GEMV && N > 0 && T > 0 && K > 0 && q4::tc_supported(N, K, T))
+  if (route != Q4LIN_ROUTE_GEMV && route != Q4LIN_ROUTE_STREAM_MMA && N > 0 && T > 0 && K > 0 &&
+      q4::tc_supported(N, K, T))
     pl = q4::tc_plan_current_device(route, N, K, T);
   *tile_n = pl.bn;
   *split_k = pl.splitk;
@@ -207,6 +229,7 @@ int q4lin_kernel_launches(int64_t N, int64_t K, int64_t T) {
     case Q4LIN_ROUTE_TC:
     case Q4LIN_ROUTE_TC_SPLITK:
     case Q4LIN_ROUTE_TC_FP16: return q4::tc_launch_count(route, N, K, T);
+    case Q4LIN_ROUTE_STREAM_MMA: return q4::mma_launch_count(N, K, T);
     default: return 0;
   }
 }
@@ -237,14 +260,80 @@ int q4lin_linear_add(const uint8_t* wq, const uint16_t* scales, const uint16_t* 
   return st;
 }
 
+int q4lin_linear_swiglu(const uint8_t* wq, const uint16_t* scales, const uint16_t* x, uint16_t* y, int64_t F,
+                        int64_t K, int64_t T, void* stream) {
+  q4::set_error_detail("");
+  int st = Q4LIN_OK;
+  if (F < 0 || F > kMaxDim / 2) st = Q4LIN_ERR_INVALID_ARG;
+  if (st == Q4LIN_OK) st = validate(wq, scales, x, y, 2 * F, K, T);
+  if (st == Q4LIN_OK && F > 0 && T > 0 && K > 0 && !q4::tc_supported(2 * F, K, T)) st = Q4LIN_ERR_INVALID_ARG;
+  if (st == Q4LIN_OK && F > 0 && T > 0) st = check_device();
+  if (st == Q4LIN_OK && F > 0 && T > 0) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) {  // gate = up = 0: silu(0) * 0 = +0
+      st = q4::cuda_check(cudaMemsetAsync(y, 0, (size_t)F * (size_t)T * 2, s), "zero fill of y");
+    } else {
+      q4::LinearArgs a{wq, scales, x, y, F, K, T, nullptr, s};
+      a.mode = 1;
+      st = q4::tc_launch(a, Q4LIN_ROUTE_TC_SPLITK);
+    }
+  }
+  if (st != Q4LIN_OK && q4::g_detail[0] == 0) q4::set_error_detail(q4lin_status_string(st));
+  return st;
+}
+
+int q4lin_linear_pair(const uint8_t* wq_a, const uint16_t* scales_a, const uint8_t* wq_b, const uint16_t* scales_b,
+                      const uint16_t* x, uint16_t* y_a, uint16_t* y_b, int64_t N_a, int64_t N_b, int64_t K, int64_t T,
+                      void* stream) {
+  q4::set_error_detail("");
+  int st = validate(wq_a, scales_a, x, y_a, N_a, K, T);
+  if (st == Q4LIN_OK) st = validate(wq_b, scales_b, x, y_b, N_b, K, T);
+  const int64_t n_plan = 128 * ((N_a + 127) / 128 + (N_b + 127) / 128);
+  if (st == Q4LIN_OK && T > 0 && K > 0 && N_a + N_b > 0 && !q4::tc_supported(n_plan, K, T))
+    st = Q4LIN_ERR_INVALID_ARG;
+  const bool work = st == Q4LIN_OK && T > 0 && N_a + N_b > 0;
+  if (work) st = check_device();
+  if (st == Q4LIN_OK && work) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) {
+      if (N_a > 0) st = q4::cuda_check(cudaMemsetAsync(y_a, 0, (size_t)N_a * (size_t)T * 2, s), "zero fill of y_a");
+      if (st == Q4LIN_OK && N_b > 0)
+        st = q4::cuda_check(cudaMemsetAsync(y_b, 0, (size_t)N_b * (size_t)T * 2, s), "zero fill of y_b");
+    } else if (N_a == 0 || N_b == 0) {  // one weight: the plain layer on its exact tile route
+      q4::LinearArgs a = N_a > 0 ? q4::LinearArgs{wq_a, scales_a, x, y_a, N_a, K, T, nullptr, s}
+                                 : q4::LinearArgs{wq_b, scales_b, x, y_b, N_b, K, T, nullptr, s};
+      st = q4::tc_launch(a, Q4LIN_ROUTE_TC_SPLITK);
+    } else {
+      q4::LinearArgs a{wq_a, scales_a, x, y_a, N_a, K, T, nullptr, s};
+      a.mode = 2;
+      a.wq_b = wq_b;
+      a.scales_b = scales_b;
+      a.y_b = y_b;
+      a.n_b = N_b;
+      st = q4::tc_launch(a, Q4LIN_ROUTE_TC_SPLITK);
+    }
+  }
+  if (st != Q4LIN_OK && q4::g_detail[0] == 0) q4::set_error_detail(q4lin_status_string(st));
+  return st;
+}
+
 int q4lin_qtype_kernel_launches(int qtype, int64_t N, int64_t K, int64_t T) {
   if (qtype == Q4LIN_QTYPE_Q4G64) return q4lin_kernel_launches(N, K, T);
   if (qtype < Q4LIN_QTYPE_Q5G64 || qtype > Q4LIN_QTYPE_W8G32) return 0;
   if (validate_sizes(N, K, T) != Q4LIN_OK || N == 0 || T == 0) return 0;
   if (K == 0) return 1;  // the zero fill
   if (q4::gemv_stream_ok(N, K, T, qtype)) return 1;
-  if (qtype == Q4LIN_QTYPE_W8G32 || !q4::tc_supported(N, K, T)) return 0;  // refused
+  if (qtype == Q4LIN_QTYPE_W8G32) return q4::mma_supported(N, K, T, 3) ? q4::mma_launch_count(N, K, T) : 0;
+  if (!q4::tc_supported(N, K, T)) return 0;  // refused
   return q4::tc_launch_count(Q4LIN_ROUTE_TC_SPLITK, N, K, T, qtype);
+}
+
+size_t q4lin_qtype_workspace_bytes(int qtype, int64_t N, int64_t K, int64_t T) {
+  if (qtype == Q4LIN_QTYPE_Q4G64) return q4lin_workspace_bytes(N, K, T);
+  if (qtype != Q4LIN_QTYPE_W8G32) return 0;
+  if (validate_sizes(N, K, T) != Q4LIN_OK || N == 0 || K == 0 || T == 0) return 0;
+  if (q4::gemv_stream_ok(N, K, T, qtype)) return 0;
+  return round256(q4::mma_workspace_bytes(N, K, T, 3));
 }
 
 int q4lin_linear(const uint8_t* wq, const uint16_t* scales, const uint16_t* x, uint16_t* y,
@@ -284,7 +373,7 @@ int q4lin_linear_qtype(int qtype, const uint8_t* codes, const uint8_t* high, con
     return Q4LIN_ERR_INVALID_ARG;
   }
   q4::set_error_detail("");
-  const int st = run_qtype_impl(qtype, codes, high, scales, x, y, N, K, T, stream);
+  const int st = run_qtype_impl(qtype, codes, high, scales, x, y, N, K, T, workspace, stream);
   if (st != Q4LIN_OK && q4::g_detail[0] == 0) q4::set_error_detail(q4lin_status_string(st));
   return st;
 }
@@ -315,6 +404,8 @@ static int read_status(bool clear) {
   if (q4::tc_status(&v, clear) != Q4LIN_OK) return Q4LIN_ERR_CUDA;
   if (v) worst = v;
   if (q4::probe_status(&v, clear) != Q4LIN_OK) return Q4LIN_ERR_CUDA;
+  if (v) worst = v;
+  if (q4::mma_status(&v, clear) != Q4LIN_OK) return Q4LIN_ERR_CUDA;
   if (v) worst = v;
   return worst;
 }

@@ -15,9 +15,9 @@ LIB_PATH = os.path.join(_PKG, "libq4lin.so")
 OK = 0
 STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED_SHAPE", 3: "MISALIGNED", 4: "WORKSPACE",
           5: "DEVICE", 6: "CUDA", 7: "TIMEOUT"}
-ROUTE_AUTO, ROUTE_GEMV, ROUTE_TC_SPLITK, ROUTE_TC, ROUTE_TC_FP16 = 0, 1, 2, 3, 4
+ROUTE_AUTO, ROUTE_GEMV, ROUTE_TC_SPLITK, ROUTE_TC, ROUTE_TC_FP16, ROUTE_STREAM_MMA = 0, 1, 2, 3, 4, 5
 ROUTE_NAMES = {ROUTE_AUTO: "auto", ROUTE_GEMV: "gemv", ROUTE_TC_SPLITK: "tc_splitk", ROUTE_TC: "tc",
-               ROUTE_TC_FP16: "tc_fp16"}
+               ROUTE_TC_FP16: "tc_fp16", ROUTE_STREAM_MMA: "stream_mma"}
 
 QTYPES = {"q4g64": 0, "q5g64": 1, "q6g64": 2, "w8g32": 3}
 
@@ -26,7 +26,8 @@ EXPORTS = ("q4lin_workspace_bytes", "q4lin_linear", "q4lin_linear_route", "q4lin
            "q4lin_route_workspace_bytes", "q4lin_select_route", "q4lin_tile_plan", "q4lin_kernel_launches",
            "q4lin_status_string",
            "q4lin_device_status", "q4lin_clear_device_status", "q4lin_last_error_detail",
-           "q4lin_hbm_read_probe", "q4lin_diag_wait_expiry", "q4lin_version")
+           "q4lin_hbm_read_probe", "q4lin_diag_wait_expiry", "q4lin_linear_swiglu", "q4lin_linear_pair",
+           "q4lin_qtype_workspace_bytes", "q4lin_version")
 
 _lib = None
 
@@ -89,6 +90,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q4lin_hbm_read_probe.restype = ctypes.c_int
     lib.q4lin_diag_wait_expiry.argtypes = [ctypes.c_uint32, vp, vp]
     lib.q4lin_diag_wait_expiry.restype = ctypes.c_int
+    lib.q4lin_qtype_workspace_bytes.argtypes = [ctypes.c_int, i64, i64, i64]
+    lib.q4lin_qtype_workspace_bytes.restype = sz
+    lib.q4lin_linear_swiglu.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
+    lib.q4lin_linear_swiglu.restype = ctypes.c_int
+    lib.q4lin_linear_pair.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, vp]
+    lib.q4lin_linear_pair.restype = ctypes.c_int
     lib.q4lin_version.argtypes = []
     lib.q4lin_version.restype = ctypes.c_char_p
     if path is None:
@@ -137,7 +144,7 @@ def kernel_launches(N: int, K: int, T: int, qtype: str = "q4g64") -> int:
     return int(load().q4lin_qtype_kernel_launches(QTYPES[qtype], N, K, T))
 
 
-_IMPLEMENTED = (ROUTE_GEMV, ROUTE_TC_SPLITK, ROUTE_TC, ROUTE_TC_FP16)
+_IMPLEMENTED = (ROUTE_GEMV, ROUTE_TC_SPLITK, ROUTE_TC, ROUTE_TC_FP16, ROUTE_STREAM_MMA)
 
 
 def implemented_routes():
@@ -229,7 +236,7 @@ def linear_qtype(qtype: str, planes, scales, x, y=None, stream=None):
 
     planes: (codes,) for q4g64 / w8g32, (low codes, high bits) for q5g64 / q6g64;
     planes and scales stored for Kp = K rounded up to 128 columns (see q4lin.h);
-    all CUDA, contiguous.  Q5 / Q6 / W8 run for 1..4 tokens.
+    all CUDA, contiguous.  Workspace (W8 beyond the decode GEMV) is allocated here.
     """
     import torch
 
@@ -251,7 +258,7 @@ def linear_qtype(qtype: str, planes, scales, x, y=None, stream=None):
             raise ValueError(f"{name} must be a contiguous CUDA tensor")
     if y is None:
         y = torch.empty((T, N), dtype=torch.bfloat16, device=x.device)
-    need = workspace_bytes(N, K, T) if qtype == "q4g64" else 0   # Q4 is q4lin_linear
+    need = int(load().q4lin_qtype_workspace_bytes(qt, N, K, T))
     ws = torch.empty(need, dtype=torch.uint8, device=x.device) if need else None
     s = (stream or torch.cuda.current_stream(x.device)).cuda_stream
     st = int(load().q4lin_linear_qtype(qt, _ptr(codes), _ptr(high) if bits else None, _ptr(scales), _ptr(x),
@@ -282,3 +289,51 @@ def diag_wait_expiry(limit: int, out, stream=None) -> None:
     st = int(load().q4lin_diag_wait_expiry(int(limit), _ptr(out), ctypes.c_void_p(s)))
     if st != OK:
         raise Q4LinError(st, "wait expiry check: ")
+
+
+def _check_planes(wq, scales, K, what):
+    Kp = (K + 127) // 128 * 128
+    if wq.shape[1] != Kp // 2 or tuple(scales.shape) != (wq.shape[0], Kp // 64):
+        raise ValueError(f"{what}: shape mismatch wq {tuple(wq.shape)} scales {tuple(scales.shape)} K {K}")
+    for name, t in (("wq", wq), ("scales", scales)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{what}: {name} must be a contiguous CUDA tensor")
+
+
+def linear_swiglu(wq, scales, x, y=None, stream=None):
+    """LinearSwiGLU: Y[T, F] = silu(W[:F] . X) * (W[F:] . X) for a packed weight of 2F rows."""
+    import torch
+
+    T, K = x.shape
+    n2 = wq.shape[0]
+    if n2 % 2:
+        raise ValueError("the gate/up weight has an even number of rows")
+    F = n2 // 2
+    _check_planes(wq, scales, K, "linear_swiglu")
+    if y is None:
+        y = torch.empty((T, F), dtype=torch.bfloat16, device=x.device)
+    s = (stream or torch.cuda.current_stream(x.device)).cuda_stream
+    st = int(load().q4lin_linear_swiglu(_ptr(wq), _ptr(scales), _ptr(x), _ptr(y), F, K, T, ctypes.c_void_p(s)))
+    if st != OK:
+        raise Q4LinError(st)
+    return y
+
+
+def linear_pair(wq_a, scales_a, wq_b, scales_b, x, y_a=None, y_b=None, stream=None):
+    """LinearPair: (W_a . X, W_b . X) in one call; returns (Y_a [T, N_a], Y_b [T, N_b])."""
+    import torch
+
+    T, K = x.shape
+    _check_planes(wq_a, scales_a, K, "linear_pair a")
+    _check_planes(wq_b, scales_b, K, "linear_pair b")
+    Na, Nb = wq_a.shape[0], wq_b.shape[0]
+    if y_a is None:
+        y_a = torch.empty((T, Na), dtype=torch.bfloat16, device=x.device)
+    if y_b is None:
+        y_b = torch.empty((T, Nb), dtype=torch.bfloat16, device=x.device)
+    s = (stream or torch.cuda.current_stream(x.device)).cuda_stream
+    st = int(load().q4lin_linear_pair(_ptr(wq_a), _ptr(scales_a), _ptr(wq_b), _ptr(scales_b), _ptr(x), _ptr(y_a),
+                                      _ptr(y_b), Na, Nb, K, T, ctypes.c_void_p(s)))
+    if st != OK:
+        raise Q4LinError(st)
+    return y_a, y_b
