@@ -184,7 +184,7 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* v) {
   else tmem_ld4(taddr, *reinterpret_cast<uint32_t(*)[4]>(v));
 }
 
-template <int BN, bool kFold, int FMT>
+template <int BN, bool kFold, int FMT, int MODE = 0>
 __global__ void __launch_bounds__(TcSmem<BN, kFold, FMT>::threads, 1)
 q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_x,
              const __grid_constant__ CUtensorMap tm_high, const TcParams p) {
@@ -229,8 +229,9 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
   const int64_t t0 = (int64_t)(tile / p.tiles_m) * BN;
   // the weight this tile reads: first row (the gate rows' first row for SwiGLU), row count,
   // and for LinearPair which of the two weights
-  const bool wsel_b = p.mode == 2 && mt >= p.tiles_a;
-  const int64_t m0 = p.mode == 1 ? (int64_t)mt * 64 : (int64_t)(wsel_b ? mt - p.tiles_a : mt) * kTileM;
+  // (MODE, a template parameter so that the plain layer's code is untouched by the fused forms)
+  const bool wsel_b = MODE == 2 && mt >= p.tiles_a;
+  const int64_t m0 = MODE == 1 ? (int64_t)mt * 64 : (int64_t)(wsel_b ? mt - p.tiles_a : mt) * kTileM;
   const int64_t n_rows = wsel_b ? p.n_b : p.N;   // rows of this tile's output (SwiGLU: F)
 
   // This CTA's share of the K groups (the whole K without a split).
@@ -265,7 +266,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
     fence_mbar_init();
     prefetch_tmap(&tm_codes);
     prefetch_tmap(&tm_x);
-    if (kHB > 0 || p.mode == 2) prefetch_tmap(&tm_high);
+    if constexpr (kHB > 0 || MODE == 2) prefetch_tmap(&tm_high);
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), L::tmem_cols);
   tc_fence_before();
@@ -299,14 +300,18 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
         const int slot = ws % SW;
         if (!(ok = mbar_wait(c_empty(slot), ((ws / SW) & 1) ^ 1, abort_flag, &g_tc_status))) break;
         mbar_expect_tx(c_full(slot), kWBytes + L::kHBytes);
-        if (p.mode == 1) {  // SwiGLU: gate rows into tile rows 0..63, up rows into 64..127 (64-row boxes)
+        if constexpr (MODE == 1) {  // SwiGLU: gate rows into tile rows 0..63, up rows into 64..127 (64-row boxes)
           tma_load_2d(sbase + L::c_off + slot * kWBytes, &tm_codes, c_full(slot), (g_begin + ws * kGroupsPerW) * 32,
                       (int32_t)m0);
           tma_load_2d(sbase + L::c_off + slot * kWBytes + kWBytes / 2, &tm_codes, c_full(slot),
                       (g_begin + ws * kGroupsPerW) * 32, (int32_t)(p.N + m0));
         } else {
-          tma_load_2d(sbase + L::c_off + slot * kWBytes, wsel_b ? &tm_high : &tm_codes, c_full(slot),
-                      (g_begin + ws * kGroupsPerW) * 32, (int32_t)m0);
+          if (MODE == 2 && wsel_b)
+            tma_load_2d(sbase + L::c_off + slot * kWBytes, &tm_high, c_full(slot), (g_begin + ws * kGroupsPerW) * 32,
+                        (int32_t)m0);
+          else
+            tma_load_2d(sbase + L::c_off + slot * kWBytes, &tm_codes, c_full(slot), (g_begin + ws * kGroupsPerW) * 32,
+                        (int32_t)m0);
         }
         if constexpr (kHB > 0)  // the stage's high bits: 8 * kHB bytes per group and row
           tma_load_2d(sbase + L::h_off + slot * L::kHBytes, &tm_high, c_full(slot),
@@ -498,8 +503,8 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
     for (int i = 0; i < kCols / 2; ++i) acc[i] = make_float2(0.f, 0.f);
     bool acc_ok = true;
     // weight row of this tile row (SwiGLU: gate rows then up rows), and whether it is a real row
-    const int64_t row = p.mode == 1 ? (r_acc < 64 ? m0 + r_acc : p.N + m0 + (r_acc - 64)) : m0 + r_acc;
-    const bool row_ok = p.mode == 1 ? (m0 + (r_acc & 63) < p.N) : row < n_rows;
+    const int64_t row = MODE == 1 ? (r_acc < 64 ? m0 + r_acc : p.N + m0 + (r_acc - 64)) : m0 + r_acc;
+    const bool row_ok = MODE == 1 ? (m0 + (r_acc & 63) < p.N) : row < n_rows;
     const uint16_t* scl = wsel_b ? p.scales_b : p.scales;
     const uint32_t tlane = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(cq * kCols);
     if constexpr (kFold) {
@@ -628,7 +633,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
     }
 
     // ----------------------------------------------------------- epilogue: Y[t, row] = bf16(acc [+ R[t, row]])
-    if (p.mode == 1) {
+    if constexpr (MODE == 1) {
       // SwiGLU: the up rows (tile rows 64..127) hand their FP32 sums to the gate rows through
       // shared memory (the pipeline buffers are free: every MMA and copy has completed); the
       // gate rows store y[t, f] = bf16(silu(g) * u), silu(g) = g / (1 + e^-g) in FP32
@@ -796,17 +801,18 @@ bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint6
   return encode_map_2d(m, dt, base, inner, outer, row_bytes, box_inner, box_outer, swizzle);
 }
 
-template <int BN, bool kFold, int FMT = 0>
+template <int BN, bool kFold, int FMT = 0, int MODE = 0>
 int set_kernel_attrs() {
   using L = TcSmem<BN, kFold, FMT>;
   static bool attr_set[64] = {};
   int dev = 0;
   if (cuda_check(cudaGetDevice(&dev), "cudaGetDevice")) return Q4LIN_ERR_CUDA;
   if (dev < 64 && attr_set[dev]) return Q4LIN_OK;
-  if (cuda_check(cudaFuncSetAttribute(q4_tc_kernel<BN, kFold, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc),
+  if (cuda_check(cudaFuncSetAttribute(q4_tc_kernel<BN, kFold, FMT, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      L::alloc),
                  "tc: cudaFuncSetAttribute(max dynamic shared memory)"))
     return Q4LIN_ERR_CUDA;
-  if (cuda_check(cudaFuncSetAttribute(q4_tc_kernel<BN, kFold, FMT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+  if (cuda_check(cudaFuncSetAttribute(q4_tc_kernel<BN, kFold, FMT, MODE>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
                  "tc: cudaFuncSetAttribute(cluster size)"))
     return Q4LIN_ERR_CUDA;
   if (dev < 64) attr_set[dev] = true;
@@ -844,7 +850,7 @@ int resident_clusters(int size) {
   return n;
 }
 
-template <int BN, bool kFold, int FMT = 0>
+template <int BN, bool kFold, int FMT = 0, int MODE = 0>
 int launch_tile(const LinearArgs& a, int splitk, int64_t tile_base, int64_t n_tiles) {
   using L = TcSmem<BN, kFold, FMT>;
   static_assert(L::alloc <= 232448, "shared memory budget");
@@ -852,7 +858,7 @@ int launch_tile(const LinearArgs& a, int splitk, int64_t tile_base, int64_t n_ti
     set_error_detail("tc: split-K factor out of range for this tile");
     return Q4LIN_ERR_INVALID_ARG;
   }
-  if (const int rc = set_kernel_attrs<BN, kFold, FMT>()) return rc;
+  if (const int rc = set_kernel_attrs<BN, kFold, FMT, MODE>()) return rc;
   CUtensorMap tm_codes, tm_x, tm_high;
   // code plane rows hold K_pad / 2 bytes; X rows K values, whose positions k >= K read
   // as zeros (out-of-range tile elements), so a partial last group sees x = 0 beyond K.
@@ -915,7 +921,7 @@ int launch_tile(const LinearArgs& a, int splitk, int64_t tile_base, int64_t n_ti
   ++na;
   cfg.attrs = attr;
   cfg.numAttrs = (unsigned)na;
-  return cuda_check(cudaLaunchKernelEx(&cfg, q4_tc_kernel<BN, kFold, FMT>, tm_codes, tm_x, tm_high, p),
+  return cuda_check(cudaLaunchKernelEx(&cfg, q4_tc_kernel<BN, kFold, FMT, MODE>, tm_codes, tm_x, tm_high, p),
                     "tc: kernel launch");
 }
 
@@ -1137,6 +1143,24 @@ int tc_launch(const LinearArgs& a, int route) {
         case 64: return launch_tile<64, true>(a, splitk, base, n);
         case 32: return launch_tile<32, true>(a, splitk, base, n);
         default: return launch_tile<16, true>(a, splitk, base, n);
+      }
+    }
+    if (a.mode == 1) {
+      switch (pl.bn) {
+        case 256: return launch_tile<256, false, 0, 1>(a, splitk, base, n);
+        case 128: return launch_tile<128, false, 0, 1>(a, splitk, base, n);
+        case 64: return launch_tile<64, false, 0, 1>(a, splitk, base, n);
+        case 32: return launch_tile<32, false, 0, 1>(a, splitk, base, n);
+        default: return launch_tile<16, false, 0, 1>(a, splitk, base, n);
+      }
+    }
+    if (a.mode == 2) {
+      switch (pl.bn) {
+        case 256: return launch_tile<256, false, 0, 2>(a, splitk, base, n);
+        case 128: return launch_tile<128, false, 0, 2>(a, splitk, base, n);
+        case 64: return launch_tile<64, false, 0, 2>(a, splitk, base, n);
+        case 32: return launch_tile<32, false, 0, 2>(a, splitk, base, n);
+        default: return launch_tile<16, false, 0, 2>(a, splitk, base, n);
       }
     }
     switch (pl.bn) {
