@@ -14,14 +14,13 @@
 // two fp16 bit patterns q and q': fp16 subnormals worth q * 2^-24 exactly.  The
 // odd nibbles, w & 0x00F000F0, are 16 q * 2^-24, also exact (at most 240 < 2^10),
 // and meet x / 16 on the other side.  X is converted to fp16 once per call by a
-// prep kernel, taken per token at the power of two 2^-e that puts its largest
-// |x| in [2^14, 2^15) (bf16 -> fp16 is then exact down to 2^-38 of that largest
-// value).  Every product q * x is exact in FP32, so the MMA of one 64-wide group
-// gives D = 2^-24 sum q x, and
-//     sum_k (q - 8) x  =  2^24 D - 8 sum_k x,
-// where the prep kernel has summed -8 sum_k x per group and token.  The group
-// scale multiplies that FP32 partial; the powers of two are undone on the FP32
-// result before the one bf16 rounding.  No product is rounded.
+// prep kernel, each 64-wide group of each token taken at the power of two 2^-e that
+// puts the group's largest |x| in [2^14, 2^15) (bf16 -> fp16 is then exact down to
+// 2^-38 of that largest value).  Every product q * x-hat is exact in FP32, so the MMA
+// of one group gives D = 2^-24 sum q x-hat, and
+//     sum_k (q - 8) x  =  2^(24 + e) D - 8 2^e sum_k x-hat  =  F D + Z,
+// with F and Z written by the prep kernel per group and token.  The group scale
+// multiplies that FP32 partial before the one bf16 rounding.  No product is rounded.
 //
 // Operand layout.  In one m16n8k16 MMA a thread (g = lane / 4, c = lane % 4) holds
 // A elements of rows g and g + 8 at K slots 2c, 2c + 1, 2c + 8, 2c + 9, and B
@@ -68,8 +67,7 @@ struct MmaParams {
   const uint8_t* wq;       // packed codes [N, Kp/2]
   const uint16_t* scales;  // fp16 bits [N, Kp/64]
   const uint8_t* xf;       // B fragments [galloc][NT][2][lanes][16 bytes]
-  const float* zs;         // zero-point terms -8 sum x [galloc][NT][4][2]
-  const int* xe;           // per token of the pass: X was taken as x * 2^-xe[t]
+  const float* zs;         // per (group, token tile, c): (Z[t], Z[t + 1], F[t], F[t + 1]), t = 2c
   uint16_t* y;             // bf16 [T, N]
   const uint16_t* r;       // LinearAdd: bf16 residual [T, N], added before the bf16 store (may be y)
   int64_t N, Kp, T;
@@ -99,7 +97,7 @@ __host__ __device__ inline MmaLayout mma_layout(int nt, int br, int ks, int mt, 
   MmaLayout L;
   L.code_bytes = (uint32_t)(ks * br * 128);  // ks sub-boxes of br rows x 128 bytes (128-byte swizzle)
   L.xf_bytes = (uint32_t)(4 * ks * nt * lanes * fbytes);
-  L.zs_bytes = (uint32_t)(4 * ks * nt * 32);
+  L.zs_bytes = (uint32_t)(4 * ks * nt * 64);
   L.stage_bytes = (L.code_bytes + L.xf_bytes + L.zs_bytes + 1023) / 1024 * 1024;
   // a band's scale run: br rows of Kp / 64 scales, plus up to 15 bytes of alignment slack
   // on either side
@@ -122,12 +120,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 __device__ __forceinline__ uint2 lds_u64(uint32_t addr) {
   uint2 v;
   asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-  return v;
-}
-
-__device__ __forceinline__ float2 lds_f2(uint32_t addr) {
-  float2 v;
-  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
   return v;
 }
 
@@ -229,7 +221,7 @@ q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const MmaParams p) {
   // before the first epilogue.
 
   const uint32_t xf_chunk = (uint32_t)(4 * KS * NT * p.lanes * FB);  // B-fragment bytes per chunk
-  const uint32_t zs_chunk = (uint32_t)(4 * KS * NT * 32);
+  const uint32_t zs_chunk = (uint32_t)(4 * KS * NT * 64);
   if (warp == 0) {
     // ------------------------------------------------------------- producer (lane 0 issues)
     if (lane == 0) {
@@ -241,7 +233,7 @@ q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const MmaParams p) {
         const int gq = (q % NCH) * 4 * KS;
         const uint32_t sq = stage(q % NS);
         bulk_g2s(sq + p.xf_off, p.xf + (size_t)gq * NT * p.lanes * FB, xf_chunk, full(q % NS));
-        bulk_g2s(sq + p.zs_off, reinterpret_cast<const uint8_t*>(p.zs) + (size_t)gq * NT * 32, zs_chunk,
+        bulk_g2s(sq + p.zs_off, reinterpret_cast<const uint8_t*>(p.zs) + (size_t)gq * NT * 64, zs_chunk,
                  full(q % NS));
       };
       for (int b = 0; ok && b < nbands; ++b) {
@@ -310,7 +302,6 @@ q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const MmaParams p) {
   const int g = lane >> 2, c = lane & 3;
   const int ra = 16 * m + 2 * g, rb = ra + 1;  // band rows of mma rows g and g + 8
   const bool bload = lane < p.lanes;           // this lane's B fragment is stored (the others are zero)
-  const float k2p24 = 16777216.f;  // 2^24
   int it = 0;
   bool ok = true;
   for (int b = 0; b < nbands; ++b) {
@@ -331,7 +322,7 @@ q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const MmaParams p) {
         const uint32_t code = stage(s) + (uint32_t)(sub * BR * 128);
         const uint32_t rowa = code + (uint32_t)(ra * 128), rowb = code + (uint32_t)(rb * 128);
         const uint32_t xf = stage(s) + p.xf_off + (uint32_t)(4 * sub * NT * p.lanes * FB) + (uint32_t)lane * 16u;
-        const uint32_t zs = stage(s) + p.zs_off + (uint32_t)(4 * sub * NT * 32) + (uint32_t)c * 8u;
+        const uint32_t zs = stage(s) + p.zs_off + (uint32_t)(4 * sub * NT * 64) + (uint32_t)c * 16u;
 #pragma unroll
         for (int gl = 0; gl < 4; ++gl) {
           const int G = gb + gl;
@@ -364,9 +355,11 @@ q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const MmaParams p) {
               mma_16816(d, pa[4], pb[4], pa[5], pb[5], b1.x, b1.y);
               mma_16816(d, pa[6], pb[6], pa[7], pb[7], b1.z, b1.w);
             }
-            const float2 z = lds_f2(zs + (uint32_t)((gl * NT + n) * 32));
-            const float2 e01 = ffma2(make_float2(d[0], d[1]), make_float2(k2p24, k2p24), z);
-            const float2 e23 = ffma2(make_float2(d[2], d[3]), make_float2(k2p24, k2p24), z);
+            // (Z, F) of this thread's two tokens: sum (q - zero) x = F D + Z
+            const float4 zf = ld_shared_f4(zs + (uint32_t)((gl * NT + n) * 64));
+            const float2 z = make_float2(zf.x, zf.y), f = make_float2(zf.z, zf.w);
+            const float2 e01 = ffma2(make_float2(d[0], d[1]), f, z);
+            const float2 e23 = ffma2(make_float2(d[2], d[3]), f, z);
             const float2 a01 = ffma2(make_float2(sa, sa), e01, make_float2(acc[n][0], acc[n][1]));
             const float2 a23 = ffma2(make_float2(sbv, sbv), e23, make_float2(acc[n][2], acc[n][3]));
             acc[n][0] = a01.x;
@@ -402,7 +395,6 @@ q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const MmaParams p) {
         const int t = e / rows, rw = e - (e / rows) * rows;
         float v = 0.f;
         for (int q = 0; q < KS; ++q) v += red[((size_t)q * MR + rw) * TP + t];
-        v *= exp2i(__ldg(p.xe + t));
         const int64_t gi = (int64_t)(p.t0 + t) * p.N + R0 + rw;
         if (p.r != nullptr) v += __uint_as_float((uint32_t)p.r[gi] << 16);
         p.y[gi] = float_to_bf16_bits(v);
@@ -413,70 +405,59 @@ q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const MmaParams p) {
 }
 
 // ----------------------------------------------------------------- operand pass
-// One CTA per token slot of the pass (8 NT of them; slots past the pass's tokens
-// write zeros): the token's largest |x| (compared as bf16 magnitude bits) fixes the
-// power of two 2^-e[t] that puts it in [2^14, 2^15); then every (group, c) pair --
-// the 16 values k = 64 G + 16 c .. + 15 -- becomes the eight fp16x2 B registers of
-// lane 4 (t mod 8) + c in the order the decode produces A, and the group's
-// -8 sum x is reduced over its four c.  Tokens holding Inf or NaN keep e = 0.
-// W8G32 (FMT 3): a group is 32 wide, a (group, c) pair holds the 8 values k = 32 G + 8 c
-// .. + 7 as four fp16x2 registers (no 1/16 halves), and the zero-point term is -128 sum x.
+// One thread per (token slot t of the pass, group G, c): the values of token t in group G
+// that thread c of an MMA feeds -- k = 64 G + 16 c .. + 15 (Q4) or 32 G + 8 c .. + 7 (W8)
+// -- become its fp16x2 B registers, in the order the decode produces A.  The four c of a
+// (t, G) are adjacent lanes: they take the group's largest |x| (compared as bf16 magnitude
+// bits) and the power of two 2^-e that puts it in [2^14, 2^15), so every value of the group
+// down to 2^-38 of that largest one converts to fp16 exactly, and the group's terms
+//     Z = -zero * 2^e * sum x-hat,   F = 2^(24 + e)
+// make sum_k (q_k - zero) x_k = F D + Z for the MMA result D = 2^-24 sum q x-hat (zero = 8 for
+// Q4, 128 for W8's offset codes).  No pass over a whole token is needed, so the threads of
+// any number of CTAs share the work.  Slots past the pass's tokens write zeros.  Groups holding
+// Inf or NaN keep e = 0 so those values propagate.
 constexpr int kPrepThreads = 256;
 
 template <int NT, int FMT>
 __global__ void __launch_bounds__(kPrepThreads)
 q4_mma_prep_kernel(const uint16_t* __restrict__ x, uint8_t* __restrict__ xf, float* __restrict__ zs,
-                   int* __restrict__ xe, int64_t K, int tp, int galloc, int lanes) {
+                   int64_t K, int tp, int galloc, int lanes) {
   // Wait for the previous kernel (it may write x, or still read these buffers), and only
   // then let the streaming kernel launch: it reads the weight planes as soon as it starts.
   pdl_wait_previous();
   pdl_launch_dependents();
-  __shared__ uint32_t red[kPrepThreads / 32];
-  const int t = blockIdx.x;  // token slot of the pass
-  const bool live = t < tp;
-  const uint16_t* xr = x + (int64_t)(live ? t : 0) * K;
-  // largest |x| of the token
-  uint32_t m2 = 0;
-  if (live)
-    for (int64_t i = threadIdx.x; i < K / 8; i += kPrepThreads) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr) + i);
-      m2 = __vmaxu2(m2, v.x & 0x7FFF7FFFu);
-      m2 = __vmaxu2(m2, v.y & 0x7FFF7FFFu);
-      m2 = __vmaxu2(m2, v.z & 0x7FFF7FFFu);
-      m2 = __vmaxu2(m2, v.w & 0x7FFF7FFFu);
-    }
-  uint32_t mx = __reduce_max_sync(0xffffffffu, max(m2 & 0xFFFFu, m2 >> 16));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
-  __syncthreads();
-#pragma unroll
-  for (int w = 0; w < kPrepThreads / 32; ++w) mx = max(mx, red[w]);
-  const int E = (int)(mx >> 7);  // bf16 biased exponent of the largest |x|
-  const int e = (mx == 0 || E == 255) ? 0 : min(max(E - 141, -100), 100);
-  const float s1 = exp2i(-e), s16 = exp2i(-e - 4);
-  const int n = t / 8, tl = t % 8;
-  const bool stored = (tl * 4) < lanes;  // this token's B lanes exist in the buffer
   constexpr bool kW8 = FMT == 3;
-  constexpr int kVals = kW8 ? 8 : 16;    // values of one (group, c) pair
-  // every thread runs the same number of iterations (the group sums below shuffle across
-  // the four threads of a group, with the whole warp taking part)
-  for (int base = 0; base < galloc * 4; base += kPrepThreads) {
-    const int idx = base + (int)threadIdx.x;
-    const bool act = idx < galloc * 4;
-    const int G = idx >> 2, c = idx & 3;
+  constexpr int kVals = kW8 ? 8 : 16;  // values of one (group, c) unit
+  const int64_t units = (int64_t)8 * NT * galloc * 4;   // a multiple of 32: whole warps take part
+  for (int64_t u = (int64_t)blockIdx.x * kPrepThreads + threadIdx.x; u - (threadIdx.x & 31) < units;
+       u += (int64_t)gridDim.x * kPrepThreads) {
+    const bool act = u < units;
+    const int c = (int)(u & 3);
+    const int64_t tg = u >> 2;
+    const int G = (int)(tg % galloc), t = (int)(tg / galloc);
+    const bool live = act && t < tp;
     const int64_t k0 = (int64_t)G * (4 * kVals) + kVals * c;
+    const uint16_t* xr = x + (int64_t)(live ? t : 0) * K;
     float v[16];
+    uint32_t m2 = 0;
 #pragma unroll
     for (int h = 0; h < kVals / 8; ++h) {
       // K is a multiple of 8: each run of 8 columns is either wholly inside or wholly past K
-      const bool in = act && live && k0 + 8 * h < K;
+      const bool in = live && k0 + 8 * h < K;
       const uint4 q = in ? __ldg(reinterpret_cast<const uint4*>(xr + k0 + 8 * h)) : make_uint4(0u, 0u, 0u, 0u);
+      m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(q.x & 0x7FFF7FFFu, q.y & 0x7FFF7FFFu), __vmaxu2(q.z & 0x7FFF7FFFu, q.w & 0x7FFF7FFFu)));
       v[8 * h + 0] = bf16lo(q.x); v[8 * h + 1] = bf16hi(q.x);
       v[8 * h + 2] = bf16lo(q.y); v[8 * h + 3] = bf16hi(q.y);
       v[8 * h + 4] = bf16lo(q.z); v[8 * h + 5] = bf16hi(q.z);
       v[8 * h + 6] = bf16lo(q.w); v[8 * h + 7] = bf16hi(q.w);
     }
-    // x-hat = fp16(x 2^-e) (exact in fp16's normal range); the zero-point term sums the
-    // same fp16 values
+    uint32_t mx = max(m2 & 0xFFFFu, m2 >> 16);
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const int E = (int)(mx >> 7);  // bf16 biased exponent of the group's largest |x|
+    const int e = (mx == 0 || E == 255) ? 0 : min(max(E - 141, -100), 100);
+    const float s1 = exp2i(-e), s16 = exp2i(-e - 4);
+    // x-hat = fp16(x 2^-e) (exact in fp16's normal range); the zero-point term sums the same values
     float sum = 0.f;
 #pragma unroll
     for (int i = 0; i < kVals; ++i) sum += __half2float(__float2half_rn(v[i] * s1));
@@ -486,7 +467,8 @@ q4_mma_prep_kernel(const uint16_t* __restrict__ x, uint8_t* __restrict__ xf, flo
       return (uint32_t)__half_as_ushort(__float2half_rn(v[i0] * sc)) |
              ((uint32_t)__half_as_ushort(__float2half_rn(v[i1] * sc)) << 16);
     };
-    if (act && stored) {
+    const int n = t / 8, tl = t % 8;
+    if (act && tl * 4 < lanes) {  // this token's B lanes exist in the buffer
       const int L = tl * 4 + c;
       if constexpr (kW8) {
         // registers per MMA kk: (x[k0 + 4kk], x[+2]) then (x[+1], x[+3])
@@ -494,16 +476,18 @@ q4_mma_prep_kernel(const uint16_t* __restrict__ x, uint8_t* __restrict__ xf, flo
         dst[L] = make_uint4(pk(0, 2, s1), pk(1, 3, s1), pk(4, 6, s1), pk(5, 7, s1));
       } else {
         // registers per MMA kk: (x[k0 + 2kk'], x[+4]) then (x[+1] / 16, x[+5] / 16), kk' = 0, 1, 4, 5
-        const uint4 h0 = make_uint4(pk(0, 4, s1), pk(1, 5, s16), pk(2, 6, s1), pk(3, 7, s16));
-        const uint4 h1 = make_uint4(pk(8, 12, s1), pk(9, 13, s16), pk(10, 14, s1), pk(11, 15, s16));
         uint4* dst = reinterpret_cast<uint4*>(xf + ((size_t)(G * NT + n) * 2) * lanes * 16);
-        dst[L] = h0;
-        dst[lanes + L] = h1;
+        dst[L] = make_uint4(pk(0, 4, s1), pk(1, 5, s16), pk(2, 6, s1), pk(3, 7, s16));
+        dst[lanes + L] = make_uint4(pk(8, 12, s1), pk(9, 13, s16), pk(10, 14, s1), pk(11, 15, s16));
       }
     }
-    if (act && c == 0) zs[((size_t)(G * NT + n) * 4 + tl / 2) * 2 + (tl & 1)] = (kW8 ? -128.f : -8.f) * sum;
+    if (act && c == 0) {
+      // (Z[t], Z[t + 1], F[t], F[t + 1]) of MMA thread c' = tl / 2 of this group and token tile
+      float* zq = zs + ((size_t)(G * NT + n) * 4 + tl / 2) * 4;
+      zq[tl & 1] = live ? (kW8 ? -128.f : -8.f) * exp2i(e) * sum : 0.f;
+      zq[2 + (tl & 1)] = live ? exp2i(24 + e) : 0.f;
+    }
   }
-  if (threadIdx.x == 0) xe[t] = e;
 }
 
 // ----------------------------------------------------------------- host side
@@ -577,10 +561,10 @@ int mma_sm_count() {
   return n;
 }
 
-// Workspace of one pass: B fragments, zero-point terms, exponents (each 256-byte aligned).
+// Workspace of one pass: B fragments, then the zero-point terms and factors (each 256-byte aligned).
 size_t mma_ws_xf(const MmaPlan& pl) { return ((size_t)pl.galloc * pl.nt * pl.lanes * pl.fbytes + 255) / 256 * 256; }
-size_t mma_ws_zs(const MmaPlan& pl) { return ((size_t)pl.galloc * pl.nt * 32 + 255) / 256 * 256; }
-size_t mma_ws_total(const MmaPlan& pl) { return mma_ws_xf(pl) + mma_ws_zs(pl) + 256; }
+size_t mma_ws_zs(const MmaPlan& pl) { return ((size_t)pl.galloc * pl.nt * 64 + 255) / 256 * 256; }
+size_t mma_ws_total(const MmaPlan& pl) { return mma_ws_xf(pl) + mma_ws_zs(pl); }
 
 template <int NT, int FMT>
 int mma_launch_pass(const LinearArgs& a, const MmaPlan& pl, const CUtensorMap& tm, int64_t t0, int tp) {
@@ -597,18 +581,20 @@ int mma_launch_pass(const LinearArgs& a, const MmaPlan& pl, const CUtensorMap& t
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   uint8_t* xf = ws;
   float* zs = reinterpret_cast<float*>(ws + mma_ws_xf(pl));
-  int* xe = reinterpret_cast<int*>(ws + mma_ws_xf(pl) + mma_ws_zs(pl));
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
   {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(8 * NT), 1, 1);
+    const int64_t units = (int64_t)8 * NT * pl.galloc * 4;
+    int64_t blocks = (units + kPrepThreads - 1) / kPrepThreads;
+    if (blocks > 4 * (int64_t)pl.grid) blocks = 4 * (int64_t)pl.grid;
+    cfg.gridDim = dim3((unsigned)blocks, 1, 1);
     cfg.blockDim = dim3(kPrepThreads, 1, 1);
     cfg.stream = a.stream;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    if (cuda_check(cudaLaunchKernelEx(&cfg, q4_mma_prep_kernel<NT, FMT>, a.x + t0 * a.K, xf, zs, xe, a.K, tp,
+    if (cuda_check(cudaLaunchKernelEx(&cfg, q4_mma_prep_kernel<NT, FMT>, a.x + t0 * a.K, xf, zs, a.K, tp,
                                       pl.galloc, pl.lanes),
                    "mma: prep kernel launch"))
       return Q4LIN_ERR_CUDA;
@@ -618,7 +604,6 @@ int mma_launch_pass(const LinearArgs& a, const MmaPlan& pl, const CUtensorMap& t
   p.scales = a.scales;
   p.xf = xf;
   p.zs = zs;
-  p.xe = xe;
   p.y = a.y;
   p.r = a.r;
   p.N = a.N;
