@@ -170,10 +170,14 @@ struct TcSmem {
 
 // Registers per thread after the split (four accumulate warpgroups only; with
 // one, the launch allocation of 128 per thread covers every role).  The split
-// sums to at most the launch allocation: 896 threads x 72.
+// sums to at most the launch allocation: 896 threads x 72.  Chosen so that no role
+// spills (ptxas -v): with shared-memory A stages the decode teams need 48 and the
+// producers and issuer more than 40 (a decode split of 40 spilled in the decode
+// loop and cost about 10 % at T = 1024); with A in tensor memory the decode teams
+// need 72.
 template <bool kATmem> struct TcRegs;
-template <> struct TcRegs<true> { static constexpr int ctl = 32, dec = 64, acc = 80; };
-template <> struct TcRegs<false> { static constexpr int ctl = 40, dec = 40, acc = 96; };
+template <> struct TcRegs<true> { static constexpr int ctl = 32, dec = 72, acc = 80; };
+template <> struct TcRegs<false> { static constexpr int ctl = 56, dec = 48, acc = 88; };
 static_assert(128 * TcRegs<true>::ctl + 256 * TcRegs<true>::dec + 512 * TcRegs<true>::acc <= 896 * 72, "register split");
 static_assert(128 * TcRegs<false>::ctl + 256 * TcRegs<false>::dec + 512 * TcRegs<false>::acc <= 896 * 72, "register split");
 
@@ -990,7 +994,7 @@ struct TileCost {
 };
 // exact form (per-group accumulators read back and scaled in FP32)
 constexpr TileCost kTileCostExact[] = {
-    {16, 310.0, 4300.0}, {32, 330.0, 4400.0}, {64, 335.0, 6500.0}, {128, 440.0, 5300.0}, {256, 615.0, 7800.0}};
+    {16, 310.0, 4300.0}, {32, 330.0, 4400.0}, {64, 335.0, 6500.0}, {128, 440.0, 5300.0}, {256, 580.0, 7800.0}};
 // folded form (one accumulator per K share; the 256 entry measured at T = 1024 on
 // 6144 x 5120 and 34816 x 5120, the others estimated from the exact form's)
 constexpr TileCost kTileCostFold[] = {
