@@ -660,14 +660,34 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
       }
     } else if (crank == 0 && acc_ok && !*abort_flag && row_ok) {
       uint16_t* yo = wsel_b ? p.y_b : p.y;
+      // (a residual exists only for LinearAdd: the plain exact Q4 form)
+      if (kFold || FMT != 0 || MODE != 0 || p.r == nullptr) {
 #pragma unroll
-      for (int j = 0; j < kCols; ++j) {
-        const int64_t t = t0 + cq * kCols + j;
-        float v = (j & 1) ? acc[j / 2].y : acc[j / 2].x;
-        if (t < p.T) {
-          // LinearAdd: the residual joins the FP32 sum; read before the store, so R may be Y
-          if (p.r != nullptr) v += __uint_as_float((uint32_t)p.r[t * n_rows + row] << 16);
-          yo[t * n_rows + row] = float_to_bf16_bits(v);
+        for (int j = 0; j < kCols; ++j) {
+          const int64_t t = t0 + cq * kCols + j;
+          const float v = (j & 1) ? acc[j / 2].y : acc[j / 2].x;
+          if (t < p.T) yo[t * n_rows + row] = float_to_bf16_bits(v);
+        }
+      } else {
+        // LinearAdd: the residual joins the FP32 sum.  R may be Y, so each element is read
+        // before it is stored; the reads of a 4-token chunk are issued together (one round
+        // trip to memory per chunk, not one per element; larger chunks spill the 256-wide
+        // tile's accumulate warps).
+        constexpr int kChunk = kCols < 4 ? kCols : 4;
+#pragma unroll
+        for (int j0 = 0; j0 < kCols; j0 += kChunk) {
+          uint32_t rv[kChunk];
+#pragma unroll
+          for (int j = 0; j < kChunk; ++j) {
+            const int64_t t = t0 + cq * kCols + j0 + j;
+            rv[j] = t < p.T ? (uint32_t)p.r[t * n_rows + row] : 0u;
+          }
+#pragma unroll
+          for (int j = 0; j < kChunk; ++j) {
+            const int64_t t = t0 + cq * kCols + j0 + j;
+            const float v = ((j0 + j) & 1) ? acc[(j0 + j) / 2].y : acc[(j0 + j) / 2].x;
+            if (t < p.T) yo[t * n_rows + row] = float_to_bf16_bits(v + __uint_as_float(rv[j] << 16));
+          }
         }
       }
     }
