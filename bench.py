@@ -363,10 +363,14 @@ def measure_ours(args, wl, rank, world, local, sampler=None, with_e2e=True):
         launches = 1 if T <= 4 else -(-T // 4)
     stream = torch.cuda.Stream(dev)
 
-    if qtype != "q4g64":   # the streaming GEMV (1..4 tokens), else Q5 / Q6 tiles, W8 warp-MMA
+    if qtype != "q4g64":   # the streaming GEMV (1..4 tokens), else Q5 / Q6 tiles, W8 warp-MMA to 24 tokens, tiles beyond
         launches = q4lin.kernel_launches(N, K, T, qtype)
-        route = q4lin.ROUTE_GEMV if launches == 1 else (
-            q4lin.ROUTE_STREAM_MMA if qtype == "w8g32" else q4lin.ROUTE_TC_SPLITK)
+        if T <= 4 and launches == 1:
+            route = q4lin.ROUTE_GEMV
+        elif qtype == "w8g32" and T <= 24:
+            route = q4lin.ROUTE_STREAM_MMA
+        else:
+            route = q4lin.ROUTE_TC_SPLITK
 
     if op != "linear":   # the exact tile route for every T: one launch, or two with a tail launch
         n_plan = 128 * 2 * -(-N // 128) if op == "pair" else N
@@ -492,7 +496,8 @@ def measure_ours(args, wl, rank, world, local, sampler=None, with_e2e=True):
     del flush
     return dict(sample_us=sample_us, steps=K_steps, samples=S, copies=R, cold_us=cold_us, clocks=clocks,
                 route=q4lin.ROUTE_NAMES.get(route, str(route)), launches=launches, e2e=e2e,
-                tile=(pl if op != "linear" else q4lin.tile_plan_full(N, K, T, route_arg)), ws_bytes=ws_n)
+                tile=(pl if op != "linear" else
+                      q4lin.tile_plan_full(N, K, T, route_arg) if qtype == "q4g64" else None), ws_bytes=ws_n)
 
 
 def measure_read_probe(local, logical_bytes):

@@ -72,12 +72,18 @@ def test_q4_through_the_format_entry_is_q4lin_linear():
 
 @pytest.mark.parametrize("N,K,T", [(64, 256, 5), (300, 200, 37), (1001, 4096, 130), (640, 4304, 33),
                                    (77, 17408, 8), (6144, 5120, 24), (257, 1152, 517), (5, 128, 1000),
-                                   (6144, 5120, 1024)])
+                                   (6144, 5120, 1024), (129, 8192, 25), (1000, 2048, 40), (333, 640, 70)])
 def test_w8_beyond_four_tokens_matches_oracle(N, K, T):
-    """W8G32 beyond the decode GEMV: the streaming warp-MMA route (signed codes offset by
-    128 as exact fp16 subnormals, two MMAs per 32-wide group, passes of 32 tokens)."""
+    """W8G32 beyond the decode GEMV: up to 24 tokens the streaming warp-MMA route (signed
+    codes offset by 128 as exact fp16 subnormals, two MMAs per 32-wide group), beyond it the
+    exact tile route (codes as exact bf16, one tensor-memory accumulator per 32-wide scale
+    group, token tiles up to 64 wide)."""
     planes, s, x = synth.make_problem_fmt("w8g32", N, K, T, w_seed=N + 5, x_seed=K + T)
-    assert q4lin.kernel_launches(N, K, T, "w8g32") == 2 * -(-T // 32)
+    if T <= 24:
+        assert q4lin.kernel_launches(N, K, T, "w8g32") == 2
+    else:
+        assert q4lin.kernel_launches(N, K, T, "w8g32") in (1, 2)   # the tile route (and a tail launch)
+        assert q4lin.load().q4lin_qtype_workspace_bytes(3, N, K, T) == 0
     assert_close(_run("w8g32", planes, s, x), sf.linear("w8g32", planes, s, x), f"w8g32 {N}x{K} T={T}")
 
 

@@ -135,18 +135,23 @@ template <> struct TcCfg<16> { static constexpr int SX = 8, SA = 8, NB = 8, NACC
 template <int BN, bool kFold, int FMT = 0>
 struct TcSmem {
   using C = TcCfg<BN>;
-  static constexpr int kHB = FMT;  // high bits per weight
+  static constexpr int kHB = (FMT == 1 || FMT == 2) ? FMT : 0;  // high bits per weight (Q5 / Q6)
+  static constexpr bool kW8 = FMT == 3;  // W8G32: one code byte per weight, two 32-wide scale groups per 64-wide group
   static_assert(FMT == 0 || (!kFold && BN <= 128), "sibling formats: exact form, BN <= 128");
+  static_assert(!kW8 || BN <= 64, "W8G32: token tiles up to 64 wide");
   // The folded form keeps one accumulator for the whole K share, which leaves tensor
   // memory room for A at BN = 256 too; the shared memory freed there holds six X
   // stages instead of four (measured 8-12 % faster at T = 1024).
   static constexpr bool kWide = kFold && BN == 256;
-  static constexpr int SX = kWide ? 6 : C::SX, SA = C::SA, NB = kFold ? 1 : C::NB, NACC = C::NACC, SW = C::SW;
+  // W8G32 keeps two accumulators per group in flight (one per 32-wide scale group)
+  static constexpr int SX = kWide ? 6 : C::SX, SA = C::SA, NB = kFold ? 1 : kW8 ? 2 : C::NB, NACC = C::NACC, SW = C::SW;
+  static constexpr int kAccPerGroup = kW8 ? 2 : 1;
+  static constexpr uint32_t kCB = kW8 ? 2 * kWBytes : kWBytes;  // one code stage (4 groups)
   static constexpr bool kATmem = kWide ? true : C::kATmem;
   static_assert(SA % 2 == 0 && SX % 2 == 0, "the A and X ring depths must be even (one decode team per slot)");
   static_assert(kRing % 2 == 0 && kRing >= SX && kRing >= SA && kRing >= NB,
                 "the barrier rings must cover every buffer ring (no waiter two phases behind)");
-  static_assert(NB * BN + (kATmem ? SA * 32 : 0) <= 512, "tensor memory budget");
+  static_assert(kAccPerGroup * NB * BN + (kATmem ? SA * 32 : 0) <= 512, "tensor memory budget");
   static constexpr int threads = 128 * (3 + NACC);
   // decode team + issuer, and (exact form) the accumulate warps handing back a buffer
   static constexpr uint32_t issue_threads = 128 + (kFold ? 0 : 128 * NACC) + 32;
@@ -155,14 +160,14 @@ struct TcSmem {
   static constexpr uint32_t a_off = x_off + SX * kB;  // shared-memory A stages (A not in tensor memory)
   static constexpr uint32_t c_off = a_off + (kATmem ? 0 : SA * kABytes);
   static constexpr uint32_t kHBytes = kTileM * kGroupsPerW * 8 * kHB;  // one high-bit stage
-  static constexpr uint32_t h_off = c_off + SW * kWBytes;
+  static constexpr uint32_t h_off = c_off + SW * kCB;
   static constexpr uint32_t bar_off = h_off + SW * kHBytes;
   // x_full[SX], c_full[SW], c_empty[SW], mma_done[kRing], done, fin
   static constexpr uint32_t n_bars = SX + 2 * SW + kRing + 2;
   static constexpr uint32_t misc_off = bar_off + n_bars * 8;
   static constexpr uint32_t bytes = misc_off + 16;
   static constexpr uint32_t alloc = bytes + 1024;  // slack for 1024-byte alignment
-  static constexpr uint32_t a_col = NB * BN;       // first A column in tensor memory
+  static constexpr uint32_t a_col = kAccPerGroup * NB * BN;  // first A column in tensor memory
   static constexpr uint32_t tmem_cols = 512;
   // split-K partial sums of the other CTAs of the cluster reuse the pipeline buffers
   static constexpr int max_splitk = 1 + (int)(bar_off / (kTileM * BN * 4));
@@ -181,6 +186,16 @@ template <> struct TcRegs<false> { static constexpr int ctl = 56, dec = 48, acc 
 static_assert(128 * TcRegs<true>::ctl + 256 * TcRegs<true>::dec + 512 * TcRegs<true>::acc <= 896 * 72, "register split");
 static_assert(128 * TcRegs<false>::ctl + 256 * TcRegs<false>::dec + 512 * TcRegs<false>::acc <= 896 * 72, "register split");
 
+// W8G32: the four signed codes of one code word (weights k .. k + 3, byte j = weight
+// k + j) as two exact bf16 pairs, even k in the low half: |code| <= 128 fits bf16's
+// 8-bit significand.
+__device__ __forceinline__ void w8_word_bf16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const float f0 = (float)(int8_t)(w & 0xFFu), f1 = (float)(int8_t)((w >> 8) & 0xFFu);
+  const float f2 = (float)(int8_t)((w >> 16) & 0xFFu), f3 = (float)(int8_t)(w >> 24);
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(f1), "f"(f0));  // upper half: the first operand
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hi) : "f"(f3), "f"(f2));
+}
+
 template <int N>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* v) {
   if constexpr (N == 16) tmem_ld16(taddr, *reinterpret_cast<uint32_t(*)[16]>(v));
@@ -194,6 +209,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
              const __grid_constant__ CUtensorMap tm_high, const TcParams p) {
   using L = TcSmem<BN, kFold, FMT>;
   constexpr int kHB = L::kHB;
+  constexpr bool kW8 = L::kW8;
   using R = TcRegs<L::kATmem>;
   constexpr int SX = L::SX, SA = L::SA, NB = L::NB, NACC = L::NACC, SW = L::SW;
   constexpr int kAccWarps = 4 * NACC;
@@ -303,8 +319,13 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
       for (int ws = 0; ws < nws; ++ws) {
         const int slot = ws % SW;
         if (!(ok = mbar_wait(c_empty(slot), ((ws / SW) & 1) ^ 1, abort_flag, &g_tc_status))) break;
-        mbar_expect_tx(c_full(slot), kWBytes + L::kHBytes);
-        if constexpr (MODE == 1) {  // SwiGLU: gate rows into tile rows 0..63, up rows into 64..127 (64-row boxes)
+        mbar_expect_tx(c_full(slot), L::kCB + L::kHBytes);
+        if constexpr (kW8) {  // 64 code bytes per group and row: two 128-byte boxes of two groups each
+          tma_load_2d(sbase + L::c_off + slot * L::kCB, &tm_codes, c_full(slot), (g_begin + ws * kGroupsPerW) * 64,
+                      (int32_t)m0);
+          tma_load_2d(sbase + L::c_off + slot * L::kCB + kWBytes, &tm_codes, c_full(slot),
+                      (g_begin + ws * kGroupsPerW + 2) * 64, (int32_t)m0);
+        } else if constexpr (MODE == 1) {  // SwiGLU: gate rows into tile rows 0..63, up rows into 64..127 (64-row boxes)
           tma_load_2d(sbase + L::c_off + slot * kWBytes, &tm_codes, c_full(slot), (g_begin + ws * kGroupsPerW) * 32,
                       (int32_t)m0);
           tma_load_2d(sbase + L::c_off + slot * kWBytes + kWBytes / 2, &tm_codes, c_full(slot),
@@ -340,10 +361,16 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
         if (lane == 0) {
           const int s = i % SX, sa = i % SA, b = i % NB;
           const uint32_t b_lo = b_lo0 + ((uint32_t)(s * L::kB) >> 4);
-          const uint32_t d = tmem_base + (uint32_t)(b * BN);
+          const uint32_t d = tmem_base + (uint32_t)(b * L::kAccPerGroup * BN);
           // exact form: each group starts its own buffer; folded form: one sum over the share
           const bool first = kFold ? i == 0 : true;
-          if constexpr (L::kATmem) {
+          if constexpr (kW8) {
+            // W8G32: K 0..31 of the group into buffer d, K 32..63 into d + BN (one per scale group)
+            const uint32_t a = tmem_base + L::a_col + (uint32_t)(sa * 32);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16_ts32(d + (uint32_t)((kk >> 1) * BN), a + 8 * kk, b_lo + 2 * kk, b_hi, idesc, (kk & 1) != 0);
+          } else if constexpr (L::kATmem) {
             const uint32_t a = tmem_base + L::a_col + (uint32_t)(sa * 32);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
@@ -404,13 +431,28 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
         }
       }
       ok = ok && warp_wait(c_full(slot), (ws / SW) & 1, abort_flag, &g_tc_status);
-      const uint32_t csrc = sbase + L::c_off + slot * kWBytes + r * 128;
-      uint4 cw[4];
+      const uint32_t csrc = sbase + L::c_off + slot * L::kCB + r * 128;
+      uint4 cw[4] = {};
+      // W8G32: group gl of the stage is 64 code bytes of the row, 16-byte chunks
+      // 4 (gl % 2) .. + 3 of the 128-byte box gl / 2
+      uint4 cw8[kW8 ? 8 : 1];
+      if constexpr (kW8) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int c0 = 2 * (team + 2 * h);  // first 16-byte chunk of group team + 2h
-        cw[2 * h] = ok ? ld_shared_v4(csrc + ((c0 ^ (r & 7)) << 4)) : make_uint4(0, 0, 0, 0);
-        cw[2 * h + 1] = ok ? ld_shared_v4(csrc + (((c0 + 1) ^ (r & 7)) << 4)) : make_uint4(0, 0, 0, 0);
+        for (int h = 0; h < 2; ++h) {
+          const int gl = team + 2 * h;
+          const uint32_t bsrc = csrc + (uint32_t)((gl >> 1) * kWBytes);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            cw8[4 * h + j] = ok ? ld_shared_v4(bsrc + ((uint32_t)((4 * (gl & 1) + j) ^ (r & 7)) << 4))
+                                : make_uint4(0, 0, 0, 0);
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int c0 = 2 * (team + 2 * h);  // first 16-byte chunk of group team + 2h
+          cw[2 * h] = ok ? ld_shared_v4(csrc + ((c0 ^ (r & 7)) << 4)) : make_uint4(0, 0, 0, 0);
+          cw[2 * h + 1] = ok ? ld_shared_v4(csrc + (((c0 + 1) ^ (r & 7)) << 4)) : make_uint4(0, 0, 0, 0);
+        }
       }
       // Q5 / Q6: the two groups' high bits (8 * kHB bytes per group in a row of the
       // unswizzled high-bit stage)
@@ -461,14 +503,25 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
             s2 = hb | (hb << 16);
           }
           if constexpr (L::kATmem) {
-            uint32_t v[32];  // column j = code byte j = (k = 2j, k = 2j + 1)
+            uint32_t v[32];  // column j = (k = 2j, k = 2j + 1) of the group
+            if constexpr (kW8) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const uint4 d4 = decode(j, s2);
-              v[4 * j + 0] = d4.x;
-              v[4 * j + 1] = d4.y;
-              v[4 * j + 2] = d4.z;
-              v[4 * j + 3] = d4.w;
+              for (int j = 0; j < 4; ++j) {  // chunk j: k = 16 j .. 16 j + 15
+                const uint4 c4 = cw8[4 * h + j];
+                w8_word_bf16(c4.x, v[8 * j + 0], v[8 * j + 1]);
+                w8_word_bf16(c4.y, v[8 * j + 2], v[8 * j + 3]);
+                w8_word_bf16(c4.z, v[8 * j + 4], v[8 * j + 5]);
+                w8_word_bf16(c4.w, v[8 * j + 6], v[8 * j + 7]);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const uint4 d4 = decode(j, s2);
+                v[4 * j + 0] = d4.x;
+                v[4 * j + 1] = d4.y;
+                v[4 * j + 2] = d4.z;
+                v[4 * j + 3] = d4.w;
+              }
             }
             tmem_st32(a_lane + (uint32_t)(sa * 32), v);
             tmem_st_wait();
@@ -535,6 +588,39 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
                                            __uint_as_float(v[j + 1]) * exp2i(rfr + e1));
           }
         }
+      }
+    } else if constexpr (kW8) {
+      // W8G32: a row holds K_pad / 32 scales; group i (64 wide) has the pair 2 ga, 2 ga + 1,
+      // one 32-bit load, fetched a group ahead.  Its two partials sit in buffers 2b, 2b + 1.
+      const uint32_t* srow8 = reinterpret_cast<const uint32_t*>(scl + (row_ok ? row : 0) * (p.Kp >> 5));
+      uint32_t sp_next = (row_ok && ng > 0) ? __ldg(srow8 + g_begin) : 0u;
+      for (int i = 0; i < NB && i < ng; ++i) named_bar_arrive(issue_bar(i), L::issue_threads);
+      for (int i = 0; i < ng; ++i) {
+        const int b = i % NB;
+        const uint32_t sp = sp_next;
+        if (row_ok && i + 1 < ng) sp_next = __ldg(srow8 + g_begin + i + 1);
+        acc_ok = acc_ok && warp_wait(mma_done(i), ring_par(i), abort_flag, &g_tc_status);
+        if (acc_ok) {
+          tc_fence_after();
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const float sf = fp16_bits_to_float((uint16_t)(hh ? (sp >> 16) : (sp & 0xFFFFu)));
+            const float2 s2 = make_float2(sf, sf);
+            const uint32_t dcol = tlane + (uint32_t)((2 * b + hh) * BN);
+#pragma unroll
+            for (int c = 0; c < kCols; c += 16) {
+              uint32_t v[16];
+              tmem_ld_cols<16>(dcol + c, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 16; j += 2)
+                acc[(c + j) / 2] = ffma2(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), s2, acc[(c + j) / 2]);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (i + NB < ng) named_bar_arrive(issue_bar(i + NB), L::issue_threads);  // buffers 2b, 2b + 1 are free
       }
     } else {
       // Scales are read as pairs of groups (a row holds K_pad / 64 scales, an even
@@ -892,8 +978,9 @@ int launch_tile(const LinearArgs& a, int splitk, int64_t tile_base, int64_t n_ti
   const void* xsrc = kFold ? static_cast<const void*>(ws) : static_cast<const void*>(a.x);
   // SwiGLU: the code plane holds 2N rows and a tile loads 64 gate rows and 64 up rows
   const uint64_t code_rows = a.mode == 1 ? (uint64_t)(2 * a.N) : (uint64_t)a.N;
-  if (!make_map_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.wq, (uint64_t)(Kp / 2), code_rows,
-                   (uint64_t)(Kp / 2), 128, a.mode == 1 ? kTileM / 2 : kTileM) ||
+  const uint64_t code_row_bytes = (uint64_t)(L::kW8 ? Kp : Kp / 2);  // W8G32: one byte per weight
+  if (!make_map_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.wq, code_row_bytes, code_rows, code_row_bytes, 128,
+                   a.mode == 1 ? kTileM / 2 : kTileM) ||
       !make_map_2d(&tm_x, kFold ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xsrc,
                    (uint64_t)a.K, (uint64_t)a.T, (uint64_t)a.K * 2, 64, BN)) {
     set_error_detail("tc: cuTensorMapEncodeTiled failed (or is unavailable)");
@@ -1048,7 +1135,10 @@ TcPlan tc_plan(int route, int64_t N, int64_t K, int64_t T, int sms, int fmt) {
   // 152 tiles, then 40 tiles in clusters of 2; 100.8 us instead of 113.3 us).
   int cand[2] = {0, 0};
   int ncand = 0;
-  if (T > 128 && fmt != 0) {  // Q5 / Q6: the high-bit stages leave no room for 256-wide tiles
+  if (fmt == 3) {  // W8G32: two accumulators per group leave tensor memory for 64-wide tiles at most
+    cand[0] = T > 32 ? 64 : T > 16 ? 32 : 16;
+    ncand = 1;
+  } else if (T > 128 && fmt != 0) {  // Q5 / Q6: the high-bit stages leave no room for 256-wide tiles
     cand[0] = 128;
     ncand = 1;
   } else if (T > 128) {
@@ -1135,8 +1225,8 @@ int tc_launch(const LinearArgs& a, int route) {
     set_error_detail("tc: shape beyond the tensor-core route's limits");
     return Q4LIN_ERR_INVALID_ARG;
   }
-  if (a.fmt != 0 && (route_folds(route) || (a.fmt != 1 && a.fmt != 2))) {
-    set_error_detail("tc: sibling formats run on the exact tile routes, Q5G64 and Q6G64 only");
+  if (a.fmt != 0 && (route_folds(route) || a.fmt < 1 || a.fmt > 3)) {
+    set_error_detail("tc: sibling formats run on the exact tile routes (Q5G64, Q6G64, W8G32)");
     return Q4LIN_ERR_UNSUPPORTED_SHAPE;
   }
   // rows the tile space covers: SwiGLU 2N (64 + 64 per tile), Pair both weights' row tiles
@@ -1150,6 +1240,14 @@ int tc_launch(const LinearArgs& a, int route) {
   const TcPlan pl = tc_plan_current_device(route, n_plan, a.K, a.T, a.fmt);
   const bool fold = route_folds(route);
   auto launch = [&](int splitk, int64_t base, int64_t n) {
+    if (a.fmt == 3) {
+      switch (pl.bn) {
+        case 64: return launch_tile<64, false, 3>(a, splitk, base, n);
+        case 32: return launch_tile<32, false, 3>(a, splitk, base, n);
+        case 16: return launch_tile<16, false, 3>(a, splitk, base, n);
+        default: set_error_detail("tc: no tile width for this format"); return (int)Q4LIN_ERR_UNSUPPORTED_SHAPE;
+      }
+    }
     if (a.fmt != 0) {
       const bool q5 = a.fmt == 1;
       switch (pl.bn) {

@@ -148,6 +148,9 @@ int run_impl(int route, const uint8_t* wq, const uint16_t* scales, const uint16_
 
 // Sibling formats: the same checks as the Q4 layer, plus the high-bit plane for
 // Q5G64 / Q6G64, then the streaming GEMV (1..4 tokens) or UNSUPPORTED_SHAPE.
+// W8G32 beyond the warp-MMA route's token range takes the tile route.
+bool w8_tile(int64_t N, int64_t K, int64_t T) { return T > kMmaMaxT && q4::tc_supported(N, K, T); }
+
 int run_qtype_impl(int qtype, const uint8_t* codes, const uint8_t* high, const uint16_t* scales,
                    const uint16_t* x, uint16_t* y, int64_t N, int64_t K, int64_t T, void* workspace, void* stream) {
   int st = validate(codes, scales, x, y, N, K, T);
@@ -165,8 +168,10 @@ int run_qtype_impl(int qtype, const uint8_t* codes, const uint8_t* high, const u
   a.wh = needs_high ? high : nullptr;
   // The streaming GEMV where it has a plan (1..4 tokens); otherwise Q5 / Q6 run on the
   // exact tile route (token tiles up to 128 wide), and W8 on the streaming warp-MMA route
-  // (passes of 32 tokens; its operand pass needs workspace).
+  // up to 24 tokens (its operand pass needs workspace) and on the exact tile route beyond
+  // (token tiles up to 64 wide).
   if (q4::gemv_stream_ok(N, K, T, qtype)) return q4::gemv_launch_fmt(a);
+  if (qtype == Q4LIN_QTYPE_W8G32 && w8_tile(N, K, T)) return q4::tc_launch(a, Q4LIN_ROUTE_TC_SPLITK);
   if (qtype == Q4LIN_QTYPE_W8G32 && q4::mma_supported(N, K, T, 3)) {
     const size_t ws = round256(q4::mma_workspace_bytes(N, K, T, 3));
     if (ws > 0 && workspace == nullptr) return Q4LIN_ERR_WORKSPACE;
@@ -323,6 +328,7 @@ int q4lin_qtype_kernel_launches(int qtype, int64_t N, int64_t K, int64_t T) {
   if (validate_sizes(N, K, T) != Q4LIN_OK || N == 0 || T == 0) return 0;
   if (K == 0) return 1;  // the zero fill
   if (q4::gemv_stream_ok(N, K, T, qtype)) return 1;
+  if (qtype == Q4LIN_QTYPE_W8G32 && w8_tile(N, K, T)) return q4::tc_launch_count(Q4LIN_ROUTE_TC_SPLITK, N, K, T, qtype);
   if (qtype == Q4LIN_QTYPE_W8G32) return q4::mma_supported(N, K, T, 3) ? q4::mma_launch_count(N, K, T) : 0;
   if (!q4::tc_supported(N, K, T)) return 0;  // refused
   return q4::tc_launch_count(Q4LIN_ROUTE_TC_SPLITK, N, K, T, qtype);
@@ -332,7 +338,7 @@ size_t q4lin_qtype_workspace_bytes(int qtype, int64_t N, int64_t K, int64_t T) {
   if (qtype == Q4LIN_QTYPE_Q4G64) return q4lin_workspace_bytes(N, K, T);
   if (qtype != Q4LIN_QTYPE_W8G32) return 0;
   if (validate_sizes(N, K, T) != Q4LIN_OK || N == 0 || K == 0 || T == 0) return 0;
-  if (q4::gemv_stream_ok(N, K, T, qtype)) return 0;
+  if (q4::gemv_stream_ok(N, K, T, qtype) || w8_tile(N, K, T)) return 0;
   return round256(q4::mma_workspace_bytes(N, K, T, 3));
 }
 
