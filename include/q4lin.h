@@ -136,10 +136,11 @@ typedef enum {
  * Q4G64 is exactly q4lin_linear (workspace as q4lin_workspace_bytes).  The
  * other formats run on the decode GEMV for 1..4 tokens where its shared-memory
  * plan fits.  Other shapes of Q5G64 and Q6G64 run on the exact tile route
- * (token tiles up to 128 wide; the high-bit plane is staged beside the codes), and
- * other shapes of W8G32 on the streaming warp-MMA route (passes of 32 tokens), whose
- * operand pass needs workspace: q4lin_qtype_workspace_bytes (256-byte aligned, NULL
- * allowed where that is 0).  W8G32 shapes no route can plan return
+ * (token tiles up to 128 wide; the high-bit plane is staged beside the codes).  W8G32
+ * runs on the streaming warp-MMA route for 5..24 tokens, whose operand pass needs
+ * workspace: q4lin_qtype_workspace_bytes (256-byte aligned, NULL allowed where that is
+ * 0), and on the exact tile route beyond (codes as exact bf16, one accumulator per
+ * 32-wide scale group, token tiles up to 64 wide; no workspace).  W8G32 shapes no route can plan return
  * Q4LIN_ERR_UNSUPPORTED_SHAPE.
  */
 int q4lin_linear_qtype(int qtype, const uint8_t* codes, const uint8_t* high, const uint16_t* scales,
