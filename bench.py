@@ -3,6 +3,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--samples S] [--impl ours|reference]
                     [--workload NAME] [--t T] [--qtype FMT] [--route R] [--op OP] [--profile]
+    python bench.py --workload q4_6144x5120 --sweep 1:128:1,384,385,512,640,641,1024 [--csv-out F]
 
 A step is one call of the layer on one batch of the workload's synthetic input.
 With no --workload the run times three records of the 6144 x 5120 layer: the
@@ -19,6 +20,12 @@ ms_per_step = median sample / K; value = the metric at that time; min and p95
 are reported too.  The linear-benchmark contract's own method (section 6: one
 call per sample behind the flush, median) is reported as cold_call.  Metrics
 follow the contract's sections 4-5 (weight_only_bit_q4_gb300.metrics).
+
+--sweep times a contiguous T range (and single T values) of one workload under the
+contract's cold-cache method only (section 6: per T, the first call untimed, 3 warm-up
+calls, then 20 samples of one public call behind a 256 MiB flush; median, min, p95), and
+prints the contract's console header and one line per T (section 7) with the change of the
+median against the previous T (delta_%), optionally to a CSV file as well.
 
 --qtype times a sibling weight format (Q5G64, Q6G64, W8G32) on the same geometry
 through q4lin_linear_qtype; its bytes are that format's.  Under torchrun (N > 1)
@@ -96,6 +103,11 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-probe", action="store_true", help="skip the HBM read probe")
+    p.add_argument("--sweep", default=None,
+                   help="T values of one workload: comma-separated A:B:S ranges and single values "
+                        "(cold-cache per-call timing, one line per T with delta_%%)")
+    p.add_argument("--repeat", type=int, default=20, help="--sweep: timed samples per T")
+    p.add_argument("--csv-out", default=None, help="--sweep: also write the lines to this CSV file")
     a = p.parse_args(argv)
     a.warmup = max(a.warmup, 3)
     a.steps = max(a.steps, 1)
@@ -772,8 +784,136 @@ def record_summary(wl, res, peaks, world, dev):
     }
 
 
+# ----------------------------------------------------------------------------- T sweep
+DRAM_SPEC_GBS = 7900.0   # GB300 HBM3e, nominal
+
+
+def parse_sweep(spec):
+    """T values of a --sweep spec: comma-separated A:B:S ranges (inclusive) and single values."""
+    ts = []
+    for part in spec.split(","):
+        part = part.strip()
+        if not part:
+            continue
+        if ":" in part:
+            f = [int(v) for v in part.split(":")]
+            a, b, st = (f + [1])[:3] if len(f) == 2 else f
+            if st < 1 or a < 1 or b < a:
+                raise SystemExit(f"bad sweep range {part}")
+            ts.extend(range(a, b + 1, st))
+        else:
+            ts.append(int(part))
+    out = []
+    for t in ts:
+        if t < 1:
+            raise SystemExit(f"bad sweep value {t}")
+        if t not in out:
+            out.append(t)
+    return out
+
+
+SWEEP_COLUMNS = ("label", "qtype", "policy", "N", "K", "T", "median_us", "min_us", "p95_us", "model_GB",
+                 "effective_GB/s", "DRAM_%", "READ_%", "useful_TFLOP/s", "memory_floor_pct", "delta_%")
+
+
+def sweep_row(label, qtype, N, K, T, us_sorted, sustained_read, prev_median):
+    """One line of the sweep (the contract's section 7 fields, from section 4-5 formulas)."""
+    med = statistics.median(us_sorted)
+    mb = metrics.model_bytes(N, K, T, qtype)
+    eff = mb / (med * 1e-6) / 1e9
+    floor_us = mb / (DRAM_SPEC_GBS * 1e9) * 1e6
+    return {
+        "label": label, "qtype": qtype, "policy": "a16", "N": N, "K": K, "T": T,
+        "median_us": round(med, 3), "min_us": round(us_sorted[0], 3),
+        "p95_us": round(metrics.percentile(us_sorted, 95), 3), "model_GB": round(mb / 1e9, 6),
+        "effective_GB/s": round(eff, 1), "DRAM_%": round(100.0 * eff / DRAM_SPEC_GBS, 2),
+        "READ_%": round(100.0 * eff / sustained_read, 2) if sustained_read else None,
+        "useful_TFLOP/s": round(metrics.useful_flops(N, K, T) / (med * 1e-6) / 1e12, 3),
+        "memory_floor_pct": round(100.0 * floor_us / med, 2),
+        "delta_%": None if prev_median is None else round(100.0 * (med - prev_median) / prev_median, 2),
+    }
+
+
+def measure_sweep_point(wl, ts_repeat, dev, stream, flush, sink, weights):
+    """Cold-cache per-call samples (us, sorted) of one sweep point through the public call."""
+    import numpy as np
+    import torch
+    from weight_only_bit_q4_gb300 import q4lin
+
+    N, K, T = wl["N"], wl["K"], wl["T"]
+    x = synth.activations(T, K, wl["x_seed"], outliers=wl["outliers"])
+    x_d = torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+    y = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
+    ws_n = q4lin.workspace_bytes(N, K, T)
+    ws = torch.empty(max(ws_n, 256), dtype=torch.uint8, device=dev)
+    wq_d, sc_d = weights
+
+    def call():
+        q4lin.linear(wq_d, sc_d, x_d, y=y, workspace=ws if ws_n else None, stream=stream)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(ts_repeat)]
+    with torch.cuda.stream(stream):
+        call()                      # first public call: not timed
+        for _ in range(3):          # warm-up
+            call()
+        for i, (a, b) in enumerate(ev):
+            flush.fill_(i & 0x7FFF)                 # 256 MiB written, then read: L2 holds none of the call's data
+            torch.sum(flush, dim=0, out=sink)
+            a.record(stream)
+            call()
+            b.record(stream)
+    torch.cuda.synchronize(dev)
+    return sorted(a.elapsed_time(b) * 1e3 for a, b in ev)
+
+
+def run_sweep(args):
+    import numpy as np
+    import torch
+    from weight_only_bit_q4_gb300 import q4lin
+
+    if args.qtype != "q4g64" or args.op != "linear" or args.route != "auto":
+        raise SystemExit("--sweep times the Q4 layer (q4lin_linear) only")
+    name = args.workload or "q4_6144x5120"
+    if WORKLOADS[name][2] is not None:
+        raise SystemExit(f"--sweep needs a workload whose T is free (not {name})")
+    ts = parse_sweep(args.sweep)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(dev)
+    wl0 = workload(args, name, ts[0])
+    N, K = wl0["N"], wl0["K"]
+    wq = synth.packed_codes(N, K, wl0["w_seed"])
+    sc = synth.group_scales(N, K, wl0["w_seed"], wl0["dist"])
+    weights = (torch.from_numpy(wq).to(dev), torch.from_numpy(sc.view(np.int16)).to(dev))
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    sink = torch.empty((), dtype=torch.int32, device=dev)
+    probe = measure_read_probe(0, metrics.model_bytes(N, K, 1))
+    sustained = probe["gbs_4gib"]
+    print(f"gpu={torch.cuda.get_device_name(dev)}")
+    print(f"dram_spec={DRAM_SPEC_GBS:.1f} GB/s")
+    print(f"sustained_read={sustained:.1f} GB/s")
+    print("cache=cold")
+    print(" ".join(SWEEP_COLUMNS))
+    rows, prev = [], None
+    for t in ts:
+        wl = workload(args, name, t)
+        us = measure_sweep_point(wl, args.repeat, dev, stream, flush, sink, weights)
+        row = sweep_row(f"{name}_t{t}", "q4g64", N, K, t, us, sustained, prev)
+        prev = row["median_us"]
+        rows.append(row)
+        print(" ".join("-" if row[c] is None else str(row[c]) for c in SWEEP_COLUMNS), flush=True)
+    if args.csv_out:
+        import csv
+        with open(args.csv_out, "w", newline="") as f:
+            w = csv.DictWriter(f, fieldnames=list(SWEEP_COLUMNS))
+            w.writeheader()
+            w.writerows(rows)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.sweep is not None:
+        return run_sweep(args)
     rank, world, local = dist_env()
     specs = record_specs(args)
     wls = [workload(args, n, t) for (n, t) in specs]

@@ -72,3 +72,22 @@ def test_secondary_records(line):
         for k in ("us", "roofline", "cold_call", "clocks", "steps", "samples", "route", "tile"):
             assert k in r, k
         assert r["steps"] == 10
+
+
+def test_sweep_spec_and_line():
+    # --sweep: ranges and single values in order, duplicates dropped; one line per T with the
+    # contract's fields and the change of the median against the previous T
+    assert bench.parse_sweep("1:4:1,8,2:3,384,385") == [1, 2, 3, 4, 8, 384, 385]
+    assert bench.parse_sweep("4:16:4") == [4, 8, 12, 16]
+    with pytest.raises(SystemExit):
+        bench.parse_sweep("0:4:1")
+    r1 = bench.sweep_row("w_t1", "q4g64", 6144, 5120, 1, [8.0, 8.0, 9.0], 7200.0, None)
+    mb = metrics.model_bytes(6144, 5120, 1)
+    assert r1["median_us"] == 8.0 and r1["min_us"] == 8.0 and r1["delta_%"] is None
+    assert r1["effective_GB/s"] == pytest.approx(mb / 8e-6 / 1e9, rel=1e-3)
+    assert r1["DRAM_%"] == pytest.approx(100 * mb / 8e-6 / 1e9 / bench.DRAM_SPEC_GBS, rel=1e-3)
+    assert r1["READ_%"] == pytest.approx(100 * mb / 8e-6 / 1e9 / 7200.0, rel=1e-3)
+    assert r1["memory_floor_pct"] == pytest.approx(r1["DRAM_%"], rel=1e-3)   # both against the spec
+    r2 = bench.sweep_row("w_t2", "q4g64", 6144, 5120, 2, [10.0, 10.0], 7200.0, r1["median_us"])
+    assert r2["delta_%"] == pytest.approx(25.0)
+    assert list(r2) == list(bench.SWEEP_COLUMNS)

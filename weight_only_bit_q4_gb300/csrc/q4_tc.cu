@@ -138,16 +138,20 @@ struct TcSmem {
   static constexpr int kHB = (FMT == 1 || FMT == 2) ? FMT : 0;  // high bits per weight (Q5 / Q6)
   static constexpr bool kW8 = FMT == 3;  // W8G32: one code byte per weight, two 32-wide scale groups per 64-wide group
   static_assert(FMT == 0 || (!kFold && BN <= 128), "sibling formats: exact form, BN <= 128");
-  static_assert(!kW8 || BN <= 64, "W8G32: token tiles up to 64 wide");
+  static_assert(!kW8 || BN <= 128, "W8G32: token tiles up to 128 wide");
+  // W8G32 at 128-token tiles: two accumulators per group in flight fill tensor memory, so A
+  // is staged in shared memory (four X, A and code stages fit beside it)
+  static constexpr bool kW8Wide = kW8 && BN == 128;
   // The folded form keeps one accumulator for the whole K share, which leaves tensor
   // memory room for A at BN = 256 too; the shared memory freed there holds six X
   // stages instead of four (measured 8-12 % faster at T = 1024).
   static constexpr bool kWide = kFold && BN == 256;
   // W8G32 keeps two accumulators per group in flight (one per 32-wide scale group)
-  static constexpr int SX = kWide ? 6 : C::SX, SA = C::SA, NB = kFold ? 1 : kW8 ? 2 : C::NB, NACC = C::NACC, SW = C::SW;
+  static constexpr int SX = kWide ? 6 : kW8Wide ? 4 : C::SX, SA = kW8Wide ? 4 : C::SA, NB = kFold ? 1 : kW8 ? 2 : C::NB,
+                       NACC = C::NACC, SW = kW8Wide ? 2 : C::SW;
   static constexpr int kAccPerGroup = kW8 ? 2 : 1;
   static constexpr uint32_t kCB = kW8 ? 2 * kWBytes : kWBytes;  // one code stage (4 groups)
-  static constexpr bool kATmem = kWide ? true : C::kATmem;
+  static constexpr bool kATmem = kWide ? true : kW8Wide ? false : C::kATmem;
   static_assert(SA % 2 == 0 && SX % 2 == 0, "the A and X ring depths must be even (one decode team per slot)");
   static_assert(kRing % 2 == 0 && kRing >= SX && kRing >= SA && kRing >= NB,
                 "the barrier rings must cover every buffer ring (no waiter two phases behind)");
@@ -364,12 +368,17 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
           const uint32_t d = tmem_base + (uint32_t)(b * L::kAccPerGroup * BN);
           // exact form: each group starts its own buffer; folded form: one sum over the share
           const bool first = kFold ? i == 0 : true;
-          if constexpr (kW8) {
+          if constexpr (kW8 && L::kATmem) {
             // W8G32: K 0..31 of the group into buffer d, K 32..63 into d + BN (one per scale group)
             const uint32_t a = tmem_base + L::a_col + (uint32_t)(sa * 32);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               mma_f16_ts32(d + (uint32_t)((kk >> 1) * BN), a + 8 * kk, b_lo + 2 * kk, b_hi, idesc, (kk & 1) != 0);
+          } else if constexpr (kW8) {
+            const uint32_t a_lo = a_lo0 + ((uint32_t)(sa * kABytes) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16_ss(d + (uint32_t)((kk >> 1) * BN), a_lo + 2 * kk, a_hi, b_lo + 2 * kk, b_hi, idesc, (kk & 1) != 0);
           } else if constexpr (L::kATmem) {
             const uint32_t a = tmem_base + L::a_col + (uint32_t)(sa * 32);
 #pragma unroll
@@ -434,19 +443,12 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
       const uint32_t csrc = sbase + L::c_off + slot * L::kCB + r * 128;
       uint4 cw[4] = {};
       // W8G32: group gl of the stage is 64 code bytes of the row, 16-byte chunks
-      // 4 (gl % 2) .. + 3 of the 128-byte box gl / 2
-      uint4 cw8[kW8 ? 8 : 1];
-      if constexpr (kW8) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int gl = team + 2 * h;
-          const uint32_t bsrc = csrc + (uint32_t)((gl >> 1) * kWBytes);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            cw8[4 * h + j] = ok ? ld_shared_v4(bsrc + ((uint32_t)((4 * (gl & 1) + j) ^ (r & 7)) << 4))
-                                : make_uint4(0, 0, 0, 0);
-        }
-      } else {
+      // 4 (gl % 2) .. + 3 of the 128-byte box gl / 2, read where the group is decoded (the
+      // stage is released after the team's last group)
+      auto w8_chunk = [&](int gl, int j) -> uint4 {
+        return ld_shared_v4(csrc + (uint32_t)((gl >> 1) * kWBytes) + ((uint32_t)((4 * (gl & 1) + j) ^ (r & 7)) << 4));
+      };
+      if constexpr (!kW8) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int c0 = 2 * (team + 2 * h);  // first 16-byte chunk of group team + 2h
@@ -472,9 +474,11 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
         }
       }
       // The code slot is free once both teams have their chunks in registers (a TMA
-      // refill must not race the reads above).
-      __syncwarp();
-      if (lane == 0) mbar_arrive(c_empty(slot));
+      // refill must not race the reads above); W8G32 reads its chunks below.
+      if constexpr (!kW8) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(c_empty(slot));
+      }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int i = ws * kGroupsPerW + team + 2 * h;
@@ -507,7 +511,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
             if constexpr (kW8) {
 #pragma unroll
               for (int j = 0; j < 4; ++j) {  // chunk j: k = 16 j .. 16 j + 15
-                const uint4 c4 = cw8[4 * h + j];
+                const uint4 c4 = w8_chunk(team + 2 * h, j);
                 w8_word_bf16(c4.x, v[8 * j + 0], v[8 * j + 1]);
                 w8_word_bf16(c4.y, v[8 * j + 2], v[8 * j + 3]);
                 w8_word_bf16(c4.z, v[8 * j + 4], v[8 * j + 5]);
@@ -528,9 +532,23 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
           } else {
             // row r of the 128-byte-swizzled K-major A stage: 16-byte chunk j holds k = 8j .. 8j + 7
             const uint32_t adst = sbase + L::a_off + sa * kABytes + r * 128;
+            if constexpr (kW8) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              st_shared_v4(adst + ((j ^ (r & 7)) << 4), decode(j, s2));
+              for (int j = 0; j < 4; ++j) {  // code chunk j (k = 16 j .. + 15) -> A chunks 2 j, 2 j + 1
+                const uint4 c4 = w8_chunk(team + 2 * h, j);
+                uint32_t q[8];
+                w8_word_bf16(c4.x, q[0], q[1]);
+                w8_word_bf16(c4.y, q[2], q[3]);
+                w8_word_bf16(c4.z, q[4], q[5]);
+                w8_word_bf16(c4.w, q[6], q[7]);
+                st_shared_v4(adst + ((uint32_t)((2 * j) ^ (r & 7)) << 4), make_uint4(q[0], q[1], q[2], q[3]));
+                st_shared_v4(adst + ((uint32_t)((2 * j + 1) ^ (r & 7)) << 4), make_uint4(q[4], q[5], q[6], q[7]));
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                st_shared_v4(adst + ((j ^ (r & 7)) << 4), decode(j, s2));
+            }
             fence_proxy_async();  // generic-proxy stores -> the tensor core's (async-proxy) reads
           }
         }
@@ -538,6 +556,10 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
         tc_fence_before();
         __syncwarp();
         named_bar_arrive(issue_bar(i), L::issue_threads);  // always: the issuer must never wait forever
+      }
+      if constexpr (kW8) {  // the team's chunks of this stage are read
+        __syncwarp();
+        if (lane == 0) mbar_arrive(c_empty(slot));
       }
     }
     __syncwarp();
@@ -1135,8 +1157,8 @@ TcPlan tc_plan(int route, int64_t N, int64_t K, int64_t T, int sms, int fmt) {
   // 152 tiles, then 40 tiles in clusters of 2; 100.8 us instead of 113.3 us).
   int cand[2] = {0, 0};
   int ncand = 0;
-  if (fmt == 3) {  // W8G32: two accumulators per group leave tensor memory for 64-wide tiles at most
-    cand[0] = T > 32 ? 64 : T > 16 ? 32 : 16;
+  if (fmt == 3) {  // W8G32: two accumulators per group (A in shared memory at 128-wide tiles)
+    cand[0] = T > 64 ? 128 : T > 32 ? 64 : T > 16 ? 32 : 16;
     ncand = 1;
   } else if (T > 128 && fmt != 0) {  // Q5 / Q6: the high-bit stages leave no room for 256-wide tiles
     cand[0] = 128;
@@ -1242,6 +1264,7 @@ int tc_launch(const LinearArgs& a, int route) {
   auto launch = [&](int splitk, int64_t base, int64_t n) {
     if (a.fmt == 3) {
       switch (pl.bn) {
+        case 128: return launch_tile<128, false, 3>(a, splitk, base, n);
         case 64: return launch_tile<64, false, 3>(a, splitk, base, n);
         case 32: return launch_tile<32, false, 3>(a, splitk, base, n);
         case 16: return launch_tile<16, false, 3>(a, splitk, base, n);
