@@ -62,7 +62,9 @@ typedef enum {
   Q4LIN_ROUTE_AUTO = 0,     /* let the library choose (what q4lin_linear does) */
   Q4LIN_ROUTE_GEMV = 1,     /* CUDA-core GEMV, weights decoded once per token block of <= 4 */
   Q4LIN_ROUTE_TC_SPLITK = 2,/* tcgen05 tile, K split across a thread-block cluster where the
-                               planner finds it pays (what q4lin_linear uses from 5 tokens) */
+                               planner finds it pays (what q4lin_linear uses from 33 tokens;
+                               clusters up to 8, reducing through distributed shared memory
+                               in rounds of as many partial tiles as the buffers hold) */
   Q4LIN_ROUTE_TC = 3,       /* tcgen05 tile, whole K per CTA */
   Q4LIN_ROUTE_TC_FP16 = 4,  /* opt-in: tcgen05 tile on fp16-rounded weights (see below) */
   Q4LIN_ROUTE_STREAM_MMA = 5/* streaming warp-MMA: weights streamed once by TMA, decoded in

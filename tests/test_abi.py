@@ -150,11 +150,11 @@ def test_workspace_query_and_route_selection(lib):
         ws = q4lin.workspace_bytes(N, K, T)
         assert ws % 256 == 0
         assert q4lin.select_route(N, K, T) in (1, 2, 3, 5)
-    # 2..24 tokens: the streaming warp-MMA route, whose operand pass needs workspace
-    for T in (2, 8, 16, 24):
+    # 2..32 tokens: the streaming warp-MMA route, whose operand pass needs workspace
+    for T in (2, 8, 16, 24, 32):
         assert q4lin.select_route(6144, 5120, T) == q4lin.ROUTE_STREAM_MMA
         assert q4lin.workspace_bytes(6144, 5120, T) > 0
-    assert q4lin.select_route(6144, 5120, 25) == q4lin.ROUTE_TC_SPLITK
+    assert q4lin.select_route(6144, 5120, 33) == q4lin.ROUTE_TC_SPLITK
     assert q4lin.workspace_bytes(-1, 128, 1) == 0
     assert q4lin.workspace_bytes(4, 100, 1) == 0
     assert q4lin.workspace_bytes(0, 128, 1) == 0

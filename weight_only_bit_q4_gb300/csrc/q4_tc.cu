@@ -173,8 +173,11 @@ struct TcSmem {
   static constexpr uint32_t alloc = bytes + 1024;  // slack for 1024-byte alignment
   static constexpr uint32_t a_col = kAccPerGroup * NB * BN;  // first A column in tensor memory
   static constexpr uint32_t tmem_cols = 512;
-  // split-K partial sums of the other CTAs of the cluster reuse the pipeline buffers
-  static constexpr int max_splitk = 1 + (int)(bar_off / (kTileM * BN * 4));
+  // split-K partial sums of the other CTAs of the cluster reuse the pipeline buffers: that
+  // many partial tiles fit at once, and larger clusters reduce in rounds of that many
+  static constexpr int kRedSlots = (int)(bar_off / (kTileM * BN * 4));
+  static_assert(kRedSlots >= 1, "one partial tile must fit in the pipeline buffers");
+  static constexpr int max_splitk = 8;  // portable cluster size
 };
 
 // Registers per thread after the split (four accumulate warpgroups only; with
@@ -276,6 +279,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
   }
   const int ng = g_end - g_begin;
   const int nws = (ng + kGroupsPerW - 1) / kGroupsPerW;
+  const int red_rounds = splitk > 1 ? (splitk - 1 + L::kRedSlots - 1) / L::kRedSlots : 0;  // split-K reduction rounds
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < SX; ++s) mbar_init(x_full(s), 1);
@@ -397,7 +401,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
       if (lane == 0) mma_commit(fin_bar);  // arrives once every MMA issued here has completed
     }
     __syncwarp();
-    if (splitk > 1) {  // the accumulate warpgroups reduce between these two cluster barriers
+    for (int rr = 0; rr < red_rounds; ++rr) {  // the accumulate warpgroups reduce between these cluster barriers
       cluster_sync();
       cluster_sync();
     }
@@ -563,7 +567,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
       }
     }
     __syncwarp();
-    if (splitk > 1) {
+    for (int rr = 0; rr < red_rounds; ++rr) {
       cluster_sync();
       cluster_sync();
     }
@@ -719,23 +723,28 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant
 
     // ----------------------------------------------------------- split-K reduction across the cluster
     __syncwarp();
-    if (splitk > 1) {
-      cluster_sync();  // every CTA of the cluster is past its main loop: rank 0's buffers are free
-      if (crank > 0) {
+    // rounds of kRedSlots partial tiles; rank 0 adds them in rank order (deterministic)
+    for (int rr = 0; rr < red_rounds; ++rr) {
+      const int q0 = 1 + rr * L::kRedSlots;
+      const int q1 = q0 + L::kRedSlots < splitk ? q0 + L::kRedSlots : splitk;
+      // every CTA of the cluster is past its main loop, and rank 0 has added the previous
+      // round: rank 0's buffers are free
+      cluster_sync();
+      if ((int)crank >= q0 && (int)crank < q1) {
         const uint32_t remote0 = mapa_shared(sbase, 0);
 #pragma unroll
         for (int c = 0; c < kCols; c += 4) {
-          const uint32_t off = (((crank - 1) * (BN / 4) + (cq * kCols + c) / 4) * kTileM + r_acc) * 16;
+          const uint32_t off = ((((int)crank - q0) * (BN / 4) + (cq * kCols + c) / 4) * kTileM + r_acc) * 16;
           st_cluster_v4(remote0 + off, acc[c / 2].x, acc[c / 2].y, acc[c / 2 + 1].x, acc[c / 2 + 1].y);
         }
       }
-      cluster_sync();  // partial sums have landed in rank 0
+      cluster_sync();  // this round's partial sums have landed in rank 0
       if (crank == 0) {
 #pragma unroll 1
-        for (int q = 1; q < splitk; ++q) {
+        for (int q = q0; q < q1; ++q) {
 #pragma unroll
           for (int c = 0; c < kCols; c += 4) {
-            const uint32_t off = (((q - 1) * (BN / 4) + (cq * kCols + c) / 4) * kTileM + r_acc) * 16;
+            const uint32_t off = (((q - q0) * (BN / 4) + (cq * kCols + c) / 4) * kTileM + r_acc) * 16;
             const float4 v = ld_shared_f4(sbase + off);
             acc[c / 2] = fadd2(acc[c / 2], make_float2(v.x, v.y));
             acc[c / 2 + 1] = fadd2(acc[c / 2 + 1], make_float2(v.z, v.w));
@@ -1078,6 +1087,16 @@ int launch_prep(const LinearArgs& a) {
                     "tc: prep kernel launch");
 }
 
+int red_slots_for(int bn) {  // partial tiles the reduction moves per round (the folded layout's: fewest)
+  switch (bn) {
+    case 256: return TcSmem<256, true>::kRedSlots;
+    case 128: return TcSmem<128, true>::kRedSlots;
+    case 64: return TcSmem<64, true>::kRedSlots;
+    case 32: return TcSmem<32, true>::kRedSlots;
+    default: return TcSmem<16, true>::kRedSlots;
+  }
+}
+
 int max_splitk_for(int bn) {  // the same shared-memory layout in both forms
   switch (bn) {
     case 256: return TcSmem<256, true>::max_splitk;
@@ -1187,8 +1206,10 @@ TcPlan tc_plan(int route, int64_t N, int64_t K, int64_t T, int sms, int fmt) {
       }
       return per_wave;
     };
+    const int slots = red_slots_for(bn);
     auto cta_ns = [&](int s) -> double {
-      return (double)((nk + s - 1) / s) * tc.group_ns + tc.fixed_ns + (s > 1 ? kSplitNsPerColumn * bn : 0.0);
+      const int rounds = s > 1 ? (s - 1 + slots - 1) / slots : 0;
+      return (double)((nk + s - 1) / s) * tc.group_ns + tc.fixed_ns + rounds * kSplitNsPerColumn * bn;
     };
     for (int s = 1; s <= smax && s <= nk; ++s) {
       const int64_t per_wave = wave_capacity(s);

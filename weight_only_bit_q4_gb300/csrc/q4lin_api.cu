@@ -90,7 +90,8 @@ int check_device() {
 // Tokens at or below which the streaming warp-MMA route is chosen (where it has a plan):
 // measured on 6144 x 5120 against the tile route, 12.5 against 18.1 us at T = 8, 16.5 us
 // at T = 24, level at T = 32.
-constexpr int64_t kMmaMaxT = 24;
+constexpr int64_t kMmaMaxT = 32;     // Q4: one pass of the warp-MMA route (measured faster than 32-token tiles)
+constexpr int64_t kW8MmaMaxT = 24;   // W8G32: the warp-MMA route up to here, the tile route beyond
 
 int route_for(int64_t N, int64_t K, int64_t T) {
   // One token: the streaming CUDA-core GEMV.  Two to kMmaMaxT tokens: the streaming
@@ -149,7 +150,7 @@ int run_impl(int route, const uint8_t* wq, const uint16_t* scales, const uint16_
 // Sibling formats: the same checks as the Q4 layer, plus the high-bit plane for
 // Q5G64 / Q6G64, then the streaming GEMV (1..4 tokens) or UNSUPPORTED_SHAPE.
 // W8G32 beyond the warp-MMA route's token range takes the tile route.
-bool w8_tile(int64_t N, int64_t K, int64_t T) { return T > kMmaMaxT && q4::tc_supported(N, K, T); }
+bool w8_tile(int64_t N, int64_t K, int64_t T) { return T > kW8MmaMaxT && q4::tc_supported(N, K, T); }
 
 int run_qtype_impl(int qtype, const uint8_t* codes, const uint8_t* high, const uint16_t* scales,
                    const uint16_t* x, uint16_t* y, int64_t N, int64_t K, int64_t T, void* workspace, void* stream) {
