@@ -62,6 +62,9 @@ constexpr int kMaxConsumers = kMmaWarps - 1;
 constexpr int kMaxBand = 240;  // rows per band: TMA box height <= 256, 15 m-tiles
 constexpr uint32_t kMmaSmem = 232448;  // dynamic shared memory per CTA (incl. 1024-byte alignment slack)
 constexpr int kRedBar = 1;             // named barrier of the consumer warps
+// Early launch order: L2 prefetch of one CTA's code rows before the dependency wait, at
+// most (the whole share of a 6144-row layer on 152 SMs: 103 KB at K = 5120).
+constexpr int64_t kMmaPrefetchCap = 128 * 1024;
 
 struct MmaParams {
   const uint8_t* wq;       // packed codes [N, Kp/2]
@@ -80,6 +83,7 @@ struct MmaParams {
   int nchunks;  // chunks per band
   int stages;
   int lanes;    // B-fragment lanes stored per (group, token tile)
+  int early;    // launch order: 1 early (launched before the prep kernel's wait), 0 late
   uint32_t stage_bytes, xf_off, zs_off;  // stage size; B fragments and zero points inside a stage
   uint32_t scl_off, scl_bytes;           // the two band scale buffers
   uint32_t red_off, bar_off;
@@ -115,6 +119,12 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
                : "memory");
+}
+
+// Pull global bytes into L2 (no destination, no completion): a hint that never changes
+// what a later load returns.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ uint2 lds_u64(uint32_t addr) {
@@ -213,12 +223,19 @@ q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const MmaParams p) {
     prefetch_tmap(&tm_codes);
   }
   __syncthreads();
-  // Launch order (programmatic dependent launch): the prep kernel waits for its own
-  // predecessor before it lets this kernel launch, so every kernel before this call has
-  // completed when this one starts, and the weight planes can be streamed at once.
-  // Only what the prep kernel writes (B fragments, zero points, exponents) waits for
-  // griddepcontrol.wait: the producer before its first fragment copy, the consumers
-  // before the first epilogue.
+  // Launch order (programmatic dependent launch), one of two per call (p.early):
+  //  - late: the prep kernel waits for its own predecessor before it lets this kernel
+  //    launch, so every kernel before this call has completed when this one starts, and
+  //    the weight planes are streamed at once, while the prep kernel works.  Only what
+  //    the prep kernel writes (B fragments, zero points, exponents) waits for
+  //    griddepcontrol.wait: the producer before its first fragment copy, the consumers
+  //    before the first epilogue.
+  //  - early: the prep kernel lets this kernel launch at once, so its CTAs take their SMs
+  //    as the previous kernel's CTAs leave.  Until griddepcontrol.wait returns (the prep
+  //    kernel, and with it every earlier kernel, has completed) the producer only pulls
+  //    the head of the CTA's weight rows into L2 -- the previous kernel may still write
+  //    the planes, and an L2 prefetch never changes what a later load returns -- then
+  //    streams them from there.
 
   const uint32_t xf_chunk = (uint32_t)(4 * KS * NT * p.lanes * FB);  // B-fragment bytes per chunk
   const uint32_t zs_chunk = (uint32_t)(4 * KS * NT * 64);
@@ -228,6 +245,22 @@ q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const MmaParams p) {
       const uint8_t* sc_plane = reinterpret_cast<const uint8_t*>(p.scales);
       const int64_t plane_bytes = p.N * srb;
       bool ok = true, waited = false;
+      if (p.early) {
+        // the first kMmaPrefetchCap bytes of the CTA's code rows (contiguous) and the
+        // 16-byte-aligned interior of those rows' scale run, 32 KB per prefetch
+        const int64_t code_row = kW8 ? p.Kp : p.Kp / 2;
+        const uint8_t* cb = p.wq + r0 * code_row;
+        int64_t len = (r1 - r0) * code_row;
+        if (len > kMmaPrefetchCap) len = kMmaPrefetchCap;
+        for (int64_t off = 0; off < len; off += 32768)
+          bulk_prefetch_l2(cb + off, (uint32_t)(len - off < 32768 ? len - off : 32768));
+        const int64_t pf_end = r0 + (len + code_row - 1) / code_row;  // <= r1
+        const int64_t a0 = (r0 * srb + 15) & ~(int64_t)15, a1 = (pf_end * srb) & ~(int64_t)15;
+        for (int64_t off = a0; off < a1; off += 32768)
+          bulk_prefetch_l2(sc_plane + off, (uint32_t)(a1 - off < 32768 ? a1 - off : 32768));
+        pdl_wait_previous();  // before the first copy into shared memory
+        waited = true;
+      }
       int it = 0, last_it = -1, last_band = -1, frag_next = 0;
       auto issue_frags = [&](int q) {  // the B fragments and zero points of iteration q
         const int gq = (q % NCH) * 4 * KS;
@@ -269,8 +302,8 @@ q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const MmaParams p) {
           mbar_expect_tx(full(s), (uint32_t)(nsub * BR * 128) + xf_chunk + zs_chunk);
           for (int k = 0; k < nsub; ++k)
             tma_load_2d(sb + (uint32_t)(k * BR * 128), &tm_codes, full(s), (j * KS + k) * 128, (int32_t)R0);
-          // band 0's first stages carry their code sub-boxes before the wait; every later
-          // wait of the producer (a free stage, a free scale buffer) comes after it
+          // late order: band 0's first stages carry their code sub-boxes before the wait;
+          // every later wait of the producer (a free stage, a free scale buffer) comes after it
           if (waited || it == (NS < NCH ? NS : NCH) - 1) {
             if (!waited) {
               pdl_wait_previous();
@@ -421,11 +454,14 @@ constexpr int kPrepThreads = 256;
 template <int NT, int FMT>
 __global__ void __launch_bounds__(kPrepThreads)
 q4_mma_prep_kernel(const uint16_t* __restrict__ x, uint8_t* __restrict__ xf, float* __restrict__ zs,
-                   int64_t K, int tp, int galloc, int lanes) {
-  // Wait for the previous kernel (it may write x, or still read these buffers), and only
-  // then let the streaming kernel launch: it reads the weight planes as soon as it starts.
+                   int64_t K, int tp, int galloc, int lanes, int early) {
+  // Wait for the previous kernel (it may write x, or still read these buffers).  The
+  // streaming kernel launches after that wait (late order: it copies weight rows as soon
+  // as it starts) or before it (early order: it only prefetches them into L2 until its
+  // own wait).
+  if (early) pdl_launch_dependents();
   pdl_wait_previous();
-  pdl_launch_dependents();
+  if (!early) pdl_launch_dependents();
   constexpr bool kW8 = FMT == 3;
   constexpr int kVals = kW8 ? 8 : 16;  // values of one (group, c) unit
   const int64_t units = (int64_t)8 * NT * galloc * 4;   // a multiple of 32: whole warps take part
@@ -492,13 +528,23 @@ q4_mma_prep_kernel(const uint16_t* __restrict__ x, uint8_t* __restrict__ xf, flo
 
 // ----------------------------------------------------------------- host side
 struct MmaPlan {
-  int fmt, nt, grid, br, ks, mt, nchunks, stages, lanes, galloc, nk, fbytes;
+  int fmt, nt, grid, br, ks, mt, nchunks, stages, lanes, galloc, nk, fbytes, early;
   int64_t code_row, srb;  // bytes of one row of the code plane and of the scale plane
   MmaLayout L;
 };
 
 // Token tiles per pass: T <= 8, 16, 24 or 32; a call with more tokens runs passes of 32.
 int mma_nt(int64_t T) { return T >= 32 ? 4 : (int)((T + 7) / 8); }
+
+// Launch order of a pass.  Early hides the streaming kernel's launch behind the previous
+// kernel but copies its weight rows into shared memory only after the prep kernel has
+// finished; late streams them while the prep kernel works.  Early pays off while the B
+// fragments are small against the weight rows and the CTA's rows fit the L2 prefetch.
+// Measured on 6144 x 5120, back-to-back calls (late -> early): Q4 T = 2, 3, 4: 10.54 ->
+// 9.83, 10.63 -> 9.90, 10.70 -> 9.96 us; T = 5, 6: 11.02 -> 10.90, 11.07 -> 10.95;
+// T = 7 even; T = 8: 10.92 -> 11.24; T = 12: 13.0 -> 13.9; W8G32 T = 5..8 about 1.1 us
+// slower early (its code rows are twice as long).
+int mma_early_order(int fmt, int lanes, int nt) { return (fmt == 0 && nt == 1 && lanes <= 24) ? 1 : 0; }
 
 // fmt 0: Q4G64; fmt 3: W8G32 (the other formats have no plan here)
 bool mma_plan_for(int64_t N, int64_t K, int64_t T, int sms, MmaPlan* pl, int fmt = 0) {
@@ -515,6 +561,7 @@ bool mma_plan_for(int64_t N, int64_t K, int64_t T, int sms, MmaPlan* pl, int fmt
   pl->nt = mma_nt(T);
   const int tpass = (int)(T < 8 * pl->nt ? T : 8 * pl->nt);
   pl->lanes = (pl->nt == 1 && tpass < 8) ? 4 * tpass : 32;
+  pl->early = mma_early_order(fmt, pl->lanes, pl->nt);
   int64_t grid = (N + 7) / 8;  // at least 8 rows per CTA
   if (grid > sms) grid = sms;
   pl->grid = (int)grid;
@@ -595,7 +642,7 @@ int mma_launch_pass(const LinearArgs& a, const MmaPlan& pl, const CUtensorMap& t
     cfg.attrs = at;
     cfg.numAttrs = 1;
     if (cuda_check(cudaLaunchKernelEx(&cfg, q4_mma_prep_kernel<NT, FMT>, a.x + t0 * a.K, xf, zs, a.K, tp,
-                                      pl.galloc, pl.lanes),
+                                      pl.galloc, pl.lanes, pl.early),
                    "mma: prep kernel launch"))
       return Q4LIN_ERR_CUDA;
   }
@@ -618,6 +665,7 @@ int mma_launch_pass(const LinearArgs& a, const MmaPlan& pl, const CUtensorMap& t
   p.nchunks = pl.nchunks;
   p.stages = pl.stages;
   p.lanes = pl.lanes;
+  p.early = pl.early;
   p.stage_bytes = pl.L.stage_bytes;
   p.xf_off = pl.L.code_bytes;
   p.zs_off = pl.L.code_bytes + pl.L.xf_bytes;
