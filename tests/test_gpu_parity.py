@@ -197,7 +197,7 @@ def test_graph_replay_after_input_change():
     t = torch()
     N, K = 6144, 5120
     wq, s, w = weights(N, K)
-    for T in [1, 8, 64, 1024]:
+    for T in [1, 4, 8, 64, 1024]:
         x1 = synth.activations(T, K, 100 + T)
         x2 = synth.activations(T, K, 200 + T)
         wq_d, s_d, x_d = to_dev(wq, s, x1)
