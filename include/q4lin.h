@@ -233,6 +233,30 @@ int q4lin_linear_route(int route, const uint8_t* wq, const uint16_t* scales, con
  */
 int q4lin_linear_fp16_static(const uint8_t* wq, const uint16_t* scales, const uint16_t* x, uint16_t* y,
                              int64_t N, int64_t K, int64_t T, void* stream);
+
+/*
+ * q4lin_linear with X and Y in page-locked host memory (cudaHostAlloc, or
+ * cudaHostRegister'ed and mapped), for callers whose activations live on the host.
+ * The pages describe no such entry point.  In stream order: a kernel copies X from
+ * x_host into the workspace, q4lin_linear runs on it (its own route choice), and a
+ * kernel copies Y back to y_host.  The copies are SM loads and stores of the
+ * page-locked memory, chained to the layer by programmatic dependent launch; on a
+ * host the GPU reaches coherently they start within a launch.
+ *   x_host     page-locked host, bf16 [T, K], 16-byte aligned (read only)
+ *   y_host     page-locked host, bf16 [T, N], 16-byte aligned (fully overwritten
+ *              once the stream reaches the end of the call)
+ *   workspace  device, >= q4lin_host_workspace_bytes(N, K, T) bytes, 256-byte
+ *              aligned: X staging (2TK bytes), Y staging (2TN bytes), each rounded
+ *              up to 256, then q4lin_linear's own workspace
+ *   wq, scales, N, K, T, stream: as q4lin_linear.
+ * A pointer that is not page-locked host memory of this process (pageable memory,
+ * device memory) returns Q4LIN_ERR_INVALID_ARG with a detail, before any launch.
+ * The host buffers belong to the call until the stream passes it: do not touch them
+ * (or free them) before then.
+ */
+size_t q4lin_host_workspace_bytes(int64_t N, int64_t K, int64_t T);
+int q4lin_linear_host(const uint8_t* wq, const uint16_t* scales, const uint16_t* x_host, uint16_t* y_host,
+                      int64_t N, int64_t K, int64_t T, void* workspace, void* stream);
 size_t q4lin_route_workspace_bytes(int route, int64_t N, int64_t K, int64_t T);
 
 /* The route q4lin_linear picks for (N, K, T) on the current device (host-only logic). */

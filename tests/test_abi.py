@@ -267,3 +267,19 @@ def test_fused_entry_points_host_checks(lib):
     assert pr(a, a, a, a, a, b, vp(8), 64, 64, 256, 4, None) == 3
     assert pr(a, a, a, a, a, b, b, 64, 64, 100, 4, None) == 2
     assert pr(None, None, None, None, None, None, None, 0, 0, 256, 4, None) == 0
+
+
+def test_host_entry_workspace_and_host_checks(lib):
+    # q4lin_linear_host: X staging, Y staging (each rounded up to 256), then the layer's own workspace
+    def r256(b):
+        return -(-b // 256) * 256
+    for N, K, T in [(6144, 5120, 1), (6144, 5120, 16), (333, 640, 37), (40, 0, 3)]:
+        want = r256(2 * T * K) + r256(2 * T * N) + q4lin.workspace_bytes(N, K, T)
+        assert q4lin.host_workspace_bytes(N, K, T) == want
+    assert q4lin.host_workspace_bytes(0, 128, 4) == 0 and q4lin.host_workspace_bytes(4, 100, 1) == 0
+    f, vp = lib.q4lin_linear_host, ctypes.c_void_p
+    assert f(vp(16), vp(16), vp(16), vp(16), 64, 256, 4, None, None) == 4        # no workspace
+    assert f(vp(16), vp(16), vp(16), vp(16), 64, 256, 4, vp(128), None) == 3     # workspace not 256-aligned
+    assert f(vp(16), vp(16), None, vp(16), 64, 256, 4, vp(256), None) == 1       # no X
+    assert f(vp(16), vp(16), vp(16), vp(8), 64, 256, 4, vp(256), None) == 3      # y not 16-byte aligned
+    assert f(None, None, None, None, 0, 256, 4, None, None) == 0                 # empty

@@ -14,7 +14,7 @@ def _fake_measure(args, wl, rank, world, local, sampler=None, with_e2e=True):
     return dict(sample_us=[us] * 60, steps=args.steps, samples=60, copies=8,
                 cold_us=[12.0] * 200, route="gemv" if wl["T"] == 1 else "tc_splitk", launches=1,
                 clocks={"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 5},
-                e2e=dict(us=[32.0] * 100, h2d=2 * wl["K"] * wl["T"], d2h=2 * wl["N"] * wl["T"]) if with_e2e else None,
+                e2e=dict(us=[32.0] * 100, memcpy_us=[36.0] * 100, eager_us=[40.0] * 100, host_entry=True, h2d=2 * wl["K"] * wl["T"], d2h=2 * wl["N"] * wl["T"]) if with_e2e else None,
                 tile={"n": 0, "split_k": 1, "main_tiles": 0, "tail_split_k": 0}, ws_bytes=0)
 
 
@@ -56,6 +56,8 @@ def test_derived_figures(line):
     assert line["roofline"]["frac"] == pytest.approx(line["roofline"]["achieved"] / line["roofline"]["peak"], rel=1e-3)
     assert line["e2e"]["value"] == pytest.approx(mb / 32e-6 / 1e9, rel=1e-3)
     assert line["e2e"]["h2d_bytes_per_step"] == 2 * 5120 and line["e2e"]["d2h_bytes_per_step"] == 2 * 6144
+    assert line["e2e"]["eager_us"] == pytest.approx(40.0) and line["e2e"]["memcpy_us"] == pytest.approx(36.0)
+    assert "q4lin_linear_host" in line["e2e"]["method"]
     assert line["gpu_launches"] == 10 * 60
 
 

@@ -91,6 +91,9 @@ int probe_status(int* value, bool clear);
 
 // Diagnostics: HBM read probe and the bounded-wait expiry check.
 int hbm_read_probe(const void* src, size_t bytes, uint32_t* sink, int blocks, cudaStream_t stream);
+// Copies `bytes` (a multiple of 2; both pointers 16-byte aligned and device-accessible,
+// page-locked host memory included) in stream order, chained by programmatic launch.
+int stage_copy(const void* src, void* dst, size_t bytes, cudaStream_t stream);
 int wait_expiry(uint32_t limit, int* out, cudaStream_t stream);
 
 }  // namespace q4

@@ -192,9 +192,58 @@ int run(int route, const uint8_t* wq, const uint16_t* scales, const uint16_t* x,
   return st;
 }
 
+// The device-side address of page-locked host memory of this process (nullptr for
+// pageable or device memory): what the staging kernels of q4lin_linear_host access.
+const void* host_device_ptr(const void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
+int run_host_impl(const uint8_t* wq, const uint16_t* scales, const uint16_t* x_host, uint16_t* y_host, int64_t N,
+                  int64_t K, int64_t T, void* workspace, void* stream) {
+  int st = validate(wq, scales, x_host, y_host, N, K, T);
+  if (st != Q4LIN_OK || N == 0 || T == 0) return st;
+  if (workspace == nullptr) return Q4LIN_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return Q4LIN_ERR_MISALIGNED;
+  st = check_device();
+  if (st != Q4LIN_OK) return st;
+  const void* xd = K > 0 ? host_device_ptr(x_host) : nullptr;   // K == 0: X is not read
+  void* yd = const_cast<void*>(host_device_ptr(y_host));
+  if ((K > 0 && xd == nullptr) || yd == nullptr) {
+    q4::set_error_detail("x_host and y_host must be page-locked host memory of this process "
+                         "(cudaHostAlloc, or cudaHostRegister and mapped)");
+    return Q4LIN_ERR_INVALID_ARG;
+  }
+  const size_t xb = round256((size_t)T * (size_t)K * 2), yb = round256((size_t)T * (size_t)N * 2);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint16_t* xs = reinterpret_cast<uint16_t*>(ws);
+  uint16_t* ys = reinterpret_cast<uint16_t*>(ws + xb);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K > 0 && (st = q4::stage_copy(xd, xs, (size_t)T * (size_t)K * 2, s)) != Q4LIN_OK) return st;
+  if ((st = run_impl(Q4LIN_ROUTE_AUTO, wq, scales, xs, ys, N, K, T, ws + xb + yb, stream)) != Q4LIN_OK) return st;
+  return q4::stage_copy(ys, yd, (size_t)T * (size_t)N * 2, s);
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t q4lin_host_workspace_bytes(int64_t N, int64_t K, int64_t T) {
+  if (validate_sizes(N, K, T) != Q4LIN_OK || N == 0 || T == 0) return 0;
+  return round256((size_t)T * (size_t)K * 2) + round256((size_t)T * (size_t)N * 2) + q4lin_workspace_bytes(N, K, T);
+}
+
+int q4lin_linear_host(const uint8_t* wq, const uint16_t* scales, const uint16_t* x_host, uint16_t* y_host,
+                      int64_t N, int64_t K, int64_t T, void* workspace, void* stream) {
+  q4::set_error_detail("");
+  const int st = run_host_impl(wq, scales, x_host, y_host, N, K, T, workspace, stream);
+  if (st != Q4LIN_OK && q4::g_detail[0] == 0) q4::set_error_detail(q4lin_status_string(st));
+  return st;
+}
 
 size_t q4lin_workspace_bytes(int64_t N, int64_t K, int64_t T) {
   if (validate_sizes(N, K, T) != Q4LIN_OK || N == 0 || K == 0 || T == 0) return 0;

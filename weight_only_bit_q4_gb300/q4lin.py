@@ -27,7 +27,7 @@ EXPORTS = ("q4lin_workspace_bytes", "q4lin_linear", "q4lin_linear_route", "q4lin
            "q4lin_status_string",
            "q4lin_device_status", "q4lin_clear_device_status", "q4lin_last_error_detail",
            "q4lin_hbm_read_probe", "q4lin_diag_wait_expiry", "q4lin_linear_swiglu", "q4lin_linear_pair",
-           "q4lin_qtype_workspace_bytes", "q4lin_version")
+           "q4lin_qtype_workspace_bytes", "q4lin_host_workspace_bytes", "q4lin_linear_host", "q4lin_version")
 
 _lib = None
 
@@ -96,6 +96,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q4lin_linear_swiglu.restype = ctypes.c_int
     lib.q4lin_linear_pair.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, vp]
     lib.q4lin_linear_pair.restype = ctypes.c_int
+    lib.q4lin_host_workspace_bytes.argtypes = [i64, i64, i64]
+    lib.q4lin_host_workspace_bytes.restype = sz
+    lib.q4lin_linear_host.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp]
+    lib.q4lin_linear_host.restype = ctypes.c_int
     lib.q4lin_version.argtypes = []
     lib.q4lin_version.restype = ctypes.c_char_p
     if path is None:
@@ -207,6 +211,44 @@ def linear(wq, scales, x, y=None, workspace=None, stream=None, route: int = ROUT
     if st != OK:
         raise Q4LinError(st)
     return y
+
+
+def host_workspace_bytes(N: int, K: int, T: int) -> int:
+    return int(load().q4lin_host_workspace_bytes(N, K, T))
+
+
+def linear_host(wq, scales, x_host, y_host=None, workspace=None, stream=None):
+    """q4lin_linear_host: X and Y in page-locked host memory, the weights on the GPU.
+
+    x_host: pinned CPU bf16 [T, K] (or int16 bit patterns); ``y_host`` (pinned CPU bf16
+    [T, N]) and ``workspace`` (CUDA uint8, >= host_workspace_bytes) are allocated here if
+    not given.  The call is stream-ordered: y_host holds the result once ``stream`` (a
+    torch.cuda.Stream, default the current one) has passed it.
+    """
+    import torch
+
+    T, K = x_host.shape
+    N = wq.shape[0]
+    Kp = (K + 127) // 128 * 128
+    if tuple(wq.shape) != (N, Kp // 2) or tuple(scales.shape) != (N, Kp // 64):
+        raise ValueError(f"shape mismatch: wq {tuple(wq.shape)} scales {tuple(scales.shape)} x {tuple(x_host.shape)}")
+    for name, t in (("wq", wq), ("scales", scales)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if x_host.is_cuda or not x_host.is_contiguous() or x_host.element_size() != 2:
+        raise ValueError("x_host must be a contiguous 2-byte CPU tensor (pinned)")
+    if y_host is None:
+        y_host = torch.empty((T, N), dtype=torch.bfloat16).pin_memory()
+    elif y_host.is_cuda or tuple(y_host.shape) != (T, N) or y_host.element_size() != 2 or not y_host.is_contiguous():
+        raise ValueError("y_host must be a contiguous 2-byte CPU [T, N] tensor (pinned)")
+    if workspace is None:
+        workspace = torch.empty(max(host_workspace_bytes(N, K, T), 256), dtype=torch.uint8, device=wq.device)
+    s = (stream or torch.cuda.current_stream(wq.device)).cuda_stream
+    st = int(load().q4lin_linear_host(_ptr(wq), _ptr(scales), _ptr(x_host), _ptr(y_host), N, K, T,
+                                      _ptr(workspace), ctypes.c_void_p(s)))
+    if st != OK:
+        raise Q4LinError(st)
+    return y_host
 
 
 def linear_add(wq, scales, x, r, y=None, stream=None):
