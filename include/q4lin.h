@@ -238,16 +238,16 @@ int q4lin_linear_fp16_static(const uint8_t* wq, const uint16_t* scales, const ui
  * q4lin_linear with X and Y in page-locked host memory (cudaHostAlloc, or
  * cudaHostRegister'ed and mapped), for callers whose activations live on the host.
  * The pages describe no such entry point.  In stream order: a kernel copies X from
- * x_host into the workspace, q4lin_linear runs on it (its own route choice), and a
- * kernel copies Y back to y_host.  The copies are SM loads and stores of the
- * page-locked memory, chained to the layer by programmatic dependent launch; on a
- * host the GPU reaches coherently they start within a launch.
+ * x_host into the workspace (SM loads of the page-locked memory, chained to the
+ * layer by programmatic dependent launch), then q4lin_linear runs on it (its own
+ * route choice) and its kernels store Y straight into y_host (every route writes Y
+ * with plain stores; K == 0 stages the zeros in the workspace and copies them out).
  *   x_host     page-locked host, bf16 [T, K], 16-byte aligned (read only)
  *   y_host     page-locked host, bf16 [T, N], 16-byte aligned (fully overwritten
  *              once the stream reaches the end of the call)
  *   workspace  device, >= q4lin_host_workspace_bytes(N, K, T) bytes, 256-byte
- *              aligned: X staging (2TK bytes), Y staging (2TN bytes), each rounded
- *              up to 256, then q4lin_linear's own workspace
+ *              aligned: X staging (2TK bytes), Y staging (2TN bytes, used when
+ *              K == 0), each rounded up to 256, then q4lin_linear's own workspace
  *   wq, scales, N, K, T, stream: as q4lin_linear.
  * A pointer that is not page-locked host memory of this process (pageable memory,
  * device memory) returns Q4LIN_ERR_INVALID_ARG with a detail, before any launch.

@@ -1,5 +1,6 @@
 // Host-buffer staging of q4lin_linear_host: X copied from page-locked host memory
-// into the workspace before the layer, Y copied back after it.
+// into the workspace before the layer (the routes read X with bulk and tensor copies;
+// they store Y with plain stores, straight into the page-locked output).
 //
 // The copies are kernels rather than copy-engine transfers: on a host whose memory
 // the GPU reaches coherently, SM loads and stores of page-locked memory start within
@@ -7,7 +8,7 @@
 // Both kernels take part in the layer's programmatic-dependent-launch chain: each
 // lets the next kernel launch at once and waits for the previous one before it
 // touches memory the previous kernel may use (the X staging area the previous
-// call's kernels read; the Y staging area the layer writes).
+// call's kernels read).
 #include "q4_internal.h"
 #include "q4_sm100.cuh"
 

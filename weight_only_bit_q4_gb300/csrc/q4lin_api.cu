@@ -223,9 +223,14 @@ int run_host_impl(const uint8_t* wq, const uint16_t* scales, const uint16_t* x_h
   uint16_t* xs = reinterpret_cast<uint16_t*>(ws);
   uint16_t* ys = reinterpret_cast<uint16_t*>(ws + xb);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (K > 0 && (st = q4::stage_copy(xd, xs, (size_t)T * (size_t)K * 2, s)) != Q4LIN_OK) return st;
-  if ((st = run_impl(Q4LIN_ROUTE_AUTO, wq, scales, xs, ys, N, K, T, ws + xb + yb, stream)) != Q4LIN_OK) return st;
-  return q4::stage_copy(ys, yd, (size_t)T * (size_t)N * 2, s);
+  if (K == 0) {  // the empty sum: zeros staged on the device, then copied out
+    if ((st = run_impl(Q4LIN_ROUTE_AUTO, wq, scales, xs, ys, N, K, T, ws + xb + yb, stream)) != Q4LIN_OK) return st;
+    return q4::stage_copy(ys, yd, (size_t)T * (size_t)N * 2, s);
+  }
+  // X is staged (the routes read it with bulk and tensor copies); every route stores Y with
+  // plain stores, which write the page-locked buffer directly
+  if ((st = q4::stage_copy(xd, xs, (size_t)T * (size_t)K * 2, s)) != Q4LIN_OK) return st;
+  return run_impl(Q4LIN_ROUTE_AUTO, wq, scales, xs, static_cast<uint16_t*>(yd), N, K, T, ws + xb + yb, stream);
 }
 
 }  // namespace
