@@ -5,10 +5,10 @@
 // The copies are kernels rather than copy-engine transfers: on a host whose memory
 // the GPU reaches coherently, SM loads and stores of page-locked memory start within
 // a launch, where a small cudaMemcpyAsync pays the copy engine's setup per transfer.
-// Both kernels take part in the layer's programmatic-dependent-launch chain: each
-// lets the next kernel launch at once and waits for the previous one before it
+// The staging kernel takes part in the layer's programmatic-dependent-launch chain:
+// it lets the next kernel launch at once and waits for the previous one before it
 // touches memory the previous kernel may use (the X staging area the previous
-// call's kernels read).
+// call's kernels read).  With K == 0 the same kernel copies the staged zeros out.
 #include "q4_internal.h"
 #include "q4_sm100.cuh"
 
