@@ -384,7 +384,11 @@ def measure_ours(args, wl, rank, world, local, sampler=None, with_e2e=True):
         else:
             route = q4lin.ROUTE_TC_SPLITK
 
-    if op != "linear":   # the exact tile route for every T: one launch, or two with a tail launch
+    if op != "linear" and q4lin.fused_route(op, n_out, K, T) == q4lin.ROUTE_STREAM_MMA:
+        # a few tokens: the warp-MMA route's one-launch form, one launch per weight
+        route = q4lin.ROUTE_STREAM_MMA
+        launches = 2 if op == "pair" else 1
+    elif op != "linear":   # the exact tile route: one launch, or two with a tail launch
         n_plan = 128 * 2 * -(-N // 128) if op == "pair" else N
         pl = q4lin.tile_plan_full(n_plan, K, T, q4lin.ROUTE_TC_SPLITK)
         route = q4lin.ROUTE_TC_SPLITK
@@ -558,7 +562,7 @@ def measure_ours(args, wl, rank, world, local, sampler=None, with_e2e=True):
     del flush
     return dict(sample_us=sample_us, steps=K_steps, samples=S, copies=R, cold_us=cold_us, clocks=clocks,
                 route=q4lin.ROUTE_NAMES.get(route, str(route)), launches=launches, e2e=e2e,
-                tile=(pl if op != "linear" else
+                tile=((pl if route == q4lin.ROUTE_TC_SPLITK else None) if op != "linear" else
                       q4lin.tile_plan_full(N, K, T, route_arg) if qtype == "q4g64" else None), ws_bytes=ws_n)
 
 

@@ -158,9 +158,11 @@ size_t q4lin_qtype_workspace_bytes(int qtype, int64_t N, int64_t K, int64_t T);
  * own benchmark; the reading here): y = W . x + r, the bf16 residual r [T, N]
  * (row-major like y, 16-byte aligned) added to the FP32 sum before y's one bf16
  * rounding.  r may be y itself (in-place residual add); otherwise r and y must not
- * overlap.  Runs the exact tile route for every T (a fused GEMV form for 1..4
- * tokens is not built); no workspace.  Other arguments and errors as q4lin_linear;
- * r NULL gives Q4LIN_ERR_INVALID_ARG.  K = 0 gives y = r.
+ * overlap.  No workspace: up to 8 tokens it runs the streaming warp-MMA route's
+ * one-launch form (its kernel converts X into shared memory itself; the residual joins
+ * the sum in the epilogue) where that form's shared-memory plan fits, otherwise the
+ * exact tile route (q4lin_fused_route tells which).  Other arguments and errors as
+ * q4lin_linear; r NULL gives Q4LIN_ERR_INVALID_ARG.  K = 0 gives y = r.
  */
 int q4lin_linear_add(const uint8_t* wq, const uint16_t* scales, const uint16_t* x, const uint16_t* r, uint16_t* y,
                      int64_t N, int64_t K, int64_t T, void* stream);
@@ -174,9 +176,12 @@ int q4lin_linear_add(const uint8_t* wq, const uint16_t* scales, const uint16_t* 
  *   silu(z) = z / (1 + e^-z), all in FP32 before the one bf16 rounding.
  *   wq        device, uint8 [2F, Kp/2]; scales device, fp16 [2F, Kp/64]
  *   x         device, bf16 [T, K];     y device, bf16 [T, F] (output)
- * Runs the exact tile route for every T: a tile stacks 64 gate rows over the matching
- * 64 up rows, and the product is formed in the epilogue.  No workspace.  Alignment,
- * sizes and errors as q4lin_linear (with N = 2F).  K = 0 gives y = +0.
+ * No workspace.  Up to 8 tokens, where its shared-memory plan fits, the streaming
+ * warp-MMA route's one-launch form: each CTA streams a band of gate rows, then the band
+ * of up rows that pairs with it, and forms the product at the up band's end.  Otherwise
+ * the exact tile route: a tile stacks 64 gate rows over the matching 64 up rows, and the
+ * product is formed in the epilogue.  Alignment, sizes and errors as q4lin_linear (with
+ * N = 2F).  K = 0 gives y = +0.
  */
 int q4lin_linear_swiglu(const uint8_t* wq, const uint16_t* scales, const uint16_t* x, uint16_t* y, int64_t F,
                         int64_t K, int64_t T, void* stream);
@@ -186,14 +191,24 @@ int q4lin_linear_swiglu(const uint8_t* wq, const uint16_t* scales, const uint16_
  * two packed weights applied to the same x in one call, y_a = W_a x and y_b = W_b x.
  *   wq_a / scales_a  [N_a, Kp/2] / [N_a, Kp/64];  wq_b / scales_b  [N_b, Kp/2] / [N_b, Kp/64]
  *   x  bf16 [T, K];  y_a  bf16 [T, N_a];  y_b  bf16 [T, N_b] (outputs, must not overlap)
- * Runs the exact tile route for every T in one launch (plus a tail launch where the
- * planner splits the last wave): the row tiles of W_a are followed by those of W_b,
- * and both read the same X tiles.  No workspace.  Alignment and errors as q4lin_linear;
- * N_a or N_b may be 0 (that output is not touched).  K = 0 gives zeros.
+ * Up to 8 tokens, where the streaming warp-MMA route's one-launch form fits both
+ * weights, one launch of it per weight; otherwise the exact tile route in one launch
+ * (plus a tail launch where the planner splits the last wave): the row tiles of W_a are
+ * followed by those of W_b, and both read the same X tiles.  No workspace.  Alignment
+ * and errors as q4lin_linear; N_a or N_b may be 0 (that output is not touched).  K = 0
+ * gives zeros.
  */
 int q4lin_linear_pair(const uint8_t* wq_a, const uint16_t* scales_a, const uint8_t* wq_b, const uint16_t* scales_b,
                       const uint16_t* x, uint16_t* y_a, uint16_t* y_b, int64_t N_a, int64_t N_b, int64_t K, int64_t T,
                       void* stream);
+
+/*
+ * The route a fused operation takes for (N, K, T) on the current device (host-only
+ * logic): op 1 LinearAdd (N rows), 2 LinearSwiGLU (N = F), 3 LinearPair (N = rows of
+ * each weight).  Returns Q4LIN_ROUTE_STREAM_MMA (the one-launch warp-MMA form, one
+ * launch per weight) or Q4LIN_ROUTE_TC_SPLITK, -1 for an unknown op or invalid sizes.
+ */
+int q4lin_fused_route(int op, int64_t N, int64_t K, int64_t T);
 
 /*
  * Kernels one q4lin_linear_qtype call of this format and shape launches (0 for a

@@ -1,7 +1,9 @@
-"""GPU parity for LinearAdd (q4lin_linear_add): Y = W . X + R with the bf16 residual R
-added to the FP32 sum before Y's bf16 rounding, against the FP64 fused-operation
-oracle within the layer's tolerance.  Covers one token to 1024, padded K, a K split
-across a cluster, the in-place form (R is Y) and K = 0 (Y = R)."""
+"""GPU parity of the fused operations against the FP64 fused-operation oracle within the
+layer's tolerance.  LinearAdd (q4lin_linear_add): Y = W . X + R with the bf16 residual R
+added to the FP32 sum before Y's bf16 rounding -- one token to 1024 (the warp-MMA route's
+one-launch form up to 8 tokens, the tile route beyond or where that form does not fit),
+padded K, a K split across a cluster, the in-place form (R is Y) and K = 0 (Y = R).
+LinearSwiGLU and LinearPair (one launch per weight up to 8 tokens) likewise."""
 import numpy as np
 import pytest
 
@@ -24,7 +26,8 @@ def _lib():
 
 
 @pytest.mark.parametrize("N,K,T", [(6144, 5120, 1), (1000, 1152, 37), (640, 4304, 300), (77, 17408, 8),
-                                   (6144, 5120, 1024)])
+                                   (6144, 5120, 1024), (6144, 5120, 8), (333, 640, 7), (129, 1160, 2),
+                                   (1000, 2048, 5), (34816, 5120, 4)])
 def test_linear_add_matches_oracle(N, K, T):
     t = torch()
     wq, s, x = synth.make_problem(N, K, T, w_seed=N + 2, x_seed=K + T)
@@ -42,6 +45,17 @@ def test_linear_add_matches_oracle(N, K, T):
     assert np.array_equal(y_bits(y2), y_bits(y))
 
 
+def test_fused_ops_routes():
+    # up to 8 tokens the one-launch warp-MMA form where its whole-K operands fit, the tile route otherwise
+    assert q4lin.fused_route("add", 6144, 5120, 8) == q4lin.ROUTE_STREAM_MMA
+    assert q4lin.fused_route("add", 6144, 5120, 1) == q4lin.ROUTE_STREAM_MMA
+    assert q4lin.fused_route("add", 6144, 5120, 9) == q4lin.ROUTE_TC_SPLITK
+    assert q4lin.fused_route("add", 77, 17408, 8) == q4lin.ROUTE_TC_SPLITK    # 278 KB of operands
+    assert q4lin.fused_route("pair", 6144, 5120, 8) == q4lin.ROUTE_STREAM_MMA
+    assert q4lin.fused_route("swiglu", 17408, 5120, 8) == q4lin.ROUTE_STREAM_MMA
+    assert q4lin.fused_route("swiglu", 17408, 5120, 9) == q4lin.ROUTE_TC_SPLITK
+
+
 def test_linear_add_empty_k_copies_the_residual():
     t = torch()
     r = x_to_dev(synth.activations(3, 64, seed=5))
@@ -52,7 +66,8 @@ def test_linear_add_empty_k_copies_the_residual():
 
 
 @pytest.mark.parametrize("F,K,T", [(64, 128, 1), (100, 1152, 37), (5, 72, 17), (300, 4304, 8), (2176, 5120, 300),
-                                   (17408, 5120, 1024), (129, 17408, 3)])
+                                   (17408, 5120, 1024), (129, 17408, 3), (17408, 5120, 8), (1000, 2048, 5),
+                                   (3, 8, 2), (500, 1160, 1)])
 def test_linear_swiglu_matches_oracle(F, K, T):
     """LinearSwiGLU on a 2F-row gate/up weight (34816 x 5120 at T = 1024 among them):
     y = silu(gate) * up in FP32 before the bf16 rounding, held to the layer's bound."""
@@ -80,7 +95,8 @@ def test_linear_swiglu_guard_bands():
 
 
 @pytest.mark.parametrize("Na,Nb,K,T", [(6144, 1024, 5120, 8), (300, 77, 1152, 100), (128, 128, 256, 1024),
-                                       (1000, 3000, 2048, 257), (5, 7, 72, 2), (0, 64, 256, 3), (64, 0, 256, 3)])
+                                       (1000, 3000, 2048, 257), (5, 7, 72, 2), (0, 64, 256, 3), (64, 0, 256, 3),
+                                       (6144, 6144, 5120, 1), (200, 300, 17408, 4)])
 def test_linear_pair_matches_oracle(Na, Nb, K, T):
     """LinearPair: two weights on one X in one call, each output against its own oracle."""
     t = torch()

@@ -80,8 +80,12 @@ bool encode_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uin
 // fmt: 0 Q4G64, 3 W8G32
 bool mma_supported(int64_t N, int64_t K, int64_t T, int fmt = 0);
 size_t mma_workspace_bytes(int64_t N, int64_t K, int64_t T, int fmt = 0);
-int mma_launch_count(int64_t N, int64_t K, int64_t T);
-int mma_launch(const LinearArgs& a);
+int mma_launch_count(int64_t N, int64_t K, int64_t T, int fmt = 0);
+// fused: the one-launch form without workspace (up to 8 tokens, where the whole-K operands
+// fit in shared memory), for the entry points that take no workspace
+// (swiglu: LinearSwiGLU with N = F output rows over a 2F-row weight)
+bool mma_fused_supported(int64_t N, int64_t K, int64_t T, int fmt = 0, bool swiglu = false);
+int mma_launch(const LinearArgs& a, bool fused = false);
 int mma_status(int* value, bool clear);
 
 // Reads (and optionally clears) the device error word of one translation unit.

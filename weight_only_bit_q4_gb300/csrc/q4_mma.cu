@@ -69,11 +69,12 @@ constexpr int64_t kMmaPrefetchCap = 128 * 1024;
 struct MmaParams {
   const uint8_t* wq;       // packed codes [N, Kp/2]
   const uint16_t* scales;  // fp16 bits [N, Kp/64]
-  const uint8_t* xf;       // B fragments [galloc][NT][2][lanes][16 bytes]
+  const uint8_t* xf;       // B fragments [galloc][NT][2][lanes][16 bytes] (prep kernel's buffer)
   const float* zs;         // per (group, token tile, c): (Z[t], Z[t + 1], F[t], F[t + 1]), t = 2c
+  const uint16_t* x;       // fused form: bf16 X [T, K], converted in the kernel
   uint16_t* y;             // bf16 [T, N]
   const uint16_t* r;       // LinearAdd: bf16 residual [T, N], added before the bf16 store (may be y)
-  int64_t N, Kp, T;
+  int64_t N, K, Kp, T;
   int t0;       // first token of this pass
   int tp;       // tokens of this pass (<= 8 NT)
   int nk;       // groups holding columns < K
@@ -84,33 +85,46 @@ struct MmaParams {
   int stages;
   int lanes;    // B-fragment lanes stored per (group, token tile)
   int early;    // launch order: 1 early (launched before the prep kernel's wait), 0 late
-  uint32_t stage_bytes, xf_off, zs_off;  // stage size; B fragments and zero points inside a stage
+  int galloc;   // groups of the B-fragment buffer
+  uint32_t stage_bytes, xf_off, zs_off;  // stage size; B fragments and zero points (inside a stage, or
+                                         // the fused form's whole-K buffers)
   uint32_t scl_off, scl_bytes;           // the two band scale buffers
-  uint32_t red_off, bar_off;
+  uint32_t red_off, gate_off, bar_off;
 };
 
-// Shared-memory layout of one launch.
+// Shared-memory layout of one launch.  Stages hold a chunk's code sub-boxes and (two-kernel
+// form) its B fragments and zero-point terms; the fused form keeps the whole K extent of
+// both, written by the kernel itself, after the stages (fx_off, fz_off).
 struct MmaLayout {
   uint32_t code_bytes, xf_bytes, zs_bytes, stage_bytes, scl_bytes, red_bytes;
-  uint32_t scl_off, red_off, bar_off, total;
+  uint32_t fx_off, fx_bytes, fz_off, fz_bytes;
+  uint32_t scl_off, red_off, gate_off, bar_off, total;
 };
 
 // fbytes: B-fragment bytes per lane per group and token tile (Q4: 32, four MMAs; W8: 16, two)
 __host__ __device__ inline MmaLayout mma_layout(int nt, int br, int ks, int mt, int stages, int lanes, int64_t Kp,
-                                                int fbytes = 32, int64_t srb = 0) {
+                                                int fbytes = 32, int64_t srb = 0, bool fused = false,
+                                                int galloc = 0, bool swiglu = false) {
   MmaLayout L;
   L.code_bytes = (uint32_t)(ks * br * 128);  // ks sub-boxes of br rows x 128 bytes (128-byte swizzle)
-  L.xf_bytes = (uint32_t)(4 * ks * nt * lanes * fbytes);
-  L.zs_bytes = (uint32_t)(4 * ks * nt * 64);
+  L.xf_bytes = fused ? 0u : (uint32_t)(4 * ks * nt * lanes * fbytes);
+  L.zs_bytes = fused ? 0u : (uint32_t)(4 * ks * nt * 64);
   L.stage_bytes = (L.code_bytes + L.xf_bytes + L.zs_bytes + 1023) / 1024 * 1024;
+  L.fx_off = (uint32_t)stages * L.stage_bytes;
+  L.fx_bytes = fused ? (uint32_t)galloc * (uint32_t)(nt * lanes * fbytes) : 0u;
+  L.fz_off = L.fx_off + L.fx_bytes;
+  L.fz_bytes = fused ? (uint32_t)galloc * (uint32_t)(nt * 64) : 0u;
   // a band's scale run: br rows of Kp / 64 scales, plus up to 15 bytes of alignment slack
   // on either side
   if (srb == 0) srb = Kp / 32;  // bytes of a scale row (Q4: Kp / 64 scales)
   L.scl_bytes = (uint32_t)((br * srb + 32 + 15) / 16 * 16);
   L.red_bytes = (uint32_t)(ks * mt * 16 * 8 * nt * 4);
-  L.scl_off = (uint32_t)stages * L.stage_bytes;
+  L.scl_off = L.fz_off + L.fz_bytes;
   L.red_off = L.scl_off + 2 * L.scl_bytes;
-  L.bar_off = (L.red_off + L.red_bytes + 15) / 16 * 16;
+  // LinearSwiGLU: a gate band's FP32 sums wait here for the matching up band
+  L.gate_off = L.red_off + L.red_bytes;
+  const uint32_t gate_bytes = swiglu ? (uint32_t)(mt * 16 * 8 * nt * 4) : 0u;
+  L.bar_off = (L.gate_off + gate_bytes + 15) / 16 * 16;
   L.total = L.bar_off + (uint32_t)(2 * stages + 4) * 8 + 16;
   return L;
 }
@@ -184,9 +198,134 @@ __device__ __forceinline__ void decode_w8_pairs(uint32_t w0, uint32_t w1, uint32
   p[4] = p[5] = p[6] = p[7] = 0u;
 }
 
+// ----------------------------------------------------------------- operand pass
+// One thread per (token slot t of the pass, group G, c): the values of token t in group G
+// that thread c of an MMA feeds -- k = 64 G + 16 c .. + 15 (Q4) or 32 G + 8 c .. + 7 (W8)
+// -- become its fp16x2 B registers, in the order the decode produces A.  The four c of a
+// (t, G) are adjacent lanes: they take the group's largest |x| (compared as bf16 magnitude
+// bits) and the power of two 2^-e that puts it in [2^14, 2^15), so every value of the group
+// down to 2^-38 of that largest one converts to fp16 exactly, and the group's terms
+//     Z = -zero * 2^e * sum x-hat,   F = 2^(24 + e)
+// make sum_k (q_k - zero) x_k = F D + Z for the MMA result D = 2^-24 sum q x-hat (zero = 8 for
+// Q4, 128 for W8's offset codes).  No pass over a whole token is needed, so the threads of
+// any number of CTAs share the work.  Slots past the pass's tokens write zeros.  Groups holding
+// Inf or NaN keep e = 0 so those values propagate.
+constexpr int kPrepThreads = 256;
+
+// Operand unit u = (token slot t, group G, c) of a pass whose tokens start at x, in two
+// phases so that a thread can keep the loads of several units in flight: the load of its
+// X values, then the conversion.  The conversion is called by all 32 lanes of a warp
+// together (the four c of a (t, G) are adjacent lanes and exchange their maxima and sums
+// by shuffles); act is false for the lanes past the last unit.  xf and zs are the
+// B-fragment and zero-point buffers, laid out as the streaming kernel reads them (global
+// memory for the prep kernel, shared memory for the fused form).
 template <int NT, int FMT>
+__device__ __forceinline__ void mma_operand_load(const uint16_t* __restrict__ x, int64_t K, int tp, int galloc,
+                                                 int64_t u, bool act, uint4 (&q)[2]) {
+  constexpr int kVals = FMT == 3 ? 8 : 16;  // values of one (group, c) unit
+  const int c = (int)(u & 3);
+  const int64_t tg = u >> 2;
+  const int G = (int)(tg % galloc), t = (int)(tg / galloc);
+  const bool live = act && t < tp;
+  const int64_t k0 = (int64_t)G * (4 * kVals) + kVals * c;
+  const uint16_t* xr = x + (int64_t)(live ? t : 0) * K;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    // K is a multiple of 8: each run of 8 columns is either wholly inside or wholly past K
+    const bool in = h < kVals / 8 && live && k0 + 8 * h < K;
+    q[h] = in ? __ldg(reinterpret_cast<const uint4*>(xr + k0 + 8 * h)) : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+template <int NT, int FMT>
+__device__ __forceinline__ void mma_operand_convert(int tp, int galloc, int lanes, int64_t u, bool act,
+                                                    const uint4 (&q)[2], uint8_t* xf, float* zs) {
+  constexpr bool kW8 = FMT == 3;
+  constexpr int kVals = kW8 ? 8 : 16;  // values of one (group, c) unit
+  const int c = (int)(u & 3);
+  const int64_t tg = u >> 2;
+  const int G = (int)(tg % galloc), t = (int)(tg / galloc);
+  const bool live = act && t < tp;
+  float v[16];
+  uint32_t m2 = 0;
+#pragma unroll
+  for (int h = 0; h < kVals / 8; ++h) {
+    m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(q[h].x & 0x7FFF7FFFu, q[h].y & 0x7FFF7FFFu),
+                               __vmaxu2(q[h].z & 0x7FFF7FFFu, q[h].w & 0x7FFF7FFFu)));
+    v[8 * h + 0] = bf16lo(q[h].x); v[8 * h + 1] = bf16hi(q[h].x);
+    v[8 * h + 2] = bf16lo(q[h].y); v[8 * h + 3] = bf16hi(q[h].y);
+    v[8 * h + 4] = bf16lo(q[h].z); v[8 * h + 5] = bf16hi(q[h].z);
+    v[8 * h + 6] = bf16lo(q[h].w); v[8 * h + 7] = bf16hi(q[h].w);
+  }
+  uint32_t mx = max(m2 & 0xFFFFu, m2 >> 16);
+  mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  const int E = (int)(mx >> 7);  // bf16 biased exponent of the group's largest |x|
+  const int e = (mx == 0 || E == 255) ? 0 : min(max(E - 141, -100), 100);
+  const float s1 = exp2i(-e), s16 = exp2i(-e - 4);
+  // x-hat = fp16(x 2^-e) (exact in fp16's normal range); the zero-point term sums the same values
+  float sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < kVals; ++i) sum += __half2float(__float2half_rn(v[i] * s1));
+  sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+  sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+  auto pk = [&](int i0, int i1, float sc) -> uint32_t {
+    return (uint32_t)__half_as_ushort(__float2half_rn(v[i0] * sc)) |
+           ((uint32_t)__half_as_ushort(__float2half_rn(v[i1] * sc)) << 16);
+  };
+  const int n = t / 8, tl = t % 8;
+  if (act && tl * 4 < lanes) {  // this token's B lanes exist in the buffer
+    const int L = tl * 4 + c;
+    if constexpr (kW8) {
+      // registers per MMA kk: (x[k0 + 4kk], x[+2]) then (x[+1], x[+3])
+      uint4* dst = reinterpret_cast<uint4*>(xf + (size_t)(G * NT + n) * lanes * 16);
+      dst[L] = make_uint4(pk(0, 2, s1), pk(1, 3, s1), pk(4, 6, s1), pk(5, 7, s1));
+    } else {
+      // registers per MMA kk: (x[k0 + 2kk'], x[+4]) then (x[+1] / 16, x[+5] / 16), kk' = 0, 1, 4, 5
+      uint4* dst = reinterpret_cast<uint4*>(xf + ((size_t)(G * NT + n) * 2) * lanes * 16);
+      dst[L] = make_uint4(pk(0, 4, s1), pk(1, 5, s16), pk(2, 6, s1), pk(3, 7, s16));
+      dst[lanes + L] = make_uint4(pk(8, 12, s1), pk(9, 13, s16), pk(10, 14, s1), pk(11, 15, s16));
+    }
+  }
+  if (act && c == 0) {
+    // (Z[t], Z[t + 1], F[t], F[t + 1]) of MMA thread c' = tl / 2 of this group and token tile
+    float* zq = zs + ((size_t)(G * NT + n) * 4 + tl / 2) * 4;
+    zq[tl & 1] = live ? (kW8 ? -128.f : -8.f) * exp2i(e) * sum : 0.f;
+    zq[2 + (tl & 1)] = live ? exp2i(24 + e) : 0.f;
+  }
+}
+
+template <int NT, int FMT>
+__global__ void __launch_bounds__(kPrepThreads)
+q4_mma_prep_kernel(const uint16_t* __restrict__ x, uint8_t* __restrict__ xf, float* __restrict__ zs,
+                   int64_t K, int tp, int galloc, int lanes, int early) {
+  // Wait for the previous kernel (it may write x, or still read these buffers).  The
+  // streaming kernel launches after that wait (late order: it copies weight rows as soon
+  // as it starts) or before it (early order: it only prefetches them into L2 until its
+  // own wait).
+  if (early) pdl_launch_dependents();
+  pdl_wait_previous();
+  if (!early) pdl_launch_dependents();
+  const int64_t units = (int64_t)8 * NT * galloc * 4;   // a multiple of 32: whole warps take part
+  for (int64_t u = (int64_t)blockIdx.x * kPrepThreads + threadIdx.x; u - (threadIdx.x & 31) < units;
+       u += (int64_t)gridDim.x * kPrepThreads)
+  {
+    uint4 q[2];
+    mma_operand_load<NT, FMT>(x, K, tp, galloc, u, u < units, q);
+    mma_operand_convert<NT, FMT>(tp, galloc, lanes, u, u < units, q, xf, zs);
+  }
+}
+
+// ----------------------------------------------------------------- streaming kernel
+// kFuse (one token tile, the B fragments of the whole K extent fit in shared memory): the
+// consumer warps run the operand pass themselves, every CTA for all groups, into shared
+// memory, while the producer streams the weight rows -- one launch, no workspace, and no
+// wait for a second kernel's completion.  Always the early launch order.
+template <int NT, int FMT, bool kFuse = false, bool kSwi = false>
 __global__ void __launch_bounds__(kMmaThreads, 1)
 q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const MmaParams p) {
+  static_assert(!kFuse || NT == 1, "the fused operand pass covers one token tile");
+  static_assert(!kSwi || (kFuse && FMT == 0), "LinearSwiGLU: the one-launch Q4 form");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -197,7 +336,17 @@ q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const MmaParams p) {
   const int64_t r1 = (int64_t)(blockIdx.x + 1) * p.N / gridDim.x;
   const int BR = p.br, KS = p.ks, NS = p.stages, NCH = p.nchunks;
   const int WC = KS * p.mt;
-  const int nbands = (int)((r1 - r0 + BR - 1) / BR);
+  // Bands of BR rows over the CTA's rows [r0, r1); LinearSwiGLU alternates a band of gate
+  // rows [r0, r1) and the band of up rows F + [r0, r1) that pairs with it.
+  const int nb1 = (int)((r1 - r0 + BR - 1) / BR);
+  const int nbands = kSwi ? 2 * nb1 : nb1;
+  auto band_row = [&](int b) -> int64_t {  // first weight row of band b
+    return kSwi ? (b & 1 ? p.N : 0) + r0 + (int64_t)(b >> 1) * BR : r0 + (int64_t)b * BR;
+  };
+  auto band_rows = [&](int b) -> int {
+    const int64_t o = r0 + (int64_t)(kSwi ? b >> 1 : b) * BR;
+    return (int)((o + BR < r1 ? o + BR : r1) - o);
+  };
   constexpr bool kW8 = FMT == 3;
   constexpr int FB = kW8 ? 16 : 32;                   // B-fragment bytes per lane per group and token tile
   const int64_t srb = kW8 ? p.Kp / 16 : p.Kp / 32;    // bytes of one row of the scale plane
@@ -223,7 +372,8 @@ q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const MmaParams p) {
     prefetch_tmap(&tm_codes);
   }
   __syncthreads();
-  // Launch order (programmatic dependent launch), one of two per call (p.early):
+  // Launch order (programmatic dependent launch) of the two-kernel form, one of two per
+  // call (p.early; the fused form has no prep kernel and always takes the early path):
   //  - late: the prep kernel waits for its own predecessor before it lets this kernel
   //    launch, so every kernel before this call has completed when this one starts, and
   //    the weight planes are streamed at once, while the prep kernel works.  Only what
@@ -243,21 +393,26 @@ q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const MmaParams p) {
     // ------------------------------------------------------------- producer (lane 0 issues)
     if (lane == 0) {
       const uint8_t* sc_plane = reinterpret_cast<const uint8_t*>(p.scales);
-      const int64_t plane_bytes = p.N * srb;
+      const int64_t plane_bytes = (kSwi ? 2 * p.N : p.N) * srb;
       bool ok = true, waited = false;
-      if (p.early) {
+      if (kFuse || p.early) {
         // the first kMmaPrefetchCap bytes of the CTA's code rows (contiguous) and the
         // 16-byte-aligned interior of those rows' scale run, 32 KB per prefetch
+        // (LinearSwiGLU: half of it for the gate rows, half for the up rows)
         const int64_t code_row = kW8 ? p.Kp : p.Kp / 2;
-        const uint8_t* cb = p.wq + r0 * code_row;
-        int64_t len = (r1 - r0) * code_row;
-        if (len > kMmaPrefetchCap) len = kMmaPrefetchCap;
-        for (int64_t off = 0; off < len; off += 32768)
-          bulk_prefetch_l2(cb + off, (uint32_t)(len - off < 32768 ? len - off : 32768));
-        const int64_t pf_end = r0 + (len + code_row - 1) / code_row;  // <= r1
-        const int64_t a0 = (r0 * srb + 15) & ~(int64_t)15, a1 = (pf_end * srb) & ~(int64_t)15;
-        for (int64_t off = a0; off < a1; off += 32768)
-          bulk_prefetch_l2(sc_plane + off, (uint32_t)(a1 - off < 32768 ? a1 - off : 32768));
+        for (int sg = 0; sg < (kSwi ? 2 : 1); ++sg) {
+          const int64_t q0 = r0 + (sg ? p.N : 0), q1 = r1 + (sg ? p.N : 0);
+          const uint8_t* cb = p.wq + q0 * code_row;
+          int64_t len = (q1 - q0) * code_row;
+          const int64_t cap = kSwi ? kMmaPrefetchCap / 2 : kMmaPrefetchCap;
+          if (len > cap) len = cap;
+          for (int64_t off = 0; off < len; off += 32768)
+            bulk_prefetch_l2(cb + off, (uint32_t)(len - off < 32768 ? len - off : 32768));
+          const int64_t pf_end = q0 + (len + code_row - 1) / code_row;  // <= q1
+          const int64_t a0 = (q0 * srb + 15) & ~(int64_t)15, a1 = (pf_end * srb) & ~(int64_t)15;
+          for (int64_t off = a0; off < a1; off += 32768)
+            bulk_prefetch_l2(sc_plane + off, (uint32_t)(a1 - off < 32768 ? a1 - off : 32768));
+        }
         pdl_wait_previous();  // before the first copy into shared memory
         waited = true;
       }
@@ -270,8 +425,8 @@ q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const MmaParams p) {
                  full(q % NS));
       };
       for (int b = 0; ok && b < nbands; ++b) {
-        const int64_t R0 = r0 + (int64_t)b * BR;
-        const int64_t Re = (R0 + BR < r1) ? R0 + BR : r1;
+        const int64_t R0 = band_row(b);
+        const int64_t Re = R0 + band_rows(b);
         if (b >= 2 && !(ok = mbar_wait(sempty0 + 8u * (b & 1), (uint32_t)(((b - 2) >> 1) & 1), abort_flag,
                                        &g_mma_status)))
           break;
@@ -299,12 +454,12 @@ q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const MmaParams p) {
           int nsub = (p.nk - g0 + 3) / 4;
           nsub = nsub < KS ? nsub : KS;
           const uint32_t sb = stage(s);
-          mbar_expect_tx(full(s), (uint32_t)(nsub * BR * 128) + xf_chunk + zs_chunk);
+          mbar_expect_tx(full(s), (uint32_t)(nsub * BR * 128) + (kFuse ? 0u : xf_chunk + zs_chunk));
           for (int k = 0; k < nsub; ++k)
             tma_load_2d(sb + (uint32_t)(k * BR * 128), &tm_codes, full(s), (j * KS + k) * 128, (int32_t)R0);
           // late order: band 0's first stages carry their code sub-boxes before the wait;
           // every later wait of the producer (a free stage, a free scale buffer) comes after it
-          if (waited || it == (NS < NCH ? NS : NCH) - 1) {
+          if (!kFuse && (waited || it == (NS < NCH ? NS : NCH) - 1)) {
             if (!waited) {
               pdl_wait_previous();
               waited = true;
@@ -317,7 +472,8 @@ q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const MmaParams p) {
       }
       if (!ok) {  // aborted: let every copy already issued land before shared memory is released
         if (!waited) pdl_wait_previous();
-        for (int q = frag_next; q <= last_it; ++q) issue_frags(q);  // complete the stages missing fragments
+        if (!kFuse)
+          for (int q = frag_next; q <= last_it; ++q) issue_frags(q);  // complete the stages missing fragments
         for (int i = (last_it - NS + 1 > 0 ? last_it - NS + 1 : 0); i <= last_it; ++i)
           mbar_drain(full(i % NS), (uint32_t)((i / NS) & 1));
         for (int q = (last_band - 1 > 0 ? last_band - 1 : 0); q <= last_band; ++q)
@@ -337,9 +493,36 @@ q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const MmaParams p) {
   const bool bload = lane < p.lanes;           // this lane's B fragment is stored (the others are zero)
   int it = 0;
   bool ok = true;
+  if constexpr (kFuse) {
+    // the operand pass of the whole K extent into shared memory, then one barrier of the
+    // consumer warps; x may come from the previous kernel
+    pdl_wait_previous();
+    // kUnits units per thread per round, their loads issued together
+    constexpr int kUnits = 3;
+    const int64_t units = (int64_t)32 * p.galloc;  // 8 token slots x 4 lanes per group
+    const int64_t wstride = (int64_t)WC * 32;
+    uint8_t* fx = smem + p.xf_off;
+    float* fz = reinterpret_cast<float*>(smem + p.zs_off);
+    const uint16_t* xp = p.x + (int64_t)p.t0 * p.K;
+    for (int64_t base = (int64_t)wc * 32; base < units; base += kUnits * wstride) {
+      uint4 q[kUnits][2];
+#pragma unroll
+      for (int j = 0; j < kUnits; ++j) {
+        const int64_t u = base + j * wstride + lane;
+        mma_operand_load<NT, FMT>(xp, p.K, p.tp, p.galloc, u, u < units, q[j]);
+      }
+#pragma unroll
+      for (int j = 0; j < kUnits; ++j) {
+        const int64_t u = base + j * wstride + lane;
+        if (base + j * wstride < units)  // warp-uniform: the shuffles need every lane
+          mma_operand_convert<NT, FMT>(p.tp, p.galloc, p.lanes, u, u < units, q[j], fx, fz);
+      }
+    }
+    named_bar_sync(kRedBar, (uint32_t)(WC * 32));
+  }
   for (int b = 0; b < nbands; ++b) {
-    const int64_t R0 = r0 + (int64_t)b * BR;
-    const int rows = (int)(((R0 + BR < r1) ? R0 + BR : r1) - R0);
+    const int64_t R0 = band_row(b);
+    const int rows = band_rows(b);
     const bool va = ra < rows, vb = rb < rows;
     ok = ok && warp_wait(sfull0 + 8u * (b & 1), (uint32_t)((b >> 1) & 1), abort_flag, &g_mma_status);
     const uint32_t sc0 = scl_buf(b) + (uint32_t)((R0 * srb) & 15);
@@ -354,8 +537,12 @@ q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const MmaParams p) {
       if (ok && gb < p.nk) {
         const uint32_t code = stage(s) + (uint32_t)(sub * BR * 128);
         const uint32_t rowa = code + (uint32_t)(ra * 128), rowb = code + (uint32_t)(rb * 128);
-        const uint32_t xf = stage(s) + p.xf_off + (uint32_t)(4 * sub * NT * p.lanes * FB) + (uint32_t)lane * 16u;
-        const uint32_t zs = stage(s) + p.zs_off + (uint32_t)(4 * sub * NT * 64) + (uint32_t)c * 16u;
+        // B fragments and zero-point terms of the chunk: in its stage, or (fused) at the chunk's
+        // first group of the whole-K buffers
+        const uint32_t xf_base = kFuse ? sbase + p.xf_off + (uint32_t)(j * 4 * KS * NT * p.lanes * FB) : stage(s) + p.xf_off;
+        const uint32_t zs_base = kFuse ? sbase + p.zs_off + (uint32_t)(j * 4 * KS * NT * 64) : stage(s) + p.zs_off;
+        const uint32_t xf = xf_base + (uint32_t)(4 * sub * NT * p.lanes * FB) + (uint32_t)lane * 16u;
+        const uint32_t zs = zs_base + (uint32_t)(4 * sub * NT * 64) + (uint32_t)c * 16u;
 #pragma unroll
         for (int gl = 0; gl < 4; ++gl) {
           const int G = gb + gl;
@@ -424,11 +611,21 @@ q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const MmaParams p) {
     named_bar_sync(kRedBar, (uint32_t)(WC * 32));
     if (b == 0) pdl_wait_previous();  // the exponents are the prep kernel's; every earlier kernel is done
     if (ok && !*abort_flag) {
+      float* gate = reinterpret_cast<float*>(smem + p.gate_off);
+      const int64_t yrow = kSwi ? r0 + (int64_t)(b >> 1) * BR : R0;  // output row of band row 0
       for (int e = wc * 32 + lane; e < rows * p.tp; e += WC * 32) {
         const int t = e / rows, rw = e - (e / rows) * rows;
         float v = 0.f;
         for (int q = 0; q < KS; ++q) v += red[((size_t)q * MR + rw) * TP + t];
-        const int64_t gi = (int64_t)(p.t0 + t) * p.N + R0 + rw;
+        if (kSwi && (b & 1) == 0) {  // gate band: keep g for the up band that follows
+          gate[rw * TP + t] = v;
+          continue;
+        }
+        const int64_t gi = (int64_t)(p.t0 + t) * p.N + yrow + rw;
+        if constexpr (kSwi) {  // y = silu(g) * u, silu(g) = g / (1 + e^-g), in FP32
+          const float g = gate[rw * TP + t];
+          v = g / (1.f + expf(-g)) * v;
+        }
         if (p.r != nullptr) v += __uint_as_float((uint32_t)p.r[gi] << 16);
         p.y[gi] = float_to_bf16_bits(v);
       }
@@ -437,98 +634,10 @@ q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const MmaParams p) {
   }
 }
 
-// ----------------------------------------------------------------- operand pass
-// One thread per (token slot t of the pass, group G, c): the values of token t in group G
-// that thread c of an MMA feeds -- k = 64 G + 16 c .. + 15 (Q4) or 32 G + 8 c .. + 7 (W8)
-// -- become its fp16x2 B registers, in the order the decode produces A.  The four c of a
-// (t, G) are adjacent lanes: they take the group's largest |x| (compared as bf16 magnitude
-// bits) and the power of two 2^-e that puts it in [2^14, 2^15), so every value of the group
-// down to 2^-38 of that largest one converts to fp16 exactly, and the group's terms
-//     Z = -zero * 2^e * sum x-hat,   F = 2^(24 + e)
-// make sum_k (q_k - zero) x_k = F D + Z for the MMA result D = 2^-24 sum q x-hat (zero = 8 for
-// Q4, 128 for W8's offset codes).  No pass over a whole token is needed, so the threads of
-// any number of CTAs share the work.  Slots past the pass's tokens write zeros.  Groups holding
-// Inf or NaN keep e = 0 so those values propagate.
-constexpr int kPrepThreads = 256;
-
-template <int NT, int FMT>
-__global__ void __launch_bounds__(kPrepThreads)
-q4_mma_prep_kernel(const uint16_t* __restrict__ x, uint8_t* __restrict__ xf, float* __restrict__ zs,
-                   int64_t K, int tp, int galloc, int lanes, int early) {
-  // Wait for the previous kernel (it may write x, or still read these buffers).  The
-  // streaming kernel launches after that wait (late order: it copies weight rows as soon
-  // as it starts) or before it (early order: it only prefetches them into L2 until its
-  // own wait).
-  if (early) pdl_launch_dependents();
-  pdl_wait_previous();
-  if (!early) pdl_launch_dependents();
-  constexpr bool kW8 = FMT == 3;
-  constexpr int kVals = kW8 ? 8 : 16;  // values of one (group, c) unit
-  const int64_t units = (int64_t)8 * NT * galloc * 4;   // a multiple of 32: whole warps take part
-  for (int64_t u = (int64_t)blockIdx.x * kPrepThreads + threadIdx.x; u - (threadIdx.x & 31) < units;
-       u += (int64_t)gridDim.x * kPrepThreads) {
-    const bool act = u < units;
-    const int c = (int)(u & 3);
-    const int64_t tg = u >> 2;
-    const int G = (int)(tg % galloc), t = (int)(tg / galloc);
-    const bool live = act && t < tp;
-    const int64_t k0 = (int64_t)G * (4 * kVals) + kVals * c;
-    const uint16_t* xr = x + (int64_t)(live ? t : 0) * K;
-    float v[16];
-    uint32_t m2 = 0;
-#pragma unroll
-    for (int h = 0; h < kVals / 8; ++h) {
-      // K is a multiple of 8: each run of 8 columns is either wholly inside or wholly past K
-      const bool in = live && k0 + 8 * h < K;
-      const uint4 q = in ? __ldg(reinterpret_cast<const uint4*>(xr + k0 + 8 * h)) : make_uint4(0u, 0u, 0u, 0u);
-      m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(q.x & 0x7FFF7FFFu, q.y & 0x7FFF7FFFu), __vmaxu2(q.z & 0x7FFF7FFFu, q.w & 0x7FFF7FFFu)));
-      v[8 * h + 0] = bf16lo(q.x); v[8 * h + 1] = bf16hi(q.x);
-      v[8 * h + 2] = bf16lo(q.y); v[8 * h + 3] = bf16hi(q.y);
-      v[8 * h + 4] = bf16lo(q.z); v[8 * h + 5] = bf16hi(q.z);
-      v[8 * h + 6] = bf16lo(q.w); v[8 * h + 7] = bf16hi(q.w);
-    }
-    uint32_t mx = max(m2 & 0xFFFFu, m2 >> 16);
-    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const int E = (int)(mx >> 7);  // bf16 biased exponent of the group's largest |x|
-    const int e = (mx == 0 || E == 255) ? 0 : min(max(E - 141, -100), 100);
-    const float s1 = exp2i(-e), s16 = exp2i(-e - 4);
-    // x-hat = fp16(x 2^-e) (exact in fp16's normal range); the zero-point term sums the same values
-    float sum = 0.f;
-#pragma unroll
-    for (int i = 0; i < kVals; ++i) sum += __half2float(__float2half_rn(v[i] * s1));
-    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-    auto pk = [&](int i0, int i1, float sc) -> uint32_t {
-      return (uint32_t)__half_as_ushort(__float2half_rn(v[i0] * sc)) |
-             ((uint32_t)__half_as_ushort(__float2half_rn(v[i1] * sc)) << 16);
-    };
-    const int n = t / 8, tl = t % 8;
-    if (act && tl * 4 < lanes) {  // this token's B lanes exist in the buffer
-      const int L = tl * 4 + c;
-      if constexpr (kW8) {
-        // registers per MMA kk: (x[k0 + 4kk], x[+2]) then (x[+1], x[+3])
-        uint4* dst = reinterpret_cast<uint4*>(xf + (size_t)(G * NT + n) * lanes * 16);
-        dst[L] = make_uint4(pk(0, 2, s1), pk(1, 3, s1), pk(4, 6, s1), pk(5, 7, s1));
-      } else {
-        // registers per MMA kk: (x[k0 + 2kk'], x[+4]) then (x[+1] / 16, x[+5] / 16), kk' = 0, 1, 4, 5
-        uint4* dst = reinterpret_cast<uint4*>(xf + ((size_t)(G * NT + n) * 2) * lanes * 16);
-        dst[L] = make_uint4(pk(0, 4, s1), pk(1, 5, s16), pk(2, 6, s1), pk(3, 7, s16));
-        dst[lanes + L] = make_uint4(pk(8, 12, s1), pk(9, 13, s16), pk(10, 14, s1), pk(11, 15, s16));
-      }
-    }
-    if (act && c == 0) {
-      // (Z[t], Z[t + 1], F[t], F[t + 1]) of MMA thread c' = tl / 2 of this group and token tile
-      float* zq = zs + ((size_t)(G * NT + n) * 4 + tl / 2) * 4;
-      zq[tl & 1] = live ? (kW8 ? -128.f : -8.f) * exp2i(e) * sum : 0.f;
-      zq[2 + (tl & 1)] = live ? exp2i(24 + e) : 0.f;
-    }
-  }
-}
-
 // ----------------------------------------------------------------- host side
 struct MmaPlan {
   int fmt, nt, grid, br, ks, mt, nchunks, stages, lanes, galloc, nk, fbytes, early;
+  int fused;  // one launch: the streaming kernel runs the operand pass itself (no workspace)
   int64_t code_row, srb;  // bytes of one row of the code plane and of the scale plane
   MmaLayout L;
 };
@@ -546,9 +655,14 @@ int mma_nt(int64_t T) { return T >= 32 ? 4 : (int)((T + 7) / 8); }
 // slower early (its code rows are twice as long).
 int mma_early_order(int fmt, int lanes, int nt) { return (fmt == 0 && nt == 1 && lanes <= 24) ? 1 : 0; }
 
-// fmt 0: Q4G64; fmt 3: W8G32 (the other formats have no plan here)
-bool mma_plan_for(int64_t N, int64_t K, int64_t T, int sms, MmaPlan* pl, int fmt = 0) {
+// fmt 0: Q4G64; fmt 3: W8G32 (the other formats have no plan here).  fused: the one-launch
+// form (at most 8 tokens, the whole-K B fragments in shared memory), for callers without a
+// workspace; otherwise the operand pass and its workspace.
+bool mma_plan_for(int64_t N, int64_t K, int64_t T, int sms, MmaPlan* pl, int fmt = 0, bool fused = false,
+                  bool swiglu = false) {
   if (N < 1 || K < 8 || T < 1 || (fmt != 0 && fmt != 3)) return false;
+  if (fused && T > 8) return false;
+  if (swiglu && !fused) return false;   // LinearSwiGLU: the one-launch form only
   if (N >= ((int64_t)1 << 31) || K >= ((int64_t)1 << 31)) return false;
   const bool w8 = fmt == 3;
   const int64_t Kp = (K + 127) / 128 * 128;
@@ -592,7 +706,20 @@ bool mma_plan_for(int64_t N, int64_t K, int64_t T, int sms, MmaPlan* pl, int fmt
     pl->stages = stages;
     pl->galloc = nchunks * chunk_groups;
     pl->L = mma_layout(pl->nt, br, ks, pl->mt, stages, pl->lanes, Kp, pl->fbytes, pl->srb);
-    return true;
+    pl->fused = 0;
+    if (!fused) return true;
+    // the whole-K B fragments beside at least two code stages (else fewer sub-boxes per chunk)
+    for (int fs = 8; fs >= 2; --fs) {
+      const MmaLayout F = mma_layout(pl->nt, br, ks, pl->mt, fs, pl->lanes, Kp, pl->fbytes, pl->srb, true,
+                                     pl->galloc, swiglu);
+      if (F.total + 1024 <= kMmaSmem) {
+        pl->fused = 1;
+        pl->early = 1;
+        pl->stages = fs;
+        pl->L = F;
+        return true;
+      }
+    }
   }
   return false;
 }
@@ -611,27 +738,40 @@ int mma_sm_count() {
 // Workspace of one pass: B fragments, then the zero-point terms and factors (each 256-byte aligned).
 size_t mma_ws_xf(const MmaPlan& pl) { return ((size_t)pl.galloc * pl.nt * pl.lanes * pl.fbytes + 255) / 256 * 256; }
 size_t mma_ws_zs(const MmaPlan& pl) { return ((size_t)pl.galloc * pl.nt * 64 + 255) / 256 * 256; }
-size_t mma_ws_total(const MmaPlan& pl) { return mma_ws_xf(pl) + mma_ws_zs(pl); }
+size_t mma_ws_total(const MmaPlan& pl) { return pl.fused ? 0 : mma_ws_xf(pl) + mma_ws_zs(pl); }
 
-template <int NT, int FMT>
-int mma_launch_pass(const LinearArgs& a, const MmaPlan& pl, const CUtensorMap& tm, int64_t t0, int tp) {
+// Opt a streaming-kernel instantiation into the large dynamic shared memory, once per device.
+template <int NT, int FMT, bool kFuse, bool kSwi = false>
+int mma_kernel_attrs() {
   static bool attr[64] = {};
   int dev = 0;
   if (cuda_check(cudaGetDevice(&dev), "cudaGetDevice")) return Q4LIN_ERR_CUDA;
   if (dev >= 64 || !attr[dev]) {
-    if (cuda_check(cudaFuncSetAttribute(q4_mma_kernel<NT, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cuda_check(cudaFuncSetAttribute(q4_mma_kernel<NT, FMT, kFuse, kSwi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)kMmaSmem),
                    "mma: cudaFuncSetAttribute"))
       return Q4LIN_ERR_CUDA;
     if (dev < 64) attr[dev] = true;
   }
-  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
-  uint8_t* xf = ws;
-  float* zs = reinterpret_cast<float*>(ws + mma_ws_xf(pl));
+  return Q4LIN_OK;
+}
+
+template <int NT, int FMT>
+int mma_launch_pass(const LinearArgs& a, const MmaPlan& pl, const CUtensorMap& tm, int64_t t0, int tp) {
+  const bool fused = NT == 1 && pl.fused;
+  const bool swi = FMT == 0 && fused && a.mode == 1;
+  if (const int rc = swi ? mma_kernel_attrs<1, 0, true, true>()
+                     : fused ? mma_kernel_attrs<1, FMT, true>() : mma_kernel_attrs<NT, FMT, false>())
+    return rc;
+  uint8_t* xf = nullptr;
+  float* zs = nullptr;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
-  {
+  if (!fused) {
+    uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+    xf = ws;
+    zs = reinterpret_cast<float*>(ws + mma_ws_xf(pl));
     cudaLaunchConfig_t cfg = {};
     const int64_t units = (int64_t)8 * NT * pl.galloc * 4;
     int64_t blocks = (units + kPrepThreads - 1) / kPrepThreads;
@@ -651,9 +791,11 @@ int mma_launch_pass(const LinearArgs& a, const MmaPlan& pl, const CUtensorMap& t
   p.scales = a.scales;
   p.xf = xf;
   p.zs = zs;
+  p.x = a.x;
   p.y = a.y;
   p.r = a.r;
   p.N = a.N;
+  p.K = a.K;
   p.Kp = k_pad(a.K);
   p.T = a.T;
   p.t0 = (int)t0;
@@ -666,12 +808,14 @@ int mma_launch_pass(const LinearArgs& a, const MmaPlan& pl, const CUtensorMap& t
   p.stages = pl.stages;
   p.lanes = pl.lanes;
   p.early = pl.early;
+  p.galloc = pl.galloc;
   p.stage_bytes = pl.L.stage_bytes;
-  p.xf_off = pl.L.code_bytes;
-  p.zs_off = pl.L.code_bytes + pl.L.xf_bytes;
+  p.xf_off = fused ? pl.L.fx_off : pl.L.code_bytes;
+  p.zs_off = fused ? pl.L.fz_off : pl.L.code_bytes + pl.L.xf_bytes;
   p.scl_off = pl.L.scl_off;
   p.scl_bytes = pl.L.scl_bytes;
   p.red_off = pl.L.red_off;
+  p.gate_off = pl.L.gate_off;
   p.bar_off = pl.L.bar_off;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)pl.grid, 1, 1);
@@ -680,7 +824,11 @@ int mma_launch_pass(const LinearArgs& a, const MmaPlan& pl, const CUtensorMap& t
   cfg.stream = a.stream;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cuda_check(cudaLaunchKernelEx(&cfg, q4_mma_kernel<NT, FMT>, tm, p), "mma: kernel launch");
+  if constexpr (NT == 1) {
+    if (swi) return cuda_check(cudaLaunchKernelEx(&cfg, q4_mma_kernel<1, 0, true, true>, tm, p), "mma: kernel launch");
+    if (fused) return cuda_check(cudaLaunchKernelEx(&cfg, q4_mma_kernel<1, FMT, true>, tm, p), "mma: kernel launch");
+  }
+  return cuda_check(cudaLaunchKernelEx(&cfg, q4_mma_kernel<NT, FMT, false>, tm, p), "mma: kernel launch");
 }
 
 template <int FMT>
@@ -713,16 +861,22 @@ size_t mma_workspace_bytes(int64_t N, int64_t K, int64_t T, int fmt) {
   return mma_ws_total(pl);
 }
 
-int mma_launch_count(int64_t, int64_t, int64_t T) { return 2 * (int)((T + 31) / 32); }
+int mma_launch_count(int64_t, int64_t, int64_t T, int) { return 2 * (int)((T + 31) / 32); }
 
-int mma_launch(const LinearArgs& a) {
+bool mma_fused_supported(int64_t N, int64_t K, int64_t T, int fmt, bool swiglu) {
   MmaPlan pl;
-  if (!mma_plan_for(a.N, a.K, a.T, mma_sm_count(), &pl, a.fmt)) {
+  return mma_plan_for(N, K, T, mma_sm_count(), &pl, fmt, true, swiglu);
+}
+
+int mma_launch(const LinearArgs& a, bool fused) {
+  MmaPlan pl;
+  const bool swiglu = a.mode == 1;
+  if (a.mode == 2 || (swiglu && a.fmt != 0) || !mma_plan_for(a.N, a.K, a.T, mma_sm_count(), &pl, a.fmt, fused, swiglu)) {
     set_error_detail("mma: no shared-memory plan for this format and shape");
     return Q4LIN_ERR_UNSUPPORTED_SHAPE;
   }
   CUtensorMap tm;
-  if (!encode_map_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.wq, (uint64_t)pl.code_row, (uint64_t)a.N,
+  if (!encode_map_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.wq, (uint64_t)pl.code_row, (uint64_t)(swiglu ? 2 * a.N : a.N),
                      (uint64_t)pl.code_row, 128, (uint32_t)pl.br, CU_TENSOR_MAP_SWIZZLE_128B)) {
     set_error_detail("mma: cuTensorMapEncodeTiled failed (or is unavailable)");
     return Q4LIN_ERR_CUDA;

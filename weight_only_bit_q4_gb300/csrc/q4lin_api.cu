@@ -233,9 +233,23 @@ int run_host_impl(const uint8_t* wq, const uint16_t* scales, const uint16_t* x_h
   return run_impl(Q4LIN_ROUTE_AUTO, wq, scales, xs, static_cast<uint16_t*>(yd), N, K, T, ws + xb + yb, stream);
 }
 
+// The fused operations take no workspace: up to 8 tokens they run the warp-MMA route's
+// one-launch form (the streaming kernel converts X itself) where its shared memory fits,
+// otherwise the exact tile route.
+constexpr int64_t kFusedMmaMaxT = 8;
+
+bool fused_op_on_mma(int64_t N, int64_t K, int64_t T, bool swiglu = false) {
+  return N > 0 && K > 0 && T > 0 && T <= kFusedMmaMaxT && q4::mma_fused_supported(N, K, T, 0, swiglu);
+}
+
 }  // namespace
 
 extern "C" {
+
+int q4lin_fused_route(int op, int64_t N, int64_t K, int64_t T) {
+  if (op < 1 || op > 3 || validate_sizes(N, K, T) != Q4LIN_OK) return -1;
+  return fused_op_on_mma(N, K, T, op == 2) ? Q4LIN_ROUTE_STREAM_MMA : Q4LIN_ROUTE_TC_SPLITK;
+}
 
 size_t q4lin_host_workspace_bytes(int64_t N, int64_t K, int64_t T) {
   if (validate_sizes(N, K, T) != Q4LIN_OK || N == 0 || T == 0) return 0;
@@ -298,10 +312,11 @@ int q4lin_linear_add(const uint8_t* wq, const uint16_t* scales, const uint16_t* 
                      int64_t N, int64_t K, int64_t T, void* stream) {
   q4::set_error_detail("");
   int st = validate(wq, scales, x, y, N, K, T);
+  const bool warp_mma = fused_op_on_mma(N, K, T);
   if (st == Q4LIN_OK && N > 0 && T > 0) {
     if (r == nullptr) st = Q4LIN_ERR_INVALID_ARG;
     else if (!aligned16(r)) st = Q4LIN_ERR_MISALIGNED;
-    else if (K > 0 && !q4::tc_supported(N, K, T)) st = Q4LIN_ERR_INVALID_ARG;
+    else if (K > 0 && !warp_mma && !q4::tc_supported(N, K, T)) st = Q4LIN_ERR_INVALID_ARG;
   }
   if (st == Q4LIN_OK && N > 0 && T > 0) st = check_device();
   if (st == Q4LIN_OK && N > 0 && T > 0) {
@@ -313,7 +328,7 @@ int q4lin_linear_add(const uint8_t* wq, const uint16_t* scales, const uint16_t* 
     } else {
       q4::LinearArgs a{wq, scales, x, y, N, K, T, nullptr, s};
       a.r = r;
-      st = q4::tc_launch(a, Q4LIN_ROUTE_TC_SPLITK);
+      st = warp_mma ? q4::mma_launch(a, true) : q4::tc_launch(a, Q4LIN_ROUTE_TC_SPLITK);
     }
   }
   if (st != Q4LIN_OK && q4::g_detail[0] == 0) q4::set_error_detail(q4lin_status_string(st));
@@ -326,7 +341,9 @@ int q4lin_linear_swiglu(const uint8_t* wq, const uint16_t* scales, const uint16_
   int st = Q4LIN_OK;
   if (F < 0 || F > kMaxDim / 2) st = Q4LIN_ERR_INVALID_ARG;
   if (st == Q4LIN_OK) st = validate(wq, scales, x, y, 2 * F, K, T);
-  if (st == Q4LIN_OK && F > 0 && T > 0 && K > 0 && !q4::tc_supported(2 * F, K, T)) st = Q4LIN_ERR_INVALID_ARG;
+  const bool warp_mma = st == Q4LIN_OK && fused_op_on_mma(F, K, T, true);
+  if (st == Q4LIN_OK && F > 0 && T > 0 && K > 0 && !warp_mma && !q4::tc_supported(2 * F, K, T))
+    st = Q4LIN_ERR_INVALID_ARG;
   if (st == Q4LIN_OK && F > 0 && T > 0) st = check_device();
   if (st == Q4LIN_OK && F > 0 && T > 0) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -335,7 +352,7 @@ int q4lin_linear_swiglu(const uint8_t* wq, const uint16_t* scales, const uint16_
     } else {
       q4::LinearArgs a{wq, scales, x, y, F, K, T, nullptr, s};
       a.mode = 1;
-      st = q4::tc_launch(a, Q4LIN_ROUTE_TC_SPLITK);
+      st = warp_mma ? q4::mma_launch(a, true) : q4::tc_launch(a, Q4LIN_ROUTE_TC_SPLITK);
     }
   }
   if (st != Q4LIN_OK && q4::g_detail[0] == 0) q4::set_error_detail(q4lin_status_string(st));
@@ -349,7 +366,9 @@ int q4lin_linear_pair(const uint8_t* wq_a, const uint16_t* scales_a, const uint8
   int st = validate(wq_a, scales_a, x, y_a, N_a, K, T);
   if (st == Q4LIN_OK) st = validate(wq_b, scales_b, x, y_b, N_b, K, T);
   const int64_t n_plan = 128 * ((N_a + 127) / 128 + (N_b + 127) / 128);
-  if (st == Q4LIN_OK && T > 0 && K > 0 && N_a + N_b > 0 && !q4::tc_supported(n_plan, K, T))
+  // a few tokens: each weight on the one-launch warp-MMA form, one launch after the other
+  const bool warp_mma = (N_a == 0 || fused_op_on_mma(N_a, K, T)) && (N_b == 0 || fused_op_on_mma(N_b, K, T));
+  if (st == Q4LIN_OK && T > 0 && K > 0 && N_a + N_b > 0 && !warp_mma && !q4::tc_supported(n_plan, K, T))
     st = Q4LIN_ERR_INVALID_ARG;
   const bool work = st == Q4LIN_OK && T > 0 && N_a + N_b > 0;
   if (work) st = check_device();
@@ -359,6 +378,10 @@ int q4lin_linear_pair(const uint8_t* wq_a, const uint16_t* scales_a, const uint8
       if (N_a > 0) st = q4::cuda_check(cudaMemsetAsync(y_a, 0, (size_t)N_a * (size_t)T * 2, s), "zero fill of y_a");
       if (st == Q4LIN_OK && N_b > 0)
         st = q4::cuda_check(cudaMemsetAsync(y_b, 0, (size_t)N_b * (size_t)T * 2, s), "zero fill of y_b");
+    } else if (warp_mma) {
+      if (N_a > 0) st = q4::mma_launch(q4::LinearArgs{wq_a, scales_a, x, y_a, N_a, K, T, nullptr, s}, true);
+      if (st == Q4LIN_OK && N_b > 0)
+        st = q4::mma_launch(q4::LinearArgs{wq_b, scales_b, x, y_b, N_b, K, T, nullptr, s}, true);
     } else if (N_a == 0 || N_b == 0) {  // one weight: the plain layer on its exact tile route
       q4::LinearArgs a = N_a > 0 ? q4::LinearArgs{wq_a, scales_a, x, y_a, N_a, K, T, nullptr, s}
                                  : q4::LinearArgs{wq_b, scales_b, x, y_b, N_b, K, T, nullptr, s};

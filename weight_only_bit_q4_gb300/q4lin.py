@@ -27,7 +27,7 @@ EXPORTS = ("q4lin_workspace_bytes", "q4lin_linear", "q4lin_linear_route", "q4lin
            "q4lin_status_string",
            "q4lin_device_status", "q4lin_clear_device_status", "q4lin_last_error_detail",
            "q4lin_hbm_read_probe", "q4lin_diag_wait_expiry", "q4lin_linear_swiglu", "q4lin_linear_pair",
-           "q4lin_qtype_workspace_bytes", "q4lin_host_workspace_bytes", "q4lin_linear_host", "q4lin_version")
+           "q4lin_qtype_workspace_bytes", "q4lin_host_workspace_bytes", "q4lin_linear_host", "q4lin_fused_route", "q4lin_version")
 
 _lib = None
 
@@ -100,6 +100,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q4lin_host_workspace_bytes.restype = sz
     lib.q4lin_linear_host.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp]
     lib.q4lin_linear_host.restype = ctypes.c_int
+    lib.q4lin_fused_route.argtypes = [ctypes.c_int, i64, i64, i64]
+    lib.q4lin_fused_route.restype = ctypes.c_int
     lib.q4lin_version.argtypes = []
     lib.q4lin_version.restype = ctypes.c_char_p
     if path is None:
@@ -211,6 +213,14 @@ def linear(wq, scales, x, y=None, workspace=None, stream=None, route: int = ROUT
     if st != OK:
         raise Q4LinError(st)
     return y
+
+
+FUSED_OPS = {"add": 1, "swiglu": 2, "pair": 3}
+
+
+def fused_route(op: str, N: int, K: int, T: int) -> int:
+    """Route of a fused operation ("add", "swiglu", "pair"; N = F for swiglu, rows per weight for pair)."""
+    return int(load().q4lin_fused_route(FUSED_OPS[op], N, K, T))
 
 
 def host_workspace_bytes(N: int, K: int, T: int) -> int:
