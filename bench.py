@@ -375,14 +375,9 @@ def measure_ours(args, wl, rank, world, local, sampler=None, with_e2e=True):
         launches = 1 if T <= 4 else -(-T // 4)
     stream = torch.cuda.Stream(dev)
 
-    if qtype != "q4g64":   # the streaming GEMV (1..4 tokens), else Q5 / Q6 tiles, W8 warp-MMA to 24 tokens, tiles beyond
+    if qtype != "q4g64":   # the library's own choice for the format (GEMV, warp-MMA or tile route)
         launches = q4lin.kernel_launches(N, K, T, qtype)
-        if T <= 4 and launches == 1:
-            route = q4lin.ROUTE_GEMV
-        elif qtype == "w8g32" and T <= 24:
-            route = q4lin.ROUTE_STREAM_MMA
-        else:
-            route = q4lin.ROUTE_TC_SPLITK
+        route = q4lin.qtype_route(qtype, N, K, T)
 
     if op != "linear" and q4lin.fused_route(op, n_out, K, T) == q4lin.ROUTE_STREAM_MMA:
         # a few tokens: the warp-MMA route's one-launch form, one launch per weight

@@ -136,13 +136,15 @@ typedef enum {
  * Y = W . X for any of the formats above (arguments as q4lin_linear; `high`
  * is the Q5 / Q6 high-bit plane, 16-byte aligned, and is ignored otherwise).
  * Q4G64 is exactly q4lin_linear (workspace as q4lin_workspace_bytes).  The
- * other formats run on the decode GEMV for 1..4 tokens where its shared-memory
- * plan fits.  Other shapes of Q5G64 and Q6G64 run on the exact tile route
- * (token tiles up to 128 wide; the high-bit plane is staged beside the codes).  W8G32
- * runs on the streaming warp-MMA route for 5..24 tokens, whose operand pass needs
- * workspace: q4lin_qtype_workspace_bytes (256-byte aligned, NULL allowed where that is
- * 0), and on the exact tile route beyond (codes as exact bf16, one accumulator per
- * 32-wide scale group, token tiles up to 64 wide; no workspace).  W8G32 shapes no route can plan return
+ * other formats: Q5G64 and Q6G64 run on the decode GEMV for one token, on the
+ * streaming warp-MMA route for 2..32 tokens (the high bits joined to the nibble
+ * operands) and on the exact tile route beyond (token tiles up to 128 wide; the
+ * high-bit plane is staged beside the codes); W8G32 runs on the decode GEMV for 1..4
+ * tokens, on the warp-MMA route for 5..24 and on the exact tile route beyond (codes as
+ * exact bf16, one accumulator per 32-wide scale group, token tiles up to 64 wide).  The
+ * warp-MMA route's operand pass needs workspace: q4lin_qtype_workspace_bytes (256-byte
+ * aligned, NULL allowed where that is 0).  Where a route has no shared-memory plan the
+ * call falls back to another; shapes no route can plan return
  * Q4LIN_ERR_UNSUPPORTED_SHAPE.
  */
 int q4lin_linear_qtype(int qtype, const uint8_t* codes, const uint8_t* high, const uint16_t* scales,
@@ -152,6 +154,11 @@ int q4lin_linear_qtype(int qtype, const uint8_t* codes, const uint8_t* high, con
 /* Workspace bytes q4lin_linear_qtype needs for this format and shape (0: none; a
  * multiple of 256; 0 for invalid sizes or an unknown format). */
 size_t q4lin_qtype_workspace_bytes(int qtype, int64_t N, int64_t K, int64_t T);
+
+/* The route q4lin_linear_qtype takes for this format and shape on the current device
+ * (host-only logic; Q4LIN_ROUTE_GEMV also for shapes it refuses), -1 for an unknown
+ * format or invalid sizes. */
+int q4lin_qtype_route(int qtype, int64_t N, int64_t K, int64_t T);
 
 /*
  * LinearAdd (a fused operation the linear-benchmark page names and leaves to its

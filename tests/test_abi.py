@@ -283,3 +283,18 @@ def test_host_entry_workspace_and_host_checks(lib):
     assert f(vp(16), vp(16), None, vp(16), 64, 256, 4, vp(256), None) == 1       # no X
     assert f(vp(16), vp(16), vp(16), vp(8), 64, 256, 4, vp(256), None) == 3      # y not 16-byte aligned
     assert f(None, None, None, None, 0, 256, 4, None, None) == 0                 # empty
+
+
+def test_format_routes(lib):
+    # Q5 / Q6: GEMV for one token, warp-MMA for 2..32, tiles beyond; W8: GEMV 1..4, warp-MMA 5..24, tiles beyond
+    for q in ("q5g64", "q6g64"):
+        assert q4lin.qtype_route(q, 6144, 5120, 1) == q4lin.ROUTE_GEMV
+        for T in (2, 8, 32):
+            assert q4lin.qtype_route(q, 6144, 5120, T) == q4lin.ROUTE_STREAM_MMA, (q, T)
+            assert q4lin.kernel_launches(6144, 5120, T, q) == 2
+        assert q4lin.qtype_route(q, 6144, 5120, 33) == q4lin.ROUTE_TC_SPLITK
+    assert q4lin.qtype_route("w8g32", 6144, 5120, 4) == q4lin.ROUTE_GEMV
+    assert q4lin.qtype_route("w8g32", 6144, 5120, 8) == q4lin.ROUTE_STREAM_MMA
+    assert q4lin.qtype_route("w8g32", 6144, 5120, 25) == q4lin.ROUTE_TC_SPLITK
+    assert q4lin.qtype_route("q4g64", 6144, 5120, 8) == q4lin.select_route(6144, 5120, 8)
+    assert lib.q4lin_qtype_route(9, 64, 256, 8) == -1 and lib.q4lin_qtype_route(1, 64, 100, 8) == -1

@@ -1,9 +1,10 @@
 """GPU parity for the sibling weight formats Q5G64, Q6G64 and W8G32 (linear-benchmark.md
-section 4, format table) against the FP64 oracle for those formats: the decode GEMV for
-1..4 tokens (K a multiple of 128 or padded, ragged N), and for Q5G64 / Q6G64 the exact
-tile route beyond that (token tiles up to 128 wide, K split across clusters where the
-planner chooses it).  Q4 through the same entry point is q4lin_linear itself; W8G32
-shapes outside the GEMV's reach are refused, not approximated."""
+section 4, format table) against the FP64 oracle for those formats: the decode GEMV (one
+token for Q5 / Q6, 1..4 for W8; K a multiple of 128 or padded, ragged N), the streaming
+warp-MMA route (Q5 / Q6 at 2..32 tokens with the high bits joined to the nibble operands,
+W8 at 5..24), and the exact tile route beyond (token tiles up to 128 wide, K split across
+clusters where the planner chooses it).  Q4 through the same entry point is q4lin_linear
+itself."""
 import numpy as np
 import pytest
 
@@ -106,8 +107,23 @@ def test_q5_q6_tile_route_matches_oracle(qtype, N, K, T):
 
 
 @pytest.mark.parametrize("qtype", ["q5g64", "q6g64"])
+@pytest.mark.parametrize("N,K,T", [(6144, 5120, 8), (6144, 5120, 2), (1001, 4096, 16), (300, 200, 7),
+                                   (257, 1152, 32), (640, 4304, 24), (77, 17408, 9), (4097, 512, 31),
+                                   (33, 1160, 3), (2000, 5120, 17)])
+def test_q5_q6_warp_mma_route_matches_oracle(qtype, N, K, T):
+    """Q5G64 / Q6G64 on the streaming warp-MMA route (2..32 tokens): the high bits of each
+    weight join its nibble as 16 h in the exact fp16-subnormal operand (16 q <= 1008 stays
+    subnormal), zero points 16 and 32 in the operand pass's term."""
+    qt = {"q5g64": 1, "q6g64": 2}[qtype]
+    assert q4lin.kernel_launches(N, K, T, qtype) == 2
+    assert q4lin.load().q4lin_qtype_workspace_bytes(qt, N, K, T) > 0
+    planes, s, x = synth.make_problem_fmt(qtype, N, K, T, w_seed=N + 7, x_seed=K + T)
+    assert_close(_run(qtype, planes, s, x), sf.linear(qtype, planes, s, x), f"{qtype} {N}x{K} T={T}")
+
+
+@pytest.mark.parametrize("qtype", ["q5g64", "q6g64"])
 def test_q5_q6_gemv_without_plan_goes_to_tiles(qtype):
-    # four tokens whose x does not fit the streaming GEMV's shared memory: the tile route
+    # four tokens of a long K: whichever route has a plan (the warp-MMA route here)
     N, K, T = 128, 17408, 4
     planes, s, x = synth.make_problem_fmt(qtype, N, K, T, w_seed=9, x_seed=10)
     assert_close(_run(qtype, planes, s, x), sf.linear(qtype, planes, s, x), f"{qtype} {N}x{K} T={T}")

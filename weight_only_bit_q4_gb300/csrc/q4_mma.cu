@@ -86,6 +86,7 @@ struct MmaParams {
   int lanes;    // B-fragment lanes stored per (group, token tile)
   int early;    // launch order: 1 early (launched before the prep kernel's wait), 0 late
   int galloc;   // groups of the B-fragment buffer
+  uint32_t hi_off;                        // Q5 / Q6: the high-bit sub-boxes inside a stage
   uint32_t stage_bytes, xf_off, zs_off;  // stage size; B fragments and zero points (inside a stage, or
                                          // the fused form's whole-K buffers)
   uint32_t scl_off, scl_bytes;           // the two band scale buffers
@@ -96,7 +97,7 @@ struct MmaParams {
 // form) its B fragments and zero-point terms; the fused form keeps the whole K extent of
 // both, written by the kernel itself, after the stages (fx_off, fz_off).
 struct MmaLayout {
-  uint32_t code_bytes, xf_bytes, zs_bytes, stage_bytes, scl_bytes, red_bytes;
+  uint32_t code_bytes, hi_bytes, xf_bytes, zs_bytes, stage_bytes, scl_bytes, red_bytes;
   uint32_t fx_off, fx_bytes, fz_off, fz_bytes;
   uint32_t scl_off, red_off, gate_off, bar_off, total;
 };
@@ -104,12 +105,13 @@ struct MmaLayout {
 // fbytes: B-fragment bytes per lane per group and token tile (Q4: 32, four MMAs; W8: 16, two)
 __host__ __device__ inline MmaLayout mma_layout(int nt, int br, int ks, int mt, int stages, int lanes, int64_t Kp,
                                                 int fbytes = 32, int64_t srb = 0, bool fused = false,
-                                                int galloc = 0, bool swiglu = false) {
+                                                int galloc = 0, bool swiglu = false, int hb = 0) {
   MmaLayout L;
   L.code_bytes = (uint32_t)(ks * br * 128);  // ks sub-boxes of br rows x 128 bytes (128-byte swizzle)
+  L.hi_bytes = (uint32_t)(ks * br * 32 * hb);   // Q5 / Q6: ks sub-boxes of br rows x 32 hb bytes
   L.xf_bytes = fused ? 0u : (uint32_t)(4 * ks * nt * lanes * fbytes);
   L.zs_bytes = fused ? 0u : (uint32_t)(4 * ks * nt * 64);
-  L.stage_bytes = (L.code_bytes + L.xf_bytes + L.zs_bytes + 1023) / 1024 * 1024;
+  L.stage_bytes = (L.code_bytes + L.hi_bytes + L.xf_bytes + L.zs_bytes + 1023) / 1024 * 1024;
   L.fx_off = (uint32_t)stages * L.stage_bytes;
   L.fx_bytes = fused ? (uint32_t)galloc * (uint32_t)(nt * lanes * fbytes) : 0u;
   L.fz_off = L.fx_off + L.fx_bytes;
@@ -144,6 +146,12 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
 __device__ __forceinline__ uint2 lds_u64(uint32_t addr) {
   uint2 v;
   asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
 }
 
@@ -183,8 +191,27 @@ __device__ __forceinline__ void decode_q4_pairs(uint32_t w0, uint32_t w1, uint32
   p[7] = v1 & 0x00F000F0u;
 }
 
-// FMT: 0 Q4G64 (64-wide groups, four MMAs per group), 3 W8G32 (32-wide groups of signed
-// bytes, two MMAs per group; the scale plane has Kp / 32 scales per row).
+// Q5G64 / Q6G64: the high bits of the same 16 weights (hw: Q5 bit j, Q6 bits 2j..2j+1 belong
+// to weight k + j) joined to the nibbles of decode_q4_pairs, as 16 h (even registers) and
+// 256 h (odd registers, which hold 16 q): q = nibble + 16 h stays below 64, so 16 q <= 1008
+// is still an exact fp16 subnormal pattern.  For register j (weights j and j + 4, or 8 + j
+// and 12 + j) the spread y = h | h << 12 (Q5) or h | h << 8 (Q6) puts the two weights' bits
+// 16 positions apart.
+template <int kHB>
+__device__ __forceinline__ void add_high_pairs(uint32_t hw, uint32_t (&p)[8]) {
+  constexpr uint32_t kMask = kHB == 1 ? 0x00010001u : 0x00030003u;
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const uint32_t h = kHB == 1 ? (hw >> (8 * half)) & 0xFFu : (hw >> (16 * half)) & 0xFFFFu;
+    const uint32_t y = kHB == 1 ? h | (h << 12) : h | (h << 8);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) p[4 * half + j] |= ((y >> (kHB * j)) & kMask) << ((j & 1) ? 8 : 4);
+  }
+}
+
+// FMT: 0 Q4G64 (64-wide groups, four MMAs per group), 1 Q5G64 / 2 Q6G64 (the same, with 1 or
+// 2 high bits per weight from the high-bit plane), 3 W8G32 (32-wide groups of signed bytes, two
+// MMAs per group; the scale plane has Kp / 32 scales per row).
 // W8G32: the 8 signed codes k = 8c .. 8c + 7 of one row of a 32-wide group (words w0, w1) as
 // the four A registers of the group's two MMAs: each code offset to u = code + 128 (the sign
 // bit flipped) and read as the fp16 subnormal u * 2^-24 (u <= 255).  K order: p[0] = (0, 2),
@@ -207,7 +234,7 @@ __device__ __forceinline__ void decode_w8_pairs(uint32_t w0, uint32_t w1, uint32
 // down to 2^-38 of that largest one converts to fp16 exactly, and the group's terms
 //     Z = -zero * 2^e * sum x-hat,   F = 2^(24 + e)
 // make sum_k (q_k - zero) x_k = F D + Z for the MMA result D = 2^-24 sum q x-hat (zero = 8 for
-// Q4, 128 for W8's offset codes).  No pass over a whole token is needed, so the threads of
+// Q4, 16 for Q5, 32 for Q6, 128 for W8's offset codes).  No pass over a whole token is needed, so the threads of
 // any number of CTAs share the work.  Slots past the pass's tokens write zeros.  Groups holding
 // Inf or NaN keep e = 0 so those values propagate.
 constexpr int kPrepThreads = 256;
@@ -290,7 +317,8 @@ __device__ __forceinline__ void mma_operand_convert(int tp, int galloc, int lane
   if (act && c == 0) {
     // (Z[t], Z[t + 1], F[t], F[t + 1]) of MMA thread c' = tl / 2 of this group and token tile
     float* zq = zs + ((size_t)(G * NT + n) * 4 + tl / 2) * 4;
-    zq[tl & 1] = live ? (kW8 ? -128.f : -8.f) * exp2i(e) * sum : 0.f;
+    constexpr float kZero = FMT == 3 ? 128.f : FMT == 2 ? 32.f : FMT == 1 ? 16.f : 8.f;
+    zq[tl & 1] = live ? -kZero * exp2i(e) * sum : 0.f;
     zq[2 + (tl & 1)] = live ? exp2i(24 + e) : 0.f;
   }
 }
@@ -323,7 +351,8 @@ q4_mma_prep_kernel(const uint16_t* __restrict__ x, uint8_t* __restrict__ xf, flo
 // wait for a second kernel's completion.  Always the early launch order.
 template <int NT, int FMT, bool kFuse = false, bool kSwi = false>
 __global__ void __launch_bounds__(kMmaThreads, 1)
-q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const MmaParams p) {
+q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_high,
+              const MmaParams p) {
   static_assert(!kFuse || NT == 1, "the fused operand pass covers one token tile");
   static_assert(!kSwi || (kFuse && FMT == 0), "LinearSwiGLU: the one-launch Q4 form");
   extern __shared__ uint8_t smem_raw[];
@@ -348,6 +377,8 @@ q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const MmaParams p) {
     return (int)((o + BR < r1 ? o + BR : r1) - o);
   };
   constexpr bool kW8 = FMT == 3;
+  constexpr int kHB = (FMT == 1 || FMT == 2) ? FMT : 0;  // Q5 / Q6: high bits per weight
+  constexpr uint32_t kHRow = 32u * kHB;                // high-plane bytes of one sub-box row (256 weights)
   constexpr int FB = kW8 ? 16 : 32;                   // B-fragment bytes per lane per group and token tile
   const int64_t srb = kW8 ? p.Kp / 16 : p.Kp / 32;    // bytes of one row of the scale plane
   const uint32_t bars = sbase + p.bar_off;
@@ -370,6 +401,7 @@ q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const MmaParams p) {
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_codes);
+    if constexpr (kHB > 0) prefetch_tmap(&tm_high);
   }
   __syncthreads();
   // Launch order (programmatic dependent launch) of the two-kernel form, one of two per
@@ -454,9 +486,13 @@ q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const MmaParams p) {
           int nsub = (p.nk - g0 + 3) / 4;
           nsub = nsub < KS ? nsub : KS;
           const uint32_t sb = stage(s);
-          mbar_expect_tx(full(s), (uint32_t)(nsub * BR * 128) + (kFuse ? 0u : xf_chunk + zs_chunk));
+          mbar_expect_tx(full(s), (uint32_t)(nsub * BR) * (128u + kHRow) + (kFuse ? 0u : xf_chunk + zs_chunk));
           for (int k = 0; k < nsub; ++k)
             tma_load_2d(sb + (uint32_t)(k * BR * 128), &tm_codes, full(s), (j * KS + k) * 128, (int32_t)R0);
+          if constexpr (kHB > 0)  // the sub-boxes' high bits: kHRow bytes per row, unswizzled
+            for (int k = 0; k < nsub; ++k)
+              tma_load_2d(sb + p.hi_off + (uint32_t)(k * BR) * kHRow, &tm_high, full(s), (j * KS + k) * (int)kHRow,
+                          (int32_t)R0);
           // late order: band 0's first stages carry their code sub-boxes before the wait;
           // every later wait of the producer (a free stage, a free scale buffer) comes after it
           if (!kFuse && (waited || it == (NS < NCH ? NS : NCH) - 1)) {
@@ -561,6 +597,21 @@ q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const MmaParams p) {
             decode_q4_pairs(wa.x, wa.y, pa);
             decode_q4_pairs(wb.x, wb.y, pb);
           }
+          if constexpr (kHB > 0) {
+            // the high bits of the same 16 weights of each row: 2 (Q5) or 4 (Q6) bytes at
+            // 8 kHB bytes per group and 2 kHB per thread column c
+            const uint32_t hrow = stage(s) + p.hi_off + (uint32_t)(sub * BR) * kHRow + (uint32_t)(gl * 8 * kHB + c * 2 * kHB);
+            uint32_t ha, hb;
+            if constexpr (kHB == 1) {
+              ha = lds_u16(hrow + (uint32_t)ra * kHRow);
+              hb = lds_u16(hrow + (uint32_t)rb * kHRow);
+            } else {
+              ha = lds_u32(hrow + (uint32_t)ra * kHRow);
+              hb = lds_u32(hrow + (uint32_t)rb * kHRow);
+            }
+            add_high_pairs<kHB>(ha, pa);
+            add_high_pairs<kHB>(hb, pb);
+          }
           const float sa = va ? fp16_bits_to_float(lds_u16(sca + 2u * (uint32_t)G)) : 0.f;
           const float sbv = vb ? fp16_bits_to_float(lds_u16(scb + 2u * (uint32_t)G)) : 0.f;
 #pragma unroll
@@ -660,7 +711,9 @@ int mma_early_order(int fmt, int lanes, int nt) { return (fmt == 0 && nt == 1 &&
 // workspace; otherwise the operand pass and its workspace.
 bool mma_plan_for(int64_t N, int64_t K, int64_t T, int sms, MmaPlan* pl, int fmt = 0, bool fused = false,
                   bool swiglu = false) {
-  if (N < 1 || K < 8 || T < 1 || (fmt != 0 && fmt != 3)) return false;
+  if (N < 1 || K < 8 || T < 1 || fmt < 0 || fmt > 3) return false;
+  if (fused && (fmt == 1 || fmt == 2)) return false;   // (no fused operation takes Q5 / Q6)
+  const int hb = (fmt == 1 || fmt == 2) ? fmt : 0;       // Q5 / Q6 high bits per weight
   if (fused && T > 8) return false;
   if (swiglu && !fused) return false;   // LinearSwiGLU: the one-launch form only
   if (N >= ((int64_t)1 << 31) || K >= ((int64_t)1 << 31)) return false;
@@ -697,7 +750,8 @@ bool mma_plan_for(int64_t N, int64_t K, int64_t T, int sms, MmaPlan* pl, int fmt
     const int nchunks = (nk + chunk_groups - 1) / chunk_groups;
     int stages = 8;
     for (; stages >= 2; --stages) {
-      const MmaLayout L = mma_layout(pl->nt, br, ks, pl->mt, stages, pl->lanes, Kp, pl->fbytes, pl->srb);
+      const MmaLayout L = mma_layout(pl->nt, br, ks, pl->mt, stages, pl->lanes, Kp, pl->fbytes, pl->srb, false, 0,
+                                     false, hb);
       if (L.total + 1024 <= kMmaSmem) break;
     }
     if (stages < 2) continue;
@@ -705,7 +759,7 @@ bool mma_plan_for(int64_t N, int64_t K, int64_t T, int sms, MmaPlan* pl, int fmt
     pl->nchunks = nchunks;
     pl->stages = stages;
     pl->galloc = nchunks * chunk_groups;
-    pl->L = mma_layout(pl->nt, br, ks, pl->mt, stages, pl->lanes, Kp, pl->fbytes, pl->srb);
+    pl->L = mma_layout(pl->nt, br, ks, pl->mt, stages, pl->lanes, Kp, pl->fbytes, pl->srb, false, 0, false, hb);
     pl->fused = 0;
     if (!fused) return true;
     // the whole-K B fragments beside at least two code stages (else fewer sub-boxes per chunk)
@@ -757,12 +811,17 @@ int mma_kernel_attrs() {
 }
 
 template <int NT, int FMT>
-int mma_launch_pass(const LinearArgs& a, const MmaPlan& pl, const CUtensorMap& tm, int64_t t0, int tp) {
-  const bool fused = NT == 1 && pl.fused;
+int mma_launch_pass(const LinearArgs& a, const MmaPlan& pl, const CUtensorMap& tm, const CUtensorMap& th, int64_t t0,
+                    int tp) {
+  const bool fused = NT == 1 && pl.fused && (FMT == 0 || FMT == 3);
   const bool swi = FMT == 0 && fused && a.mode == 1;
-  if (const int rc = swi ? mma_kernel_attrs<1, 0, true, true>()
-                     : fused ? mma_kernel_attrs<1, FMT, true>() : mma_kernel_attrs<NT, FMT, false>())
-    return rc;
+  int rc0 = Q4LIN_OK;
+  if constexpr (FMT == 0 || FMT == 3)
+    rc0 = swi ? mma_kernel_attrs<1, 0, true, true>()
+              : fused ? mma_kernel_attrs<1, FMT, true>() : mma_kernel_attrs<NT, FMT, false>();
+  else
+    rc0 = mma_kernel_attrs<NT, FMT, false>();
+  if (rc0 != Q4LIN_OK) return rc0;
   uint8_t* xf = nullptr;
   float* zs = nullptr;
   cudaLaunchAttribute at[1];
@@ -810,8 +869,9 @@ int mma_launch_pass(const LinearArgs& a, const MmaPlan& pl, const CUtensorMap& t
   p.early = pl.early;
   p.galloc = pl.galloc;
   p.stage_bytes = pl.L.stage_bytes;
-  p.xf_off = fused ? pl.L.fx_off : pl.L.code_bytes;
-  p.zs_off = fused ? pl.L.fz_off : pl.L.code_bytes + pl.L.xf_bytes;
+  p.hi_off = pl.L.code_bytes;
+  p.xf_off = fused ? pl.L.fx_off : pl.L.code_bytes + pl.L.hi_bytes;
+  p.zs_off = fused ? pl.L.fz_off : pl.L.code_bytes + pl.L.hi_bytes + pl.L.xf_bytes;
   p.scl_off = pl.L.scl_off;
   p.scl_bytes = pl.L.scl_bytes;
   p.red_off = pl.L.red_off;
@@ -824,24 +884,24 @@ int mma_launch_pass(const LinearArgs& a, const MmaPlan& pl, const CUtensorMap& t
   cfg.stream = a.stream;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  if constexpr (NT == 1) {
-    if (swi) return cuda_check(cudaLaunchKernelEx(&cfg, q4_mma_kernel<1, 0, true, true>, tm, p), "mma: kernel launch");
-    if (fused) return cuda_check(cudaLaunchKernelEx(&cfg, q4_mma_kernel<1, FMT, true>, tm, p), "mma: kernel launch");
+  if constexpr (NT == 1 && (FMT == 0 || FMT == 3)) {
+    if (swi) return cuda_check(cudaLaunchKernelEx(&cfg, q4_mma_kernel<1, 0, true, true>, tm, th, p), "mma: kernel launch");
+    if (fused) return cuda_check(cudaLaunchKernelEx(&cfg, q4_mma_kernel<1, FMT, true>, tm, th, p), "mma: kernel launch");
   }
-  return cuda_check(cudaLaunchKernelEx(&cfg, q4_mma_kernel<NT, FMT, false>, tm, p), "mma: kernel launch");
+  return cuda_check(cudaLaunchKernelEx(&cfg, q4_mma_kernel<NT, FMT, false>, tm, th, p), "mma: kernel launch");
 }
 
 template <int FMT>
-int mma_launch_fmt(const LinearArgs& a, const MmaPlan& pl, const CUtensorMap& tm) {
+int mma_launch_fmt(const LinearArgs& a, const MmaPlan& pl, const CUtensorMap& tm, const CUtensorMap& th) {
   // passes of at most 32 tokens (8 NT each), sharing the workspace in stream order
   for (int64_t t0 = 0; t0 < a.T; t0 += 8 * pl.nt) {
     const int tp = (int)((a.T - t0) < 8 * pl.nt ? (a.T - t0) : 8 * pl.nt);
     int rc;
     switch (pl.nt) {
-      case 1: rc = mma_launch_pass<1, FMT>(a, pl, tm, t0, tp); break;
-      case 2: rc = mma_launch_pass<2, FMT>(a, pl, tm, t0, tp); break;
-      case 3: rc = mma_launch_pass<3, FMT>(a, pl, tm, t0, tp); break;
-      default: rc = mma_launch_pass<4, FMT>(a, pl, tm, t0, tp); break;
+      case 1: rc = mma_launch_pass<1, FMT>(a, pl, tm, th, t0, tp); break;
+      case 2: rc = mma_launch_pass<2, FMT>(a, pl, tm, th, t0, tp); break;
+      case 3: rc = mma_launch_pass<3, FMT>(a, pl, tm, th, t0, tp); break;
+      default: rc = mma_launch_pass<4, FMT>(a, pl, tm, th, t0, tp); break;
     }
     if (rc != Q4LIN_OK) return rc;
   }
@@ -881,7 +941,27 @@ int mma_launch(const LinearArgs& a, bool fused) {
     set_error_detail("mma: cuTensorMapEncodeTiled failed (or is unavailable)");
     return Q4LIN_ERR_CUDA;
   }
-  return pl.fmt == 3 ? mma_launch_fmt<3>(a, pl, tm) : mma_launch_fmt<0>(a, pl, tm);
+  // Q5 / Q6: the high-bit plane, rows of K_pad * hb / 8 bytes, boxes of one sub-box (256 weights,
+  // 32 hb bytes) x band rows, unswizzled
+  CUtensorMap th = tm;  // unused for Q4 and W8
+  if (pl.fmt == 1 || pl.fmt == 2) {
+    if (a.wh == nullptr) {
+      set_error_detail("mma: Q5 / Q6 without a high-bit plane");
+      return Q4LIN_ERR_INVALID_ARG;
+    }
+    const uint64_t hrow = (uint64_t)(k_pad(a.K) * pl.fmt / 8);
+    if (!encode_map_2d(&th, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.wh, hrow, (uint64_t)a.N, hrow, (uint32_t)(32 * pl.fmt),
+                       (uint32_t)pl.br, CU_TENSOR_MAP_SWIZZLE_NONE)) {
+      set_error_detail("mma: cuTensorMapEncodeTiled failed for the high-bit plane");
+      return Q4LIN_ERR_CUDA;
+    }
+  }
+  switch (pl.fmt) {
+    case 1: return mma_launch_fmt<1>(a, pl, tm, th);
+    case 2: return mma_launch_fmt<2>(a, pl, tm, th);
+    case 3: return mma_launch_fmt<3>(a, pl, tm, th);
+    default: return mma_launch_fmt<0>(a, pl, tm, th);
+  }
 }
 
 int mma_status(int* value, bool clear) {

@@ -152,6 +152,26 @@ int run_impl(int route, const uint8_t* wq, const uint16_t* scales, const uint16_
 // W8G32 beyond the warp-MMA route's token range takes the tile route.
 bool w8_tile(int64_t N, int64_t K, int64_t T) { return T > kW8MmaMaxT && q4::tc_supported(N, K, T); }
 
+// Route of a sibling format (K > 0):
+//   Q5G64 / Q6G64: the decode GEMV for one token; the streaming warp-MMA route for 2..32
+//     tokens (the high bits joined to the nibble operands; its operand pass needs
+//     workspace); the exact tile route beyond (token tiles up to 128 wide); where a route
+//     has no plan, the GEMV up to 4 tokens, else the tile route.
+//   W8G32: the decode GEMV for 1..4 tokens, the warp-MMA route up to 24, the tile route beyond.
+int qtype_route(int qtype, int64_t N, int64_t K, int64_t T) {
+  const bool q56 = qtype == Q4LIN_QTYPE_Q5G64 || qtype == Q4LIN_QTYPE_Q6G64;
+  if (q56) {
+    if (T == 1 && q4::gemv_stream_ok(N, K, T, qtype)) return Q4LIN_ROUTE_GEMV;
+    if (T <= kMmaMaxT && q4::mma_supported(N, K, T, qtype)) return Q4LIN_ROUTE_STREAM_MMA;
+    if (q4::gemv_stream_ok(N, K, T, qtype) || !q4::tc_supported(N, K, T)) return Q4LIN_ROUTE_GEMV;
+    return Q4LIN_ROUTE_TC_SPLITK;
+  }
+  if (q4::gemv_stream_ok(N, K, T, qtype)) return Q4LIN_ROUTE_GEMV;
+  if (w8_tile(N, K, T)) return Q4LIN_ROUTE_TC_SPLITK;
+  if (q4::mma_supported(N, K, T, qtype)) return Q4LIN_ROUTE_STREAM_MMA;
+  return Q4LIN_ROUTE_GEMV;   // refused there (UNSUPPORTED_SHAPE)
+}
+
 int run_qtype_impl(int qtype, const uint8_t* codes, const uint8_t* high, const uint16_t* scales,
                    const uint16_t* x, uint16_t* y, int64_t N, int64_t K, int64_t T, void* workspace, void* stream) {
   int st = validate(codes, scales, x, y, N, K, T);
@@ -167,21 +187,17 @@ int run_qtype_impl(int qtype, const uint8_t* codes, const uint8_t* high, const u
   q4::LinearArgs a{codes, scales, x, y, N, K, T, nullptr, s};
   a.fmt = qtype;
   a.wh = needs_high ? high : nullptr;
-  // The streaming GEMV where it has a plan (1..4 tokens); otherwise Q5 / Q6 run on the
-  // exact tile route (token tiles up to 128 wide), and W8 on the streaming warp-MMA route
-  // up to 24 tokens (its operand pass needs workspace) and on the exact tile route beyond
-  // (token tiles up to 64 wide).
-  if (q4::gemv_stream_ok(N, K, T, qtype)) return q4::gemv_launch_fmt(a);
-  if (qtype == Q4LIN_QTYPE_W8G32 && w8_tile(N, K, T)) return q4::tc_launch(a, Q4LIN_ROUTE_TC_SPLITK);
-  if (qtype == Q4LIN_QTYPE_W8G32 && q4::mma_supported(N, K, T, 3)) {
-    const size_t ws = round256(q4::mma_workspace_bytes(N, K, T, 3));
-    if (ws > 0 && workspace == nullptr) return Q4LIN_ERR_WORKSPACE;
-    if (ws > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return Q4LIN_ERR_MISALIGNED;
-    a.workspace = workspace;
-    return q4::mma_launch(a);
+  switch (qtype_route(qtype, N, K, T)) {
+    case Q4LIN_ROUTE_TC_SPLITK: return q4::tc_launch(a, Q4LIN_ROUTE_TC_SPLITK);
+    case Q4LIN_ROUTE_STREAM_MMA: {
+      const size_t ws = round256(q4::mma_workspace_bytes(N, K, T, qtype));
+      if (ws > 0 && workspace == nullptr) return Q4LIN_ERR_WORKSPACE;
+      if (ws > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return Q4LIN_ERR_MISALIGNED;
+      a.workspace = workspace;
+      return q4::mma_launch(a);
+    }
+    default: return q4::gemv_launch_fmt(a);
   }
-  if (!needs_high || !q4::tc_supported(N, K, T)) return q4::gemv_launch_fmt(a);
-  return q4::tc_launch(a, Q4LIN_ROUTE_TC_SPLITK);
 }
 
 int run(int route, const uint8_t* wq, const uint16_t* scales, const uint16_t* x, uint16_t* y, int64_t N,
@@ -245,6 +261,12 @@ bool fused_op_on_mma(int64_t N, int64_t K, int64_t T, bool swiglu = false) {
 }  // namespace
 
 extern "C" {
+
+int q4lin_qtype_route(int qtype, int64_t N, int64_t K, int64_t T) {
+  if (qtype == Q4LIN_QTYPE_Q4G64) return q4lin_select_route(N, K, T);
+  if (qtype < Q4LIN_QTYPE_Q5G64 || qtype > Q4LIN_QTYPE_W8G32 || validate_sizes(N, K, T) != Q4LIN_OK) return -1;
+  return qtype_route(qtype, N, K, T);
+}
 
 int q4lin_fused_route(int op, int64_t N, int64_t K, int64_t T) {
   if (op < 1 || op > 3 || validate_sizes(N, K, T) != Q4LIN_OK) return -1;
@@ -405,19 +427,19 @@ int q4lin_qtype_kernel_launches(int qtype, int64_t N, int64_t K, int64_t T) {
   if (qtype < Q4LIN_QTYPE_Q5G64 || qtype > Q4LIN_QTYPE_W8G32) return 0;
   if (validate_sizes(N, K, T) != Q4LIN_OK || N == 0 || T == 0) return 0;
   if (K == 0) return 1;  // the zero fill
-  if (q4::gemv_stream_ok(N, K, T, qtype)) return 1;
-  if (qtype == Q4LIN_QTYPE_W8G32 && w8_tile(N, K, T)) return q4::tc_launch_count(Q4LIN_ROUTE_TC_SPLITK, N, K, T, qtype);
-  if (qtype == Q4LIN_QTYPE_W8G32) return q4::mma_supported(N, K, T, 3) ? q4::mma_launch_count(N, K, T) : 0;
-  if (!q4::tc_supported(N, K, T)) return 0;  // refused
-  return q4::tc_launch_count(Q4LIN_ROUTE_TC_SPLITK, N, K, T, qtype);
+  switch (qtype_route(qtype, N, K, T)) {
+    case Q4LIN_ROUTE_TC_SPLITK: return q4::tc_launch_count(Q4LIN_ROUTE_TC_SPLITK, N, K, T, qtype);
+    case Q4LIN_ROUTE_STREAM_MMA: return q4::mma_launch_count(N, K, T, qtype);
+    default: return q4::gemv_stream_ok(N, K, T, qtype) ? 1 : 0;   // 0: refused
+  }
 }
 
 size_t q4lin_qtype_workspace_bytes(int qtype, int64_t N, int64_t K, int64_t T) {
   if (qtype == Q4LIN_QTYPE_Q4G64) return q4lin_workspace_bytes(N, K, T);
-  if (qtype != Q4LIN_QTYPE_W8G32) return 0;
+  if (qtype < Q4LIN_QTYPE_Q5G64 || qtype > Q4LIN_QTYPE_W8G32) return 0;
   if (validate_sizes(N, K, T) != Q4LIN_OK || N == 0 || K == 0 || T == 0) return 0;
-  if (q4::gemv_stream_ok(N, K, T, qtype) || w8_tile(N, K, T)) return 0;
-  return round256(q4::mma_workspace_bytes(N, K, T, 3));
+  if (qtype_route(qtype, N, K, T) != Q4LIN_ROUTE_STREAM_MMA) return 0;
+  return round256(q4::mma_workspace_bytes(N, K, T, qtype));
 }
 
 int q4lin_linear(const uint8_t* wq, const uint16_t* scales, const uint16_t* x, uint16_t* y,

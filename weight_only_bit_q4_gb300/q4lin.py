@@ -27,7 +27,7 @@ EXPORTS = ("q4lin_workspace_bytes", "q4lin_linear", "q4lin_linear_route", "q4lin
            "q4lin_status_string",
            "q4lin_device_status", "q4lin_clear_device_status", "q4lin_last_error_detail",
            "q4lin_hbm_read_probe", "q4lin_diag_wait_expiry", "q4lin_linear_swiglu", "q4lin_linear_pair",
-           "q4lin_qtype_workspace_bytes", "q4lin_host_workspace_bytes", "q4lin_linear_host", "q4lin_fused_route", "q4lin_version")
+           "q4lin_qtype_workspace_bytes", "q4lin_host_workspace_bytes", "q4lin_linear_host", "q4lin_fused_route", "q4lin_qtype_route", "q4lin_version")
 
 _lib = None
 
@@ -100,6 +100,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q4lin_host_workspace_bytes.restype = sz
     lib.q4lin_linear_host.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp]
     lib.q4lin_linear_host.restype = ctypes.c_int
+    lib.q4lin_qtype_route.argtypes = [ctypes.c_int, i64, i64, i64]
+    lib.q4lin_qtype_route.restype = ctypes.c_int
     lib.q4lin_fused_route.argtypes = [ctypes.c_int, i64, i64, i64]
     lib.q4lin_fused_route.restype = ctypes.c_int
     lib.q4lin_version.argtypes = []
@@ -216,6 +218,11 @@ def linear(wq, scales, x, y=None, workspace=None, stream=None, route: int = ROUT
 
 
 FUSED_OPS = {"add": 1, "swiglu": 2, "pair": 3}
+
+
+def qtype_route(qtype: str, N: int, K: int, T: int) -> int:
+    """Route q4lin_linear_qtype takes for this format and shape."""
+    return int(load().q4lin_qtype_route(QTYPES[qtype], N, K, T))
 
 
 def fused_route(op: str, N: int, K: int, T: int) -> int:
