@@ -100,8 +100,10 @@ def test_w8_beyond_four_tokens_needs_workspace():
 
 @pytest.mark.parametrize("qtype", ["q5g64", "q6g64"])
 @pytest.mark.parametrize("N,K,T", [(64, 256, 5), (300, 200, 37), (1001, 4096, 130), (640, 4304, 300),
-                                   (77, 17408, 8), (6144, 5120, 128), (257, 1152, 517), (5, 128, 1000)])
+                                   (77, 17408, 8), (6144, 5120, 128), (257, 1152, 517), (5, 128, 1000),
+                                   (6144, 5120, 1024), (1000, 2048, 257)])
 def test_q5_q6_tile_route_matches_oracle(qtype, N, K, T):
+    # beyond 128 tokens 256-wide tiles (two A stages beside the high-bit stages) or 128-wide ones
     planes, s, x = synth.make_problem_fmt(qtype, N, K, T, w_seed=N + 3, x_seed=K + T)
     assert_close(_run(qtype, planes, s, x), sf.linear(qtype, planes, s, x), f"{qtype} {N}x{K} T={T}")
 

@@ -137,7 +137,7 @@ struct TcSmem {
   using C = TcCfg<BN>;
   static constexpr int kHB = (FMT == 1 || FMT == 2) ? FMT : 0;  // high bits per weight (Q5 / Q6)
   static constexpr bool kW8 = FMT == 3;  // W8G32: one code byte per weight, two 32-wide scale groups per 64-wide group
-  static_assert(FMT == 0 || (!kFold && BN <= 128), "sibling formats: exact form, BN <= 128");
+  static_assert(FMT == 0 || (!kFold && (BN <= 128 || kHB > 0)), "sibling formats: exact form, BN <= 128 (Q5 / Q6: 256)");
   static_assert(!kW8 || BN <= 128, "W8G32: token tiles up to 128 wide");
   // W8G32 at 128-token tiles: two accumulators per group in flight fill tensor memory, so A
   // is staged in shared memory (four X, A and code stages fit beside it)
@@ -147,7 +147,9 @@ struct TcSmem {
   // stages instead of four (measured 8-12 % faster at T = 1024).
   static constexpr bool kWide = kFold && BN == 256;
   // W8G32 keeps two accumulators per group in flight (one per 32-wide scale group)
-  static constexpr int SX = kWide ? 6 : kW8Wide ? 4 : C::SX, SA = kW8Wide ? 4 : C::SA, NB = kFold ? 1 : kW8 ? 2 : C::NB,
+  // Q5 / Q6 at 256-token tiles: the high-bit stages take the room of two A stages
+  static constexpr int SX = kWide ? 6 : kW8Wide ? 4 : C::SX,
+                       SA = kW8Wide ? 4 : (kHB > 0 && BN == 256) ? 2 : C::SA, NB = kFold ? 1 : kW8 ? 2 : C::NB,
                        NACC = C::NACC, SW = kW8Wide ? 2 : C::SW;
   static constexpr int kAccPerGroup = kW8 ? 2 : 1;
   static constexpr uint32_t kCB = kW8 ? 2 * kWBytes : kWBytes;  // one code stage (4 groups)
@@ -1179,9 +1181,6 @@ TcPlan tc_plan(int route, int64_t N, int64_t K, int64_t T, int sms, int fmt) {
   if (fmt == 3) {  // W8G32: two accumulators per group (A in shared memory at 128-wide tiles)
     cand[0] = T > 64 ? 128 : T > 32 ? 64 : T > 16 ? 32 : 16;
     ncand = 1;
-  } else if (T > 128 && fmt != 0) {  // Q5 / Q6: the high-bit stages leave no room for 256-wide tiles
-    cand[0] = 128;
-    ncand = 1;
   } else if (T > 128) {
     cand[0] = 256;
     cand[1] = 128;
@@ -1295,6 +1294,7 @@ int tc_launch(const LinearArgs& a, int route) {
     if (a.fmt != 0) {
       const bool q5 = a.fmt == 1;
       switch (pl.bn) {
+        case 256: return q5 ? launch_tile<256, false, 1>(a, splitk, base, n) : launch_tile<256, false, 2>(a, splitk, base, n);
         case 128: return q5 ? launch_tile<128, false, 1>(a, splitk, base, n) : launch_tile<128, false, 2>(a, splitk, base, n);
         case 64: return q5 ? launch_tile<64, false, 1>(a, splitk, base, n) : launch_tile<64, false, 2>(a, splitk, base, n);
         case 32: return q5 ? launch_tile<32, false, 1>(a, splitk, base, n) : launch_tile<32, false, 2>(a, splitk, base, n);
