@@ -27,8 +27,15 @@ calls, then 20 samples of one public call behind a 256 MiB flush; median, min, p
 prints the contract's console header and one line per T (section 7) with the change of the
 median against the previous T (delta_%), optionally to a CSV file as well.
 
+The first record also carries e2e: the step with X and Y in pinned host memory through
+q4lin_linear_host (the library stages X in and the layer stores Y into the pinned
+buffer), one CUDA graph replay per step, median of 200; the same step with
+cudaMemcpyAsync copies around the device-buffer call (memcpy_us) and issued eagerly from
+Python (eager_us) is reported beside it.
+
 --qtype times a sibling weight format (Q5G64, Q6G64, W8G32) on the same geometry
-through q4lin_linear_qtype; its bytes are that format's.  Under torchrun (N > 1)
+through q4lin_linear_qtype; its bytes are that format's.  --op times a fused operation
+(LinearAdd, LinearSwiGLU, LinearPair).  Under torchrun (N > 1)
 every rank runs an independent replica on its own GPU (the layer does not exchange
 data between GPUs); value = the units all ranks processed / the slowest rank's time.
 """
