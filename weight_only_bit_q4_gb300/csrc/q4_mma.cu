@@ -62,6 +62,7 @@ constexpr int kMaxConsumers = kMmaWarps - 1;
 constexpr int kMaxBand = 240;  // rows per band: TMA box height <= 256, 15 m-tiles
 constexpr uint32_t kMmaSmem = 232448;  // dynamic shared memory per CTA (incl. 1024-byte alignment slack)
 constexpr int kRedBar = 1;             // named barrier of the consumer warps
+constexpr int kConvBar = 2;            // fused form: named barrier of the warps converting X
 // Early launch order: L2 prefetch of one CTA's code rows before the dependency wait, at
 // most (the whole share of a 6144-row layer on 152 SMs: 103 KB at K = 5120).
 constexpr int64_t kMmaPrefetchCap = 128 * 1024;
@@ -519,28 +520,19 @@ q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
     __syncwarp();
     return;
   }
-  if (warp - 1 >= WC) return;
-
-  // ------------------------------------------------------------- consumers
-  const int wc = warp - 1;
-  const int m = wc / KS, sub = wc % KS;
-  const int g = lane >> 2, c = lane & 3;
-  const int ra = 16 * m + 2 * g, rb = ra + 1;  // band rows of mma rows g and g + 8
-  const bool bload = lane < p.lanes;           // this lane's B fragment is stored (the others are zero)
-  int it = 0;
-  bool ok = true;
   if constexpr (kFuse) {
-    // the operand pass of the whole K extent into shared memory, then one barrier of the
-    // consumer warps; x may come from the previous kernel
+    // the operand pass of the whole K extent into shared memory by every warp but the
+    // producer (the warps the band plan leaves idle included), then one barrier of those
+    // warps; x may come from the previous kernel
     pdl_wait_previous();
     // kUnits units per thread per round, their loads issued together
     constexpr int kUnits = 3;
     const int64_t units = (int64_t)32 * p.galloc;  // 8 token slots x 4 lanes per group
-    const int64_t wstride = (int64_t)WC * 32;
+    const int64_t wstride = (int64_t)kMaxConsumers * 32;
     uint8_t* fx = smem + p.xf_off;
     float* fz = reinterpret_cast<float*>(smem + p.zs_off);
     const uint16_t* xp = p.x + (int64_t)p.t0 * p.K;
-    for (int64_t base = (int64_t)wc * 32; base < units; base += kUnits * wstride) {
+    for (int64_t base = (int64_t)(warp - 1) * 32; base < units; base += kUnits * wstride) {
       uint4 q[kUnits][2];
 #pragma unroll
       for (int j = 0; j < kUnits; ++j) {
@@ -554,8 +546,18 @@ q4_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constan
           mma_operand_convert<NT, FMT>(p.tp, p.galloc, p.lanes, u, u < units, q[j], fx, fz);
       }
     }
-    named_bar_sync(kRedBar, (uint32_t)(WC * 32));
+    named_bar_sync(kConvBar, (uint32_t)(kMaxConsumers * 32));
   }
+  if (warp - 1 >= WC) return;
+
+  // ------------------------------------------------------------- consumers
+  const int wc = warp - 1;
+  const int m = wc / KS, sub = wc % KS;
+  const int g = lane >> 2, c = lane & 3;
+  const int ra = 16 * m + 2 * g, rb = ra + 1;  // band rows of mma rows g and g + 8
+  const bool bload = lane < p.lanes;           // this lane's B fragment is stored (the others are zero)
+  int it = 0;
+  bool ok = true;
   for (int b = 0; b < nbands; ++b) {
     const int64_t R0 = band_row(b);
     const int rows = band_rows(b);
