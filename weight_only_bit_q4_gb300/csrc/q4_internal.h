@@ -77,7 +77,7 @@ bool encode_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uin
 // writes X as fp16 MMA fragments into the workspace, then one persistent kernel
 // streams the weights.  Whether it has a shared-memory plan for (N, K, T), its
 // workspace, its launch count and the call.
-// fmt: 0 Q4G64, 3 W8G32
+// fmt: 0 Q4G64, 1 Q5G64, 2 Q6G64, 3 W8G32
 bool mma_supported(int64_t N, int64_t K, int64_t T, int fmt = 0);
 size_t mma_workspace_bytes(int64_t N, int64_t K, int64_t T, int fmt = 0);
 int mma_launch_count(int64_t N, int64_t K, int64_t T, int fmt = 0);

@@ -1,4 +1,4 @@
-// Streaming warp-MMA route of the Q4_G64_FP16 linear layer, for a few tokens.
+// Streaming warp-MMA route of the Q4_G64_FP16 linear layer (and its sibling formats), for a few tokens.
 //
 // Below a few dozen tokens the layer is a stream of packed weights: every weight
 // is read once from HBM and used T times.  The tile route's per-group pipeline
@@ -43,6 +43,13 @@
 // keeps its FP32 partial sums in registers across the band; at the end of the
 // band the KS partials of each row are summed in a fixed order through shared
 // memory (deterministic) and the band's outputs are rounded to bf16 and stored.
+//
+// Forms.  Q5G64 / Q6G64 stage their high-bit plane beside the code sub-boxes and join
+// the high bits to the nibble operands; W8G32 offsets its signed bytes to u = code + 128
+// (two MMAs per 32-wide group).  Without a workspace (the fused operations, up to 8
+// tokens) the kernel converts X itself into whole-K fragments in shared memory and no
+// prep kernel runs; LinearAdd adds its residual in the band epilogue and LinearSwiGLU
+// pairs each band of gate rows with the band of up rows it multiplies.
 //
 // Every mbarrier wait is bounded (kSpinLimit): on expiry the kernel records
 // Q4LIN_ERR_TIMEOUT, every role skips its remaining work but still passes the
