@@ -298,3 +298,17 @@ def test_format_routes(lib):
     assert q4lin.qtype_route("w8g32", 6144, 5120, 25) == q4lin.ROUTE_TC_SPLITK
     assert q4lin.qtype_route("q4g64", 6144, 5120, 8) == q4lin.select_route(6144, 5120, 8)
     assert lib.q4lin_qtype_route(9, 64, 256, 8) == -1 and lib.q4lin_qtype_route(1, 64, 100, 8) == -1
+
+
+def test_fused_operation_routes(lib):
+    # no workspace: up to 8 tokens the warp-MMA route's one-launch form where its whole-K
+    # operands fit in shared memory, the tile route otherwise
+    for op in ("add", "swiglu", "pair"):
+        N = 17408 if op == "swiglu" else 34816
+        assert q4lin.fused_route(op, N, 5120, 1) == q4lin.ROUTE_STREAM_MMA, op
+        assert q4lin.fused_route(op, N, 5120, 8) == q4lin.ROUTE_STREAM_MMA, op
+        assert q4lin.fused_route(op, N, 5120, 9) == q4lin.ROUTE_TC_SPLITK, op
+    assert q4lin.fused_route("add", 77, 17408, 8) == q4lin.ROUTE_TC_SPLITK    # 278 KB of operands
+    assert q4lin.fused_route("add", 77, 17408, 2) == q4lin.ROUTE_STREAM_MMA   # 70 KB at 8 lanes
+    assert lib.q4lin_fused_route(0, 64, 256, 4) == -1 and lib.q4lin_fused_route(4, 64, 256, 4) == -1
+    assert lib.q4lin_fused_route(1, 64, 100, 4) == -1                          # K % 8 != 0
