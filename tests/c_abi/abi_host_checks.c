@@ -45,6 +45,15 @@ int main(void) {
         "static-scratch entry refuses a shape beyond its array");
   CHECK(q4lin_linear_add(wq, sc, x, NULL, y, 64, 256, 8, NULL) == Q4LIN_ERR_INVALID_ARG,
         "LinearAdd without a residual refused");
+  CHECK(q4lin_host_workspace_bytes(6144, 5120, 1) == (size_t)2 * 5120 + 2 * 6144,
+        "host entry workspace: X and Y staging, 256-byte parts");
+  CHECK(q4lin_linear_host(wq, sc, x, y, 64, 256, 4, NULL, NULL) == Q4LIN_ERR_WORKSPACE,
+        "host entry without workspace refused");
+  CHECK(q4lin_qtype_route(Q4LIN_QTYPE_Q5G64, 6144, 5120, 8) == Q4LIN_ROUTE_STREAM_MMA,
+        "Q5 at 8 tokens: the warp-MMA route");
+  CHECK(q4lin_fused_route(1, 6144, 5120, 8) == Q4LIN_ROUTE_STREAM_MMA &&
+            q4lin_fused_route(1, 6144, 5120, 64) == Q4LIN_ROUTE_TC_SPLITK,
+        "LinearAdd routes: one-launch warp-MMA form up to 8 tokens, tiles beyond");
   CHECK(strcmp(q4lin_status_string(Q4LIN_ERR_TIMEOUT), "unknown status") != 0, "status strings");
   CHECK(q4lin_version() != NULL && q4lin_version()[0] != 0, "version");
   return fails ? 1 : 0;
